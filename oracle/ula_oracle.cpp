@@ -1,0 +1,517 @@
+// TEST INFRASTRUCTURE -- the CPU oracle of the KV residency path.
+//
+// Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+// load this library.  It shares no code with the CUDA path: it keeps its own
+// containers (one ordered set per slot class, a per-address location record)
+// and walks the method's steps one by one, in the order the pages give them.
+// It is slow on purpose and single-threaded.
+//
+// Source: "UlaCache: Unified Logical Addressing for Sparse LLM Serving"
+// (paper summary page).
+//   §2 "Unified logical addresses": every KV entry has a fixed logical
+//       address and a mapping entry naming the GPU slot or the CPU slot that
+//       holds it; in DP mode an entry lives on the GPU or on the CPU, never
+//       both; a layer group sharing one selection does lookup and dedup once.
+//   §3 "PB-LRU": slots accessed in one scheduling round go into one bucket;
+//       each layer group keeps a ring of buckets plus a cold bucket; each
+//       round the current bucket advances one position and what is left in
+//       the bucket about to be reused goes to the cold bucket (labels only);
+//       space comes from free slots, then the cold bucket, then the ring from
+//       oldest to newest; the current bucket is never chosen; data moves
+//       first, then the mapping is updated, then completion is signalled.
+//
+// Readings where the pages are silent (each also listed in the design notes):
+//   * one GPU slot holds the rows of all L_g layers of one address for one
+//     group; each group has its own map, pools, ring and cold bucket;
+//   * one scheduling round = one step call for that group; rotation happens
+//     at the start of the round, before hits are marked;
+//   * the ring has B buckets including the current one; the oldest ring
+//     bucket is cur+1, the newest cur-1 (mod B);
+//   * inside every class, the lowest slot index goes first;
+//   * dedup keeps first occurrences in flattened (request, query, i) order;
+//     the i-th miss in that order gets the i-th victim;
+//   * the j-th victim that holds data is written back to the j-th lowest
+//     host slot free before the step; the misses' host slots are released
+//     after all moves;
+//   * a step needing more victims than S - hits, more host slots than are
+//     free, or more output rows than the caller's buffer fails with
+//     CAPACITY before any state changes; an unallocated or out-of-range
+//     address fails with UNMAPPED before any state changes;
+//   * alloc hands out logical bases monotonically, places each new address
+//     in the lowest free GPU slot (joining the current bucket), else the
+//     lowest free host slot, and never evicts; free releases both tiers.
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <set>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+namespace {
+
+constexpr uint32_t kPad = 0xFFFFFFFFu;
+constexpr uint32_t kNone = 0xFFFFFFFFu;
+
+// Status values (same numbers as the library's documented error codes).
+enum {
+  kOk = 0,
+  kInvalidArg = 1,
+  kCapacity = 2,
+  kUnmapped = 3,
+  kInternal = 7,  // a guard that cannot fire when the steps above are right
+};
+
+// Slot class labels.
+constexpr int kFree = -1;
+constexpr int kCold = -2;
+
+enum Tier : uint8_t { kUnallocated = 0, kOnGpu = 1, kOnHost = 2 };
+
+struct Location {
+  Tier tier = kUnallocated;
+  uint32_t slot = 0;
+};
+
+struct Group {
+  uint32_t layers = 0;
+  std::vector<Location> where;          // [max_logical]: the logical-to-physical map
+  std::vector<int> cls;                 // [S]: kFree, kCold or a ring bucket index
+  std::vector<uint32_t> owner;          // [S]: logical address held, or kNone
+  std::set<uint32_t> free_slots;        // GPU slots holding nothing
+  std::set<uint32_t> cold;              // the cold bucket
+  std::vector<std::set<uint32_t>> ring; // [B] ring buckets
+  uint32_t cur = 0;                     // current ring bucket
+  std::set<uint32_t> host_free;         // free host slots
+  std::vector<uint32_t> host_owner;     // [H]
+  std::vector<uint8_t> gpu_pool;        // [S][layers][row_bytes]
+  std::vector<uint8_t> host_pool;       // [H][layers][row_bytes]
+  // decisions of the last step (for inspection by tests)
+  std::vector<uint32_t> last_victims;   // victim i paired with miss i
+  std::vector<uint32_t> last_wb_host;   // host slot of the j-th write-back
+  std::vector<int> last_victim_class;   // class each victim was taken from
+};
+
+struct Oracle {
+  uint32_t row_bytes = 0, n_groups = 0, S = 0, H = 0, B = 0, max_logical = 0;
+  uint32_t next_logical = 0;
+  std::vector<uint8_t> live;  // [max_logical]
+  std::vector<Group> groups;
+
+  size_t slot_bytes(const Group &g) const { return (size_t)g.layers * row_bytes; }
+};
+
+void remove_from_class(Group &g, uint32_t s) {
+  int c = g.cls[s];
+  if (c == kFree) g.free_slots.erase(s);
+  else if (c == kCold) g.cold.erase(s);
+  else g.ring[(size_t)c].erase(s);
+}
+
+void move_to_current_bucket(Group &g, uint32_t s) {
+  remove_from_class(g, s);
+  g.ring[g.cur].insert(s);
+  g.cls[s] = (int)g.cur;
+}
+
+}  // namespace
+
+extern "C" {
+
+void *orc_create(uint32_t row_bytes, uint32_t n_groups, const uint32_t *layers, uint32_t S,
+                 uint32_t H, uint32_t B, uint32_t max_logical) {
+  if (!row_bytes || !n_groups || !layers || !S || !B || !max_logical) return nullptr;
+  Oracle *o = new Oracle;
+  o->row_bytes = row_bytes;
+  o->n_groups = n_groups;
+  o->S = S;
+  o->H = H;
+  o->B = B;
+  o->max_logical = max_logical;
+  o->live.assign(max_logical, 0);
+  o->groups.resize(n_groups);
+  for (uint32_t gi = 0; gi < n_groups; ++gi) {
+    Group &g = o->groups[gi];
+    g.layers = layers[gi];
+    g.where.assign(max_logical, Location{});
+    g.cls.assign(S, kFree);
+    g.owner.assign(S, kNone);
+    for (uint32_t s = 0; s < S; ++s) g.free_slots.insert(s);
+    g.ring.assign(B, std::set<uint32_t>{});
+    g.cur = 0;
+    for (uint32_t h = 0; h < H; ++h) g.host_free.insert(h);
+    g.host_owner.assign(H, kNone);
+    g.gpu_pool.assign((size_t)S * o->slot_bytes(g), 0);
+    g.host_pool.assign((size_t)H * o->slot_bytes(g), 0);
+  }
+  return o;
+}
+
+void orc_destroy(void *h) { delete static_cast<Oracle *>(h); }
+
+// rows: for each group in order, [n][layers_g][row_bytes] (groups concatenated).
+int orc_alloc(void *h, uint32_t n, const uint8_t *rows, uint32_t *base_out) {
+  Oracle *o = static_cast<Oracle *>(h);
+  if (!o || !base_out || (n && !rows)) return kInvalidArg;
+  if ((uint64_t)o->next_logical + n > o->max_logical) return kCapacity;
+  for (const Group &g : o->groups)
+    if ((size_t)n > g.free_slots.size() + g.host_free.size()) return kCapacity;
+  const uint32_t base = o->next_logical;
+  size_t group_off = 0;
+  for (Group &g : o->groups) {
+    const size_t sb = o->slot_bytes(g);
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t a = base + i;
+      const uint8_t *src = rows + group_off + (size_t)i * sb;
+      if (!g.free_slots.empty()) {  // lowest free GPU slot; a prefill write counts as an access
+        uint32_t s = *g.free_slots.begin();
+        move_to_current_bucket(g, s);
+        g.owner[s] = a;
+        g.where[a] = Location{kOnGpu, s};
+        std::memcpy(&g.gpu_pool[(size_t)s * sb], src, sb);
+      } else {  // otherwise the lowest free host slot
+        uint32_t hs = *g.host_free.begin();
+        g.host_free.erase(hs);
+        g.host_owner[hs] = a;
+        g.where[a] = Location{kOnHost, hs};
+        std::memcpy(&g.host_pool[(size_t)hs * sb], src, sb);
+      }
+    }
+    group_off += (size_t)n * sb;
+  }
+  for (uint32_t i = 0; i < n; ++i) o->live[base + i] = 1;
+  o->next_logical = base + n;
+  *base_out = base;
+  return kOk;
+}
+
+int orc_free(void *h, uint32_t base, uint32_t n) {
+  Oracle *o = static_cast<Oracle *>(h);
+  if (!o || (uint64_t)base + n > o->max_logical) return kInvalidArg;
+  for (uint32_t i = 0; i < n; ++i)
+    if (!o->live[base + i]) return kInvalidArg;
+  for (Group &g : o->groups) {
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t a = base + i;
+      Location loc = g.where[a];
+      if (loc.tier == kOnGpu) {
+        remove_from_class(g, loc.slot);
+        g.free_slots.insert(loc.slot);
+        g.cls[loc.slot] = kFree;
+        g.owner[loc.slot] = kNone;
+      } else {
+        g.host_free.insert(loc.slot);
+        g.host_owner[loc.slot] = kNone;
+      }
+      g.where[a] = Location{};
+    }
+  }
+  for (uint32_t i = 0; i < n; ++i) o->live[base + i] = 0;
+  return kOk;
+}
+
+// counters (optional, [8]): uniq, hits, misses, victims from free, from cold,
+// from the ring, write-backs, rows gathered.
+int orc_step_group(void *h, uint32_t gi, const uint32_t *sel, uint32_t n_req, uint32_t q,
+                   uint32_t k, uint8_t *out, uint32_t out_cap, int32_t *entry_row,
+                   int32_t *req_off, uint64_t *counters) {
+  Oracle *o = static_cast<Oracle *>(h);
+  if (!o || gi >= o->n_groups || (n_req && (!sel || !entry_row || !req_off))) return kInvalidArg;
+  Group &g = o->groups[gi];
+  const size_t E = (size_t)n_req * q * k;
+  const size_t sb = o->slot_bytes(g);
+
+  // (1) dedup: one lookup per distinct address of the group's shared selection,
+  //     first occurrences kept in flattened (request, query, i) order.
+  std::vector<uint32_t> uniq;
+  std::unordered_map<uint32_t, int32_t> row_of;
+  row_of.reserve(E * 2 + 1);
+  for (uint32_t r = 0; r < n_req; ++r) {
+    req_off[r] = (int32_t)uniq.size();
+    for (size_t e = (size_t)r * q * k; e < (size_t)(r + 1) * q * k; ++e) {
+      const uint32_t a = sel[e];
+      if (a == kPad) continue;
+      if (a >= o->max_logical || g.where[a].tier == kUnallocated) return kUnmapped;
+      if (row_of.find(a) == row_of.end()) {
+        row_of.emplace(a, (int32_t)uniq.size());
+        uniq.push_back(a);
+      }
+    }
+  }
+  req_off[n_req] = (int32_t)uniq.size();
+
+  // (2) translate through the map: GPU-resident = hit, host-resident = miss.
+  std::vector<uint32_t> misses;
+  size_t hits = 0;
+  for (uint32_t a : uniq) {
+    if (g.where[a].tier == kOnGpu) ++hits;
+    else misses.push_back(a);
+  }
+  const size_t M = misses.size();
+
+  // capacity: victims come from everything but the current bucket, which
+  // after marking holds exactly the hits; write-backs need free host slots.
+  const size_t free_gpu = g.free_slots.size();
+  const size_t writebacks_needed = M > free_gpu ? M - free_gpu : 0;
+  if (M > (size_t)o->S - hits || writebacks_needed > g.host_free.size() || uniq.size() > out_cap)
+    return kCapacity;
+
+  for (size_t e = 0; e < E; ++e) entry_row[e] = sel[e] == kPad ? -1 : row_of[sel[e]];
+
+  // (3a) rotate: the current bucket advances one position; what is left in the
+  //      bucket about to be reused is folded into the cold bucket.
+  g.cur = (g.cur + 1) % o->B;
+  for (uint32_t s : g.ring[g.cur]) {
+    g.cold.insert(s);
+    g.cls[s] = kCold;
+  }
+  g.ring[g.cur].clear();
+
+  // (3b) hits: the slot moves into the current bucket.
+  for (uint32_t a : uniq)
+    if (g.where[a].tier == kOnGpu) move_to_current_bucket(g, g.where[a].slot);
+
+  // (4) victims: free slots, then the cold bucket, then the ring from oldest
+  //     (cur+1) to newest (cur-1); never the current bucket; lowest slot first.
+  std::vector<uint32_t> victims;
+  std::vector<int> victim_class;
+  auto take = [&](const std::set<uint32_t> &from, int label) {
+    for (uint32_t s : from) {
+      if (victims.size() == M) return;
+      victims.push_back(s);
+      victim_class.push_back(label);
+    }
+  };
+  take(g.free_slots, kFree);
+  take(g.cold, kCold);
+  for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));
+
+  if (victims.size() != M) return kInternal;
+
+  // host slots for write-backs: the j-th lowest host slot free before the step
+  std::vector<uint32_t> wb_host;
+  for (uint32_t hs : g.host_free) {
+    if (wb_host.size() == writebacks_needed) break;
+    wb_host.push_back(hs);
+  }
+
+  // (5) move the data first: victim i (if it holds data) is written back to
+  //     the host, then miss i is filled into it; then the map is updated.
+  std::vector<uint32_t> released_host;
+  size_t wb = 0;
+  uint64_t n_free = 0, n_cold = 0, n_ring = 0;
+  for (size_t i = 0; i < M; ++i) {
+    const uint32_t v = victims[i];
+    const uint32_t a = misses[i];
+    const uint32_t src_host = g.where[a].slot;
+    const uint32_t prev_owner = g.owner[v];
+    if (victim_class[i] == kFree) ++n_free;
+    else if (victim_class[i] == kCold) ++n_cold;
+    else ++n_ring;
+    if (prev_owner != kNone) {
+      if (wb >= wb_host.size()) return kInternal;
+      const uint32_t hs = wb_host[wb++];
+      std::memcpy(&g.host_pool[(size_t)hs * sb], &g.gpu_pool[(size_t)v * sb], sb);
+      g.host_free.erase(hs);
+      g.host_owner[hs] = prev_owner;
+      g.where[prev_owner] = Location{kOnHost, hs};
+    }
+    std::memcpy(&g.gpu_pool[(size_t)v * sb], &g.host_pool[(size_t)src_host * sb], sb);
+    g.where[a] = Location{kOnGpu, v};
+    g.owner[v] = a;
+    move_to_current_bucket(g, v);
+    released_host.push_back(src_host);
+  }
+  for (uint32_t hs : released_host) {
+    g.host_free.insert(hs);
+    g.host_owner[hs] = kNone;
+  }
+
+  // (6) gather through the committed map: out[j][u] = row j of uniq[u]'s slot.
+  for (uint32_t j = 0; j < g.layers; ++j)
+    for (size_t u = 0; u < uniq.size(); ++u) {
+      const Location loc = g.where[uniq[u]];
+      std::memcpy(out + ((size_t)j * out_cap + u) * o->row_bytes,
+                  &g.gpu_pool[(size_t)loc.slot * sb + (size_t)j * o->row_bytes], o->row_bytes);
+    }
+
+  g.last_victims = victims;
+  g.last_wb_host = wb_host;
+  g.last_victim_class = victim_class;
+  if (counters) {
+    counters[0] = uniq.size();
+    counters[1] = hits;
+    counters[2] = M;
+    counters[3] = n_free;
+    counters[4] = n_cold;
+    counters[5] = n_ring;
+    counters[6] = wb;
+    counters[7] = (uint64_t)uniq.size() * g.layers;
+  }
+  return kOk;
+}
+
+// Last step's decisions of group gi; returns the number of victims.
+uint32_t orc_last_decisions(void *h, uint32_t gi, uint32_t *victims, int32_t *victim_class,
+                            uint32_t *wb_host, uint32_t *n_wb) {
+  Oracle *o = static_cast<Oracle *>(h);
+  const Group &g = o->groups[gi];
+  if (victims) std::copy(g.last_victims.begin(), g.last_victims.end(), victims);
+  if (victim_class) std::copy(g.last_victim_class.begin(), g.last_victim_class.end(), victim_class);
+  if (wb_host) std::copy(g.last_wb_host.begin(), g.last_wb_host.end(), wb_host);
+  if (n_wb) *n_wb = (uint32_t)g.last_wb_host.size();
+  return (uint32_t)g.last_victims.size();
+}
+
+// State of group gi.  tier/slot: [max_logical]; cls/owner: [S]; host_free: [H] (1 = free).
+void orc_export(void *h, uint32_t gi, uint8_t *tier, uint32_t *slot, int32_t *cls,
+                uint32_t *owner, uint8_t *host_free, uint32_t *host_owner, uint32_t *cur) {
+  Oracle *o = static_cast<Oracle *>(h);
+  const Group &g = o->groups[gi];
+  for (uint32_t a = 0; a < o->max_logical; ++a) {
+    if (tier) tier[a] = g.where[a].tier;
+    if (slot) slot[a] = g.where[a].tier == kUnallocated ? 0 : g.where[a].slot;
+  }
+  if (cls) std::copy(g.cls.begin(), g.cls.end(), cls);
+  if (owner) std::copy(g.owner.begin(), g.owner.end(), owner);
+  if (host_free) {
+    std::memset(host_free, 0, o->H);
+    for (uint32_t hs : g.host_free) host_free[hs] = 1;
+  }
+  if (host_owner) std::copy(g.host_owner.begin(), g.host_owner.end(), host_owner);
+  if (cur) *cur = g.cur;
+}
+
+const uint8_t *orc_gpu_pool(void *h, uint32_t gi) {
+  return static_cast<Oracle *>(h)->groups[gi].gpu_pool.data();
+}
+const uint8_t *orc_host_pool(void *h, uint32_t gi) {
+  return static_cast<Oracle *>(h)->groups[gi].host_pool.data();
+}
+
+// ---------------------------------------------------------------------------
+// Exact LRU companion (hit rate only).  The pages' baseline policy keeps one
+// timestamp per slot and chooses victims by scanning for the oldest (§3
+// "PB-LRU", first paragraph; §4 compares hit rates).  Here: a timestamp per
+// GPU slot = the last round it was accessed (hit or filled); victims are free
+// slots (lowest first), then the smallest timestamp, ties to the lowest slot.
+// It keeps its own placement, so only hit/miss counts are comparable.
+
+namespace {
+struct LruGroup {
+  std::vector<int64_t> where;  // [max_logical]: GPU slot, -1 on host, -2 unallocated
+  std::vector<uint64_t> stamp; // [S]
+  std::vector<uint32_t> owner; // [S]
+  std::set<uint32_t> free_slots;
+  std::set<std::pair<uint64_t, uint32_t>> by_age;  // (stamp, slot) of occupied slots
+  uint64_t round = 0;
+};
+struct Lru {
+  uint32_t S = 0, max_logical = 0, next_logical = 0;
+  std::vector<LruGroup> groups;
+};
+}  // namespace
+
+void *orc_lru_create(uint32_t n_groups, uint32_t S, uint32_t max_logical) {
+  Lru *l = new Lru;
+  l->S = S;
+  l->max_logical = max_logical;
+  l->groups.resize(n_groups);
+  for (LruGroup &g : l->groups) {
+    g.where.assign(max_logical, -2);
+    g.stamp.assign(S, 0);
+    g.owner.assign(S, kNone);
+    for (uint32_t s = 0; s < S; ++s) g.free_slots.insert(s);
+  }
+  return l;
+}
+
+void orc_lru_destroy(void *h) { delete static_cast<Lru *>(h); }
+
+int orc_lru_alloc(void *h, uint32_t n, uint32_t *base_out) {
+  Lru *l = static_cast<Lru *>(h);
+  if ((uint64_t)l->next_logical + n > l->max_logical) return kCapacity;
+  const uint32_t base = l->next_logical;
+  for (LruGroup &g : l->groups)
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t a = base + i;
+      if (!g.free_slots.empty()) {
+        uint32_t s = *g.free_slots.begin();
+        g.free_slots.erase(s);
+        g.stamp[s] = g.round;
+        g.owner[s] = a;
+        g.by_age.insert({g.round, s});
+        g.where[a] = s;
+      } else {
+        g.where[a] = -1;
+      }
+    }
+  l->next_logical = base + n;
+  *base_out = base;
+  return kOk;
+}
+
+int orc_lru_free(void *h, uint32_t base, uint32_t n) {
+  Lru *l = static_cast<Lru *>(h);
+  for (LruGroup &g : l->groups)
+    for (uint32_t i = 0; i < n; ++i) {
+      const int64_t w = g.where[base + i];
+      if (w >= 0) {
+        g.by_age.erase({g.stamp[w], (uint32_t)w});
+        g.free_slots.insert((uint32_t)w);
+        g.owner[w] = kNone;
+      }
+      g.where[base + i] = -2;
+    }
+  return kOk;
+}
+
+// Returns kOk and adds (uniq, hits) to acc[0], acc[1].
+int orc_lru_step(void *h, uint32_t gi, const uint32_t *sel, size_t n_entries, uint64_t *acc) {
+  Lru *l = static_cast<Lru *>(h);
+  LruGroup &g = l->groups[gi];
+  g.round++;
+  std::unordered_map<uint32_t, char> seen;
+  std::vector<uint32_t> uniq;
+  for (size_t e = 0; e < n_entries; ++e) {
+    const uint32_t a = sel[e];
+    if (a == kPad) continue;
+    if (a >= l->max_logical || g.where[a] == -2) return kUnmapped;
+    if (seen.emplace(a, 1).second) uniq.push_back(a);
+  }
+  uint64_t hits = 0;
+  std::vector<uint32_t> misses;
+  for (uint32_t a : uniq) {
+    const int64_t w = g.where[a];
+    if (w >= 0) {
+      ++hits;
+      g.by_age.erase({g.stamp[w], (uint32_t)w});
+      g.stamp[w] = g.round;
+      g.by_age.insert({g.round, (uint32_t)w});
+    } else {
+      misses.push_back(a);
+    }
+  }
+  for (uint32_t a : misses) {
+    uint32_t s;
+    if (!g.free_slots.empty()) {
+      s = *g.free_slots.begin();
+      g.free_slots.erase(s);
+    } else {
+      if (g.by_age.empty() || g.by_age.begin()->first == g.round) return kCapacity;
+      s = g.by_age.begin()->second;
+      g.by_age.erase(g.by_age.begin());
+      g.where[g.owner[s]] = -1;
+    }
+    g.stamp[s] = g.round;
+    g.owner[s] = a;
+    g.by_age.insert({g.round, s});
+    g.where[a] = s;
+  }
+  acc[0] += uniq.size();
+  acc[1] += hits;
+  return kOk;
+}
+
+}  // extern "C"
