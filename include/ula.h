@@ -1,0 +1,224 @@
+/*
+ * ula.h -- C ABI of the per-decode-step KV residency path for index-based
+ * sparse attention, single-GPU DP mode (one HBM slot pool plus one pinned
+ * host slot pool per layer group form one logical address space).
+ *
+ * Source of the operations: "UlaCache: Unified Logical Addressing for Sparse
+ * LLM Serving" (paper summary page):
+ *   §2 "Unified logical addresses" -- the engine allocates and selects KV by
+ *      logical address only; a mapping table names the GPU slot or CPU slot
+ *      holding each entry; in DP mode a GPU owns its GPU pool and CPU pool and
+ *      an entry lives in one of them, never both; a layer group sharing one
+ *      sparse selection does address lookup and dedup once and prefetches
+ *      later layers on a separate CUDA stream.
+ *   §3 "PB-LRU" -- bucketed replacement for the shared GPU pool: one bucket
+ *      per scheduling round, a ring of buckets plus a cold bucket per layer
+ *      group, rotation/fold by relabelling, victims from free slots, then
+ *      cold, then ring oldest to newest, never the current bucket; bitmaps
+ *      with summary levels; data moves first, then the map, then a signal.
+ *
+ * Conventions for every call:
+ *   - Pointers are plain pointers.  "device" = CUDA device memory of the
+ *     context's device; "host" = host memory; "device-accessible" = device
+ *     memory or pinned (page-locked) host memory.
+ *   - Streams and events are cudaStream_t / cudaEvent_t passed as void*.
+ *   - Every call returns ULA_OK or an error code.  Errors the host can see
+ *     (bad arguments, capacity known on the host) return at once and change
+ *     nothing.  Errors only the device can see (an unmapped selected address,
+ *     a step needing more GPU slots than are evictable) are latched on the
+ *     device, the step's remaining kernels do nothing, and the code is
+ *     returned by the next ula_sync; from then on the context is poisoned and
+ *     every call except ula_destroy returns ULA_ERR_POISONED.
+ *   - A context is used from one host thread at a time.
+ */
+#ifndef ULA_H
+#define ULA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ULA_MAX_GROUPS 64
+#define ULA_MAX_BUCKETS 64
+#define ULA_ADDR_PAD 0xFFFFFFFFu /* a selection entry that selects nothing */
+
+enum {
+  ULA_OK = 0,
+  ULA_ERR_INVALID_ARG = 1, /* bad argument; nothing changed */
+  ULA_ERR_CAPACITY = 2,    /* pools, logical space or output buffer too small */
+  ULA_ERR_UNMAPPED = 3,    /* a selected address is out of range or not allocated */
+  ULA_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  ULA_ERR_TIMEOUT = 5,     /* a bounded device wait expired */
+  ULA_ERR_POISONED = 6,    /* an earlier device-side error poisoned the context */
+  ULA_ERR_INTERNAL = 7     /* a device-side consistency check failed */
+};
+
+typedef struct ula_ctx ula_ctx;
+
+typedef struct ula_config {
+  uint32_t row_bytes;        /* bytes of one KV row of one layer; multiple of 16 (656 for an
+                                FP8 MLA row: 512 e4m3 + 4 fp32 scales + 64 bf16 rope) */
+  uint32_t n_groups;         /* G: layer groups, each sharing one selection (1..ULA_MAX_GROUPS) */
+  uint32_t layers_per_group[ULA_MAX_GROUPS]; /* L_g >= 1 for g < n_groups */
+  uint32_t gpu_slots;        /* S: GPU slots per group (1 .. 2^31-1) */
+  uint32_t host_slots;       /* H: host slots per group (0 .. 2^31-1) */
+  uint32_t ring_buckets;     /* B: ring buckets per group, including the current one (1..64) */
+  uint32_t max_logical;      /* logical addresses live in [0, max_logical) (1 .. 2^31-1) */
+  uint32_t max_entries;      /* largest n_req*q*k of one ula_step_group call */
+  uint32_t flags;            /* reserved, must be 0 */
+} ula_config;
+
+/* Counters accumulated since ula_create, summed over groups. */
+typedef struct ula_stats {
+  uint64_t steps;          /* ula_step_group calls completed */
+  uint64_t entries;        /* selection entries (pads included) */
+  uint64_t uniq;           /* distinct addresses after dedup */
+  uint64_t hits;           /* distinct addresses found on the GPU */
+  uint64_t misses;         /* distinct addresses filled from the host pool */
+  uint64_t victims_free;   /* victims taken from free slots */
+  uint64_t victims_cold;   /* victims taken from the cold bucket */
+  uint64_t victims_ring;   /* victims taken from ring buckets */
+  uint64_t writebacks;     /* victims that held data and were written back */
+  uint64_t rows_gathered;  /* (address, layer) rows written to gather outputs */
+  uint64_t bytes_h2d;      /* fill bytes moved host -> GPU */
+  uint64_t bytes_d2h;      /* write-back bytes moved GPU -> host */
+} ula_stats;
+
+/*
+ * ula_create -- set up one residency context over caller-owned pools (§2, DP mode).
+ *   cfg        : host; copied.
+ *   gpu_pools  : host array [G] of device pointers; pool g is [S][L_g][row_bytes] bytes,
+ *                16-byte aligned, owned by the caller, borrowed until ula_destroy.
+ *   host_pools : host array [G] of pinned host pointers (cudaHostAlloc / pinned tensors);
+ *                pool g is [H][L_g][row_bytes]; may be NULL when H == 0.  Borrowed.
+ *   stream     : the context's home stream (alloc/free run there); NULL = legacy stream.
+ *   out        : receives the context.
+ * The library allocates its metadata (map, slot stamps, bitmaps, scratch) with
+ * cudaMalloc here and frees it in ula_destroy; it creates one side stream.
+ * All slots start free; the current ring bucket starts at 0.
+ */
+int ula_create(const ula_config *cfg, void *const *gpu_pools, void *const *host_pools,
+               void *stream, ula_ctx **out);
+
+/*
+ * ula_alloc -- allocate n new logical addresses [*logical_base, *logical_base + n) (§2).
+ * Bases are handed out monotonically and never reused.  For each group, each new
+ * address takes the lowest free GPU slot (and joins the current ring bucket, as
+ * an access in the latest round) or, when none is free, the lowest free host slot,
+ * in address order.  Alloc never evicts.
+ *   rows : device-accessible; for each group in order, [n][L_g][row_bytes] bytes
+ *          (groups concatenated); copied into the chosen slots.  Must stay valid
+ *          until the work completes on the home stream (e.g. ula_sync).
+ * Errors (host-detected, nothing changed): INVALID_ARG (rows not device-accessible),
+ * CAPACITY (n exceeds free slots of both tiers, or the logical space).
+ * Asynchronous on the home stream.
+ */
+int ula_alloc(ula_ctx *ctx, uint32_t n, const void *rows, uint32_t *logical_base);
+
+/*
+ * ula_free -- release logical addresses [logical_base, logical_base + n) in every
+ * group: their GPU slots become free (leaving their bucket), their host slots free.
+ * Errors (host-detected, nothing changed): INVALID_ARG if any address is not live.
+ * Asynchronous on the home stream.
+ */
+int ula_free(ula_ctx *ctx, uint32_t logical_base, uint32_t n);
+
+/*
+ * ula_step_group -- one scheduling round of group g for one decode step (§2, §3).
+ * In stream order, all on the device:
+ *   (1) dedup the selection (first occurrences in flattened (request, query, i) order),
+ *   (2) translate through the map (GPU slot = hit, host slot = miss),
+ *   (3) rotate the ring (the current bucket advances; the reused bucket's slots fold
+ *       into cold -- labels only) and move every hit into the current bucket,
+ *   (4) pick one victim per miss through the summary bitmaps: free slots, then cold,
+ *       then ring buckets oldest to newest, never the current bucket, lowest slot
+ *       first; victim i serves miss i,
+ *   (5) write each victim that holds data back to the host pool (the j-th such victim
+ *       to the j-th lowest free host slot), fill each miss from its host slot, then
+ *       update the map (moves complete before the map changes) and signal,
+ *   (6) gather out[j][u] = layer j of unique address u, for every layer of the group:
+ *       layer 0 on `stream`, layers 1.. on the context's side stream (prefetch).
+ *   d_sel       : device [n_req][q][k] uint32 logical addresses; ULA_ADDR_PAD = none.
+ *   d_out       : device [L_g][out_cap_rows][row_bytes]; rows [0, U) are written.
+ *   d_entry_row : device [n_req*q*k] int32: row u of each entry, -1 for pads.
+ *   d_req_off   : device [n_req+1] int32: unique rows first seen in request r are
+ *                 [req_off[r], req_off[r+1]); req_off[n_req] = U.
+ *   layer_ready : host array [L_g] of cudaEvent_t recorded when layer j of d_out is
+ *                 ready (layer 0 on `stream`, others on the side stream), or NULL.
+ *   stream      : the caller's stream; the step is ordered after every earlier call on
+ *                 this context.  Returns without waiting for the device.
+ * Device-detected errors (latched, returned by ula_sync, nothing changed by the step):
+ * UNMAPPED (an address >= max_logical or not allocated), CAPACITY (misses > S - hits,
+ * write-backs > free host slots, or U > out_cap_rows).
+ * Host-detected: INVALID_ARG (group out of range, n_req*q*k > max_entries, NULL buffers).
+ */
+int ula_step_group(ula_ctx *ctx, uint32_t group, const uint32_t *d_sel, uint32_t n_req,
+                   uint32_t q, uint32_t k, void *d_out, uint32_t out_cap_rows,
+                   int32_t *d_entry_row, int32_t *d_req_off, void *const *layer_ready,
+                   void *stream);
+
+/*
+ * ula_sync -- wait for all work of the context (both streams), then return the first
+ * latched device error (or ULA_OK).  stats: host, optional; receives the counters.
+ */
+int ula_sync(ula_ctx *ctx, ula_stats *stats);
+
+/* ula_destroy -- wait for the context's work and free everything it allocated. */
+void ula_destroy(ula_ctx *ctx);
+
+/* Text for an error code (static storage). */
+const char *ula_error_string(int code);
+
+/* ------------------------------------------------------------ diagnostics
+ * For tests and tools: sizes of the internal arrays, a blocking copy of one group's
+ * state, and host-side fault injection.  Bitmap words are 32-bit, bit b of word w is
+ * slot 32*w + b; level 1 holds one bit per level-0 word (set iff that word is
+ * nonzero), level 2 one bit per level-1 word.  Classes: 0..B-1 ring buckets, B cold,
+ * B+1 free.  Map entries: ULA_MAP_UNALLOCATED, a GPU slot, or ULA_MAP_HOST | host slot.
+ */
+#define ULA_MAP_UNALLOCATED 0xFFFFFFFFu
+#define ULA_MAP_HOST 0x80000000u
+#define ULA_STAMP_FREE 0xFFFFFFFFu
+
+typedef struct ula_debug_layout {
+  uint32_t n0, n1, n2;   /* words per level of a GPU-slot bitmap */
+  uint32_t h0, h1, h2;   /* words per level of the host-free bitmap */
+  uint32_t n_classes;    /* B + 2 */
+  uint32_t decision_cap; /* capacity of the victim / write-back lists */
+} ula_debug_layout;
+
+typedef struct ula_debug_state {
+  /* host buffers to fill; NULL skips */
+  uint32_t *map;            /* [max_logical] */
+  uint32_t *owner;          /* [S] logical address in each GPU slot, 0xFFFFFFFF if none */
+  uint32_t *stamp;          /* [S] round of last access, ULA_STAMP_FREE if free */
+  uint32_t *class_bits;     /* [n_classes][n0] */
+  uint32_t *class_sum1;     /* [n_classes][n1] */
+  uint32_t *class_sum2;     /* [n_classes][n2] */
+  uint32_t *host_free_bits; /* [h0] */
+  uint32_t *host_free_sum1; /* [h1] */
+  uint32_t *host_free_sum2; /* [h2] */
+  uint32_t *uniq;           /* [max_entries]: last step's unique addresses */
+  uint32_t *victims;        /* [decision_cap]: last step's victims (first M) */
+  uint32_t *wb_host;        /* [decision_cap]: last step's write-back host slots (first K) */
+  /* filled always */
+  uint32_t round;           /* rounds completed by this group */
+  uint32_t cur;             /* current ring bucket = round % B */
+  uint32_t free_gpu, free_host;
+  uint32_t U, M, hits, victims_free, writebacks; /* last step */
+} ula_debug_state;
+
+int ula_debug_layout_get(const ula_ctx *ctx, ula_debug_layout *out);
+int ula_debug_export(ula_ctx *ctx, uint32_t group, ula_debug_state *st);
+/* The next ula_step_group latches `code` on the device before it changes anything
+ * (host-side fault injection for tests of the error path; no GPU fault). */
+int ula_debug_inject(ula_ctx *ctx, int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULA_H */

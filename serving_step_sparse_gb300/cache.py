@@ -1,0 +1,112 @@
+"""UlaCache: one residency context plus the PyTorch plumbing around it.
+
+PyTorch provides only device memory, pinned host memory and streams here; every
+step of the path runs in the CUDA library through the C ABI (``ula``).
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+import torch
+
+from . import ula
+
+
+def _u32(t: torch.Tensor) -> int:
+    assert t.dtype in (torch.int32, torch.uint8) and t.is_contiguous()
+    return t.data_ptr()
+
+
+class UlaCache:
+    """GPU slot pool + pinned host slot pool per layer group, one logical address space."""
+
+    def __init__(self, *, row_bytes: int, layers_per_group, gpu_slots: int, host_slots: int,
+                 ring_buckets: int, max_logical: int, max_entries: int, device="cuda",
+                 stream: torch.cuda.Stream | None = None):
+        self.device = torch.device(device)
+        self.W = int(row_bytes)
+        self.layers = [int(x) for x in layers_per_group]
+        self.G = len(self.layers)
+        self.S, self.H, self.B = int(gpu_slots), int(host_slots), int(ring_buckets)
+        self.max_logical, self.max_entries = int(max_logical), int(max_entries)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        self.gpu_pools = [torch.empty(self.S * L * self.W, dtype=torch.uint8, device=self.device)
+                          for L in self.layers]
+        self.host_pools = ([torch.empty(self.H * L * self.W, dtype=torch.uint8, pin_memory=True)
+                            for L in self.layers] if self.H else None)
+        cfg = ula.make_config(self.W, self.layers, self.S, self.H, self.B, self.max_logical,
+                              self.max_entries)
+        with torch.cuda.device(self.device):
+            self.ctx = ula.ula_create(cfg, [p.data_ptr() for p in self.gpu_pools],
+                                      [p.data_ptr() for p in self.host_pools] if self.H else None,
+                                      self.stream.cuda_stream)
+        self.layout = ula.ula_debug_layout_get(self.ctx)
+
+    # -- the five calls -------------------------------------------------------
+    def alloc(self, n: int, rows: torch.Tensor) -> int:
+        """rows: pinned host or device uint8 tensor holding, per group, [n][L_g][W]."""
+        assert rows.dtype == torch.uint8 and rows.is_contiguous()
+        assert rows.numel() == n * sum(self.layers) * self.W
+        assert rows.is_cuda or rows.is_pinned()
+        return ula.ula_alloc(self.ctx, n, rows.data_ptr())
+
+    def free(self, base: int, n: int) -> None:
+        ula.ula_free(self.ctx, base, n)
+
+    def step_group(self, g: int, sel: torch.Tensor, out: torch.Tensor, entry_row: torch.Tensor,
+                   req_off: torch.Tensor, layer_ready=None, stream: torch.cuda.Stream | None = None):
+        """sel: device int32 view of uint32 [R][Q][k]; out: device uint8 [L][cap][W]."""
+        R, Q, K = sel.shape
+        cap = out.shape[1]
+        s = stream if stream is not None else self.stream
+        ev = [e.cuda_event for e in layer_ready] if layer_ready else None
+        ula.ula_step_group(self.ctx, g, _u32(sel), R, Q, K, out.data_ptr(), cap,
+                           _u32(entry_row), _u32(req_off), ev, s.cuda_stream)
+
+    def sync(self) -> dict:
+        return ula.ula_sync(self.ctx)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            ula.ula_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- buffers --------------------------------------------------------------
+    def out_buffer(self, g: int, cap: int) -> torch.Tensor:
+        return torch.empty((self.layers[g], cap, self.W), dtype=torch.uint8, device=self.device)
+
+    # -- diagnostics ----------------------------------------------------------
+    def export(self, g: int) -> dict:
+        lay = self.layout
+        arrs = {
+            "map": np.empty(self.max_logical, np.uint32),
+            "owner": np.empty(self.S, np.uint32),
+            "stamp": np.empty(self.S, np.uint32),
+            "class_bits": np.empty((lay.n_classes, lay.n0), np.uint32),
+            "class_sum1": np.empty((lay.n_classes, lay.n1), np.uint32),
+            "class_sum2": np.empty((lay.n_classes, lay.n2), np.uint32),
+            "host_free_bits": np.empty(max(lay.h0, 1), np.uint32),
+            "host_free_sum1": np.empty(max(lay.h1, 1), np.uint32),
+            "host_free_sum2": np.empty(max(lay.h2, 1), np.uint32),
+            "uniq": np.empty(self.max_entries, np.uint32),
+            "victims": np.empty(lay.decision_cap, np.uint32),
+            "wb_host": np.empty(lay.decision_cap, np.uint32),
+        }
+        st = ula.ula_debug_state()
+        for k, a in arrs.items():
+            setattr(st, k, a.ctypes.data)
+        ula.ula_debug_export(self.ctx, g, st)
+        for k in ("round", "cur", "free_gpu", "free_host", "U", "M", "hits", "victims_free",
+                  "writebacks"):
+            arrs[k] = int(getattr(st, k))
+        return arrs
+
+    def inject(self, code: int):
+        ula.ula_debug_inject(self.ctx, code)

@@ -1,0 +1,577 @@
+// Host orchestrator behind the C ABI (include/ula.h): context set-up, argument
+// checks, stream/event ordering, and the per-call kernel sequences.
+//
+// Ordering rules (UlaCache summary page, §2 "two more details" and §3 last
+// paragraph): a step's kernels run in stream order -- dedup/translate ->
+// capacity check -> rotate/mark -> victim selection -> move+commit -> signal
+// -> gather; layer 0 is gathered on the caller's stream, later layers on the
+// context's side stream after the commit event (prefetch).  Every call is
+// ordered after the previous call on the context (event wait when the stream
+// changes), and anything touching group g first waits for group g's pending
+// side-stream gathers, so a slot is never refilled while an earlier gather of
+// it is still reading.
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "ula_device.cuh"
+
+using namespace ula;
+
+namespace {
+
+constexpr uint32_t kAllocChunk = 65536;
+
+#define ULA_CUDA(call)                      \
+  do {                                      \
+    cudaError_t e_ = (call);                \
+    if (e_ != cudaSuccess) return c->fail(e_); \
+  } while (0)
+
+}  // namespace
+
+struct ula_ctx {
+  ula_config cfg{};
+  int device = 0;
+  int sm_count = 0;
+  cudaStream_t home = nullptr, side = nullptr, last_stream = nullptr;
+  bool have_last = false;
+  cudaEvent_t last_evt = nullptr, commit_evt = nullptr;
+  cudaEvent_t side_evt[ULA_MAX_GROUPS] = {};
+  bool side_pending[ULA_MAX_GROUPS] = {};
+  Geometry geo{};
+  std::vector<GroupDev> groups_h;
+  GroupDev *groups_d = nullptr;
+  GroupCounters *cnt_d = nullptr;
+  unsigned long long *tbl = nullptr;
+  uint32_t *addr_row = nullptr;
+  uint2 *blk = nullptr;
+  uint32_t *miss_list = nullptr;
+  int *status = nullptr;
+  uint32_t decision_cap = 0;
+  uint32_t epoch = 0;
+  uint32_t round[ULA_MAX_GROUPS] = {};
+  uint32_t next_logical = 0;
+  uint64_t live_count = 0;
+  std::vector<uint8_t> live;
+  int poisoned = 0;
+  int inject = 0;
+  std::vector<void *> allocations;
+
+  int fail(cudaError_t e) {
+    (void)e;
+    poisoned = ULA_ERR_CUDA;
+    return ULA_ERR_CUDA;
+  }
+
+  template <typename T>
+  cudaError_t alloc(T **p, size_t count) {
+    void *q = nullptr;
+    cudaError_t e = cudaMalloc(&q, count ? count * sizeof(T) : sizeof(T));
+    if (e == cudaSuccess) allocations.push_back(q);
+    *p = static_cast<T *>(q);
+    return e;
+  }
+
+  // make `s` wait for the previous call on this context
+  cudaError_t order_after_previous(cudaStream_t s) {
+    if (have_last && last_stream != s) return cudaStreamWaitEvent(s, last_evt, 0);
+    return cudaSuccess;
+  }
+
+  cudaError_t wait_side(cudaStream_t s, uint32_t g) {
+    if (!side_pending[g]) return cudaSuccess;
+    side_pending[g] = false;
+    return cudaStreamWaitEvent(s, side_evt[g], 0);
+  }
+
+  cudaError_t mark_done(cudaStream_t s) {
+    last_stream = s;
+    have_last = true;
+    return cudaEventRecord(last_evt, s);
+  }
+
+  cudaError_t ensure_device() {
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    return cur == device ? cudaSuccess : cudaSetDevice(device);
+  }
+};
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// device-accessible address of a device or pinned host pointer, or nullptr
+void *device_address(const void *p, int device, bool allow_device, bool allow_host) {
+  if (!p) return nullptr;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice && allow_device && at.device == device)
+    return const_cast<void *>(p);
+  if (at.type == cudaMemoryTypeManaged && allow_device) return const_cast<void *>(p);
+  if (at.type == cudaMemoryTypeHost && allow_host) {
+    if (at.devicePointer) return at.devicePointer;  // the queried address, as the device sees it
+    void *dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, const_cast<void *>(p), 0) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return dp;
+  }
+  return nullptr;
+}
+
+int validate_config(const ula_config *c) {
+  if (!c) return ULA_ERR_INVALID_ARG;
+  if (c->row_bytes == 0 || c->row_bytes % 16) return ULA_ERR_INVALID_ARG;
+  if (c->n_groups == 0 || c->n_groups > ULA_MAX_GROUPS) return ULA_ERR_INVALID_ARG;
+  for (uint32_t g = 0; g < c->n_groups; ++g)
+    if (c->layers_per_group[g] == 0 || (uint64_t)c->layers_per_group[g] * c->row_bytes > (1u << 30))
+      return ULA_ERR_INVALID_ARG;
+  if (c->gpu_slots == 0 || c->gpu_slots > kSlotMask || c->host_slots > kSlotMask)
+    return ULA_ERR_INVALID_ARG;
+  if (c->ring_buckets == 0 || c->ring_buckets > ULA_MAX_BUCKETS) return ULA_ERR_INVALID_ARG;
+  if (c->max_logical == 0 || c->max_logical > kSlotMask) return ULA_ERR_INVALID_ARG;
+  if (c->max_entries == 0 || c->flags != 0) return ULA_ERR_INVALID_ARG;
+  return ULA_OK;
+}
+
+void destroy_resources(ula_ctx *c) {
+  for (void *p : c->allocations) cudaFree(p);
+  c->allocations.clear();
+  if (c->side) cudaStreamDestroy(c->side);
+  if (c->last_evt) cudaEventDestroy(c->last_evt);
+  if (c->commit_evt) cudaEventDestroy(c->commit_evt);
+  for (uint32_t g = 0; g < ULA_MAX_GROUPS; ++g)
+    if (c->side_evt[g]) cudaEventDestroy(c->side_evt[g]);
+}
+
+int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
+  const ula_config &cfg = c->cfg;
+  ULA_CUDA(cudaGetDevice(&c->device));
+  ULA_CUDA(cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device));
+  const uint32_t G = cfg.n_groups, S = cfg.gpu_slots, H = cfg.host_slots, B = cfg.ring_buckets;
+
+  Geometry &geo = c->geo;
+  geo.S = S;
+  geo.H = H;
+  geo.B = B;
+  geo.W = cfg.row_bytes;
+  geo.max_logical = cfg.max_logical;
+  geo.gd = dims_for(S);
+  geo.hd = dims_for(H);
+  geo.nseg = geo.gd.n1;
+  geo.nsup = geo.gd.n2;
+  geo.hseg = geo.hd.n1;
+  geo.hsup = geo.hd.n2;
+  c->decision_cap = cfg.max_entries > kAllocChunk ? cfg.max_entries : kAllocChunk;
+
+  // pools: caller-owned, borrowed
+  std::vector<uint8_t *> gp(G), hp(G);
+  for (uint32_t g = 0; g < G; ++g) {
+    void *d = device_address(gpu_pools ? gpu_pools[g] : nullptr, c->device, true, false);
+    if (!d || !aligned16(d)) return ULA_ERR_INVALID_ARG;
+    gp[g] = static_cast<uint8_t *>(d);
+    if (H) {
+      void *h = device_address(host_pools ? host_pools[g] : nullptr, c->device, false, true);
+      if (!h || !aligned16(h)) return ULA_ERR_INVALID_ARG;
+      hp[g] = static_cast<uint8_t *>(h);
+    }
+  }
+
+  ULA_CUDA(cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking));
+  ULA_CUDA(cudaEventCreateWithFlags(&c->last_evt, cudaEventDisableTiming));
+  ULA_CUDA(cudaEventCreateWithFlags(&c->commit_evt, cudaEventDisableTiming));
+  for (uint32_t g = 0; g < G; ++g)
+    ULA_CUDA(cudaEventCreateWithFlags(&c->side_evt[g], cudaEventDisableTiming));
+
+  // shared scratch (main-stream kernels only)
+  const uint32_t max_blk = (cfg.max_entries + 255) / 256 + 1;
+  ULA_CUDA(c->alloc(&c->tbl, cfg.max_logical));
+  ULA_CUDA(c->alloc(&c->addr_row, cfg.max_logical));
+  ULA_CUDA(c->alloc(&c->blk, max_blk));
+  ULA_CUDA(c->alloc(&c->miss_list, cfg.max_entries));
+  ULA_CUDA(c->alloc(&c->status, 1));
+  ULA_CUDA(c->alloc(&c->cnt_d, G));
+  ULA_CUDA(c->alloc(&c->groups_d, G));
+  cudaStream_t s = c->home;
+  ULA_CUDA(cudaMemsetAsync(c->tbl, 0, sizeof(unsigned long long) * cfg.max_logical, s));
+  ULA_CUDA(cudaMemsetAsync(c->status, 0, sizeof(int), s));
+
+  const uint32_t ncls = B + 2;
+  const size_t seg_len = (size_t)(B + 1) * geo.nseg + geo.hseg;
+  c->groups_h.resize(G);
+  std::vector<GroupCounters> cnt_h(G);
+  for (uint32_t g = 0; g < G; ++g) {
+    GroupDev &d = c->groups_h[g];
+    std::memset(&d, 0, sizeof(d));
+    d.layers = cfg.layers_per_group[g];
+    d.gpu_pool = gp[g];
+    d.host_pool = H ? hp[g] : nullptr;
+    ULA_CUDA(c->alloc(&d.map, cfg.max_logical));
+    ULA_CUDA(c->alloc(&d.owner, S));
+    ULA_CUDA(c->alloc(&d.stamp, S));
+    ULA_CUDA(c->alloc(&d.cls0, (size_t)ncls * geo.gd.n0));
+    ULA_CUDA(c->alloc(&d.cls1, (size_t)ncls * geo.gd.n1));
+    ULA_CUDA(c->alloc(&d.cls2, (size_t)ncls * geo.gd.n2));
+    ULA_CUDA(c->alloc(&d.hf0, geo.hd.n0));
+    ULA_CUDA(c->alloc(&d.hf1, geo.hd.n1));
+    ULA_CUDA(c->alloc(&d.hf2, geo.hd.n2));
+    ULA_CUDA(c->alloc(&d.uniq, cfg.max_entries));
+    ULA_CUDA(c->alloc(&d.victims, c->decision_cap));
+    ULA_CUDA(c->alloc(&d.wb_host, c->decision_cap));
+    ULA_CUDA(c->alloc(&d.seg_count, seg_len));
+    ULA_CUDA(c->alloc(&d.seg_base, seg_len));
+    d.cnt = c->cnt_d + g;
+    ULA_CUDA(cudaMemsetAsync(d.map, 0xff, sizeof(uint32_t) * cfg.max_logical, s));
+    ULA_CUDA(cudaMemsetAsync(d.owner, 0xff, sizeof(uint32_t) * S, s));
+    ULA_CUDA(cudaMemsetAsync(d.stamp, 0xff, sizeof(uint32_t) * S, s));
+    ULA_CUDA(cudaMemsetAsync(d.cls0, 0, sizeof(uint32_t) * ncls * geo.gd.n0, s));
+    ULA_CUDA(cudaMemsetAsync(d.cls1, 0, sizeof(uint32_t) * ncls * geo.gd.n1, s));
+    ULA_CUDA(cudaMemsetAsync(d.cls2, 0, sizeof(uint32_t) * ncls * geo.gd.n2, s));
+    ULA_CUDA(launch_bitmap_fill(class_bitmap(d, geo, B + 1), S, s));  // all slots free
+    ULA_CUDA(launch_bitmap_fill(host_free_bitmap(d), H, s));
+    std::memset(&cnt_h[g], 0, sizeof(GroupCounters));
+    cnt_h[g].free_gpu = S;
+    cnt_h[g].free_host = H;
+  }
+  ULA_CUDA(cudaMemcpyAsync(c->cnt_d, cnt_h.data(), sizeof(GroupCounters) * G,
+                           cudaMemcpyHostToDevice, s));
+  ULA_CUDA(cudaMemcpyAsync(c->groups_d, c->groups_h.data(), sizeof(GroupDev) * G,
+                           cudaMemcpyHostToDevice, s));
+  ULA_CUDA(cudaStreamSynchronize(s));
+  c->live.assign(cfg.max_logical, 0);
+  return ULA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *ula_error_string(int code) {
+  switch (code) {
+    case ULA_OK: return "ok";
+    case ULA_ERR_INVALID_ARG: return "invalid argument";
+    case ULA_ERR_CAPACITY: return "capacity exceeded";
+    case ULA_ERR_UNMAPPED: return "selected address out of range or not allocated";
+    case ULA_ERR_CUDA: return "CUDA runtime error";
+    case ULA_ERR_TIMEOUT: return "bounded device wait expired";
+    case ULA_ERR_POISONED: return "context poisoned by an earlier device-side error";
+    case ULA_ERR_INTERNAL: return "device-side consistency check failed";
+    default: return "unknown error";
+  }
+}
+
+int ula_create(const ula_config *cfg, void *const *gpu_pools, void *const *host_pools,
+               void *stream, ula_ctx **out) {
+  if (!out) return ULA_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  ula_ctx *c = new ula_ctx;
+  c->cfg = *cfg;
+  c->home = static_cast<cudaStream_t>(stream);
+  rc = create_impl(c, gpu_pools, host_pools);
+  if (rc) {
+    cudaDeviceSynchronize();
+    destroy_resources(c);
+    delete c;
+    return rc;
+  }
+  *out = c;
+  return ULA_OK;
+}
+
+int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) {
+  if (!c || !logical_base) return ULA_ERR_INVALID_ARG;
+  if (c->poisoned) return ULA_ERR_POISONED;
+  const ula_config &cfg = c->cfg;
+  if ((uint64_t)c->next_logical + n > cfg.max_logical) return ULA_ERR_CAPACITY;
+  if (c->live_count + n > (uint64_t)cfg.gpu_slots + cfg.host_slots) return ULA_ERR_CAPACITY;
+  *logical_base = c->next_logical;
+  if (n == 0) return ULA_OK;
+  ULA_CUDA(c->ensure_device());
+  const uint8_t *rows_d =
+      static_cast<const uint8_t *>(device_address(rows, c->device, true, true));
+  if (!rows_d || !aligned16(rows_d)) return ULA_ERR_INVALID_ARG;
+  cudaStream_t s = c->home;
+  ULA_CUDA(c->order_after_previous(s));
+  for (uint32_t g = 0; g < cfg.n_groups; ++g) ULA_CUDA(c->wait_side(s, g));
+
+  const uint32_t base = c->next_logical;
+  for (uint32_t off = 0; off < n; off += kAllocChunk) {
+    const uint32_t m = n - off < kAllocChunk ? n - off : kAllocChunk;
+    SelectParams sp{};
+    sp.geo = c->geo;
+    sp.groups = c->groups_d;
+    sp.group0 = 0;
+    sp.n_cls = 1;
+    sp.order[0] = c->geo.B + 1;  // free slots only: alloc never evicts
+    sp.quota = m;
+    sp.is_step = 0;
+    sp.status = c->status;
+    ULA_CUDA(launch_select(sp, cfg.n_groups, s));
+    AllocParams ap{};
+    ap.geo = c->geo;
+    ap.groups = c->groups_d;
+    ap.rows = rows_d;
+    unsigned long long acc = 0;
+    for (uint32_t g = 0; g < cfg.n_groups; ++g) {
+      const unsigned long long sb = (unsigned long long)cfg.layers_per_group[g] * cfg.row_bytes;
+      ap.group_off[g] = acc + (unsigned long long)off * sb;
+      ap.round[g] = c->round[g];
+      acc += (unsigned long long)n * sb;
+    }
+    ap.base = base + off;
+    ap.n = m;
+    ap.status = c->status;
+    ULA_CUDA(launch_alloc_place(ap, cfg.n_groups, c->sm_count, s));
+  }
+  ULA_CUDA(c->mark_done(s));
+  for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 1;
+  c->live_count += n;
+  c->next_logical = base + n;
+  return ULA_OK;
+}
+
+int ula_free(ula_ctx *c, uint32_t base, uint32_t n) {
+  if (!c) return ULA_ERR_INVALID_ARG;
+  if (c->poisoned) return ULA_ERR_POISONED;
+  if ((uint64_t)base + n > c->next_logical) return ULA_ERR_INVALID_ARG;
+  for (uint32_t i = 0; i < n; ++i)
+    if (!c->live[base + i]) return ULA_ERR_INVALID_ARG;
+  if (n == 0) return ULA_OK;
+  ULA_CUDA(c->ensure_device());
+  cudaStream_t s = c->home;
+  ULA_CUDA(c->order_after_previous(s));
+  for (uint32_t g = 0; g < c->cfg.n_groups; ++g) ULA_CUDA(c->wait_side(s, g));
+  FreeParams fp{};
+  fp.geo = c->geo;
+  fp.groups = c->groups_d;
+  for (uint32_t g = 0; g < c->cfg.n_groups; ++g) fp.round[g] = c->round[g];
+  fp.base = base;
+  fp.n = n;
+  fp.status = c->status;
+  ULA_CUDA(launch_free(fp, c->cfg.n_groups, s));
+  ULA_CUDA(c->mark_done(s));
+  for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 0;
+  c->live_count -= n;
+  return ULA_OK;
+}
+
+int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n_req, uint32_t q,
+                   uint32_t k, void *d_out, uint32_t out_cap_rows, int32_t *d_entry_row,
+                   int32_t *d_req_off, void *const *layer_ready, void *stream) {
+  if (!c) return ULA_ERR_INVALID_ARG;
+  if (c->poisoned) return ULA_ERR_POISONED;
+  const ula_config &cfg = c->cfg;
+  if (group >= cfg.n_groups) return ULA_ERR_INVALID_ARG;
+  const uint64_t E = (uint64_t)n_req * q * k;
+  if (E > cfg.max_entries) return ULA_ERR_INVALID_ARG;
+  if (!d_req_off || (E && (!d_sel || !d_entry_row)) || (out_cap_rows && !d_out))
+    return ULA_ERR_INVALID_ARG;
+  if (d_out && !aligned16(d_out)) return ULA_ERR_INVALID_ARG;
+  ULA_CUDA(c->ensure_device());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ULA_CUDA(c->order_after_previous(s));
+  ULA_CUDA(c->wait_side(s, group));
+
+  if (++c->epoch == 0) {  // dedup stamps wrap: clear them
+    ULA_CUDA(cudaMemsetAsync(c->tbl, 0, sizeof(unsigned long long) * cfg.max_logical, s));
+    c->epoch = 1;
+  }
+  const uint32_t r = ++c->round[group];
+  const uint32_t B = c->geo.B, cur = r % B;
+  const GroupDev &gd = c->groups_h[group];
+
+  StepParams p{};
+  p.geo = c->geo;
+  p.grp = gd;
+  p.sel = d_sel;
+  p.E = (uint32_t)E;
+  p.QK = q * k;
+  p.n_req = n_req;
+  p.epoch = c->epoch;
+  p.round = r;
+  p.cur = cur;
+  p.out_cap = out_cap_rows;
+  p.inject = c->inject;
+  p.entry_row = d_entry_row;
+  p.req_off = d_req_off;
+  p.tbl = c->tbl;
+  p.addr_row = c->addr_row;
+  p.blk = c->blk;
+  p.miss_list = c->miss_list;
+  p.status = c->status;
+  c->inject = 0;
+  // (1)(2) dedup + translate + capacity check
+  ULA_CUDA(launch_dedup(p, s));
+  // (3) rotate, hits into the current bucket; CSR and entry rows
+  ULA_CUDA(launch_rotate_mark(p, s));
+  // (4) victims: free, cold, ring oldest (cur+1) .. newest (cur-1); never cur
+  SelectParams sp{};
+  sp.geo = c->geo;
+  sp.groups = c->groups_d;
+  sp.group0 = group;
+  sp.n_cls = B + 1;
+  sp.order[0] = B + 1;
+  sp.order[1] = B;
+  for (uint32_t d = 1; d < B; ++d) sp.order[1 + d] = (cur + d) % B;
+  sp.quota = 0xffffffffu;
+  sp.is_step = 1;
+  sp.status = c->status;
+  ULA_CUDA(launch_select(sp, 1, s));
+  // (5) write-back, fill, then map commit
+  MoveParams mp{};
+  mp.geo = c->geo;
+  mp.grp = gd;
+  mp.miss_list = c->miss_list;
+  mp.round = r;
+  mp.cur = cur;
+  mp.status = c->status;
+  ULA_CUDA(launch_move(mp, c->sm_count, s));
+  // signal: the commit event; every gather is ordered after it
+  ULA_CUDA(cudaEventRecord(c->commit_evt, s));
+  // (6) gather: layer 0 now, later layers on the side stream
+  GatherParams gp{};
+  gp.geo = c->geo;
+  gp.grp = gd;
+  gp.out = static_cast<uint8_t *>(d_out);
+  gp.out_cap = out_cap_rows;
+  gp.status = c->status;
+  gp.layer = 0;
+  if (out_cap_rows) ULA_CUDA(launch_gather(gp, c->sm_count, s));
+  if (layer_ready && layer_ready[0])
+    ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[0]), s));
+  if (gd.layers > 1) {
+    ULA_CUDA(cudaStreamWaitEvent(c->side, c->commit_evt, 0));
+    for (uint32_t j = 1; j < gd.layers; ++j) {
+      gp.layer = j;
+      if (out_cap_rows) ULA_CUDA(launch_gather(gp, c->sm_count, c->side));
+      if (layer_ready && layer_ready[j])
+        ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), c->side));
+    }
+    ULA_CUDA(cudaEventRecord(c->side_evt[group], c->side));
+    c->side_pending[group] = true;
+  }
+  ULA_CUDA(c->mark_done(s));
+  return ULA_OK;
+}
+
+static int sync_impl(ula_ctx *c) {
+  ULA_CUDA(c->ensure_device());
+  for (uint32_t g = 0; g < c->cfg.n_groups; ++g)
+    if (c->side_pending[g]) {
+      ULA_CUDA(cudaEventSynchronize(c->side_evt[g]));
+      c->side_pending[g] = false;
+    }
+  if (c->have_last) ULA_CUDA(cudaEventSynchronize(c->last_evt));
+  ULA_CUDA(cudaStreamSynchronize(c->home));
+  return ULA_OK;
+}
+
+int ula_sync(ula_ctx *c, ula_stats *stats) {
+  if (!c) return ULA_ERR_INVALID_ARG;
+  if (c->poisoned) return ULA_ERR_POISONED;
+  int rc = sync_impl(c);
+  if (rc) return rc;
+  int st = 0;
+  ULA_CUDA(cudaMemcpy(&st, c->status, sizeof(int), cudaMemcpyDeviceToHost));
+  if (stats) {
+    std::vector<GroupCounters> h(c->cfg.n_groups);
+    ULA_CUDA(cudaMemcpy(h.data(), c->cnt_d, sizeof(GroupCounters) * h.size(),
+                        cudaMemcpyDeviceToHost));
+    unsigned long long acc[12] = {};
+    for (const GroupCounters &x : h)
+      for (int i = 0; i < 12; ++i) acc[i] += x.stat[i];
+    stats->steps = acc[kStSteps];
+    stats->entries = acc[kStEntries];
+    stats->uniq = acc[kStUniq];
+    stats->hits = acc[kStHits];
+    stats->misses = acc[kStMisses];
+    stats->victims_free = acc[kStVictFree];
+    stats->victims_cold = acc[kStVictCold];
+    stats->victims_ring = acc[kStVictRing];
+    stats->writebacks = acc[kStWriteback];
+    stats->rows_gathered = acc[kStRows];
+    stats->bytes_h2d = acc[kStBytesH2D];
+    stats->bytes_d2h = acc[kStBytesD2H];
+  }
+  if (st) {
+    c->poisoned = st;
+    return st;
+  }
+  return ULA_OK;
+}
+
+void ula_destroy(ula_ctx *c) {
+  if (!c) return;
+  c->ensure_device();
+  sync_impl(c);
+  destroy_resources(c);
+  delete c;
+}
+
+int ula_debug_layout_get(const ula_ctx *c, ula_debug_layout *out) {
+  if (!c || !out) return ULA_ERR_INVALID_ARG;
+  out->n0 = c->geo.gd.n0;
+  out->n1 = c->geo.gd.n1;
+  out->n2 = c->geo.gd.n2;
+  out->h0 = c->geo.hd.n0;
+  out->h1 = c->geo.hd.n1;
+  out->h2 = c->geo.hd.n2;
+  out->n_classes = c->geo.B + 2;
+  out->decision_cap = c->decision_cap;
+  return ULA_OK;
+}
+
+int ula_debug_export(ula_ctx *c, uint32_t group, ula_debug_state *st) {
+  if (!c || !st || group >= c->cfg.n_groups) return ULA_ERR_INVALID_ARG;
+  int rc = sync_impl(c);
+  if (rc) return rc;
+  const GroupDev &d = c->groups_h[group];
+  const Geometry &geo = c->geo;
+  const uint32_t ncls = geo.B + 2;
+  auto copy = [&](void *dst, const void *src, size_t bytes) -> cudaError_t {
+    if (!dst || !bytes) return cudaSuccess;
+    return cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost);
+  };
+  ULA_CUDA(copy(st->map, d.map, sizeof(uint32_t) * c->cfg.max_logical));
+  ULA_CUDA(copy(st->owner, d.owner, sizeof(uint32_t) * geo.S));
+  ULA_CUDA(copy(st->stamp, d.stamp, sizeof(uint32_t) * geo.S));
+  ULA_CUDA(copy(st->class_bits, d.cls0, sizeof(uint32_t) * ncls * geo.gd.n0));
+  ULA_CUDA(copy(st->class_sum1, d.cls1, sizeof(uint32_t) * ncls * geo.gd.n1));
+  ULA_CUDA(copy(st->class_sum2, d.cls2, sizeof(uint32_t) * ncls * geo.gd.n2));
+  ULA_CUDA(copy(st->host_free_bits, d.hf0, sizeof(uint32_t) * geo.hd.n0));
+  ULA_CUDA(copy(st->host_free_sum1, d.hf1, sizeof(uint32_t) * geo.hd.n1));
+  ULA_CUDA(copy(st->host_free_sum2, d.hf2, sizeof(uint32_t) * geo.hd.n2));
+  ULA_CUDA(copy(st->uniq, d.uniq, sizeof(uint32_t) * c->cfg.max_entries));
+  ULA_CUDA(copy(st->victims, d.victims, sizeof(uint32_t) * c->decision_cap));
+  ULA_CUDA(copy(st->wb_host, d.wb_host, sizeof(uint32_t) * c->decision_cap));
+  GroupCounters cnt;
+  ULA_CUDA(cudaMemcpy(&cnt, d.cnt, sizeof(cnt), cudaMemcpyDeviceToHost));
+  st->round = c->round[group];
+  st->cur = c->round[group] % geo.B;
+  st->free_gpu = cnt.free_gpu;
+  st->free_host = cnt.free_host;
+  st->U = cnt.U;
+  st->M = cnt.M;
+  st->hits = cnt.hits;
+  st->victims_free = cnt.F;
+  st->writebacks = cnt.K;
+  return ULA_OK;
+}
+
+int ula_debug_inject(ula_ctx *c, int code) {
+  if (!c) return ULA_ERR_INVALID_ARG;
+  if (c->poisoned) return ULA_ERR_POISONED;
+  c->inject = code;
+  return ULA_OK;
+}
+
+}  // extern "C"

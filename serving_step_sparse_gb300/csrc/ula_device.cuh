@@ -1,0 +1,180 @@
+// Device-side layout of the KV residency context and the kernel parameter
+// blocks.  Shared by the kernels (ula_kernels.cu) and the host orchestrator
+// (ula_api.cu); not part of the public ABI (include/ula.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "ula.h"
+
+namespace ula {
+
+constexpr uint32_t kPad = ULA_ADDR_PAD;
+constexpr uint32_t kUnalloc = ULA_MAP_UNALLOCATED;
+constexpr uint32_t kHostBit = ULA_MAP_HOST;
+constexpr uint32_t kSlotMask = 0x7FFFFFFFu;
+constexpr uint32_t kNone = 0xFFFFFFFFu;  // no owner / free stamp
+
+// A bitmap with two summary levels.  Level 0: one bit per slot.  Level 1: bit
+// i is set iff level-0 word i is nonzero.  Level 2: bit i is set iff level-1
+// word i is nonzero.  A level-1 word covers a "segment" of 1,024 slots, a
+// level-2 word a "superblock" of 32,768 slots.
+struct Dims {
+  uint32_t n0, n1, n2;
+};
+
+struct Bitmap {
+  uint32_t *w0, *w1, *w2;
+};
+
+__host__ __device__ inline Dims dims_for(uint32_t nbits) {
+  Dims d;
+  d.n0 = (nbits + 31) / 32;
+  d.n1 = (d.n0 + 31) / 32;
+  d.n2 = (d.n1 + 31) / 32;
+  return d;
+}
+
+// Per-group counters living in device memory.
+struct GroupCounters {
+  uint32_t free_gpu;   // free GPU slots
+  uint32_t free_host;  // free host slots
+  uint32_t U, M, hits; // last step: unique addresses, misses, hits
+  uint32_t F;          // last step: victims taken from free slots (alloc: GPU placements)
+  uint32_t K;          // last step: write-backs (alloc: host placements)
+  uint32_t pad;
+  unsigned long long stat[12];  // ula_stats order
+};
+
+enum StatIdx {
+  kStSteps = 0, kStEntries, kStUniq, kStHits, kStMisses, kStVictFree, kStVictCold,
+  kStVictRing, kStWriteback, kStRows, kStBytesH2D, kStBytesD2H
+};
+
+// Everything one group owns on the device.
+struct GroupDev {
+  uint32_t *map;       // [max_logical]: kUnalloc | GPU slot | kHostBit|host slot
+  uint32_t *owner;     // [S]: logical address in the slot or kNone
+  uint32_t *stamp;     // [S]: round of last access (defines the bucket), kNone if free
+  uint32_t *cls0;      // [B+2][n0]: ring buckets 0..B-1, cold (B), free (B+1)
+  uint32_t *cls1;      // [B+2][n1]
+  uint32_t *cls2;      // [B+2][n2]
+  uint32_t *hf0, *hf1, *hf2;  // host-free bitmap levels
+  uint8_t *gpu_pool;   // [S][L][W]
+  uint8_t *host_pool;  // [H][L][W], pinned host memory (device pointer)
+  uint32_t *uniq;      // [max_entries]: this group's unique addresses of its last step
+  uint32_t *victims;   // [decision_cap]: victim i serves miss i (alloc: GPU slots)
+  uint32_t *wb_host;   // [decision_cap]: host slot of write-back j (alloc: host slots)
+  uint32_t *seg_count; // [(B+1)*nseg + hseg]: set bits per segment, in selection order
+  uint32_t *seg_base;  // same shape: exclusive prefix of seg_count
+  GroupCounters *cnt;
+  uint32_t layers;     // L_g
+  uint32_t pad;
+};
+
+struct Geometry {
+  uint32_t S, H, B, W;   // GPU slots, host slots, ring buckets, row bytes
+  uint32_t max_logical;
+  Dims gd, hd;           // bitmap dims for GPU-slot and host-slot bitmaps
+  uint32_t nseg, hseg;   // segments (= level-1 words) per bitmap
+  uint32_t nsup, hsup;   // superblocks (= level-2 words) per bitmap
+};
+
+__host__ __device__ inline Bitmap class_bitmap(const GroupDev &g, const Geometry &geo, uint32_t c) {
+  Bitmap b;
+  b.w0 = g.cls0 + (size_t)c * geo.gd.n0;
+  b.w1 = g.cls1 + (size_t)c * geo.gd.n1;
+  b.w2 = g.cls2 + (size_t)c * geo.gd.n2;
+  return b;
+}
+
+__host__ __device__ inline Bitmap host_free_bitmap(const GroupDev &g) {
+  Bitmap b;
+  b.w0 = g.hf0;
+  b.w1 = g.hf1;
+  b.w2 = g.hf2;
+  return b;
+}
+
+// Parameters of the per-step kernels of one group.
+struct StepParams {
+  Geometry geo;
+  GroupDev grp;
+  const uint32_t *sel;      // [E]
+  uint32_t E, QK, n_req;
+  uint32_t epoch;           // dedup epoch of this call
+  uint32_t round;           // this round's number r (the current bucket is r % B)
+  uint32_t cur;             // r % B
+  uint32_t out_cap;
+  int inject;               // host-side fault injection code (0 = none)
+  int32_t *entry_row;       // [E]
+  int32_t *req_off;         // [n_req + 1]
+  unsigned long long *tbl;  // [max_logical]: (epoch << 32) | ~first entry index
+  uint32_t *addr_row;       // [max_logical]: unique row of an address this step
+  uint2 *blk;               // [blocks]: (first occurrences, misses) per block, then offsets
+  uint32_t *miss_list;      // [max_entries]: misses in first-occurrence order
+  int *status;              // latched device error (0 = none)
+};
+
+// Parameters of the victim / free-slot selection (step and alloc).
+struct SelectParams {
+  Geometry geo;
+  const GroupDev *groups;   // device array [G]
+  uint32_t group0;          // first group (blockIdx.z / blockIdx.x adds to it)
+  uint32_t n_cls;           // GPU classes in selection order
+  uint32_t order[ULA_MAX_BUCKETS + 2];  // class index at each order position
+  uint32_t quota;           // victims wanted (alloc), or 0xFFFFFFFF = take the group's M
+  uint32_t is_step;
+  int *status;
+};
+
+struct MoveParams {
+  Geometry geo;
+  GroupDev grp;
+  const uint32_t *miss_list;
+  uint32_t round, cur;
+  int *status;
+};
+
+struct GatherParams {
+  Geometry geo;
+  GroupDev grp;
+  uint8_t *out;             // [L][out_cap][W]
+  uint32_t out_cap;
+  uint32_t layer;
+  int *status;
+};
+
+struct AllocParams {
+  Geometry geo;
+  const GroupDev *groups;
+  const uint8_t *rows;      // device-accessible
+  unsigned long long group_off[ULA_MAX_GROUPS];  // byte offset of group g's rows
+  uint32_t round[ULA_MAX_GROUPS];
+  uint32_t base, n;
+  int *status;
+};
+
+struct FreeParams {
+  Geometry geo;
+  const GroupDev *groups;
+  uint32_t round[ULA_MAX_GROUPS];
+  uint32_t base, n;
+  int *status;
+};
+
+// Launchers (ula_kernels.cu).  Each returns the launch's cudaError_t.
+cudaError_t launch_bitmap_fill(Bitmap b, uint32_t nbits, cudaStream_t s);
+cudaError_t launch_dedup(const StepParams &p, cudaStream_t s);        // stamp, count, scan
+cudaError_t launch_rotate_mark(const StepParams &p, cudaStream_t s);  // rotate, emit+mark, rows
+cudaError_t launch_select(const SelectParams &p, uint32_t n_groups, cudaStream_t s);
+cudaError_t launch_move(const MoveParams &p, int sm_count, cudaStream_t s);
+cudaError_t launch_gather(const GatherParams &p, int sm_count, cudaStream_t s);
+cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int sm_count,
+                               cudaStream_t s);
+cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);
+
+}  // namespace ula

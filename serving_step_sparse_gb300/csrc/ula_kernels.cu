@@ -1,0 +1,762 @@
+// Kernels of the KV residency path (sm_103a).  Integer, bitmap and copy work:
+// no tensor cores, nothing here is a contraction.
+//
+// Source of the method: "UlaCache: Unified Logical Addressing for Sparse LLM
+// Serving" (paper summary page), §2 "Unified logical addresses" (map, DP-mode
+// exclusive tiers, per-group dedup, side-stream prefetch) and §3 "PB-LRU"
+// (bucket ring + cold bucket, rotation by relabelling, victim order, bitmaps
+// with summary levels, parallel hit detection/dedup, move -> map -> signal).
+//
+// Concurrency discipline for the bitmaps: inside one kernel a given bitmap is
+// either only set or only cleared.  That keeps the summary levels exact with
+// plain atomics: a set that finds its word empty sets the level-1 bit (and so
+// on up), a clear that empties its word clears the level-1 bit (and so on up);
+// with only one direction per kernel no set can interleave with a clear.
+#include "ula_device.cuh"
+
+namespace ula {
+
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kEntryThreads = 256;
+
+__device__ __forceinline__ void latch(int *status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    uint32_t t = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= (uint32_t)d) v += t;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+#pragma unroll
+  for (int d = 16; d; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
+  return v;
+}
+
+// Block-uniform early exit on a latched error (safe before __syncthreads).
+__device__ __forceinline__ bool block_skips(const int *status) {
+  __shared__ int s_status;
+  if (threadIdx.x == 0) s_status = *(volatile const int *)status;
+  __syncthreads();
+  return s_status != 0;
+}
+
+__device__ __forceinline__ void bm_set(Bitmap b, uint32_t bit) {
+  const uint32_t i0 = bit >> 5;
+  const uint32_t old0 = atomicOr(&b.w0[i0], 1u << (bit & 31));
+  if (old0 == 0) {
+    const uint32_t i1 = i0 >> 5;
+    const uint32_t old1 = atomicOr(&b.w1[i1], 1u << (i0 & 31));
+    if (old1 == 0) atomicOr(&b.w2[i1 >> 5], 1u << (i1 & 31));
+  }
+}
+
+__device__ __forceinline__ void bm_clear(Bitmap b, uint32_t bit) {
+  const uint32_t i0 = bit >> 5;
+  const uint32_t m0 = 1u << (bit & 31);
+  const uint32_t old0 = atomicAnd(&b.w0[i0], ~m0);
+  if (old0 == m0) {  // this clear emptied the word
+    const uint32_t i1 = i0 >> 5;
+    const uint32_t m1 = 1u << (i0 & 31);
+    const uint32_t old1 = atomicAnd(&b.w1[i1], ~m1);
+    if (old1 == m1) atomicAnd(&b.w2[i1 >> 5], ~(1u << (i1 & 31)));
+  }
+}
+
+// The class of a GPU slot from its stamp: free, cold (last access at least B
+// rounds ago: its bucket has been folded), or the ring bucket of its round.
+__device__ __forceinline__ uint32_t class_of(uint32_t stamp, uint32_t round, uint32_t B) {
+  if (stamp == kNone) return B + 1;
+  if (round - stamp >= B) return B;
+  return stamp % B;
+}
+
+// ------------------------------------------------------------------ init
+
+__global__ void k_bitmap_fill(Bitmap b, uint32_t nbits) {
+  const Dims d = dims_for(nbits);
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < d.n0; w += stride) {
+    const uint32_t lo = w * 32, n = nbits - lo;
+    b.w0[w] = n >= 32 ? 0xffffffffu : ((1u << n) - 1u);
+    if (w < d.n1) {
+      const uint32_t m = d.n0 - w * 32;
+      b.w1[w] = m >= 32 ? 0xffffffffu : ((1u << m) - 1u);
+    }
+    if (w < d.n2) {
+      const uint32_t m = d.n1 - w * 32;
+      b.w2[w] = m >= 32 ? 0xffffffffu : ((1u << m) - 1u);
+    }
+  }
+}
+
+// ----------------------------------------------------------------- dedup
+
+__device__ __forceinline__ unsigned long long first_key(uint32_t epoch, uint32_t e) {
+  return ((unsigned long long)epoch << 32) | (0xffffffffu - e);
+}
+
+// (1) every entry proposes itself as its address's first occurrence; the
+// largest key of this epoch = the smallest entry index wins.
+__global__ void k_dedup_stamp(StepParams p) {
+  if (*(volatile int *)p.status) return;
+  const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p.inject && e == 0) latch(p.status, p.inject);
+  if (e >= p.E) return;
+  const uint32_t a = p.sel[e];
+  if (a == kPad) return;
+  if (a >= p.geo.max_logical || p.grp.map[a] == kUnalloc) {
+    latch(p.status, ULA_ERR_UNMAPPED);
+    return;
+  }
+  atomicMax(&p.tbl[a], first_key(p.epoch, e));
+}
+
+struct Flags {
+  uint32_t a, first, miss;
+};
+
+__device__ __forceinline__ Flags entry_flags(const StepParams &p, uint32_t e) {
+  Flags f{kPad, 0, 0};
+  if (e < p.E) {
+    f.a = p.sel[e];
+    if (f.a != kPad && p.tbl[f.a] == first_key(p.epoch, e)) {
+      f.first = 1;
+      f.miss = (p.grp.map[f.a] & kHostBit) ? 1u : 0u;  // (2) translate
+    }
+  }
+  return f;
+}
+
+// per-block counts of first occurrences and of misses
+__global__ void __launch_bounds__(kEntryThreads) k_dedup_count(StepParams p) {
+  if (block_skips(p.status)) return;
+  const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+  const Flags f = entry_flags(p, e);
+  __shared__ uint32_t sf[kEntryThreads / 32], sm[kEntryThreads / 32];
+  const uint32_t wf = warp_sum(f.first), wm = warp_sum(f.miss);
+  if (lane_id() == 0) {
+    sf[threadIdx.x >> 5] = wf;
+    sm[threadIdx.x >> 5] = wm;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t tf = 0, tm = 0;
+    for (int w = 0; w < kEntryThreads / 32; ++w) {
+      tf += sf[w];
+      tm += sm[w];
+    }
+    p.blk[blockIdx.x] = make_uint2(tf, tm);
+  }
+}
+
+// exclusive scan of the block counts; totals; the capacity check (no state
+// changes before it passes)
+__global__ void __launch_bounds__(kScanThreads) k_dedup_scan(StepParams p, uint32_t nblk) {
+  if (block_skips(p.status)) return;
+  __shared__ uint32_t wf[32], wm[32];
+  const uint32_t per = (nblk + kScanThreads - 1) / kScanThreads;
+  const uint32_t b0 = min(threadIdx.x * per, nblk), b1 = min(b0 + per, nblk);
+  uint32_t sf = 0, sm = 0;
+  for (uint32_t b = b0; b < b1; ++b) {
+    const uint2 v = p.blk[b];
+    sf += v.x;
+    sm += v.y;
+  }
+  const uint32_t incf = warp_incl_scan(sf), incm = warp_incl_scan(sm);
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  if (lane == 31) {
+    wf[warp] = incf;
+    wm[warp] = incm;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t x = warp_incl_scan(wf[lane]), y = warp_incl_scan(wm[lane]);
+    __syncwarp();
+    wf[lane] = x;
+    wm[lane] = y;
+  }
+  __syncthreads();
+  uint32_t of = (warp ? wf[warp - 1] : 0) + incf - sf;
+  uint32_t om = (warp ? wm[warp - 1] : 0) + incm - sm;
+  for (uint32_t b = b0; b < b1; ++b) {
+    const uint2 v = p.blk[b];
+    p.blk[b] = make_uint2(of, om);
+    of += v.x;
+    om += v.y;
+  }
+  if (p.E == 0)
+    for (uint32_t r = threadIdx.x; r <= p.n_req; r += blockDim.x) p.req_off[r] = 0;
+  if (threadIdx.x == 0) {
+    const uint32_t U = wf[31], M = wm[31], hits = U - M;
+    GroupCounters *c = p.grp.cnt;
+    const bool ok = U <= p.out_cap && (uint64_t)M + hits <= p.geo.S &&
+                    (uint64_t)M <= (uint64_t)c->free_gpu + c->free_host;
+    if (!ok) {
+      latch(p.status, ULA_ERR_CAPACITY);
+    } else {
+      c->U = U;
+      c->M = M;
+      c->hits = hits;
+      c->F = 0;
+      c->K = 0;
+      p.req_off[p.n_req] = (int32_t)U;
+      const unsigned long long sb = (unsigned long long)p.grp.layers * p.geo.W;
+      c->stat[kStSteps] += 1;
+      c->stat[kStEntries] += p.E;
+      c->stat[kStUniq] += U;
+      c->stat[kStHits] += hits;
+      c->stat[kStMisses] += M;
+      c->stat[kStRows] += (unsigned long long)U * p.grp.layers;
+      c->stat[kStBytesH2D] += (unsigned long long)M * sb;
+    }
+  }
+}
+
+// (3a) rotation: the current bucket advances to `cur`; what is left in it
+// folds into the cold bucket.  Only labels change.  Sets on cold, clears on
+// the reused bucket.
+__global__ void k_rotate(StepParams p) {
+  if (*(volatile int *)p.status) return;
+  const Geometry &geo = p.geo;
+  const Bitmap bucket = class_bitmap(p.grp, geo, p.cur);
+  const Bitmap cold = class_bitmap(p.grp, geo, geo.B);
+  const uint32_t stride = gridDim.x * blockDim.x;
+  const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  for (uint32_t w = t; w < geo.gd.n0; w += stride) {
+    const uint32_t b = bucket.w0[w];
+    if (b) {
+      const uint32_t c = cold.w0[w];
+      cold.w0[w] = c | b;
+      bucket.w0[w] = 0;
+      if (c == 0) {
+        const uint32_t old1 = atomicOr(&cold.w1[w >> 5], 1u << (w & 31));
+        if (old1 == 0) atomicOr(&cold.w2[w >> 10], 1u << ((w >> 5) & 31));
+      }
+    }
+  }
+  for (uint32_t w = t; w < geo.gd.n1; w += stride) bucket.w1[w] = 0;
+  for (uint32_t w = t; w < geo.gd.n2; w += stride) bucket.w2[w] = 0;
+}
+
+// (1)+(2)+(3b): compact first occurrences into uniq (first-occurrence order),
+// misses into miss_list (same order), CSR offsets per request, and move every
+// hit into the current bucket.  Clears on non-current classes, sets on cur.
+__global__ void __launch_bounds__(kEntryThreads) k_dedup_emit(StepParams p) {
+  if (block_skips(p.status)) return;
+  const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+  const Flags f = entry_flags(p, e);
+  __shared__ uint32_t sf[kEntryThreads / 32], sm[kEntryThreads / 32];
+  const uint32_t incf = warp_incl_scan(f.first), incm = warp_incl_scan(f.miss);
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  if (lane == 31) {
+    sf[warp] = incf;
+    sm[warp] = incm;
+  }
+  __syncthreads();
+  uint32_t bf = p.blk[blockIdx.x].x, bmiss = p.blk[blockIdx.x].y;
+  for (uint32_t w = 0; w < warp; ++w) {
+    bf += sf[w];
+    bmiss += sm[w];
+  }
+  const uint32_t pos = bf + incf - f.first;   // exclusive: unique rows before e
+  const uint32_t mpos = bmiss + incm - f.miss; // exclusive: misses before e
+  if (e < p.E && (e % p.QK) == 0) p.req_off[e / p.QK] = (int32_t)pos;
+  if (!f.first) return;
+  p.grp.uniq[pos] = f.a;
+  p.addr_row[f.a] = pos;
+  if (f.miss) {
+    p.miss_list[mpos] = f.a;
+    return;
+  }
+  const uint32_t s = p.grp.map[f.a];
+  if (s >= p.geo.S) {
+    latch(p.status, ULA_ERR_INTERNAL);
+    return;
+  }
+  const uint32_t c = class_of(p.grp.stamp[s], p.round, p.geo.B);
+  if (c == p.geo.B + 1) {
+    latch(p.status, ULA_ERR_INTERNAL);
+    return;
+  }
+  if (c != p.cur) {
+    bm_clear(class_bitmap(p.grp, p.geo, c), s);
+    bm_set(class_bitmap(p.grp, p.geo, p.cur), s);
+  }
+  p.grp.stamp[s] = p.round;
+}
+
+__global__ void k_entry_rows(StepParams p) {
+  if (*(volatile int *)p.status) return;
+  const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= p.E) return;
+  const uint32_t a = p.sel[e];
+  p.entry_row[e] = a == kPad ? -1 : (int32_t)p.addr_row[a];
+}
+
+// ------------------------------------------------------------- selection
+//
+// (4) "the first q set bits" of a sequence of bitmaps taken in a fixed order
+// (step: free, cold, ring oldest -> newest; alloc: free), plus the first K
+// set bits of the host-free bitmap.  Three passes:
+//   count: per 1,024-slot segment, the number of set bits; a superblock whose
+//          level-2 word is zero, or a segment whose level-1 word is zero, is
+//          skipped without touching the level below;
+//   scan:  exclusive prefix over the segments in selection order;
+//   emit:  each non-empty segment below the quota writes its set bits'
+//          slots at their ranks (warp-wide popcount prefix).
+// Grid for count/emit: x = superblock, y = order position (last = host),
+// z = group.  One warp per segment.
+
+__device__ __forceinline__ uint32_t select_quota(const SelectParams &p, const GroupDev &g) {
+  return p.quota == 0xffffffffu ? g.cnt->M : p.quota;
+}
+
+__device__ __forceinline__ bool select_target(const SelectParams &p, const GroupDev &g,
+                                              uint32_t y, Bitmap &bm, uint32_t &nseg,
+                                              uint32_t &n0, uint32_t *&counts, uint32_t *&bases) {
+  const Geometry &geo = p.geo;
+  const uint32_t host_off = (geo.B + 1) * geo.nseg;
+  if (y == p.n_cls) {
+    bm = host_free_bitmap(g);
+    nseg = geo.hseg;
+    n0 = geo.hd.n0;
+    counts = g.seg_count + host_off;
+    bases = g.seg_base + host_off;
+  } else {
+    bm = class_bitmap(g, geo, p.order[y]);
+    nseg = geo.nseg;
+    n0 = geo.gd.n0;
+    counts = g.seg_count + (size_t)y * geo.nseg;
+    bases = g.seg_base + (size_t)y * geo.nseg;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(1024) k_select_count(SelectParams p) {
+  if (*(volatile int *)p.status) return;
+  const GroupDev g = p.groups[p.group0 + blockIdx.z];
+  if (select_quota(p, g) == 0) return;
+  Bitmap bm;
+  uint32_t nseg, n0, *counts, *bases;
+  select_target(p, g, blockIdx.y, bm, nseg, n0, counts, bases);
+  const uint32_t sup = blockIdx.x, warp = threadIdx.x >> 5, lane = lane_id();
+  const uint32_t seg = sup * 32 + warp;
+  if (seg >= nseg) return;
+  uint32_t n = 0;
+  const uint32_t s2 = bm.w2[sup];
+  if ((s2 >> warp) & 1u) {
+    const uint32_t s1 = bm.w1[seg];
+    if ((s1 >> lane) & 1u) n = __popc(bm.w0[seg * 32 + lane]);
+  }
+  n = warp_sum(n);
+  if (lane == 0) counts[seg] = n;
+}
+
+// chunked exclusive block scan of vals[0..n) into out[0..n); returns the total
+__device__ uint32_t block_exclusive_scan(const uint32_t *vals, uint32_t *out, uint32_t n) {
+  __shared__ uint32_t ws[32];
+  __shared__ uint32_t total;
+  const uint32_t per = (n + blockDim.x - 1) / blockDim.x;
+  const uint32_t i0 = min(threadIdx.x * per, n), i1 = min(i0 + per, n);
+  uint32_t s = 0;
+  for (uint32_t i = i0; i < i1; ++i) s += vals[i];
+  const uint32_t inc = warp_incl_scan(s);
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  const uint32_t nwarps = blockDim.x >> 5;
+  if (lane == 31) ws[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t x = lane < nwarps ? ws[lane] : 0u;
+    const uint32_t y = warp_incl_scan(x);
+    __syncwarp();
+    if (lane < nwarps) ws[lane] = y;
+    if (lane == 31) total = y;
+  }
+  __syncthreads();
+  uint32_t run = (warp ? ws[warp - 1] : 0) + inc - s;
+  for (uint32_t i = i0; i < i1; ++i) {
+    const uint32_t v = vals[i];
+    out[i] = run;
+    run += v;
+  }
+  const uint32_t t = total;
+  __syncthreads();
+  return t;
+}
+
+__global__ void __launch_bounds__(kScanThreads) k_select_scan(SelectParams p) {
+  if (block_skips(p.status)) return;
+  const GroupDev g = p.groups[p.group0 + blockIdx.x];
+  const Geometry &geo = p.geo;
+  const uint32_t quota = select_quota(p, g);
+  if (quota == 0) {
+    if (threadIdx.x == 0) {
+      g.cnt->F = 0;
+      g.cnt->K = 0;
+    }
+    return;
+  }
+  const uint32_t ngpu = p.n_cls * geo.nseg;
+  const uint32_t gpu_total = block_exclusive_scan(g.seg_count, g.seg_base, ngpu);
+  const uint32_t host_off = (geo.B + 1) * geo.nseg;
+  const uint32_t host_total =
+      block_exclusive_scan(g.seg_count + host_off, g.seg_base + host_off, geo.hseg);
+  __syncthreads();  // seg_base of other threads is read below
+  if (threadIdx.x != 0) return;
+  const uint32_t free_total = p.n_cls > 1 ? g.seg_base[geo.nseg] : gpu_total;
+  const uint32_t cold_end = p.n_cls > 2 ? g.seg_base[2 * geo.nseg] : gpu_total;
+  const uint32_t F = min(quota, free_total);
+  const uint32_t K = quota - F;
+  GroupCounters *c = g.cnt;
+  if (host_total < K || (p.is_step && gpu_total < quota) || free_total != c->free_gpu ||
+      host_total != c->free_host) {
+    latch(p.status, ULA_ERR_INTERNAL);
+    return;
+  }
+  c->F = F;
+  c->K = K;
+  if (p.is_step) {
+    const uint32_t from_cold = min(quota - F, cold_end - free_total);
+    c->free_gpu -= F;   // F free slots filled
+    c->free_host += F;  // K host slots taken, quota host slots released
+    c->stat[kStVictFree] += F;
+    c->stat[kStVictCold] += from_cold;
+    c->stat[kStVictRing] += quota - F - from_cold;
+    c->stat[kStWriteback] += K;
+    c->stat[kStBytesD2H] += (unsigned long long)K * g.layers * geo.W;
+  } else {
+    c->free_gpu -= F;
+    c->free_host -= K;
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_select_emit(SelectParams p) {
+  if (*(volatile int *)p.status) return;
+  const GroupDev g = p.groups[p.group0 + blockIdx.z];
+  const uint32_t quota = select_quota(p, g);
+  if (quota == 0) return;
+  const bool host = blockIdx.y == p.n_cls;
+  const uint32_t q = host ? g.cnt->K : quota;
+  Bitmap bm;
+  uint32_t nseg, n0, *counts, *bases;
+  select_target(p, g, blockIdx.y, bm, nseg, n0, counts, bases);
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  const uint32_t seg = blockIdx.x * 32 + warp;
+  if (seg >= nseg) return;
+  const uint32_t base = bases[seg];
+  if (counts[seg] == 0 || base >= q) return;
+  const uint32_t wi = seg * 32 + lane;
+  uint32_t word = wi < n0 ? bm.w0[wi] : 0u;
+  const uint32_t inc = warp_incl_scan(__popc(word));
+  uint32_t rank = base + inc - __popc(word);
+  uint32_t *dst = host ? g.wb_host : g.victims;
+  while (word && rank < q) {
+    const uint32_t b = __ffs(word) - 1;
+    word &= word - 1;
+    const uint32_t slot = wi * 32 + b;
+    dst[rank++] = slot;
+    if (host) bm_clear(bm, slot);  // claim the write-back target (clears only)
+  }
+}
+
+// -------------------------------------------------------- move and commit
+//
+// (5) per victim i (one warp): write the victim's rows back to its host slot
+// if it holds data, fill miss i's rows from its host slot, then update the map
+// (after this warp's copies), move the slot into the current bucket and
+// release the miss's host slot.  Each lane handles the same 16-byte chunks in
+// the write-back and in the fill, so its read of a chunk precedes its write
+// of the same chunk.  Host memory is reached directly over the host link.
+constexpr int kMoveUnroll = 6;
+
+__global__ void __launch_bounds__(256) k_move_commit(MoveParams p) {
+  if (*(volatile int *)p.status) return;
+  const GroupDev &g = p.grp;
+  const Geometry &geo = p.geo;
+  const uint32_t M = g.cnt->M, F = g.cnt->F;
+  const uint32_t lane = lane_id();
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const size_t sb = (size_t)g.layers * geo.W;
+  const uint32_t nvec = (uint32_t)(sb / 16);
+  for (uint32_t i = warp; i < M; i += nwarps) {
+    const uint32_t v = g.victims[i];
+    const uint32_t a = p.miss_list[i];
+    const uint32_t loc = a < geo.max_logical ? g.map[a] : kUnalloc;
+    const uint32_t hs = loc & kSlotMask;
+    const bool owned = i >= F;
+    const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
+    const uint32_t o = owned && v < geo.S ? g.owner[v] : kNone;
+    const bool bad = v >= geo.S || loc == kUnalloc || !(loc & kHostBit) || hs >= geo.H ||
+                     (owned && (hd >= geo.H || o >= geo.max_logical)) ||
+                     (!owned && v < geo.S && g.owner[v] != kNone);
+    if (bad) {
+      if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
+      continue;
+    }
+    uint4 *gp = reinterpret_cast<uint4 *>(g.gpu_pool + (size_t)v * sb);
+    const uint4 *src = reinterpret_cast<const uint4 *>(g.host_pool + (size_t)hs * sb);
+    uint4 *dst = reinterpret_cast<uint4 *>(g.host_pool + (size_t)hd * sb);
+    for (uint32_t c0 = 0; c0 < nvec; c0 += 32 * kMoveUnroll) {
+      uint4 fill[kMoveUnroll], back[kMoveUnroll];
+#pragma unroll
+      for (int u = 0; u < kMoveUnroll; ++u) {
+        const uint32_t c = c0 + u * 32 + lane;
+        if (c < nvec) fill[u] = src[c];
+      }
+      if (owned) {
+#pragma unroll
+        for (int u = 0; u < kMoveUnroll; ++u) {
+          const uint32_t c = c0 + u * 32 + lane;
+          if (c < nvec) back[u] = gp[c];
+        }
+#pragma unroll
+        for (int u = 0; u < kMoveUnroll; ++u) {
+          const uint32_t c = c0 + u * 32 + lane;
+          if (c < nvec) dst[c] = back[u];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMoveUnroll; ++u) {
+        const uint32_t c = c0 + u * 32 + lane;
+        if (c < nvec) gp[c] = fill[u];
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      if (owned) g.map[o] = kHostBit | hd;
+      g.map[a] = v;
+      g.owner[v] = a;
+      const uint32_t c = class_of(g.stamp[v], p.round, geo.B);
+      if (c != p.cur) {
+        bm_clear(class_bitmap(g, geo, c), v);
+        bm_set(class_bitmap(g, geo, p.cur), v);
+      }
+      g.stamp[v] = p.round;
+      bm_set(host_free_bitmap(g), hs);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ gather
+//
+// (6) out[layer][u] = layer `layer` of the slot the committed map gives for
+// uniq[u].  A warp takes a tile of 32 rows: lanes resolve the 32 slots, then
+// the warp streams the tile's 32 x (W/16) 16-byte chunks, consecutive lanes on
+// consecutive chunks (coalesced within each row, rows written contiguously).
+constexpr int kGatherUnroll = 8;
+
+__global__ void __launch_bounds__(256) k_gather(GatherParams p) {
+  if (*(volatile int *)p.status) return;
+  const GroupDev &g = p.grp;
+  const Geometry &geo = p.geo;
+  const uint32_t U = g.cnt->U;
+  const uint32_t lane = lane_id();
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const uint32_t CW = geo.W / 16;
+  const size_t sbv = (size_t)g.layers * CW;  // slot stride in uint4
+  const uint4 *pool = reinterpret_cast<const uint4 *>(g.gpu_pool) + (size_t)p.layer * CW;
+  uint4 *out = reinterpret_cast<uint4 *>(p.out) + (size_t)p.layer * p.out_cap * CW;
+  const uint32_t tiles = (U + 31) / 32;
+  for (uint32_t t = warp; t < tiles; t += nwarps) {
+    const uint32_t row0 = t * 32;
+    const uint32_t nrows = min(32u, U - row0);
+    uint32_t slot = 0;
+    bool bad = false;
+    if (lane < nrows) {
+      const uint32_t m = g.map[g.uniq[row0 + lane]];
+      bad = (m & kHostBit) || m >= geo.S;
+      slot = bad ? 0u : m;
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+      if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
+      continue;
+    }
+    const uint32_t total = nrows * CW;
+    uint32_t r = lane / CW, c = lane % CW;  // chunk (r, c) of f = lane
+    uint4 *orow = out + (size_t)row0 * CW;
+    for (uint32_t f0 = 0; f0 < total; f0 += 32 * kGatherUnroll) {
+      uint4 v[kGatherUnroll];
+      uint32_t rr[kGatherUnroll], cc[kGatherUnroll];
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        rr[u] = r;
+        cc[u] = c;
+        const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
+        if (f0 + u * 32 + lane < total) v[u] = __ldg(pool + (size_t)s * sbv + c);
+        c += 32;
+        while (c >= CW) {
+          c -= CW;
+          ++r;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u)
+        if (f0 + u * 32 + lane < total) orow[(size_t)rr[u] * CW + cc[u]] = v[u];
+    }
+  }
+}
+
+// ------------------------------------------------------------ alloc / free
+
+// Alloc: address i of the range goes to the i-th selected free GPU slot (the
+// lowest ones, joining the current bucket), the rest to the selected host slots.
+__global__ void __launch_bounds__(256) k_alloc_place(AllocParams p) {
+  if (*(volatile int *)p.status) return;
+  const uint32_t gi = blockIdx.y;
+  const GroupDev g = p.groups[gi];
+  const Geometry &geo = p.geo;
+  const uint32_t F = g.cnt->F;
+  const uint32_t lane = lane_id();
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const size_t sb = (size_t)g.layers * geo.W;
+  const uint32_t nvec = (uint32_t)(sb / 16);
+  const uint32_t round = p.round[gi], cur = round % geo.B;
+  for (uint32_t i = warp; i < p.n; i += nwarps) {
+    const uint32_t a = p.base + i;
+    const bool on_gpu = i < F;
+    const uint32_t slot = on_gpu ? g.victims[i] : g.wb_host[i - F];
+    if ((on_gpu && slot >= geo.S) || (!on_gpu && slot >= geo.H) || a >= geo.max_logical) {
+      if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
+      continue;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.rows + p.group_off[gi] + (size_t)i * sb);
+    uint4 *dst = reinterpret_cast<uint4 *>((on_gpu ? g.gpu_pool : g.host_pool) + (size_t)slot * sb);
+    for (uint32_t c = lane; c < nvec; c += 32) dst[c] = src[c];
+    __syncwarp();
+    if (lane == 0) {
+      if (on_gpu) {
+        g.map[a] = slot;
+        g.owner[slot] = a;
+        g.stamp[slot] = round;
+        bm_clear(class_bitmap(g, geo, geo.B + 1), slot);
+        bm_set(class_bitmap(g, geo, cur), slot);
+      } else {
+        g.map[a] = kHostBit | slot;
+      }
+    }
+  }
+}
+
+// Free: every address's slot is released (GPU: leaves its class, joins free).
+__global__ void k_free(FreeParams p) {
+  if (*(volatile int *)p.status) return;
+  const uint32_t gi = blockIdx.y;
+  const GroupDev g = p.groups[gi];
+  const Geometry &geo = p.geo;
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= p.n) return;
+  const uint32_t a = p.base + i;
+  const uint32_t m = g.map[a];
+  if (m == kUnalloc) {
+    latch(p.status, ULA_ERR_INTERNAL);
+    return;
+  }
+  if (m & kHostBit) {
+    const uint32_t hs = m & kSlotMask;
+    if (hs >= geo.H) {
+      latch(p.status, ULA_ERR_INTERNAL);
+      return;
+    }
+    bm_set(host_free_bitmap(g), hs);
+    atomicAdd(&g.cnt->free_host, 1u);
+  } else {
+    if (m >= geo.S) {
+      latch(p.status, ULA_ERR_INTERNAL);
+      return;
+    }
+    const uint32_t c = class_of(g.stamp[m], p.round[gi], geo.B);
+    if (c == geo.B + 1) {
+      latch(p.status, ULA_ERR_INTERNAL);
+      return;
+    }
+    bm_clear(class_bitmap(g, geo, c), m);
+    bm_set(class_bitmap(g, geo, geo.B + 1), m);
+    g.stamp[m] = kNone;
+    g.owner[m] = kNone;
+    atomicAdd(&g.cnt->free_gpu, 1u);
+  }
+  g.map[a] = kUnalloc;
+}
+
+inline uint32_t div_up(uint64_t a, uint64_t b) { return (uint32_t)((a + b - 1) / b); }
+
+}  // namespace
+
+// --------------------------------------------------------------- launchers
+
+cudaError_t launch_bitmap_fill(Bitmap b, uint32_t nbits, cudaStream_t s) {
+  if (nbits == 0) return cudaSuccess;
+  const Dims d = dims_for(nbits);
+  k_bitmap_fill<<<div_up(d.n0, 256), 256, 0, s>>>(b, nbits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dedup(const StepParams &p, cudaStream_t s) {
+  const uint32_t nblk = div_up(p.E, kEntryThreads);
+  if (nblk) {
+    k_dedup_stamp<<<nblk, kEntryThreads, 0, s>>>(p);
+    k_dedup_count<<<nblk, kEntryThreads, 0, s>>>(p);
+  }
+  k_dedup_scan<<<1, kScanThreads, 0, s>>>(p, nblk);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_mark(const StepParams &p, cudaStream_t s) {
+  const uint32_t rot_blocks = div_up(p.geo.gd.n0, 256);
+  k_rotate<<<rot_blocks ? rot_blocks : 1, 256, 0, s>>>(p);
+  const uint32_t nblk = div_up(p.E, kEntryThreads);
+  if (nblk) {
+    k_dedup_emit<<<nblk, kEntryThreads, 0, s>>>(p);
+    k_entry_rows<<<nblk, kEntryThreads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const SelectParams &p, uint32_t n_groups, cudaStream_t s) {
+  const uint32_t nsup = p.geo.nsup > p.geo.hsup ? p.geo.nsup : p.geo.hsup;
+  dim3 grid(nsup ? nsup : 1, p.n_cls + 1, n_groups);
+  k_select_count<<<grid, 1024, 0, s>>>(p);
+  k_select_scan<<<n_groups, kScanThreads, 0, s>>>(p);
+  k_select_emit<<<grid, 1024, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_move(const MoveParams &p, int sm_count, cudaStream_t s) {
+  k_move_commit<<<sm_count * 8, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const GatherParams &p, int sm_count, cudaStream_t s) {
+  k_gather<<<sm_count * 8, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int sm_count,
+                               cudaStream_t s) {
+  uint32_t blocks = div_up((uint64_t)p.n * 32, 256);
+  const uint32_t cap = (uint32_t)sm_count * 8;
+  if (blocks > cap) blocks = cap;
+  dim3 grid(blocks ? blocks : 1, n_groups);
+  k_alloc_place<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s) {
+  dim3 grid(div_up(p.n, 256) ? div_up(p.n, 256) : 1, n_groups);
+  k_free<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace ula

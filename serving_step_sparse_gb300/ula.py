@@ -1,0 +1,179 @@
+"""Thin Python binding of the C ABI in include/ula.h (ctypes; marshalling only).
+
+Every step of the residency path runs in the CUDA library
+``_build/libula.so``; this module only converts arguments.  There is no CPU
+fallback: importing it without the built library raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libula.so")
+
+MAX_GROUPS = 64
+MAX_BUCKETS = 64
+ADDR_PAD = 0xFFFFFFFF
+MAP_UNALLOCATED = 0xFFFFFFFF
+MAP_HOST = 0x80000000
+STAMP_FREE = 0xFFFFFFFF
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_CAPACITY = 2
+ERR_UNMAPPED = 3
+ERR_CUDA = 4
+ERR_TIMEOUT = 5
+ERR_POISONED = 6
+ERR_INTERNAL = 7
+
+EXPORTED = ["ula_create", "ula_alloc", "ula_free", "ula_step_group", "ula_sync", "ula_destroy",
+            "ula_error_string", "ula_debug_layout_get", "ula_debug_export", "ula_debug_inject"]
+
+
+class ula_config(C.Structure):
+    _fields_ = [("row_bytes", C.c_uint32), ("n_groups", C.c_uint32),
+                ("layers_per_group", C.c_uint32 * MAX_GROUPS), ("gpu_slots", C.c_uint32),
+                ("host_slots", C.c_uint32), ("ring_buckets", C.c_uint32),
+                ("max_logical", C.c_uint32), ("max_entries", C.c_uint32), ("flags", C.c_uint32)]
+
+
+class ula_stats(C.Structure):
+    _fields_ = [(n, C.c_uint64) for n in (
+        "steps", "entries", "uniq", "hits", "misses", "victims_free", "victims_cold",
+        "victims_ring", "writebacks", "rows_gathered", "bytes_h2d", "bytes_d2h")]
+
+    def as_dict(self):
+        return {n: int(getattr(self, n)) for n, _ in self._fields_}
+
+
+class ula_debug_layout(C.Structure):
+    _fields_ = [(n, C.c_uint32) for n in ("n0", "n1", "n2", "h0", "h1", "h2", "n_classes",
+                                          "decision_cap")]
+
+
+class ula_debug_state(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in (
+        "map", "owner", "stamp", "class_bits", "class_sum1", "class_sum2", "host_free_bits",
+        "host_free_sum1", "host_free_sum2", "uniq", "victims", "wb_host")] + \
+        [(n, C.c_uint32) for n in ("round", "cur", "free_gpu", "free_host", "U", "M", "hits",
+                                    "victims_free", "writebacks")]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"CUDA library not built: {LIB_PATH} (run __graft_entry__.build())")
+    lib = C.CDLL(LIB_PATH)
+    p, u32, i32 = C.c_void_p, C.c_uint32, C.c_int
+    lib.ula_create.argtypes = [C.POINTER(ula_config), p, p, p, C.POINTER(p)]
+    lib.ula_create.restype = i32
+    lib.ula_alloc.argtypes = [p, u32, p, C.POINTER(u32)]
+    lib.ula_alloc.restype = i32
+    lib.ula_free.argtypes = [p, u32, u32]
+    lib.ula_free.restype = i32
+    lib.ula_step_group.argtypes = [p, u32, p, u32, u32, u32, p, u32, p, p, p, p]
+    lib.ula_step_group.restype = i32
+    lib.ula_sync.argtypes = [p, C.POINTER(ula_stats)]
+    lib.ula_sync.restype = i32
+    lib.ula_destroy.argtypes = [p]
+    lib.ula_destroy.restype = None
+    lib.ula_error_string.argtypes = [i32]
+    lib.ula_error_string.restype = C.c_char_p
+    lib.ula_debug_layout_get.argtypes = [p, C.POINTER(ula_debug_layout)]
+    lib.ula_debug_layout_get.restype = i32
+    lib.ula_debug_export.argtypes = [p, u32, C.POINTER(ula_debug_state)]
+    lib.ula_debug_export.restype = i32
+    lib.ula_debug_inject.argtypes = [p, i32]
+    lib.ula_debug_inject.restype = i32
+    return lib
+
+
+lib = _load()
+
+
+class UlaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        msg = lib.ula_error_string(code).decode()
+        super().__init__(f"{what}: {msg} (code {code})")
+        self.code = code
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise UlaError(rc, what)
+
+
+def _ptr_array(ptrs):
+    arr = (C.c_void_p * len(ptrs))()
+    for i, x in enumerate(ptrs):
+        arr[i] = x
+    return arr
+
+
+def make_config(row_bytes, layers_per_group, gpu_slots, host_slots, ring_buckets, max_logical,
+                max_entries, flags=0) -> ula_config:
+    cfg = ula_config()
+    cfg.row_bytes = row_bytes
+    cfg.n_groups = len(layers_per_group)
+    for i, l in enumerate(layers_per_group):
+        cfg.layers_per_group[i] = l
+    cfg.gpu_slots, cfg.host_slots, cfg.ring_buckets = gpu_slots, host_slots, ring_buckets
+    cfg.max_logical, cfg.max_entries, cfg.flags = max_logical, max_entries, flags
+    return cfg
+
+
+def ula_create(cfg: ula_config, gpu_pools, host_pools, stream: int | None) -> int:
+    """gpu_pools/host_pools: lists of integer addresses; stream: cudaStream_t as int."""
+    out = C.c_void_p()
+    hp = _ptr_array(host_pools) if host_pools is not None else None
+    _check(lib.ula_create(C.byref(cfg), _ptr_array(gpu_pools), hp, stream, C.byref(out)),
+           "ula_create")
+    return out.value
+
+
+def ula_alloc(ctx: int, n: int, rows: int) -> int:
+    base = C.c_uint32()
+    _check(lib.ula_alloc(ctx, n, rows, C.byref(base)), "ula_alloc")
+    return base.value
+
+
+def ula_free(ctx: int, base: int, n: int) -> None:
+    _check(lib.ula_free(ctx, base, n), "ula_free")
+
+
+def ula_step_group(ctx: int, group: int, d_sel: int, n_req: int, q: int, k: int, d_out: int,
+                   out_cap_rows: int, d_entry_row: int, d_req_off: int, layer_ready, stream) -> None:
+    ev = _ptr_array(layer_ready) if layer_ready else None
+    _check(lib.ula_step_group(ctx, group, d_sel, n_req, q, k, d_out, out_cap_rows, d_entry_row,
+                              d_req_off, ev, stream), "ula_step_group")
+
+
+def ula_sync(ctx: int) -> dict:
+    st = ula_stats()
+    _check(lib.ula_sync(ctx, C.byref(st)), "ula_sync")
+    return st.as_dict()
+
+
+def ula_sync_rc(ctx: int) -> int:
+    """ula_sync returning the status code instead of raising."""
+    return lib.ula_sync(ctx, None)
+
+
+def ula_destroy(ctx: int) -> None:
+    lib.ula_destroy(ctx)
+
+
+def ula_debug_layout_get(ctx: int) -> ula_debug_layout:
+    lay = ula_debug_layout()
+    _check(lib.ula_debug_layout_get(ctx, C.byref(lay)), "ula_debug_layout_get")
+    return lay
+
+
+def ula_debug_export(ctx: int, group: int, st: ula_debug_state) -> ula_debug_state:
+    _check(lib.ula_debug_export(ctx, group, C.byref(st)), "ula_debug_export")
+    return st
+
+
+def ula_debug_inject(ctx: int, code: int) -> None:
+    _check(lib.ula_debug_inject(ctx, code), "ula_debug_inject")

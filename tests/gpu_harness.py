@@ -1,0 +1,149 @@
+"""GPU-side test driver: replays a workload through the CUDA library (C ABI via
+the ctypes binding) and compares its state and outputs with the oracle's."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+from oracle import COLD, FREE, TIER_GPU, TIER_HOST, TIER_UNALLOCATED
+from serving_step_sparse_gb300 import ula
+from serving_step_sparse_gb300.cache import UlaCache
+from tests.harness import ID_ROW_BYTES, apply_events, initial_allocs
+
+STAGE_ADDRS = 16384  # addresses per staged alloc chunk
+
+
+class GpuRun:
+    def __init__(self, w, out_cap: int | None = None, stage_addrs: int = STAGE_ADDRS):
+        self.w = w
+        G, L = w.n_groups, w.layers_per_group
+        self.cache = UlaCache(row_bytes=w.row_bytes, layers_per_group=[L] * G,
+                              gpu_slots=w.gpu_slots, host_slots=w.host_slots,
+                              ring_buckets=w.ring_buckets, max_logical=w.max_logical,
+                              max_entries=w.entries_per_step)
+        self.cap = out_cap if out_cap is not None else w.entries_per_step
+        self.outs = [self.cache.out_buffer(g, self.cap) for g in range(G)]
+        E = w.entries_per_step
+        dev = self.cache.device
+        self.entry_row = [torch.empty(E, dtype=torch.int32, device=dev) for _ in range(G)]
+        self.req_off = [torch.empty(w.n_live + 1, dtype=torch.int32, device=dev) for _ in range(G)]
+        self.sel_d = torch.empty((G, w.n_live, w.q, w.k), dtype=torch.int32, device=dev)
+        self.stage_addrs = stage_addrs
+        self.stage = torch.empty(stage_addrs * G * L * w.row_bytes, dtype=torch.uint8,
+                                 pin_memory=True)
+        self.trace = synth.Trace(w)
+        self.live = set()
+        for base, n in initial_allocs(w, self.trace):
+            self.alloc(base, n)
+
+    def close(self):
+        self.cache.close()
+
+    def alloc(self, expect_base, n):
+        w = self.w
+        G, L, W = w.n_groups, w.layers_per_group, w.row_bytes
+        off = 0
+        while off < n:
+            m = min(self.stage_addrs, n - off)
+            buf = self.stage[: m * G * L * W]
+            view = buf.numpy().reshape(G, m, L, W)
+            for g in range(G):
+                synth.content_range(w.seed, g, L, expect_base + off, m, W, out=view[g])
+            got = self.cache.alloc(m, buf)
+            assert got == expect_base + off, (got, expect_base + off)
+            self.cache.sync()  # the staging buffer is reused
+            off += m
+        self.live.update(range(expect_base, expect_base + n))
+        return expect_base
+
+    def free(self, base, n):
+        self.cache.free(base, n)
+        self.live.difference_update(range(base, base + n))
+
+    def run_groups(self, sel: np.ndarray):
+        self.sel_d.copy_(torch.from_numpy(np.ascontiguousarray(sel).view(np.int32)))
+        for g in range(self.w.n_groups):
+            self.cache.step_group(g, self.sel_d[g], self.outs[g], self.entry_row[g],
+                                  self.req_off[g])
+        return self.cache.sync()
+
+    def step(self):
+        sel, ev = self.trace.step()
+        stats = self.run_groups(sel)
+        apply_events(self.alloc, self.free, ev)
+        return sel, ev, stats
+
+    def results(self, g: int, full_out: bool = True):
+        req_off = self.req_off[g].cpu().numpy()
+        U = int(req_off[-1])
+        res = {"req_off": req_off, "entry_row": self.entry_row[g].cpu().numpy()}
+        if full_out:
+            res["out"] = self.outs[g][:, :U].cpu().numpy()
+        return res
+
+
+def unpack_bits(words: np.ndarray, nbits: int) -> np.ndarray:
+    return np.unpackbits(np.ascontiguousarray(words).view(np.uint8), bitorder="little")[:nbits]
+
+
+def gpu_state_in_oracle_terms(st: dict, w) -> dict:
+    """Convert the library's export into the oracle's export format."""
+    S, H, B = w.gpu_slots, w.host_slots, w.ring_buckets
+    m = st["map"]
+    tier = np.where(m == ula.MAP_UNALLOCATED, TIER_UNALLOCATED,
+                    np.where(m & ula.MAP_HOST, TIER_HOST, TIER_GPU)).astype(np.uint8)
+    slot = np.where(tier == TIER_UNALLOCATED, 0, m & 0x7FFFFFFF).astype(np.uint32)
+    bits = np.stack([unpack_bits(st["class_bits"][c], S) for c in range(B + 2)])
+    assert (bits.sum(axis=0) == 1).all(), "every GPU slot is in exactly one class"
+    which = bits.argmax(axis=0)
+    cls = np.where(which < B, which, np.where(which == B, COLD, FREE)).astype(np.int32)
+    host_free = unpack_bits(st["host_free_bits"], H).astype(np.uint8) if H else np.zeros(0, np.uint8)
+    host_owner = np.full(H, 0xFFFFFFFF, dtype=np.uint32)
+    hosted = np.nonzero(tier == TIER_HOST)[0]
+    host_owner[slot[hosted]] = hosted
+    return {"tier": tier, "slot": slot, "cls": cls, "owner": st["owner"].copy(),
+            "host_free": host_free, "host_owner": host_owner, "cur": st["cur"]}
+
+
+def check_gpu_internal(st: dict, w):
+    """Library-internal invariants: exact summaries, stamps agree with classes, counters."""
+    S, H, B = w.gpu_slots, w.host_slots, w.ring_buckets
+    for c in range(B + 2):
+        w0, w1, w2 = st["class_bits"][c], st["class_sum1"][c], st["class_sum2"][c]
+        s1 = unpack_bits(w1, len(w0))
+        assert np.array_equal(s1.astype(bool), w0 != 0), f"level-1 summary of class {c}"
+        s2 = unpack_bits(w2, len(w1))
+        assert np.array_equal(s2.astype(bool), w1 != 0), f"level-2 summary of class {c}"
+    if H:
+        w0, w1, w2 = st["host_free_bits"], st["host_free_sum1"], st["host_free_sum2"]
+        n0 = (H + 31) // 32
+        n1 = (n0 + 31) // 32
+        assert np.array_equal(unpack_bits(w1, n0).astype(bool), w0[:n0] != 0)
+        assert np.array_equal(unpack_bits(w2, n1).astype(bool), w1[:n1] != 0)
+    r = st["round"]
+    stamp = st["stamp"]
+    exp = np.where(stamp == ula.STAMP_FREE, B + 1,
+                   np.where((np.uint32(r) - stamp).astype(np.uint32) >= B, B, stamp % B))
+    bits = np.stack([unpack_bits(st["class_bits"][c], S) for c in range(B + 2)])
+    assert np.array_equal(bits.argmax(axis=0), exp), "stamps agree with class bitmaps"
+    assert st["free_gpu"] == int(bits[B + 1].sum())
+    if H:
+        assert st["free_host"] == int(unpack_bits(st["host_free_bits"], H).sum())
+
+
+def compare_states(gpu_o: dict, orc: dict, where: str):
+    for k in ("tier", "slot", "cls", "owner", "host_free", "host_owner"):
+        a, b = gpu_o[k], orc[k]
+        if not np.array_equal(a, b):
+            idx = np.nonzero(a != b)[0][:8]
+            raise AssertionError(f"{where}: {k} differs at {idx.tolist()}: gpu {a[idx].tolist()} "
+                                 f"oracle {b[idx].tolist()}")
+    assert gpu_o["cur"] == orc["cur"], where
+
+
+def expand_id_rows(ids: np.ndarray, seed: int, g: int, j: int, W: int) -> np.ndarray:
+    """Oracle id-mode rows [U][8] -> the byte rows they stand for."""
+    v = ids.view(np.uint32).reshape(-1, 2)
+    assert ((v[:, 1] >> 16) == g).all() and ((v[:, 1] & 0xFFFF) == j).all()
+    return synth.content_list(seed, g, j, v[:, 0].copy(), W)

@@ -1,0 +1,72 @@
+"""The C ABI library builds, loads without a GPU, and exports every entry point
+that include/ula.h declares; the binding mirrors the declared structs."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ula.h")
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    from serving_step_sparse_gb300.build import build
+    return build()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(ula_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("ula_create", "ula_alloc", "ula_free", "ula_step_group", "ula_sync"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    lib = C.CDLL(libpath)
+    names = declared_functions()
+    assert len(names) >= 10
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_error_strings_without_gpu(libpath):
+    lib = C.CDLL(libpath)
+    lib.ula_error_string.restype = C.c_char_p
+    for code in range(8):
+        assert lib.ula_error_string(code)
+    assert lib.ula_error_string(99) == b"unknown error"
+
+
+def test_binding_struct_sizes_match_header(libpath):
+    from serving_step_sparse_gb300 import ula
+    # ula_config: 9 uint32 + 64 layer counts
+    assert C.sizeof(ula.ula_config) == 4 * (8 + ula.MAX_GROUPS)
+    assert C.sizeof(ula.ula_stats) == 8 * 12
+    assert C.sizeof(ula.ula_debug_layout) == 4 * 8
+    assert C.sizeof(ula.ula_debug_state) == 8 * 12 + 4 * 9 + 4  # padded to 8
+    src = open(HEADER).read()
+    assert "#define ULA_MAX_GROUPS 64" in src and "#define ULA_MAX_BUCKETS 64" in src
+    for name, val in (("ULA_ERR_INVALID_ARG", 1), ("ULA_ERR_CAPACITY", 2), ("ULA_ERR_UNMAPPED", 3),
+                      ("ULA_ERR_CUDA", 4), ("ULA_ERR_TIMEOUT", 5), ("ULA_ERR_POISONED", 6),
+                      ("ULA_ERR_INTERNAL", 7)):
+        assert re.search(rf"{name}\s*=\s*{val}\b", src)
+        assert getattr(ula, name[4:]) == val
+
+
+def test_calls_reject_null_context_without_gpu(libpath):
+    from serving_step_sparse_gb300 import ula
+    base = C.c_uint32()
+    assert ula.lib.ula_alloc(None, 1, None, C.byref(base)) == ula.ERR_INVALID_ARG
+    assert ula.lib.ula_free(None, 0, 1) == ula.ERR_INVALID_ARG
+    assert ula.lib.ula_sync(None, None) == ula.ERR_INVALID_ARG
+    assert ula.lib.ula_create(None, None, None, None, None) == ula.ERR_INVALID_ARG
+    ula.lib.ula_destroy(None)

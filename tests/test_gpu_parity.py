@@ -1,0 +1,345 @@
+"""GPU path vs the CPU oracle: bit-exact on every map entry, class label,
+eviction decision, write-back slot, dedup output and gathered byte.
+
+Small workloads (every recipe, reduced) compare the full state after every
+step; the full-size workloads run in the launch configuration the benchmark
+times, with the oracle in id mode (exact: row contents are a function of the
+address), full state compared every step and gathered bytes on sampled rows.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from synth.configs import WORKLOADS, small
+from tests.harness import OracleRun, check_invariants, check_step_outputs
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from tests.gpu_harness import (GpuRun, check_gpu_internal, compare_states, expand_id_rows,
+                                   gpu_state_in_oracle_terms)
+
+
+def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2048, seed=0):
+    gpu = GpuRun(w)
+    orc = OracleRun(w, mode)
+    rng = np.random.default_rng(seed)
+    try:
+        for g in range(w.n_groups):  # initial placement
+            compare_states(gpu_state_in_oracle_terms(gpu.cache.export(g), w), orc.o.export(g),
+                           f"initial g{g}")
+        for t in range(steps):
+            sel, ev = gpu.trace.step()
+            gpu.run_groups(sel)
+            for g in range(w.n_groups):
+                ro = orc.o.step_group(g, sel[g])
+                full = (t % out_every == 0)
+                rg = gpu.results(g, full_out=full and mode == "bytes")
+                where = f"step {t} group {g}"
+                assert np.array_equal(rg["req_off"], ro["req_off"]), where
+                assert np.array_equal(rg["entry_row"], ro["entry_row"]), where
+                U = int(ro["req_off"][-1])
+                if full and mode == "bytes":
+                    assert np.array_equal(rg["out"], ro["out"][:, :U]), f"{where}: gathered bytes"
+                else:
+                    rows = rng.choice(U, min(U, sample_rows), replace=False) if U else np.zeros(0, int)
+                    rows_t = torch.from_numpy(rows).to(gpu.outs[g].device)
+                    for j in range(w.layers_per_group):
+                        got = gpu.outs[g][j].index_select(0, rows_t).cpu().numpy()
+                        if mode == "bytes":
+                            exp = ro["out"][j, rows]
+                        else:
+                            exp = expand_id_rows(ro["out"][j, rows], w.seed, g, j, w.row_bytes)
+                        assert np.array_equal(got, exp), f"{where}: gathered bytes layer {j}"
+                if t % state_every == 0 or t == steps - 1:
+                    st = gpu.cache.export(g)
+                    check_gpu_internal(st, w)
+                    go = gpu_state_in_oracle_terms(st, w)
+                    oo = orc.o.export(g)
+                    compare_states(go, oo, where)
+                    v, vc, wb = orc.o.last_decisions(g)
+                    assert st["M"] == len(v) and st["writebacks"] == len(wb), where
+                    assert np.array_equal(st["victims"][:len(v)], v), f"{where}: victims"
+                    assert np.array_equal(st["wb_host"][:len(wb)], wb), f"{where}: write-backs"
+                    check_invariants(go, w.gpu_slots, w.host_slots, orc.live)
+            from tests.harness import apply_events
+            apply_events(gpu.alloc, gpu.free, ev)
+            apply_events(orc.alloc, orc.free, ev)
+        return gpu.cache.sync()
+    finally:
+        gpu.close()
+
+
+def test_parity_cfg0_full():
+    stats = run_parity(WORKLOADS["cfg0"], WORKLOADS["cfg0"].steps)
+    assert stats["steps"] == 64 and stats["misses"] > 0 and stats["hits"] > 0
+
+
+@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3", "cfg4"])
+def test_parity_small(name):
+    w = small(name)
+    stats = run_parity(w, w.steps)
+    assert stats["misses"] > 0
+
+
+def test_parity_cfg1_full():
+    w = WORKLOADS["cfg1"]
+    stats = run_parity(w, w.steps, mode="bytes", state_every=4, out_every=16)
+    assert stats["steps"] == w.steps * w.n_groups and stats["writebacks"] > 0
+
+
+@pytest.mark.parametrize("name,steps", [("cfg2", 12), ("cfg3", 12), ("cfg4", 13)])
+def test_parity_full_size_sampled(name, steps):
+    """Full-size workloads: state compared every step, gathered bytes sampled."""
+    w = WORKLOADS[name]
+    stats = run_parity(w, steps, mode="id", state_every=1, out_every=10**9, sample_rows=4096)
+    assert stats["steps"] == steps * w.n_groups
+
+
+# ----------------------------------------------------------------- edge cases
+
+def test_pads_and_ragged_sizes():
+    # ragged: S, H not multiples of 32 or 1,024; E not a multiple of the block size
+    w = WORKLOADS["cfg0"].replace(pad_prob=0.1, gpu_slots_explicit=1000 + 7,
+                                  host_slots_explicit=3000 + 13, k=250, window=50, steps=32)
+    run_parity(w, w.steps)
+
+
+@pytest.mark.parametrize("B", [1, 2, 3])
+def test_small_rings(B):
+    w = small("cfg1").replace(ring_buckets=B, steps=24)
+    run_parity(w, w.steps)
+
+
+def test_everything_fits_on_gpu_no_host_pool():
+    w = WORKLOADS["cfg0"].replace(gpu_slots_explicit=4096, host_slots_explicit=0, steps=16)
+    stats = run_parity(w, w.steps)
+    assert stats["misses"] == 0 and stats["writebacks"] == 0
+
+
+def _direct(S=64, H=256, B=3, layers=(1, 3), W=16, max_logical=512, max_entries=64):
+    from serving_step_sparse_gb300.cache import UlaCache
+    from oracle import Oracle
+    c = UlaCache(row_bytes=W, layers_per_group=list(layers), gpu_slots=S, host_slots=H,
+                 ring_buckets=B, max_logical=max_logical, max_entries=max_entries)
+    o = Oracle(W, list(layers), S, H, B, max_logical)
+    return c, o
+
+
+def _rows(layers, base, n, W, seed=9):
+    parts = [synth.content_range(seed, g, L, base, n, W).reshape(-1) for g, L in enumerate(layers)]
+    return np.concatenate(parts)
+
+
+def _step_both(c, o, g, sel, cap=None):
+    from tests.gpu_harness import gpu_state_in_oracle_terms
+    sel = np.ascontiguousarray(sel, dtype=np.uint32)
+    R, Q, K = sel.shape
+    cap = cap if cap is not None else max(1, sel.size)
+    out = c.out_buffer(g, cap)
+    er = torch.empty(max(1, sel.size), dtype=torch.int32, device="cuda")
+    ro = torch.empty(R + 1, dtype=torch.int32, device="cuda")
+    sd = torch.from_numpy(sel.view(np.int32).copy()).cuda()
+    c.step_group(g, sd, out, er, ro)
+    c.sync()
+    res = o.step_group(g, sel, out_cap=cap)
+    U = int(res["req_off"][-1])
+    assert np.array_equal(ro.cpu().numpy(), res["req_off"])
+    assert np.array_equal(er.cpu().numpy()[:sel.size], res["entry_row"])
+    assert np.array_equal(out[:, :U].cpu().numpy(), res["out"][:, :U])
+    return res
+
+
+class _W:  # geometry shim for the state converters
+    def __init__(self, S, H, B):
+        self.gpu_slots, self.host_slots, self.ring_buckets = S, H, B
+
+
+def test_mixed_layers_duplicates_across_requests_and_empty_steps():
+    from tests.gpu_harness import gpu_state_in_oracle_terms
+    layers, W, S, H, B = (1, 3), 16, 64, 256, 3
+    c, o = _direct(S=S, H=H, B=B, layers=layers, W=W)
+    try:
+        n = 200
+        rows = _rows(layers, 0, n, W)
+        t = torch.from_numpy(rows).pin_memory()
+        assert c.alloc(n, t) == 0 and o.alloc(n, rows) == 0
+        c.sync()
+        rng = np.random.default_rng(3)
+        for step in range(40):
+            g = step % 2
+            if step % 7 == 3:  # empty selections: no requests, or k = 0
+                _step_both(c, o, g, np.zeros((0, 1, 4), np.uint32))
+                _step_both(c, o, g, np.zeros((2, 1, 0), np.uint32))
+                continue
+            R, Q, K = 3, 2, 8
+            sel = rng.choice(n, (R, Q, K)).astype(np.uint32)
+            sel[1, 0, :4] = sel[0, 1, :4]  # the same addresses in two requests
+            sel[2, 1, 3] = 0xFFFFFFFF
+            _step_both(c, o, g, sel)
+            for gg in range(2):
+                go = gpu_state_in_oracle_terms(c.export(gg), _W(S, H, B))
+                compare_states(go, o.export(gg), f"step {step} g{gg}")
+    finally:
+        c.close()
+
+
+def _export_all(c, G, S, H, B):
+    from tests.gpu_harness import gpu_state_in_oracle_terms
+    return [gpu_state_in_oracle_terms(c.export(g), _W(S, H, B)) for g in range(G)]
+
+
+def _same(a, b):
+    return all(all(np.array_equal(x[k], y[k]) for k in x) for x, y in zip(a, b))
+
+
+@pytest.mark.parametrize("case", ["capacity", "unmapped", "out_cap", "inject"])
+def test_device_errors_latch_poison_and_change_nothing(case):
+    from serving_step_sparse_gb300 import ula
+    S, H, B, layers, W = 32, 128, 4, (2,), 32
+    c, o = _direct(S=S, H=H, B=B, layers=layers, W=W, max_logical=256, max_entries=64)
+    try:
+        n = 100
+        t = torch.from_numpy(_rows(layers, 0, n, W)).pin_memory()
+        c.alloc(n, t)
+        c.sync()
+        before = _export_all(c, 1, S, H, B)
+        if case == "capacity":   # 33 distinct addresses > 32 GPU slots
+            sel = np.arange(33, dtype=np.uint32).reshape(1, 1, 33)
+            cap, want = 64, ula.ERR_CAPACITY
+        elif case == "unmapped":  # address 150 was never allocated
+            sel = np.array([[[1, 2, 150]]], dtype=np.uint32)
+            cap, want = 64, ula.ERR_UNMAPPED
+        elif case == "out_cap":
+            sel = np.arange(10, dtype=np.uint32).reshape(1, 1, 10)
+            cap, want = 9, ula.ERR_CAPACITY
+        else:
+            c.inject(ula.ERR_TIMEOUT)
+            sel = np.arange(4, dtype=np.uint32).reshape(1, 1, 4)
+            cap, want = 64, ula.ERR_TIMEOUT
+        sd = torch.from_numpy(sel.view(np.int32).copy()).cuda()
+        out = c.out_buffer(0, cap)
+        er = torch.empty(sel.size, dtype=torch.int32, device="cuda")
+        ro = torch.empty(2, dtype=torch.int32, device="cuda")
+        c.step_group(0, sd, out, er, ro)
+        assert ula.ula_sync_rc(c.ctx) == want
+        after = _export_all(c, 1, S, H, B)
+        # the round counter advanced on the host, but no label, map entry or slot changed
+        for x, y in zip(before, after):
+            for k in ("tier", "slot", "cls", "owner", "host_free", "host_owner"):
+                assert np.array_equal(x[k], y[k]), k
+        with pytest.raises(ula.UlaError) as ei:
+            c.step_group(0, sd, out, er, ro)
+        assert ei.value.code == ula.ERR_POISONED
+        with pytest.raises(ula.UlaError) as ei:
+            c.sync()
+        assert ei.value.code == ula.ERR_POISONED
+    finally:
+        c.close()
+
+
+def test_host_detected_errors_change_nothing():
+    from serving_step_sparse_gb300 import ula
+    S, H, B, layers, W = 16, 16, 2, (1,), 16
+    c, o = _direct(S=S, H=H, B=B, layers=layers, W=W, max_logical=64, max_entries=8)
+    try:
+        t = torch.from_numpy(_rows(layers, 0, 20, W)).pin_memory()
+        assert c.alloc(20, t) == 0
+        c.sync()
+        before = _export_all(c, 1, S, H, B)
+        big = torch.from_numpy(_rows(layers, 20, 13, W)).pin_memory()
+        with pytest.raises(ula.UlaError) as ei:  # 20 + 13 > S + H
+            c.alloc(13, big)
+        assert ei.value.code == ula.ERR_CAPACITY
+        pageable = torch.zeros(16, dtype=torch.uint8)
+        with pytest.raises(ula.UlaError) as ei:
+            ula.ula_alloc(c.ctx, 1, pageable.data_ptr())
+        assert ei.value.code == ula.ERR_INVALID_ARG
+        c.free(3, 2)
+        with pytest.raises(ula.UlaError) as ei:  # double free
+            c.free(4, 1)
+        assert ei.value.code == ula.ERR_INVALID_ARG
+        with pytest.raises(ula.UlaError) as ei:  # beyond what was allocated
+            c.free(19, 2)
+        assert ei.value.code == ula.ERR_INVALID_ARG
+        sd = torch.zeros((1, 1, 9), dtype=torch.int32, device="cuda")
+        out = c.out_buffer(0, 9)
+        er = torch.empty(9, dtype=torch.int32, device="cuda")
+        ro = torch.empty(2, dtype=torch.int32, device="cuda")
+        with pytest.raises(ula.UlaError) as ei:  # 9 entries > max_entries
+            c.step_group(0, sd, out, er, ro)
+        assert ei.value.code == ula.ERR_INVALID_ARG
+        with pytest.raises(ula.UlaError) as ei:
+            ula.ula_step_group(c.ctx, 1, sd.data_ptr(), 1, 1, 1, out.data_ptr(), 9,
+                               er.data_ptr(), ro.data_ptr(), None, c.stream.cuda_stream)
+        assert ei.value.code == ula.ERR_INVALID_ARG
+        c.sync()  # still healthy
+        after = _export_all(c, 1, S, H, B)
+        o.alloc(20, _rows(layers, 0, 20, W))
+        o.free(3, 2)
+        assert _same(after, [o.export(0)])
+        assert before[0]["tier"][3] != 0 and after[0]["tier"][3] == 0
+    finally:
+        c.close()
+
+
+def test_config_and_pool_validation():
+    from serving_step_sparse_gb300 import ula
+    gp = torch.empty(4 * 16, dtype=torch.uint8, device="cuda")
+    hp = torch.empty(4 * 16, dtype=torch.uint8, pin_memory=True)
+    good = dict(row_bytes=16, layers_per_group=[1], gpu_slots=4, host_slots=4, ring_buckets=2,
+                max_logical=8, max_entries=4)
+    for bad in (dict(row_bytes=20), dict(ring_buckets=0), dict(ring_buckets=65), dict(gpu_slots=0),
+                dict(max_entries=0), dict(layers_per_group=[0])):
+        cfg = ula.make_config(**{**good, **bad})
+        with pytest.raises(ula.UlaError) as ei:
+            ula.ula_create(cfg, [gp.data_ptr()], [hp.data_ptr()], None)
+        assert ei.value.code == ula.ERR_INVALID_ARG
+    cfg = ula.make_config(**good)
+    pageable = torch.empty(64, dtype=torch.uint8)
+    with pytest.raises(ula.UlaError):  # host pool must be pinned
+        ula.ula_create(cfg, [gp.data_ptr()], [pageable.data_ptr()], None)
+    with pytest.raises(ula.UlaError):  # GPU pool must be device memory
+        ula.ula_create(cfg, [hp.data_ptr()], [hp.data_ptr()], None)
+    with pytest.raises(ula.UlaError):  # 16-byte alignment
+        ula.ula_create(cfg, [gp.data_ptr() + 8], [hp.data_ptr()], None)
+    ctx = ula.ula_create(cfg, [gp.data_ptr()], [hp.data_ptr()], None)
+    ula.ula_destroy(ctx)
+
+
+def test_layer_ready_events_and_side_stream_order():
+    """Layer j's event completes after its rows are written; a consumer waiting on
+    each event (on another stream) reads the right bytes."""
+    w = small("cfg1").replace(steps=6)
+    gpu = GpuRun(w)
+    orc = OracleRun(w, "bytes")
+    consumer = torch.cuda.Stream()
+    try:
+        for t in range(w.steps):
+            sel, ev = gpu.trace.step()
+            gpu.sel_d.copy_(torch.from_numpy(sel.view(np.int32)))
+            copies = []
+            for g in range(w.n_groups):
+                events = [torch.cuda.Event() for _ in range(w.layers_per_group)]
+                gpu.cache.step_group(g, gpu.sel_d[g], gpu.outs[g], gpu.entry_row[g],
+                                     gpu.req_off[g], layer_ready=events)
+                with torch.cuda.stream(consumer):
+                    for j, e in enumerate(events):
+                        consumer.wait_event(e)
+                        copies.append((g, j, gpu.outs[g][j].clone()))
+            consumer.synchronize()
+            gpu.cache.sync()
+            for g in range(w.n_groups):
+                ro = orc.o.step_group(g, sel[g])
+                U = int(ro["req_off"][-1])
+                for gg, j, buf in copies:
+                    if gg == g:
+                        assert np.array_equal(buf[:U].cpu().numpy(), ro["out"][j, :U])
+            from tests.harness import apply_events
+            apply_events(gpu.alloc, gpu.free, ev)
+            apply_events(orc.alloc, orc.free, ev)
+    finally:
+        gpu.close()
