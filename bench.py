@@ -1,0 +1,509 @@
+#!/usr/bin/env python
+"""Benchmark of the KV residency path: selected KV rows resolved + gathered per second.
+
+One step = one decode step of the workload = every layer group's ula_step_group
+(dedup, translate, PB-LRU rotate/mark, victim selection, write-back + fill +
+commit, gather of all layers) plus the step's appended-token alloc.
+
+  value     : rows/s with the step inputs already in HBM (device-timed, CUDA events)
+  e2e       : the same through the C ABI with host buffers: per step the selections are
+              copied from pinned host memory, appended rows are read from pinned host
+              memory by the alloc, and the per-request row offsets are read back
+  roofline  : the gather kernel (dominant bytes), timed per launch with CUDA events on
+              the stream each launch runs on, against the measured HBM copy peak
+  host_link : the move kernel (write-back + fill over the host link) against the
+              measured pinned copy bandwidth
+  cpu_baseline : the CPU oracle on a bounded sample of the same workload (1 core)
+
+--impl reference times the CPU oracle alone (the reference arm of this build).
+Multi-GPU (torchrun, N > 1): independent replicas, one per GPU; value = all ranks'
+rows / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selected KV rows resolved+gathered/sec; HBM & host-link GB/s vs peak"
+FALLBACK_HBM_GBS = 6800.0
+GATHER_BYTES_PER_ROW = None  # set below from the workload's row size: read + write
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="cfg2")
+    ap.add_argument("--profile-steps", type=int, default=60)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------ distributed glue
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(values: dict, world: int, device=None) -> dict:
+    """MAX of times and SUM of work over ranks (identity when world == 1)."""
+    if world == 1:
+        return dict(values)
+    import torch
+    import torch.distributed as dist
+    keys = sorted(values)
+    t = torch.tensor([float(values[k]) for k in keys], dtype=torch.float64, device=device)
+    mx, sm = t.clone(), t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    out = {}
+    for i, k in enumerate(keys):
+        out[k] = float(mx[i]) if k.endswith("_ms") else float(sm[i])
+    return out
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+                power.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------- peaks
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_link_peaks(torch, nbytes=1 << 30):
+    """Pinned copy-engine bandwidth, each direction alone and both at once (GB/s)."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d2 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def best(fn, reps=4):
+        b = 1e9
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            b = min(b, time.perf_counter() - t0)
+        return b
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s1):
+            h.copy_(d, non_blocking=True)
+
+    def both():
+        with torch.cuda.stream(s1):
+            d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h2.copy_(d2, non_blocking=True)
+
+    out = {"h2d_gbs": nbytes / best(h2d) / 1e9, "d2h_gbs": nbytes / best(d2h) / 1e9,
+           "bidir_gbs": 2 * nbytes / best(both) / 1e9}
+    del h, h2, d, d2
+    return out
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def stage_initial(cache, w, synth, torch):
+    """Initial contexts: rows generated into a pinned staging buffer, allocated chunk by chunk."""
+    trace = synth.Trace(w)
+    ctx, base, total = trace.initial()
+    G, L, W = w.n_groups, w.layers_per_group, w.row_bytes
+    chunk = 32768
+    stage = torch.empty(chunk * G * L * W, dtype=torch.uint8, pin_memory=True)
+    for b0, n0 in zip(base.tolist(), ctx.tolist()):
+        off = 0
+        while off < n0:
+            m = min(chunk, n0 - off)
+            buf = stage[: m * G * L * W]
+            view = buf.numpy().reshape(G, m, L, W)
+            for g in range(G):
+                synth.content_range(w.seed, g, L, b0 + off, m, W, out=view[g])
+            got = cache.alloc(m, buf)
+            assert got == b0 + off, (got, b0 + off)
+            cache.sync()
+            off += m
+    return trace
+
+
+def gen_steps(trace, w, n, synth, np):
+    steps = []
+    for _ in range(n):
+        sel, ev = trace.step()
+        assert not ev["free_n"] and not ev["join_n"], "benchmark workload has no turnover"
+        rows = None
+        if ev["append_n"]:
+            G, L, W = w.n_groups, w.layers_per_group, w.row_bytes
+            rows = np.empty((G, ev["append_n"], L, W), dtype=np.uint8)
+            for g in range(G):
+                synth.content_range(w.seed, g, L, ev["append_base"], ev["append_n"], W,
+                                    out=rows[g])
+        steps.append((sel, ev, rows))
+    return steps
+
+
+def run_gpu(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import synth
+    from serving_step_sparse_gb300 import ula
+    from serving_step_sparse_gb300.cache import UlaCache
+    from synth.configs import WORKLOADS
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    G, L, W, R, Q, K = (w.n_groups, w.layers_per_group, w.row_bytes, w.n_live, w.q, w.k)
+    E = w.entries_per_step
+    stream = torch.cuda.current_stream(dev)
+
+    t_setup = time.perf_counter()
+    link = host_link_peaks(torch)
+    cache = UlaCache(row_bytes=W, layers_per_group=[L] * G, gpu_slots=w.gpu_slots,
+                     host_slots=w.host_slots, ring_buckets=w.ring_buckets,
+                     max_logical=w.max_logical, max_entries=E, device=dev, stream=stream)
+    trace = stage_initial(cache, w, synth, torch)
+    n_value, n_prof = args.steps, min(args.profile_steps, args.steps)
+    n_e2e = 0 if args.no_e2e else args.steps
+    steps = gen_steps(trace, w, args.warmup + n_value + n_prof + n_e2e, synth, np)
+    outs = [cache.out_buffer(g, E) for g in range(G)]
+    entry_row = [torch.empty(E, dtype=torch.int32, device=dev) for _ in range(G)]
+    req_off = [torch.empty(R + 1, dtype=torch.int32, device=dev) for _ in range(G)]
+    # device-resident inputs for the value and profiled passes
+    n_dev = args.warmup + n_value + n_prof
+    sel_dev = torch.from_numpy(np.stack([s[0] for s in steps[:n_dev]]).view(np.int32)).to(dev)
+    rows_dev = [torch.from_numpy(s[2].reshape(-1)).to(dev) if s[2] is not None else None
+                for s in steps[:n_dev]]
+    torch.cuda.synchronize()
+    setup_s = time.perf_counter() - t_setup
+
+    def do_step(sel_t, ev, rows_t):
+        for g in range(G):
+            cache.step_group(g, sel_t[g], outs[g], entry_row[g], req_off[g])
+        if ev["append_n"]:
+            got = cache.alloc(ev["append_n"], rows_t)
+            assert got == ev["append_base"]
+
+    for t in range(args.warmup):
+        do_step(sel_dev[t], steps[t][1], rows_dev[t])
+    st0 = cache.sync()
+    ula.ula_profile_read(cache.ctx, reset=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # ---- value: inputs resident in HBM
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for t in range(args.warmup, args.warmup + n_value):
+        do_step(sel_dev[t], steps[t][1], rows_dev[t])
+    e1.record(stream)
+    st1 = cache.sync()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    value_ms = e0.elapsed_time(e1)
+    prof_value = ula.ula_profile_read(cache.ctx, reset=True)
+    launches = sum(p["kernels"] for p in prof_value.values())
+    rows_value = st1["rows_gathered"] - st0["rows_gathered"]
+
+    # ---- profiled pass: per-launch gather / move durations on their own streams
+    ula.ula_profile_enable(cache.ctx, True)
+    st2a = cache.sync()
+    for t in range(args.warmup + n_value, n_dev):
+        do_step(sel_dev[t], steps[t][1], rows_dev[t])
+    st2 = cache.sync()
+    prof = ula.ula_profile_read(cache.ctx, reset=True)
+    ula.ula_profile_enable(cache.ctx, False)
+
+    # ---- e2e: host buffers through the C ABI
+    e2e = None
+    if n_e2e:
+        sel_host = torch.from_numpy(np.stack([s[0] for s in steps[n_dev:]]).view(np.int32))
+        sel_host = sel_host.pin_memory()
+        rows_host = [torch.from_numpy(s[2].reshape(-1)).pin_memory() if s[2] is not None else None
+                     for s in steps[n_dev:]]
+        sel_buf = [torch.empty((G, R, Q, K), dtype=torch.int32, device=dev) for _ in range(2)]
+        res_host = torch.empty((n_e2e, G, R + 1), dtype=torch.int32, pin_memory=True)
+        h2d_bytes = d2h_bytes = 0
+        st3a = cache.sync()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(n_e2e):
+            buf = sel_buf[i % 2]
+            buf.copy_(sel_host[i], non_blocking=True)
+            h2d_bytes += buf.numel() * 4
+            ev = steps[n_dev + i][1]
+            for g in range(G):
+                cache.step_group(g, buf[g], outs[g], entry_row[g], req_off[g])
+            if ev["append_n"]:
+                cache.alloc(ev["append_n"], rows_host[i])  # read from pinned host memory
+                h2d_bytes += rows_host[i].numel()
+            for g in range(G):
+                res_host[i, g].copy_(req_off[g], non_blocking=True)
+                d2h_bytes += (R + 1) * 4
+        e1.record(stream)
+        st3 = cache.sync()
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        rows_e2e = st3["rows_gathered"] - st3a["rows_gathered"]
+        assert int(res_host[-1, 0, -1]) > 0
+        e2e = {"rows": rows_e2e, "e2e_ms": e2e_ms, "h2d": h2d_bytes / n_e2e,
+               "d2h": d2h_bytes / n_e2e}
+    clk = clocks.stop()
+
+    # ---- roofline of the gather (bytes: read the row from the pool, write it to out)
+    rows_prof = st2["rows_gathered"] - st2a["rows_gathered"]
+    g_launch = prof["gather"]["timed"]
+    g_ms = prof["gather"]["ms"]
+    hbm_peak, hbm_src = measured_peaks()
+    per_launch_bytes = rows_prof / max(1, g_launch) * 2 * W
+    avg_launch_s = g_ms / max(1, g_launch) / 1e3
+    achieved = per_launch_bytes / avg_launch_s / 1e9 if avg_launch_s > 0 else 0.0
+    traffic = traffic_per_launch(rows_prof / max(1, g_launch))
+    roof = {"bound": "hbm", "kernel": "k_gather", "achieved": round(achieved, 1),
+            "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+            "traffic": traffic, "peak_source": f"{hbm_src} (hbm_gbs, STREAM-style copy)",
+            "avg_launch_us": round(avg_launch_s * 1e6, 2),
+            "rows_per_launch": round(rows_prof / max(1, g_launch), 1),
+            "bytes_per_row": 2 * W}
+    # ---- host link: the move kernel moves fills (H2D) and write-backs (D2H) at once
+    mv_s = prof["move"]["ms"] / 1e3
+    h2d_b = st2["bytes_h2d"] - st2a["bytes_h2d"]
+    d2h_b = st2["bytes_d2h"] - st2a["bytes_d2h"]
+    host = {"kernel": "k_move_commit", "fill_gbs": round(h2d_b / mv_s / 1e9, 1) if mv_s else 0,
+            "writeback_gbs": round(d2h_b / mv_s / 1e9, 1) if mv_s else 0,
+            "peak_h2d_gbs": round(link["h2d_gbs"], 1), "peak_d2h_gbs": round(link["d2h_gbs"], 1),
+            "peak_bidir_gbs": round(link["bidir_gbs"], 1),
+            "peak_source": "measured in this run: pinned cudaMemcpyAsync, 1 GiB"}
+    if mv_s:
+        host["frac_fill"] = round(h2d_b / mv_s / 1e9 / link["h2d_gbs"], 4)
+        host["frac_total"] = round((h2d_b + d2h_b) / mv_s / 1e9 / link["bidir_gbs"], 4)
+    phases = {k: round(v["ms"] / max(1, n_prof), 4) for k, v in prof.items() if v["timed"]}
+
+    agg = aggregate({"rows": rows_value, "value_ms": value_ms}, world, dev)
+    res = {
+        "rows": agg["rows"], "value_ms": agg["value_ms"], "launches": launches,
+        "roofline": roof, "host_link": host, "clocks": clk, "phases": phases, "e2e": e2e,
+        "setup_s": setup_s, "stats": {k: st1[k] - st0[k] for k in st1},
+    }
+    if e2e is not None:
+        a = aggregate({"rows": e2e["rows"], "e2e_ms": e2e["e2e_ms"]}, world, dev)
+        res["e2e"] = {"value": a["rows"] / (a["e2e_ms"] / 1e3), "unit": "rows/s",
+                      "h2d_bytes_per_step": int(e2e["h2d"]), "d2h_bytes_per_step": int(e2e["d2h"]),
+                      "ms_per_step": round(a["e2e_ms"] / n_e2e, 4)}
+    cache.close()
+    return res
+
+
+# Traffic measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for the gather
+# kernel, per gathered row, together with the hash of the kernel source it was taken on.
+# Reported only while the source is unchanged.
+GATHER_TRAFFIC = {"source_sha256": None, "bytes_per_row": None}
+
+
+def traffic_per_launch(rows_per_launch):
+    src = os.path.join(ROOT, "serving_step_sparse_gb300", "csrc", "ula_kernels.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if GATHER_TRAFFIC["source_sha256"] != sha or GATHER_TRAFFIC["bytes_per_row"] is None:
+        return None
+    return round(GATHER_TRAFFIC["bytes_per_row"] * rows_per_launch)
+
+
+# ------------------------------------------------------------- CPU oracle arm
+
+def cpu_sample_workload(name):
+    from synth.configs import WORKLOADS
+    w = WORKLOADS[name]
+    n = min(4, w.n_live)
+    kw = dict(n_live=n, name=w.name + "_cpu_sample",
+              description=w.description + f" (first {n} requests)")
+    if w.n_total is not None:
+        kw["n_total"] = n
+        kw["turnover_period"] = 0
+    return w.replace(**kw)
+
+
+def run_oracle(name, warmup, steps=None, seconds=None):
+    """The oracle as it stands, single-threaded, on a bounded sample of the workload."""
+    import numpy as np
+
+    import synth
+    from oracle import ExactLru
+    from tests.harness import OracleRun, apply_events
+
+    w = cpu_sample_workload(name)
+    run = OracleRun(w, "bytes")
+    lru = ExactLru(w.n_groups, w.gpu_slots, w.max_logical)
+    for b, n in [(int(b), int(c)) for b, c in zip(*run.trace.initial()[1::-1])]:
+        lru.alloc(n)
+    t_oracle = 0.0
+    rows = hits = uniq = 0
+    n_done = 0
+    limit = steps if steps is not None else 10 ** 9
+    while n_done < warmup + limit:
+        sel, ev = run.trace.step()
+        t0 = time.perf_counter()
+        res = [run.o.step_group(g, sel[g]) for g in range(w.n_groups)]
+        apply_events(run.alloc, run.free, ev)  # includes generating appended rows (small)
+        dt = time.perf_counter() - t0
+        for g in range(w.n_groups):
+            lru.step_group(g, sel[g])
+        if ev["append_n"]:
+            lru.alloc(ev["append_n"])
+        if n_done >= warmup:
+            t_oracle += dt
+            for r in res:
+                rows += r["counters"]["rows_gathered"]
+                hits += r["counters"]["hits"]
+                uniq += r["counters"]["uniq"]
+        n_done += 1
+        if seconds is not None and t_oracle >= seconds and n_done >= warmup + 4:
+            break
+    timed_steps = n_done - warmup
+    return {"value": rows / t_oracle if t_oracle else 0.0, "unit": "rows/s", "cores": 1,
+            "kind": "oracle", "steps": timed_steps, "seconds": round(t_oracle, 3),
+            "sample": (f"{w.description}: {w.n_live} requests, S={w.gpu_slots}, "
+                       f"H={w.host_slots}, {timed_steps} decode steps after {warmup} warm-up, "
+                       f"656-byte rows moved, single-threaded"),
+            "pblru_hit_rate": hits / max(1, uniq), "exact_lru_hit_rate": lru.hit_rate}
+
+
+# -------------------------------------------------------------------- main
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    from synth.configs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    config = dict(w.summary())
+    config["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    config["l2"] = ("inputs larger than L2: GPU pool "
+                    f"{w.gpu_slots * w.n_groups * w.layers_per_group * w.row_bytes / 1e9:.1f} GB, "
+                    "rows gathered at random slots")
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        cb = run_oracle(args.workload, args.warmup, steps=args.steps)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "rows/s",
+                "n_gpus": args.gpus, "steps": cb["steps"], "warmup": args.warmup,
+                "ms_per_step": round(cb["seconds"] / max(1, cb["steps"]) * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+                "data": "synthetic", "config": config, "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    r = run_gpu(args, rank, world, local)
+    if rank == 0:
+        value = r["rows"] / (r["value_ms"] / 1e3)
+        line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(r["value_ms"] / args.steps, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+                "data": "synthetic (seeded trace; rows are seeded random bytes)",
+                "config": config, "roofline": r["roofline"], "host_link": r["host_link"],
+                "gpu_launches": r["launches"], "clocks": r["clocks"],
+                "phases_ms_per_step": r["phases"],
+                "pblru_hit_rate": r["stats"]["hits"] / max(1, r["stats"]["uniq"])}
+        if r["e2e"] is not None:
+            line["e2e"] = r["e2e"]
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = run_oracle(args.workload, 2, seconds=args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -217,6 +217,33 @@ int ula_debug_export(ula_ctx *ctx, uint32_t group, ula_debug_state *st);
  * (host-side fault injection for tests of the error path; no GPU fault). */
 int ula_debug_inject(ula_ctx *ctx, int code);
 
+/* ------------------------------------------------------------ profiling
+ * Kernel launches are counted per phase always.  When enabled, every phase
+ * instance is bracketed by two CUDA events recorded on the stream it is launched
+ * on (the gather: once per layer, on the caller's or the side stream), and
+ * ula_profile_read sums their durations.  Reading synchronises the context.
+ */
+enum {
+  ULA_PHASE_DEDUP = 0,    /* dedup, translate, capacity check */
+  ULA_PHASE_ROTATE_MARK,  /* ring rotation, hit marking, CSR / entry rows */
+  ULA_PHASE_SELECT,       /* victim (or free-slot) selection */
+  ULA_PHASE_MOVE,         /* write-back, fill, map commit */
+  ULA_PHASE_GATHER,       /* one layer's row gather */
+  ULA_PHASE_ALLOC,        /* alloc placement and copy-in */
+  ULA_PHASE_FREE,         /* free */
+  ULA_PHASE_COUNT
+};
+
+typedef struct ula_profile {
+  uint64_t kernels[ULA_PHASE_COUNT]; /* kernel launches */
+  uint64_t timed[ULA_PHASE_COUNT];   /* phase instances timed (profiling enabled) */
+  double ms[ULA_PHASE_COUNT];        /* summed event-timed durations, milliseconds */
+} ula_profile;
+
+int ula_profile_enable(ula_ctx *ctx, int on);
+/* Copies the accumulated profile into *out (may be NULL) and, if reset != 0, zeroes it. */
+int ula_profile_read(ula_ctx *ctx, ula_profile *out, int reset);
+
 #ifdef __cplusplus
 }
 #endif

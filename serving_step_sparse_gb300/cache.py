@@ -60,7 +60,12 @@ class UlaCache:
         R, Q, K = sel.shape
         cap = out.shape[1]
         s = stream if stream is not None else self.stream
-        ev = [e.cuda_event for e in layer_ready] if layer_ready else None
+        ev = None
+        if layer_ready:
+            for e in layer_ready:  # torch creates the CUDA event on first record
+                if not e.cuda_event:
+                    e.record(s)
+            ev = [e.cuda_event for e in layer_ready]
         ula.ula_step_group(self.ctx, g, _u32(sel), R, Q, K, out.data_ptr(), cap,
                            _u32(entry_row), _u32(req_off), ev, s.cuda_stream)
 

@@ -57,6 +57,17 @@ struct ula_ctx {
   int poisoned = 0;
   int inject = 0;
   std::vector<void *> allocations;
+  // profiling: launch counts always; event pairs per phase instance when enabled
+  struct Timed {
+    int phase;
+    cudaEvent_t a, b;
+  };
+  bool prof_on = false;
+  std::vector<Timed> prof_pending;
+  std::vector<cudaEvent_t> prof_spare;
+  uint64_t prof_kernels[ULA_PHASE_COUNT] = {};
+  uint64_t prof_timed[ULA_PHASE_COUNT] = {};
+  double prof_ms[ULA_PHASE_COUNT] = {};
 
   int fail(cudaError_t e) {
     (void)e;
@@ -89,6 +100,37 @@ struct ula_ctx {
     last_stream = s;
     have_last = true;
     return cudaEventRecord(last_evt, s);
+  }
+
+  cudaError_t take_event(cudaEvent_t *e) {
+    if (!prof_spare.empty()) {
+      *e = prof_spare.back();
+      prof_spare.pop_back();
+      return cudaSuccess;
+    }
+    return cudaEventCreate(e);
+  }
+
+  // Runs `launch` (which enqueues `kernels` kernels of `phase` on `s`), bracketed
+  // by timing events on `s` when profiling is on.
+  template <typename F>
+  cudaError_t phase(int ph, cudaStream_t s, uint64_t kernels, F &&launch) {
+    Timed t{ph, nullptr, nullptr};
+    if (prof_on) {
+      cudaError_t e = take_event(&t.a);
+      if (e == cudaSuccess) e = take_event(&t.b);
+      if (e == cudaSuccess) e = cudaEventRecord(t.a, s);
+      if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = launch();
+    if (e != cudaSuccess) return e;
+    prof_kernels[ph] += kernels;
+    if (prof_on) {
+      e = cudaEventRecord(t.b, s);
+      if (e != cudaSuccess) return e;
+      prof_pending.push_back(t);
+    }
+    return cudaSuccess;
   }
 
   cudaError_t ensure_device() {
@@ -149,6 +191,11 @@ void destroy_resources(ula_ctx *c) {
   if (c->commit_evt) cudaEventDestroy(c->commit_evt);
   for (uint32_t g = 0; g < ULA_MAX_GROUPS; ++g)
     if (c->side_evt[g]) cudaEventDestroy(c->side_evt[g]);
+  for (auto &t : c->prof_pending) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (cudaEvent_t e : c->prof_spare) cudaEventDestroy(e);
 }
 
 int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
@@ -315,7 +362,7 @@ int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) 
     sp.quota = m;
     sp.is_step = 0;
     sp.status = c->status;
-    ULA_CUDA(launch_select(sp, cfg.n_groups, s));
+    ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 3, [&] { return launch_select(sp, cfg.n_groups, s); }));
     AllocParams ap{};
     ap.geo = c->geo;
     ap.groups = c->groups_d;
@@ -330,7 +377,8 @@ int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) 
     ap.base = base + off;
     ap.n = m;
     ap.status = c->status;
-    ULA_CUDA(launch_alloc_place(ap, cfg.n_groups, c->sm_count, s));
+    ULA_CUDA(c->phase(ULA_PHASE_ALLOC, s, 1,
+                      [&] { return launch_alloc_place(ap, cfg.n_groups, c->sm_count, s); }));
   }
   ULA_CUDA(c->mark_done(s));
   for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 1;
@@ -357,7 +405,7 @@ int ula_free(ula_ctx *c, uint32_t base, uint32_t n) {
   fp.base = base;
   fp.n = n;
   fp.status = c->status;
-  ULA_CUDA(launch_free(fp, c->cfg.n_groups, s));
+  ULA_CUDA(c->phase(ULA_PHASE_FREE, s, 1, [&] { return launch_free(fp, c->cfg.n_groups, s); }));
   ULA_CUDA(c->mark_done(s));
   for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 0;
   c->live_count -= n;
@@ -409,10 +457,12 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.miss_list = c->miss_list;
   p.status = c->status;
   c->inject = 0;
+  const uint64_t entry_kernels = E ? 3 : 1;
   // (1)(2) dedup + translate + capacity check
-  ULA_CUDA(launch_dedup(p, s));
+  ULA_CUDA(c->phase(ULA_PHASE_DEDUP, s, entry_kernels, [&] { return launch_dedup(p, s); }));
   // (3) rotate, hits into the current bucket; CSR and entry rows
-  ULA_CUDA(launch_rotate_mark(p, s));
+  ULA_CUDA(c->phase(ULA_PHASE_ROTATE_MARK, s, entry_kernels,
+                    [&] { return launch_rotate_mark(p, s); }));
   // (4) victims: free, cold, ring oldest (cur+1) .. newest (cur-1); never cur
   SelectParams sp{};
   sp.geo = c->geo;
@@ -425,7 +475,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   sp.quota = 0xffffffffu;
   sp.is_step = 1;
   sp.status = c->status;
-  ULA_CUDA(launch_select(sp, 1, s));
+  ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 3, [&] { return launch_select(sp, 1, s); }));
   // (5) write-back, fill, then map commit
   MoveParams mp{};
   mp.geo = c->geo;
@@ -434,7 +484,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   mp.round = r;
   mp.cur = cur;
   mp.status = c->status;
-  ULA_CUDA(launch_move(mp, c->sm_count, s));
+  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, 1, [&] { return launch_move(mp, c->sm_count, s); }));
   // signal: the commit event; every gather is ordered after it
   ULA_CUDA(cudaEventRecord(c->commit_evt, s));
   // (6) gather: layer 0 now, later layers on the side stream
@@ -445,14 +495,17 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   gp.out_cap = out_cap_rows;
   gp.status = c->status;
   gp.layer = 0;
-  if (out_cap_rows) ULA_CUDA(launch_gather(gp, c->sm_count, s));
+  if (out_cap_rows)
+    ULA_CUDA(c->phase(ULA_PHASE_GATHER, s, 1, [&] { return launch_gather(gp, c->sm_count, s); }));
   if (layer_ready && layer_ready[0])
     ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[0]), s));
   if (gd.layers > 1) {
     ULA_CUDA(cudaStreamWaitEvent(c->side, c->commit_evt, 0));
     for (uint32_t j = 1; j < gd.layers; ++j) {
       gp.layer = j;
-      if (out_cap_rows) ULA_CUDA(launch_gather(gp, c->sm_count, c->side));
+      if (out_cap_rows)
+        ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, 1,
+                          [&] { return launch_gather(gp, c->sm_count, c->side); }));
       if (layer_ready && layer_ready[j])
         ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), c->side));
     }
@@ -564,6 +617,42 @@ int ula_debug_export(ula_ctx *c, uint32_t group, ula_debug_state *st) {
   st->hits = cnt.hits;
   st->victims_free = cnt.F;
   st->writebacks = cnt.K;
+  return ULA_OK;
+}
+
+int ula_profile_enable(ula_ctx *c, int on) {
+  if (!c) return ULA_ERR_INVALID_ARG;
+  c->prof_on = on != 0;
+  return ULA_OK;
+}
+
+int ula_profile_read(ula_ctx *c, ula_profile *out, int reset) {
+  if (!c) return ULA_ERR_INVALID_ARG;
+  int rc = sync_impl(c);
+  if (rc) return rc;
+  for (auto &t : c->prof_pending) {
+    float ms = 0.f;
+    ULA_CUDA(cudaEventElapsedTime(&ms, t.a, t.b));
+    c->prof_ms[t.phase] += ms;
+    c->prof_timed[t.phase] += 1;
+    c->prof_spare.push_back(t.a);
+    c->prof_spare.push_back(t.b);
+  }
+  c->prof_pending.clear();
+  if (out) {
+    for (int i = 0; i < ULA_PHASE_COUNT; ++i) {
+      out->kernels[i] = c->prof_kernels[i];
+      out->timed[i] = c->prof_timed[i];
+      out->ms[i] = c->prof_ms[i];
+    }
+  }
+  if (reset) {
+    for (int i = 0; i < ULA_PHASE_COUNT; ++i) {
+      c->prof_kernels[i] = 0;
+      c->prof_timed[i] = 0;
+      c->prof_ms[i] = 0.0;
+    }
+  }
   return ULA_OK;
 }
 

@@ -28,8 +28,7 @@ ERR_TIMEOUT = 5
 ERR_POISONED = 6
 ERR_INTERNAL = 7
 
-EXPORTED = ["ula_create", "ula_alloc", "ula_free", "ula_step_group", "ula_sync", "ula_destroy",
-            "ula_error_string", "ula_debug_layout_get", "ula_debug_export", "ula_debug_inject"]
+PHASES = ["dedup", "rotate_mark", "select", "move", "gather", "alloc", "free"]
 
 
 class ula_config(C.Structure):
@@ -61,6 +60,15 @@ class ula_debug_state(C.Structure):
                                     "victims_free", "writebacks")]
 
 
+class ula_profile(C.Structure):
+    _fields_ = [("kernels", C.c_uint64 * len(PHASES)), ("timed", C.c_uint64 * len(PHASES)),
+                ("ms", C.c_double * len(PHASES))]
+
+    def as_dict(self):
+        return {p: {"kernels": int(self.kernels[i]), "timed": int(self.timed[i]),
+                    "ms": float(self.ms[i])} for i, p in enumerate(PHASES)}
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"CUDA library not built: {LIB_PATH} (run __graft_entry__.build())")
@@ -86,6 +94,10 @@ def _load():
     lib.ula_debug_export.restype = i32
     lib.ula_debug_inject.argtypes = [p, i32]
     lib.ula_debug_inject.restype = i32
+    lib.ula_profile_enable.argtypes = [p, i32]
+    lib.ula_profile_enable.restype = i32
+    lib.ula_profile_read.argtypes = [p, C.POINTER(ula_profile), i32]
+    lib.ula_profile_read.restype = i32
     return lib
 
 
@@ -177,3 +189,13 @@ def ula_debug_export(ctx: int, group: int, st: ula_debug_state) -> ula_debug_sta
 
 def ula_debug_inject(ctx: int, code: int) -> None:
     _check(lib.ula_debug_inject(ctx, code), "ula_debug_inject")
+
+
+def ula_profile_enable(ctx: int, on: bool) -> None:
+    _check(lib.ula_profile_enable(ctx, 1 if on else 0), "ula_profile_enable")
+
+
+def ula_profile_read(ctx: int, reset: bool = False) -> dict:
+    pr = ula_profile()
+    _check(lib.ula_profile_read(ctx, C.byref(pr), 1 if reset else 0), "ula_profile_read")
+    return pr.as_dict()

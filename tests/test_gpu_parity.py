@@ -104,7 +104,8 @@ def test_parity_full_size_sampled(name, steps):
 def test_pads_and_ragged_sizes():
     # ragged: S, H not multiples of 32 or 1,024; E not a multiple of the block size
     w = WORKLOADS["cfg0"].replace(pad_prob=0.1, gpu_slots_explicit=1000 + 7,
-                                  host_slots_explicit=3000 + 13, k=250, window=50, steps=32)
+                                  host_slots_explicit=3400 + 13, k=250, window=50, steps=32)
+    assert w.gpu_slots + w.host_slots >= w.max_live_history + w.entries_per_step
     run_parity(w, w.steps)
 
 
