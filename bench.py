@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="run the workload's recipe with fewer live requests (profiling cases)")
     return ap.parse_args(argv)
 
 
@@ -226,7 +228,7 @@ def run_gpu(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = workload_for(args)
     G, L, W, R, Q, K = (w.n_groups, w.layers_per_group, w.row_bytes, w.n_live, w.q, w.k)
     E = w.entries_per_step
     stream = torch.cuda.current_stream(dev)
@@ -274,10 +276,12 @@ def run_gpu(args, rank, world, local):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     e0.record(stream)
     for t in range(args.warmup, args.warmup + n_value):
         do_step(sel_dev[t], steps[t][1], rows_dev[t])
     e1.record(stream)
+    torch.cuda.nvtx.range_pop()
     st1 = cache.sync()
     torch.cuda.synchronize()
     if world > 1:
@@ -451,11 +455,19 @@ def run_oracle(name, warmup, steps=None, seconds=None):
 
 # -------------------------------------------------------------------- main
 
+def workload_for(args):
+    from synth.configs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.requests is not None and args.requests != w.n_live:
+        w = w.replace(n_live=args.requests, name=f"{w.name}_r{args.requests}",
+                      description=w.description + f" (recipe with {args.requests} requests)")
+    return w
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
-    from synth.configs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = workload_for(args)
     config = dict(w.summary())
     config["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
     config["l2"] = ("inputs larger than L2: GPU pool "
