@@ -94,7 +94,8 @@ typedef struct ula_stats {
  *                16-byte aligned, owned by the caller, borrowed until ula_destroy.
  *   host_pools : host array [G] of pinned host pointers (cudaHostAlloc / pinned tensors);
  *                pool g is [H][L_g][row_bytes]; may be NULL when H == 0.  Borrowed.
- *   stream     : the context's home stream (alloc/free run there); NULL = legacy stream.
+ *   stream     : the context's home stream: alloc/free are ordered after the work already
+ *                on it, and it waits for them; NULL = legacy stream.
  *   out        : receives the context.
  * The library allocates its metadata (map, slot stamps, bitmaps, scratch) with
  * cudaMalloc here and frees it in ula_destroy; it creates one side stream.
@@ -140,14 +141,18 @@ int ula_free(ula_ctx *ctx, uint32_t logical_base, uint32_t n);
  *       to the j-th lowest free host slot), fill each miss from its host slot, then
  *       update the map (moves complete before the map changes) and signal,
  *   (6) gather out[j][u] = layer j of unique address u, for every layer of the group:
- *       layer 0 on `stream`, layers 1.. on the context's side stream (prefetch).
+ *       layer 0 before the call's work joins `stream`, layers 1.. on the context's
+ *       low-priority side stream (prefetch).
+ * The work runs on the context's internal highest-priority stream, ordered after
+ * everything already enqueued on `stream`; `stream` is made to wait for it (through
+ * layer 0), so work the caller enqueues next on `stream` sees layer 0 and the outputs.
  *   d_sel       : device [n_req][q][k] uint32 logical addresses; ULA_ADDR_PAD = none.
  *   d_out       : device [L_g][out_cap_rows][row_bytes]; rows [0, U) are written.
  *   d_entry_row : device [n_req*q*k] int32: row u of each entry, -1 for pads.
  *   d_req_off   : device [n_req+1] int32: unique rows first seen in request r are
  *                 [req_off[r], req_off[r+1]); req_off[n_req] = U.
  *   layer_ready : host array [L_g] of cudaEvent_t recorded when layer j of d_out is
- *                 ready (layer 0 on `stream`, others on the side stream), or NULL.
+ *                 ready (on the stream that wrote it), or NULL.
  *   stream      : the caller's stream; the step is ordered after every earlier call on
  *                 this context.  Returns without waiting for the device.
  * Device-detected errors (latched, returned by ula_sync, nothing changed by the step):

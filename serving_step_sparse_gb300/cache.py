@@ -13,6 +13,55 @@ import torch
 from . import ula
 
 
+def _thp_bytes() -> int:
+    try:
+        with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
+            return int(f.read().strip())
+    except (OSError, ValueError):
+        return 2 << 20
+
+
+class PinnedHostBuffer:
+    """Page-locked host memory for a host slot pool.
+
+    An anonymous mapping aligned to the transparent-huge-page size, advised
+    MADV_HUGEPAGE and registered with CUDA.  The kernels reach host slots at
+    random over the host link; with base-size pages a pool of tens of GB needs
+    more GPU address translations than stay cached, and random-slot bandwidth
+    falls to about a third.  Huge pages keep the translations in reach.
+    """
+
+    def __init__(self, nbytes: int, huge: bool = True):
+        import mmap
+        self.nbytes = int(nbytes)
+        align = _thp_bytes() if huge else mmap.PAGESIZE
+        self._mm = mmap.mmap(-1, self.nbytes + align,
+                             flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        if huge and hasattr(mmap, "MADV_HUGEPAGE"):
+            self._mm.madvise(mmap.MADV_HUGEPAGE)
+        whole = torch.frombuffer(self._mm, dtype=torch.uint8)
+        off = (-whole.data_ptr()) % align
+        self.tensor = whole[off:off + self.nbytes]
+        del whole
+        rt = torch.cuda.cudart()
+        rc = rt.cudaHostRegister(self.tensor.data_ptr(), self.nbytes, 0)
+        if getattr(rc, "value", rc) != 0:
+            raise RuntimeError(f"cudaHostRegister failed: {rc}")
+        self._registered = True
+
+    def close(self):
+        if getattr(self, "_registered", False):
+            torch.cuda.cudart().cudaHostUnregister(self.tensor.data_ptr())
+            self._registered = False
+        self.tensor = None
+        mm, self._mm = getattr(self, "_mm", None), None
+        if mm is not None:
+            try:
+                mm.close()
+            except BufferError:
+                pass
+
+
 def _u32(t: torch.Tensor) -> int:
     assert t.dtype in (torch.int32, torch.uint8) and t.is_contiguous()
     return t.data_ptr()
@@ -23,7 +72,7 @@ class UlaCache:
 
     def __init__(self, *, row_bytes: int, layers_per_group, gpu_slots: int, host_slots: int,
                  ring_buckets: int, max_logical: int, max_entries: int, device="cuda",
-                 stream: torch.cuda.Stream | None = None):
+                 stream: torch.cuda.Stream | None = None, huge_host_pages: bool = True):
         self.device = torch.device(device)
         self.W = int(row_bytes)
         self.layers = [int(x) for x in layers_per_group]
@@ -33,8 +82,9 @@ class UlaCache:
         self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
         self.gpu_pools = [torch.empty(self.S * L * self.W, dtype=torch.uint8, device=self.device)
                           for L in self.layers]
-        self.host_pools = ([torch.empty(self.H * L * self.W, dtype=torch.uint8, pin_memory=True)
-                            for L in self.layers] if self.H else None)
+        self._host_bufs = ([PinnedHostBuffer(self.H * L * self.W, huge_host_pages)
+                            for L in self.layers] if self.H else [])
+        self.host_pools = [b.tensor for b in self._host_bufs] if self.H else None
         cfg = ula.make_config(self.W, self.layers, self.S, self.H, self.B, self.max_logical,
                               self.max_entries)
         with torch.cuda.device(self.device):
@@ -76,6 +126,10 @@ class UlaCache:
         if getattr(self, "ctx", None):
             ula.ula_destroy(self.ctx)
             self.ctx = None
+        self.host_pools = None
+        for b in getattr(self, "_host_bufs", []):
+            b.close()
+        self._host_bufs = []
 
     def __del__(self):
         try:

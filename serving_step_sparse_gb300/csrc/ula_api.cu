@@ -34,9 +34,11 @@ struct ula_ctx {
   ula_config cfg{};
   int device = 0;
   int sm_count = 0;
-  cudaStream_t home = nullptr, side = nullptr, last_stream = nullptr;
-  bool have_last = false;
-  cudaEvent_t last_evt = nullptr, commit_evt = nullptr;
+  cudaStream_t home = nullptr;  // the caller's stream given at create (alloc/free order)
+  cudaStream_t crit = nullptr;  // internal, highest priority: the step's critical path
+  cudaStream_t side = nullptr;  // internal, lowest priority: later-layer gathers
+  cudaEvent_t in_evt = nullptr, out_evt = nullptr, commit_evt = nullptr;
+  int move_blocks = 0, gather_blocks = 0;  // persistent grids (resident blocks)
   cudaEvent_t side_evt[ULA_MAX_GROUPS] = {};
   bool side_pending[ULA_MAX_GROUPS] = {};
   Geometry geo{};
@@ -84,10 +86,16 @@ struct ula_ctx {
     return e;
   }
 
-  // make `s` wait for the previous call on this context
-  cudaError_t order_after_previous(cudaStream_t s) {
-    if (have_last && last_stream != s) return cudaStreamWaitEvent(s, last_evt, 0);
-    return cudaSuccess;
+  // the call's work on `crit` starts after everything already on the caller's stream
+  cudaError_t enter(cudaStream_t caller) {
+    cudaError_t e = cudaEventRecord(in_evt, caller);
+    return e != cudaSuccess ? e : cudaStreamWaitEvent(crit, in_evt, 0);
+  }
+
+  // the caller's stream continues after the call's work on `crit`
+  cudaError_t leave(cudaStream_t caller) {
+    cudaError_t e = cudaEventRecord(out_evt, crit);
+    return e != cudaSuccess ? e : cudaStreamWaitEvent(caller, out_evt, 0);
   }
 
   cudaError_t wait_side(cudaStream_t s, uint32_t g) {
@@ -96,11 +104,6 @@ struct ula_ctx {
     return cudaStreamWaitEvent(s, side_evt[g], 0);
   }
 
-  cudaError_t mark_done(cudaStream_t s) {
-    last_stream = s;
-    have_last = true;
-    return cudaEventRecord(last_evt, s);
-  }
 
   cudaError_t take_event(cudaEvent_t *e) {
     if (!prof_spare.empty()) {
@@ -187,7 +190,9 @@ void destroy_resources(ula_ctx *c) {
   for (void *p : c->allocations) cudaFree(p);
   c->allocations.clear();
   if (c->side) cudaStreamDestroy(c->side);
-  if (c->last_evt) cudaEventDestroy(c->last_evt);
+  if (c->crit) cudaStreamDestroy(c->crit);
+  if (c->in_evt) cudaEventDestroy(c->in_evt);
+  if (c->out_evt) cudaEventDestroy(c->out_evt);
   if (c->commit_evt) cudaEventDestroy(c->commit_evt);
   for (uint32_t g = 0; g < ULA_MAX_GROUPS; ++g)
     if (c->side_evt[g]) cudaEventDestroy(c->side_evt[g]);
@@ -231,9 +236,16 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
     }
   }
 
-  ULA_CUDA(cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking));
-  ULA_CUDA(cudaEventCreateWithFlags(&c->last_evt, cudaEventDisableTiming));
+  int prio_least = 0, prio_greatest = 0;
+  ULA_CUDA(cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest));
+  ULA_CUDA(cudaStreamCreateWithPriority(&c->crit, cudaStreamNonBlocking, prio_greatest));
+  ULA_CUDA(cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, prio_least));
+  ULA_CUDA(cudaEventCreateWithFlags(&c->in_evt, cudaEventDisableTiming));
+  ULA_CUDA(cudaEventCreateWithFlags(&c->out_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->commit_evt, cudaEventDisableTiming));
+  ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks));
+  c->move_blocks *= c->sm_count;
+  c->gather_blocks *= c->sm_count;
   for (uint32_t g = 0; g < G; ++g)
     ULA_CUDA(cudaEventCreateWithFlags(&c->side_evt[g], cudaEventDisableTiming));
 
@@ -346,8 +358,8 @@ int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) 
   const uint8_t *rows_d =
       static_cast<const uint8_t *>(device_address(rows, c->device, true, true));
   if (!rows_d || !aligned16(rows_d)) return ULA_ERR_INVALID_ARG;
-  cudaStream_t s = c->home;
-  ULA_CUDA(c->order_after_previous(s));
+  cudaStream_t s = c->crit;
+  ULA_CUDA(c->enter(c->home));
   for (uint32_t g = 0; g < cfg.n_groups; ++g) ULA_CUDA(c->wait_side(s, g));
 
   const uint32_t base = c->next_logical;
@@ -378,9 +390,9 @@ int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) 
     ap.n = m;
     ap.status = c->status;
     ULA_CUDA(c->phase(ULA_PHASE_ALLOC, s, 1,
-                      [&] { return launch_alloc_place(ap, cfg.n_groups, c->sm_count, s); }));
+                      [&] { return launch_alloc_place(ap, cfg.n_groups, c->move_blocks, s); }));
   }
-  ULA_CUDA(c->mark_done(s));
+  ULA_CUDA(c->leave(c->home));
   for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 1;
   c->live_count += n;
   c->next_logical = base + n;
@@ -395,8 +407,8 @@ int ula_free(ula_ctx *c, uint32_t base, uint32_t n) {
     if (!c->live[base + i]) return ULA_ERR_INVALID_ARG;
   if (n == 0) return ULA_OK;
   ULA_CUDA(c->ensure_device());
-  cudaStream_t s = c->home;
-  ULA_CUDA(c->order_after_previous(s));
+  cudaStream_t s = c->crit;
+  ULA_CUDA(c->enter(c->home));
   for (uint32_t g = 0; g < c->cfg.n_groups; ++g) ULA_CUDA(c->wait_side(s, g));
   FreeParams fp{};
   fp.geo = c->geo;
@@ -406,7 +418,7 @@ int ula_free(ula_ctx *c, uint32_t base, uint32_t n) {
   fp.n = n;
   fp.status = c->status;
   ULA_CUDA(c->phase(ULA_PHASE_FREE, s, 1, [&] { return launch_free(fp, c->cfg.n_groups, s); }));
-  ULA_CUDA(c->mark_done(s));
+  ULA_CUDA(c->leave(c->home));
   for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 0;
   c->live_count -= n;
   return ULA_OK;
@@ -425,8 +437,9 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
     return ULA_ERR_INVALID_ARG;
   if (d_out && !aligned16(d_out)) return ULA_ERR_INVALID_ARG;
   ULA_CUDA(c->ensure_device());
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  ULA_CUDA(c->order_after_previous(s));
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  cudaStream_t s = c->crit;
+  ULA_CUDA(c->enter(caller));
   ULA_CUDA(c->wait_side(s, group));
 
   if (++c->epoch == 0) {  // dedup stamps wrap: clear them
@@ -484,7 +497,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   mp.round = r;
   mp.cur = cur;
   mp.status = c->status;
-  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, 1, [&] { return launch_move(mp, c->sm_count, s); }));
+  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, 1, [&] { return launch_move(mp, c->move_blocks, s); }));
   // signal: the commit event; every gather is ordered after it
   ULA_CUDA(cudaEventRecord(c->commit_evt, s));
   // (6) gather: layer 0 now, later layers on the side stream
@@ -496,7 +509,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   gp.status = c->status;
   gp.layer = 0;
   if (out_cap_rows)
-    ULA_CUDA(c->phase(ULA_PHASE_GATHER, s, 1, [&] { return launch_gather(gp, c->sm_count, s); }));
+    ULA_CUDA(c->phase(ULA_PHASE_GATHER, s, 1, [&] { return launch_gather(gp, c->gather_blocks, s); }));
   if (layer_ready && layer_ready[0])
     ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[0]), s));
   if (gd.layers > 1) {
@@ -505,14 +518,14 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
       gp.layer = j;
       if (out_cap_rows)
         ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, 1,
-                          [&] { return launch_gather(gp, c->sm_count, c->side); }));
+                          [&] { return launch_gather(gp, c->gather_blocks, c->side); }));
       if (layer_ready && layer_ready[j])
         ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), c->side));
     }
     ULA_CUDA(cudaEventRecord(c->side_evt[group], c->side));
     c->side_pending[group] = true;
   }
-  ULA_CUDA(c->mark_done(s));
+  ULA_CUDA(c->leave(caller));
   return ULA_OK;
 }
 
@@ -523,7 +536,7 @@ static int sync_impl(ula_ctx *c) {
       ULA_CUDA(cudaEventSynchronize(c->side_evt[g]));
       c->side_pending[g] = false;
     }
-  if (c->have_last) ULA_CUDA(cudaEventSynchronize(c->last_evt));
+  ULA_CUDA(cudaStreamSynchronize(c->crit));
   ULA_CUDA(cudaStreamSynchronize(c->home));
   return ULA_OK;
 }

@@ -171,10 +171,12 @@ cudaError_t launch_bitmap_fill(Bitmap b, uint32_t nbits, cudaStream_t s);
 cudaError_t launch_dedup(const StepParams &p, cudaStream_t s);        // stamp, count, scan
 cudaError_t launch_rotate_mark(const StepParams &p, cudaStream_t s);  // rotate, emit+mark, rows
 cudaError_t launch_select(const SelectParams &p, uint32_t n_groups, cudaStream_t s);
-cudaError_t launch_move(const MoveParams &p, int sm_count, cudaStream_t s);
-cudaError_t launch_gather(const GatherParams &p, int sm_count, cudaStream_t s);
-cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int sm_count,
+cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s);
+cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
+cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s);
+// resident 256-thread blocks per SM of the persistent kernels
+cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm);
 cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);
 
 }  // namespace ula

@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(1024) k_select_emit(SelectParams p) {
 // of the same chunk.  Host memory is reached directly over the host link.
 constexpr int kMoveUnroll = 6;
 
-__global__ void __launch_bounds__(256) k_move_commit(MoveParams p) {
+__global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -550,12 +550,14 @@ __global__ void __launch_bounds__(256) k_move_commit(MoveParams p) {
 // ------------------------------------------------------------------ gather
 //
 // (6) out[layer][u] = layer `layer` of the slot the committed map gives for
-// uniq[u].  A warp takes a tile of 32 rows: lanes resolve the 32 slots, then
-// the warp streams the tile's 32 x (W/16) 16-byte chunks, consecutive lanes on
-// consecutive chunks (coalesced within each row, rows written contiguously).
+// uniq[u].  The U rows are spread over all warps (rows_per_warp = ceil(U /
+// warps), at most 32): lanes resolve the warp's slots through the map, then the
+// warp streams the rows' 16-byte chunks, consecutive lanes on consecutive chunks
+// (coalesced within a row; the warp's output rows are contiguous).  Loads are
+// issued kGatherUnroll deep before the stores.
 constexpr int kGatherUnroll = 8;
 
-__global__ void __launch_bounds__(256) k_gather(GatherParams p) {
+__global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -567,10 +569,11 @@ __global__ void __launch_bounds__(256) k_gather(GatherParams p) {
   const size_t sbv = (size_t)g.layers * CW;  // slot stride in uint4
   const uint4 *pool = reinterpret_cast<const uint4 *>(g.gpu_pool) + (size_t)p.layer * CW;
   uint4 *out = reinterpret_cast<uint4 *>(p.out) + (size_t)p.layer * p.out_cap * CW;
-  const uint32_t tiles = (U + 31) / 32;
-  for (uint32_t t = warp; t < tiles; t += nwarps) {
-    const uint32_t row0 = t * 32;
-    const uint32_t nrows = min(32u, U - row0);
+  uint32_t rpw = (U + nwarps - 1) / nwarps;
+  rpw = rpw < 1 ? 1 : (rpw > 32 ? 32 : rpw);
+  const uint32_t r0 = lane / CW, c0 = lane % CW;  // chunk (row, col) of f = lane
+  for (uint32_t row0 = warp * rpw; row0 < U; row0 += nwarps * rpw) {
+    const uint32_t nrows = min(rpw, U - row0);
     uint32_t slot = 0;
     bool bad = false;
     if (lane < nrows) {
@@ -583,26 +586,32 @@ __global__ void __launch_bounds__(256) k_gather(GatherParams p) {
       continue;
     }
     const uint32_t total = nrows * CW;
-    uint32_t r = lane / CW, c = lane % CW;  // chunk (r, c) of f = lane
     uint4 *orow = out + (size_t)row0 * CW;
+    uint32_t r = r0, c = c0;
     for (uint32_t f0 = 0; f0 < total; f0 += 32 * kGatherUnroll) {
       uint4 v[kGatherUnroll];
-      uint32_t rr[kGatherUnroll], cc[kGatherUnroll];
+      const uint32_t rs = r, cs = c;
 #pragma unroll
       for (int u = 0; u < kGatherUnroll; ++u) {
-        rr[u] = r;
-        cc[u] = c;
         const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
-        if (f0 + u * 32 + lane < total) v[u] = __ldg(pool + (size_t)s * sbv + c);
+        if (f0 + u * 32 + lane < total) v[u] = __ldcs(pool + (size_t)s * sbv + c);
         c += 32;
         while (c >= CW) {
           c -= CW;
           ++r;
         }
       }
+      r = rs;
+      c = cs;
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u)
-        if (f0 + u * 32 + lane < total) orow[(size_t)rr[u] * CW + cc[u]] = v[u];
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        if (f0 + u * 32 + lane < total) orow[(size_t)r * CW + c] = v[u];
+        c += 32;
+        while (c >= CW) {
+          c -= CW;
+          ++r;
+        }
+      }
     }
   }
 }
@@ -733,20 +742,26 @@ cudaError_t launch_select(const SelectParams &p, uint32_t n_groups, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_move(const MoveParams &p, int sm_count, cudaStream_t s) {
-  k_move_commit<<<sm_count * 8, 256, 0, s>>>(p);
+cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm) {
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move_commit, 256, 0);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather, 256, 0);
+}
+
+cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
+  k_move_commit<<<blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const GatherParams &p, int sm_count, cudaStream_t s) {
-  k_gather<<<sm_count * 8, 256, 0, s>>>(p);
+cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s) {
+  k_gather<<<blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int sm_count,
+cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s) {
   uint32_t blocks = div_up((uint64_t)p.n * 32, 256);
-  const uint32_t cap = (uint32_t)sm_count * 8;
+  const uint32_t cap = (uint32_t)max_blocks;
   if (blocks > cap) blocks = cap;
   dim3 grid(blocks ? blocks : 1, n_groups);
   k_alloc_place<<<grid, 256, 0, s>>>(p);
