@@ -1,0 +1,61 @@
+"""Replica aggregation of the benchmark (N > 1): world_size-2 gloo ranks on CPU.
+
+The path has no exchange step (DP ranks are independent replicas), so the only
+collectives are the timing barrier and the MAX-of-times / SUM-of-work reduction
+that turns per-rank results into the whole-job value.
+"""
+from __future__ import annotations
+
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    r, w, l = bench.dist_env()
+    assert (r, w, l) == (rank, world, rank)
+    dist.barrier()
+    out = bench.aggregate({"rows": 1000.0 * (rank + 1), "value_ms": 10.0 + 5 * rank,
+                           "e2e_ms": 3.0 - rank}, world, torch.device("cpu"))
+    q.put((rank, out))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2])
+def test_replica_aggregation_gloo(world):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for r in range(world):
+        assert res[r]["rows"] == 3000.0          # SUM of work over replicas
+        assert res[r]["value_ms"] == 15.0        # the slowest rank's time
+        assert res[r]["e2e_ms"] == 3.0
+    # whole-job value = all ranks' rows / the slowest time
+    assert res[0]["rows"] / (res[0]["value_ms"] / 1e3) == pytest.approx(200000.0)
+
+
+def test_single_rank_aggregation_is_identity():
+    import bench
+    assert bench.aggregate({"rows": 5.0, "value_ms": 2.0}, 1) == {"rows": 5.0, "value_ms": 2.0}
