@@ -249,6 +249,32 @@ int ula_profile_enable(ula_ctx *ctx, int on);
 /* Copies the accumulated profile into *out (may be NULL) and, if reset != 0, zeroes it. */
 int ula_profile_read(ula_ctx *ctx, ula_profile *out, int reset);
 
+/* ------------------------------------------------------------ no-allocation dedup
+ * The pages have no counterpart for this entry point; it serves callers that must
+ * not allocate device memory where they dedup: an engine that reserved nearly all
+ * HBM for its KV pools at start-up (a cudaMalloc would fail or fragment the pool),
+ * or a latency-critical path that cannot take cudaMalloc's implicit device
+ * synchronisation.  It computes the same dedup as ula_step_group's first step,
+ * without a context and without allocating: its scratch is a fixed array of about
+ * 1.3 MB inside this library, resident on every device that loads the library
+ * until the process exits.
+ *   d_sel       : device [n] uint32 addresses; ULA_ADDR_PAD entries select nothing.
+ *   d_uniq      : device [n] out: distinct addresses in order of first occurrence.
+ *   d_entry_row : device [n] out: index into d_uniq of each entry's address, -1 for pads.
+ *   d_n_uniq    : device [1] out: number of distinct addresses.
+ *   stream      : cudaStream_t (void*); the call is asynchronous on it.
+ * n above ULA_NOALLOC_MAX_ENTRIES returns ULA_ERR_CAPACITY; NULL buffers return
+ * ULA_ERR_INVALID_ARG (nothing is launched in either case).  The first call on a
+ * device looks up the scratch array's device address (with that device current);
+ * make that first call before any stream capture.  Every call on a device uses the
+ * same scratch and clears what it needs first, so calls that overlap on the GPU
+ * (on different streams, or from different host threads) race and must not be
+ * issued; calls on one stream are ordered and safe.
+ */
+#define ULA_NOALLOC_MAX_ENTRIES 65536u
+int ula_dedup_noalloc(const uint32_t *d_sel, uint32_t n, uint32_t *d_uniq,
+                      int32_t *d_entry_row, uint32_t *d_n_uniq, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,6 +29,7 @@ ERR_POISONED = 6
 ERR_INTERNAL = 7
 
 PHASES = ["dedup", "rotate_mark", "select", "move", "gather", "alloc", "free"]
+NOALLOC_MAX_ENTRIES = 65536
 
 
 class ula_config(C.Structure):
@@ -98,6 +99,8 @@ def _load():
     lib.ula_profile_enable.restype = i32
     lib.ula_profile_read.argtypes = [p, C.POINTER(ula_profile), i32]
     lib.ula_profile_read.restype = i32
+    lib.ula_dedup_noalloc.argtypes = [p, u32, p, p, p, p]
+    lib.ula_dedup_noalloc.restype = i32
     return lib
 
 
@@ -199,3 +202,10 @@ def ula_profile_read(ctx: int, reset: bool = False) -> dict:
     pr = ula_profile()
     _check(lib.ula_profile_read(ctx, C.byref(pr), 1 if reset else 0), "ula_profile_read")
     return pr.as_dict()
+
+
+def ula_dedup_noalloc(d_sel: int, n: int, d_uniq: int, d_entry_row: int, d_n_uniq: int,
+                      stream) -> None:
+    """First-occurrence dedup without a context and without allocating (fixed scratch)."""
+    _check(lib.ula_dedup_noalloc(d_sel, n, d_uniq, d_entry_row, d_n_uniq, stream),
+           "ula_dedup_noalloc")
