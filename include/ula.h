@@ -209,6 +209,9 @@ typedef struct ula_debug_state {
   uint32_t *uniq;           /* [max_entries]: last step's unique addresses */
   uint32_t *victims;        /* [decision_cap]: last step's victims (first M) */
   uint32_t *wb_host;        /* [decision_cap]: last step's write-back host slots (first K) */
+  uint32_t *class_seg_count;/* [n_classes][n1]: set bits per 1,024-slot segment */
+  uint32_t *host_seg_count; /* [h1] */
+  uint32_t *row_slot;       /* [max_entries]: GPU slot of each unique row after the commit */
   /* filled always */
   uint32_t round;           /* rounds completed by this group */
   uint32_t cur;             /* current ring bucket = round % B */

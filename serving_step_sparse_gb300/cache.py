@@ -157,6 +157,9 @@ class UlaCache:
             "uniq": np.empty(self.max_entries, np.uint32),
             "victims": np.empty(lay.decision_cap, np.uint32),
             "wb_host": np.empty(lay.decision_cap, np.uint32),
+            "class_seg_count": np.empty((lay.n_classes, lay.n1), np.uint32),
+            "host_seg_count": np.empty(max(lay.h1, 1), np.uint32),
+            "row_slot": np.empty(self.max_entries, np.uint32),
         }
         st = ula.ula_debug_state()
         for k, a in arrs.items():

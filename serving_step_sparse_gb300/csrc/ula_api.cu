@@ -39,6 +39,7 @@ struct ula_ctx {
   cudaStream_t side = nullptr;  // internal, lowest priority: later-layer gathers
   cudaEvent_t in_evt = nullptr, out_evt = nullptr, commit_evt = nullptr;
   int move_blocks = 0, gather_blocks = 0;  // persistent grids (resident blocks)
+  int emit_blocks = 0;
   cudaEvent_t side_evt[ULA_MAX_GROUPS] = {};
   bool side_pending[ULA_MAX_GROUPS] = {};
   Geometry geo{};
@@ -218,9 +219,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   geo.gd = dims_for(S);
   geo.hd = dims_for(H);
   geo.nseg = geo.gd.n1;
-  geo.nsup = geo.gd.n2;
   geo.hseg = geo.hd.n1;
-  geo.hsup = geo.hd.n2;
   c->decision_cap = cfg.max_entries > kAllocChunk ? cfg.max_entries : kAllocChunk;
 
   // pools: caller-owned, borrowed
@@ -246,6 +245,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks));
   c->move_blocks *= c->sm_count;
   c->gather_blocks *= c->sm_count;
+  c->emit_blocks = c->sm_count;
   for (uint32_t g = 0; g < G; ++g)
     ULA_CUDA(cudaEventCreateWithFlags(&c->side_evt[g], cudaEventDisableTiming));
 
@@ -263,7 +263,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(cudaMemsetAsync(c->status, 0, sizeof(int), s));
 
   const uint32_t ncls = B + 2;
-  const size_t seg_len = (size_t)(B + 1) * geo.nseg + geo.hseg;
+  const size_t work_len = (size_t)(B + 1) * geo.nseg + geo.hseg + 1;
   c->groups_h.resize(G);
   std::vector<GroupCounters> cnt_h(G);
   for (uint32_t g = 0; g < G; ++g) {
@@ -278,14 +278,16 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
     ULA_CUDA(c->alloc(&d.cls0, (size_t)ncls * geo.gd.n0));
     ULA_CUDA(c->alloc(&d.cls1, (size_t)ncls * geo.gd.n1));
     ULA_CUDA(c->alloc(&d.cls2, (size_t)ncls * geo.gd.n2));
+    ULA_CUDA(c->alloc(&d.clsc, (size_t)ncls * geo.gd.n1));
     ULA_CUDA(c->alloc(&d.hf0, geo.hd.n0));
     ULA_CUDA(c->alloc(&d.hf1, geo.hd.n1));
     ULA_CUDA(c->alloc(&d.hf2, geo.hd.n2));
+    ULA_CUDA(c->alloc(&d.hfc, geo.hd.n1));
     ULA_CUDA(c->alloc(&d.uniq, cfg.max_entries));
+    ULA_CUDA(c->alloc(&d.row_slot, cfg.max_entries));
     ULA_CUDA(c->alloc(&d.victims, c->decision_cap));
     ULA_CUDA(c->alloc(&d.wb_host, c->decision_cap));
-    ULA_CUDA(c->alloc(&d.seg_count, seg_len));
-    ULA_CUDA(c->alloc(&d.seg_base, seg_len));
+    ULA_CUDA(c->alloc(&d.work, work_len));
     d.cnt = c->cnt_d + g;
     ULA_CUDA(cudaMemsetAsync(d.map, 0xff, sizeof(uint32_t) * cfg.max_logical, s));
     ULA_CUDA(cudaMemsetAsync(d.owner, 0xff, sizeof(uint32_t) * S, s));
@@ -293,6 +295,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
     ULA_CUDA(cudaMemsetAsync(d.cls0, 0, sizeof(uint32_t) * ncls * geo.gd.n0, s));
     ULA_CUDA(cudaMemsetAsync(d.cls1, 0, sizeof(uint32_t) * ncls * geo.gd.n1, s));
     ULA_CUDA(cudaMemsetAsync(d.cls2, 0, sizeof(uint32_t) * ncls * geo.gd.n2, s));
+    ULA_CUDA(cudaMemsetAsync(d.clsc, 0, sizeof(uint32_t) * ncls * geo.gd.n1, s));
     ULA_CUDA(launch_bitmap_fill(class_bitmap(d, geo, B + 1), S, s));  // all slots free
     ULA_CUDA(launch_bitmap_fill(host_free_bitmap(d), H, s));
     std::memset(&cnt_h[g], 0, sizeof(GroupCounters));
@@ -365,16 +368,18 @@ int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) 
   const uint32_t base = c->next_logical;
   for (uint32_t off = 0; off < n; off += kAllocChunk) {
     const uint32_t m = n - off < kAllocChunk ? n - off : kAllocChunk;
-    SelectParams sp{};
+    EmitParams sp{};
     sp.geo = c->geo;
     sp.groups = c->groups_d;
     sp.group0 = 0;
-    sp.n_cls = 1;
-    sp.order[0] = c->geo.B + 1;  // free slots only: alloc never evicts
+    sp.order.n_cls = 1;
+    sp.order.cls[0] = c->geo.B + 1;  // free slots only: alloc never evicts
     sp.quota = m;
-    sp.is_step = 0;
     sp.status = c->status;
-    ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 3, [&] { return launch_select(sp, cfg.n_groups, s); }));
+    ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 2, [&] {
+      cudaError_t e = launch_alloc_select(sp, cfg.n_groups, s);
+      return e != cudaSuccess ? e : launch_select_emit(sp, cfg.n_groups, c->emit_blocks, s);
+    }));
     AllocParams ap{};
     ap.geo = c->geo;
     ap.groups = c->groups_d;
@@ -470,30 +475,33 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.miss_list = c->miss_list;
   p.status = c->status;
   c->inject = 0;
-  const uint64_t entry_kernels = E ? 3 : 1;
+  p.order.n_cls = B + 1;  // victims: free, cold, ring oldest (cur+1) .. newest (cur-1)
+  p.order.cls[0] = B + 1;
+  p.order.cls[1] = B;
+  for (uint32_t d = 1; d < B; ++d) p.order.cls[1 + d] = (cur + d) % B;
   // (1)(2) dedup + translate + capacity check
-  ULA_CUDA(c->phase(ULA_PHASE_DEDUP, s, entry_kernels, [&] { return launch_dedup(p, s); }));
-  // (3) rotate, hits into the current bucket; CSR and entry rows
-  ULA_CUDA(c->phase(ULA_PHASE_ROTATE_MARK, s, entry_kernels,
-                    [&] { return launch_rotate_mark(p, s); }));
-  // (4) victims: free, cold, ring oldest (cur+1) .. newest (cur-1); never cur
-  SelectParams sp{};
-  sp.geo = c->geo;
-  sp.groups = c->groups_d;
-  sp.group0 = group;
-  sp.n_cls = B + 1;
-  sp.order[0] = B + 1;
-  sp.order[1] = B;
-  for (uint32_t d = 1; d < B; ++d) sp.order[1 + d] = (cur + d) % B;
-  sp.quota = 0xffffffffu;
-  sp.is_step = 1;
-  sp.status = c->status;
-  ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 3, [&] { return launch_select(sp, 1, s); }));
+  ULA_CUDA(c->phase(ULA_PHASE_DEDUP, s, E ? 2 : 1, [&] { return launch_dedup(p, s); }));
+  // (3) rotate + compaction; hits into the current bucket, entry rows, victim walk
+  ULA_CUDA(c->phase(ULA_PHASE_ROTATE_MARK, s, 2, [&] {
+    cudaError_t e = launch_rotate_emit(p, s);
+    return e != cudaSuccess ? e : launch_mark_select(p, s);
+  }));
+  // (4) victims' and write-back slots' indices
+  EmitParams ep{};
+  ep.geo = c->geo;
+  ep.groups = c->groups_d;
+  ep.group0 = group;
+  ep.order = p.order;
+  ep.quota = 0xffffffffu;
+  ep.status = c->status;
+  ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
+                    [&] { return launch_select_emit(ep, 1, c->emit_blocks, s); }));
   // (5) write-back, fill, then map commit
   MoveParams mp{};
   mp.geo = c->geo;
   mp.grp = gd;
   mp.miss_list = c->miss_list;
+  mp.addr_row = c->addr_row;
   mp.round = r;
   mp.cur = cur;
   mp.status = c->status;
@@ -616,6 +624,9 @@ int ula_debug_export(ula_ctx *c, uint32_t group, ula_debug_state *st) {
   ULA_CUDA(copy(st->host_free_bits, d.hf0, sizeof(uint32_t) * geo.hd.n0));
   ULA_CUDA(copy(st->host_free_sum1, d.hf1, sizeof(uint32_t) * geo.hd.n1));
   ULA_CUDA(copy(st->host_free_sum2, d.hf2, sizeof(uint32_t) * geo.hd.n2));
+  ULA_CUDA(copy(st->class_seg_count, d.clsc, sizeof(uint32_t) * ncls * geo.gd.n1));
+  ULA_CUDA(copy(st->host_seg_count, d.hfc, sizeof(uint32_t) * geo.hd.n1));
+  ULA_CUDA(copy(st->row_slot, d.row_slot, sizeof(uint32_t) * c->cfg.max_entries));
   ULA_CUDA(copy(st->uniq, d.uniq, sizeof(uint32_t) * c->cfg.max_entries));
   ULA_CUDA(copy(st->victims, d.victims, sizeof(uint32_t) * c->decision_cap));
   ULA_CUDA(copy(st->wb_host, d.wb_host, sizeof(uint32_t) * c->decision_cap));

@@ -16,18 +16,24 @@ constexpr uint32_t kPad = ULA_ADDR_PAD;
 constexpr uint32_t kUnalloc = ULA_MAP_UNALLOCATED;
 constexpr uint32_t kHostBit = ULA_MAP_HOST;
 constexpr uint32_t kSlotMask = 0x7FFFFFFFu;
-constexpr uint32_t kNone = 0xFFFFFFFFu;  // no owner / free stamp
+constexpr uint32_t kNone = 0xFFFFFFFFu;     // no owner / free stamp
+constexpr uint32_t kHostPos = 0xFFFFFFFFu;  // work entry on the host-free bitmap
+constexpr uint32_t kSegBits = 1024;         // slots per segment (one level-1 word)
 
 // A bitmap with two summary levels.  Level 0: one bit per slot.  Level 1: bit
 // i is set iff level-0 word i is nonzero.  Level 2: bit i is set iff level-1
 // word i is nonzero.  A level-1 word covers a "segment" of 1,024 slots, a
-// level-2 word a "superblock" of 32,768 slots.
+// level-2 word a "superblock" of 32,768 slots.  Beside the bitmap, `cnt`
+// holds the number of set bits of every segment, kept exact by the same
+// atomics that flip the bits; victim selection walks these counts in class
+// order and stops as soon as the quota is reached.
 struct Dims {
   uint32_t n0, n1, n2;
 };
 
 struct Bitmap {
   uint32_t *w0, *w1, *w2;
+  uint32_t *cnt;  // [n1] set bits per segment
 };
 
 __host__ __device__ inline Dims dims_for(uint32_t nbits) {
@@ -45,7 +51,9 @@ struct GroupCounters {
   uint32_t U, M, hits; // last step: unique addresses, misses, hits
   uint32_t F;          // last step: victims taken from free slots (alloc: GPU placements)
   uint32_t K;          // last step: write-backs (alloc: host placements)
-  uint32_t pad;
+  uint32_t n_work;     // selection work entries (GPU classes, then host)
+  uint32_t n_work_gpu; // of which on GPU-slot classes
+  uint32_t done[3];    // "last block" tickets of the multi-block kernels
   unsigned long long stat[12];  // ula_stats order
 };
 
@@ -62,14 +70,15 @@ struct GroupDev {
   uint32_t *cls0;      // [B+2][n0]: ring buckets 0..B-1, cold (B), free (B+1)
   uint32_t *cls1;      // [B+2][n1]
   uint32_t *cls2;      // [B+2][n2]
-  uint32_t *hf0, *hf1, *hf2;  // host-free bitmap levels
+  uint32_t *clsc;      // [B+2][n1]: set bits per segment
+  uint32_t *hf0, *hf1, *hf2, *hfc;  // host-free bitmap levels and segment counts
   uint8_t *gpu_pool;   // [S][L][W]
   uint8_t *host_pool;  // [H][L][W], pinned host memory (device pointer)
   uint32_t *uniq;      // [max_entries]: this group's unique addresses of its last step
+  uint32_t *row_slot;  // [max_entries]: GPU slot of unique row u after the commit
   uint32_t *victims;   // [decision_cap]: victim i serves miss i (alloc: GPU slots)
   uint32_t *wb_host;   // [decision_cap]: host slot of write-back j (alloc: host slots)
-  uint32_t *seg_count; // [(B+1)*nseg + hseg]: set bits per segment, in selection order
-  uint32_t *seg_base;  // same shape: exclusive prefix of seg_count
+  uint4 *work;         // [(B+1)*nseg + hseg]: (order position, segment, first rank, count)
   GroupCounters *cnt;
   uint32_t layers;     // L_g
   uint32_t pad;
@@ -80,7 +89,6 @@ struct Geometry {
   uint32_t max_logical;
   Dims gd, hd;           // bitmap dims for GPU-slot and host-slot bitmaps
   uint32_t nseg, hseg;   // segments (= level-1 words) per bitmap
-  uint32_t nsup, hsup;   // superblocks (= level-2 words) per bitmap
 };
 
 __host__ __device__ inline Bitmap class_bitmap(const GroupDev &g, const Geometry &geo, uint32_t c) {
@@ -88,6 +96,7 @@ __host__ __device__ inline Bitmap class_bitmap(const GroupDev &g, const Geometry
   b.w0 = g.cls0 + (size_t)c * geo.gd.n0;
   b.w1 = g.cls1 + (size_t)c * geo.gd.n1;
   b.w2 = g.cls2 + (size_t)c * geo.gd.n2;
+  b.cnt = g.clsc + (size_t)c * geo.gd.n1;
   return b;
 }
 
@@ -96,19 +105,28 @@ __host__ __device__ inline Bitmap host_free_bitmap(const GroupDev &g) {
   b.w0 = g.hf0;
   b.w1 = g.hf1;
   b.w2 = g.hf2;
+  b.cnt = g.hfc;
   return b;
 }
+
+// Victim (or free-slot) selection order: classes at positions 0..n_cls-1.
+struct Order {
+  uint32_t n_cls;
+  uint32_t cls[ULA_MAX_BUCKETS + 2];
+};
 
 // Parameters of the per-step kernels of one group.
 struct StepParams {
   Geometry geo;
   GroupDev grp;
+  Order order;              // free, cold, ring oldest -> newest
   const uint32_t *sel;      // [E]
   uint32_t E, QK, n_req;
   uint32_t epoch;           // dedup epoch of this call
   uint32_t round;           // this round's number r (the current bucket is r % B)
   uint32_t cur;             // r % B
   uint32_t out_cap;
+  uint32_t emit_blocks;     // blocks of the rotate+emit kernel that emit (the rest rotate)
   int inject;               // host-side fault injection code (0 = none)
   int32_t *entry_row;       // [E]
   int32_t *req_off;         // [n_req + 1]
@@ -119,15 +137,13 @@ struct StepParams {
   int *status;              // latched device error (0 = none)
 };
 
-// Parameters of the victim / free-slot selection (step and alloc).
-struct SelectParams {
+// Selection emit (step and alloc): work entries -> victims / host slots.
+struct EmitParams {
   Geometry geo;
   const GroupDev *groups;   // device array [G]
-  uint32_t group0;          // first group (blockIdx.z / blockIdx.x adds to it)
-  uint32_t n_cls;           // GPU classes in selection order
-  uint32_t order[ULA_MAX_BUCKETS + 2];  // class index at each order position
-  uint32_t quota;           // victims wanted (alloc), or 0xFFFFFFFF = take the group's M
-  uint32_t is_step;
+  uint32_t group0;          // first group (blockIdx.y adds to it)
+  Order order;
+  uint32_t quota;           // GPU quota (alloc), or 0xFFFFFFFF = the group's M (step)
   int *status;
 };
 
@@ -135,6 +151,7 @@ struct MoveParams {
   Geometry geo;
   GroupDev grp;
   const uint32_t *miss_list;
+  const uint32_t *addr_row;
   uint32_t round, cur;
   int *status;
 };
@@ -168,15 +185,20 @@ struct FreeParams {
 
 // Launchers (ula_kernels.cu).  Each returns the launch's cudaError_t.
 cudaError_t launch_bitmap_fill(Bitmap b, uint32_t nbits, cudaStream_t s);
-cudaError_t launch_dedup(const StepParams &p, cudaStream_t s);        // stamp, count, scan
-cudaError_t launch_rotate_mark(const StepParams &p, cudaStream_t s);  // rotate, emit+mark, rows
-cudaError_t launch_select(const SelectParams &p, uint32_t n_groups, cudaStream_t s);
+// step: (1)(2) dedup + translate + capacity check; (3) rotate + compaction;
+// (3b)(4) hit marking, entry rows and the victim walk; (4) victim emit
+cudaError_t launch_dedup(const StepParams &p, cudaStream_t s);
+cudaError_t launch_rotate_emit(const StepParams &p, cudaStream_t s);
+cudaError_t launch_mark_select(const StepParams &p, cudaStream_t s);
+cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int blocks, cudaStream_t s);
+// alloc: walk of the free class and the host-free bitmap for a quota of n, per group
+cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s);
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s);
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s);
+cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);
 // resident 256-thread blocks per SM of the persistent kernels
 cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm);
-cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);
 
 }  // namespace ula

@@ -7,11 +7,25 @@
 // (bucket ring + cold bucket, rotation by relabelling, victim order, bitmaps
 // with summary levels, parallel hit detection/dedup, move -> map -> signal).
 //
+// One step of one group is six launches on the critical path:
+//   k_dedup_stamp       (1) every entry bids to be its address's first occurrence
+//   k_dedup_count_scan  (1)(2) per-block counts of first occurrences / misses; the
+//                       last block scans them and runs the capacity check
+//   k_rotate_emit       (3a) ring rotation + cold fold (labels only), and the
+//                       compaction of unique rows / misses / CSR offsets
+//   k_mark_select       (3b) hits move to the current bucket, entry rows; the last
+//                       block walks the segment counts (4) in class order
+//   k_select_emit       (4) the victims' and write-back slots' indices
+//   k_move_commit       (5) write-back, fill, map commit
+// and then k_gather (6), layer 0 on the critical path, the other layers on the
+// prefetch stream.
+//
 // Concurrency discipline for the bitmaps: inside one kernel a given bitmap is
-// either only set or only cleared.  That keeps the summary levels exact with
-// plain atomics: a set that finds its word empty sets the level-1 bit (and so
-// on up), a clear that empties its word clears the level-1 bit (and so on up);
-// with only one direction per kernel no set can interleave with a clear.
+// either only set or only cleared.  That keeps the summary levels and the
+// segment counts exact with plain atomics: a set that finds its word empty sets
+// the level-1 bit (and so on up), a clear that empties its word clears the
+// level-1 bit (and so on up); with only one direction per kernel no set can
+// interleave with a clear.
 #include "ula_device.cuh"
 
 namespace ula {
@@ -49,9 +63,49 @@ __device__ __forceinline__ bool block_skips(const int *status) {
   return s_status != 0;
 }
 
+// Block-wide inclusive scan of one value per thread (T threads); *total gets the sum.
+template <int T>
+__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *total) {
+  __shared__ uint32_t ws[T / 32];
+  __shared__ uint32_t tot;
+  const uint32_t inc = warp_incl_scan(v);
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  if (lane == 31) ws[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t x = lane < T / 32 ? ws[lane] : 0u;
+    const uint32_t y = warp_incl_scan(x);
+    if (lane < T / 32) ws[lane] = y;
+    if (lane == 31) tot = y;
+  }
+  __syncthreads();
+  const uint32_t r = inc + (warp ? ws[warp - 1] : 0u);
+  *total = tot;
+  __syncthreads();
+  return r;
+}
+
+// "Last block done": true in exactly one block, after every block has passed
+// this point; that block then sees all other blocks' global writes.
+__device__ __forceinline__ bool last_block(uint32_t *ticket) {
+  __shared__ bool s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t t = atomicAdd(ticket, 1u);
+    s_last = (t == gridDim.x * gridDim.y - 1);
+    if (s_last) *ticket = 0;  // ready for the next launch
+  }
+  __syncthreads();
+  if (s_last) __threadfence();
+  return s_last;
+}
+
 __device__ __forceinline__ void bm_set(Bitmap b, uint32_t bit) {
   const uint32_t i0 = bit >> 5;
-  const uint32_t old0 = atomicOr(&b.w0[i0], 1u << (bit & 31));
+  const uint32_t m0 = 1u << (bit & 31);
+  const uint32_t old0 = atomicOr(&b.w0[i0], m0);
+  if (!(old0 & m0)) atomicAdd(&b.cnt[bit >> 10], 1u);
   if (old0 == 0) {
     const uint32_t i1 = i0 >> 5;
     const uint32_t old1 = atomicOr(&b.w1[i1], 1u << (i0 & 31));
@@ -63,6 +117,7 @@ __device__ __forceinline__ void bm_clear(Bitmap b, uint32_t bit) {
   const uint32_t i0 = bit >> 5;
   const uint32_t m0 = 1u << (bit & 31);
   const uint32_t old0 = atomicAnd(&b.w0[i0], ~m0);
+  if (old0 & m0) atomicSub(&b.cnt[bit >> 10], 1u);
   if (old0 == m0) {  // this clear emptied the word
     const uint32_t i1 = i0 >> 5;
     const uint32_t m1 = 1u << (i0 & 31);
@@ -81,15 +136,18 @@ __device__ __forceinline__ uint32_t class_of(uint32_t stamp, uint32_t round, uin
 
 // ------------------------------------------------------------------ init
 
+// all of [0, nbits) set, with exact summaries and segment counts
 __global__ void k_bitmap_fill(Bitmap b, uint32_t nbits) {
   const Dims d = dims_for(nbits);
   const uint32_t stride = gridDim.x * blockDim.x;
   for (uint32_t w = blockIdx.x * blockDim.x + threadIdx.x; w < d.n0; w += stride) {
-    const uint32_t lo = w * 32, n = nbits - lo;
+    const uint32_t n = nbits - w * 32;
     b.w0[w] = n >= 32 ? 0xffffffffu : ((1u << n) - 1u);
     if (w < d.n1) {
       const uint32_t m = d.n0 - w * 32;
       b.w1[w] = m >= 32 ? 0xffffffffu : ((1u << m) - 1u);
+      const uint32_t left = nbits - w * kSegBits;
+      b.cnt[w] = left >= kSegBits ? kSegBits : left;
     }
     if (w < d.n2) {
       const uint32_t m = d.n1 - w * 32;
@@ -136,8 +194,10 @@ __device__ __forceinline__ Flags entry_flags(const StepParams &p, uint32_t e) {
   return f;
 }
 
-// per-block counts of first occurrences and of misses
-__global__ void __launch_bounds__(kEntryThreads) k_dedup_count(StepParams p) {
+// Per-block counts of first occurrences and misses; the last block turns them
+// into exclusive offsets, totals U and M, and runs the capacity check -- no
+// state changes before it passes.
+__global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p) {
   if (block_skips(p.status)) return;
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   const Flags f = entry_flags(p, e);
@@ -156,48 +216,25 @@ __global__ void __launch_bounds__(kEntryThreads) k_dedup_count(StepParams p) {
     }
     p.blk[blockIdx.x] = make_uint2(tf, tm);
   }
-}
-
-// exclusive scan of the block counts; totals; the capacity check (no state
-// changes before it passes)
-__global__ void __launch_bounds__(kScanThreads) k_dedup_scan(StepParams p, uint32_t nblk) {
-  if (block_skips(p.status)) return;
-  __shared__ uint32_t wf[32], wm[32];
-  const uint32_t per = (nblk + kScanThreads - 1) / kScanThreads;
-  const uint32_t b0 = min(threadIdx.x * per, nblk), b1 = min(b0 + per, nblk);
-  uint32_t sf = 0, sm = 0;
-  for (uint32_t b = b0; b < b1; ++b) {
-    const uint2 v = p.blk[b];
-    sf += v.x;
-    sm += v.y;
-  }
-  const uint32_t incf = warp_incl_scan(sf), incm = warp_incl_scan(sm);
-  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  if (lane == 31) {
-    wf[warp] = incf;
-    wm[warp] = incm;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t x = warp_incl_scan(wf[lane]), y = warp_incl_scan(wm[lane]);
-    __syncwarp();
-    wf[lane] = x;
-    wm[lane] = y;
-  }
-  __syncthreads();
-  uint32_t of = (warp ? wf[warp - 1] : 0) + incf - sf;
-  uint32_t om = (warp ? wm[warp - 1] : 0) + incm - sm;
-  for (uint32_t b = b0; b < b1; ++b) {
-    const uint2 v = p.blk[b];
-    p.blk[b] = make_uint2(of, om);
-    of += v.x;
-    om += v.y;
+  GroupCounters *c = p.grp.cnt;
+  if (!last_block(&c->done[0])) return;
+  // the last block: exclusive scan over the block counts
+  const uint32_t nblk = gridDim.x;
+  uint32_t runf = 0, runm = 0;
+  for (uint32_t b0 = 0; b0 < nblk; b0 += kEntryThreads) {
+    const uint32_t b = b0 + threadIdx.x;
+    const uint2 v = b < nblk ? __ldcg(&p.blk[b]) : make_uint2(0, 0);
+    uint32_t totf, totm;
+    const uint32_t incf = block_incl_scan<kEntryThreads>(v.x, &totf);
+    const uint32_t incm = block_incl_scan<kEntryThreads>(v.y, &totm);
+    if (b < nblk) p.blk[b] = make_uint2(runf + incf - v.x, runm + incm - v.y);
+    runf += totf;
+    runm += totm;
   }
   if (p.E == 0)
     for (uint32_t r = threadIdx.x; r <= p.n_req; r += blockDim.x) p.req_off[r] = 0;
   if (threadIdx.x == 0) {
-    const uint32_t U = wf[31], M = wm[31], hits = U - M;
-    GroupCounters *c = p.grp.cnt;
+    const uint32_t U = runf, M = runm, hits = U - M;
     const bool ok = U <= p.out_cap && (uint64_t)M + hits <= p.geo.S &&
                     (uint64_t)M <= (uint64_t)c->free_gpu + c->free_host;
     if (!ok) {
@@ -208,6 +245,8 @@ __global__ void __launch_bounds__(kScanThreads) k_dedup_scan(StepParams p, uint3
       c->hits = hits;
       c->F = 0;
       c->K = 0;
+      c->n_work = 0;
+      c->n_work_gpu = 0;
       p.req_off[p.n_req] = (int32_t)U;
       const unsigned long long sb = (unsigned long long)p.grp.layers * p.geo.W;
       c->stat[kStSteps] += 1;
@@ -221,37 +260,42 @@ __global__ void __launch_bounds__(kScanThreads) k_dedup_scan(StepParams p, uint3
   }
 }
 
-// (3a) rotation: the current bucket advances to `cur`; what is left in it
-// folds into the cold bucket.  Only labels change.  Sets on cold, clears on
-// the reused bucket.
-__global__ void k_rotate(StepParams p) {
-  if (*(volatile int *)p.status) return;
+// Blocks [0, emit_blocks): compact first occurrences into uniq (first-occurrence
+// order), misses into miss_list (same order), CSR offsets per request, and the
+// unique row of every selected address.  Blocks from emit_blocks on: (3a) the
+// rotation -- the current bucket advances to `cur` and what is left in it folds
+// into the cold bucket (sets on cold, clears on the reused bucket; labels only).
+__global__ void __launch_bounds__(kEntryThreads) k_rotate_emit(StepParams p) {
+  if (block_skips(p.status)) return;
   const Geometry &geo = p.geo;
-  const Bitmap bucket = class_bitmap(p.grp, geo, p.cur);
-  const Bitmap cold = class_bitmap(p.grp, geo, geo.B);
-  const uint32_t stride = gridDim.x * blockDim.x;
-  const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
-  for (uint32_t w = t; w < geo.gd.n0; w += stride) {
-    const uint32_t b = bucket.w0[w];
-    if (b) {
-      const uint32_t c = cold.w0[w];
-      cold.w0[w] = c | b;
-      bucket.w0[w] = 0;
-      if (c == 0) {
-        const uint32_t old1 = atomicOr(&cold.w1[w >> 5], 1u << (w & 31));
-        if (old1 == 0) atomicOr(&cold.w2[w >> 10], 1u << ((w >> 5) & 31));
+  if (blockIdx.x >= p.emit_blocks) {
+    const Bitmap bucket = class_bitmap(p.grp, geo, p.cur);
+    const Bitmap cold = class_bitmap(p.grp, geo, geo.B);
+    const uint32_t nthr = (gridDim.x - p.emit_blocks) * blockDim.x;
+    const uint32_t t = (blockIdx.x - p.emit_blocks) * blockDim.x + threadIdx.x;
+    for (uint32_t w = t; w < geo.gd.n0; w += nthr) {
+      const uint32_t b = bucket.w0[w];
+      if (b) {
+        const uint32_t c = cold.w0[w];
+        cold.w0[w] = c | b;
+        bucket.w0[w] = 0;
+        if (c == 0) {
+          const uint32_t old1 = atomicOr(&cold.w1[w >> 5], 1u << (w & 31));
+          if (old1 == 0) atomicOr(&cold.w2[w >> 10], 1u << ((w >> 5) & 31));
+        }
       }
     }
+    for (uint32_t w = t; w < geo.gd.n1; w += nthr) {
+      const uint32_t moved = bucket.cnt[w];  // disjoint classes: counts add
+      if (moved) {
+        cold.cnt[w] += moved;
+        bucket.cnt[w] = 0;
+      }
+      bucket.w1[w] = 0;
+    }
+    for (uint32_t w = t; w < geo.gd.n2; w += nthr) bucket.w2[w] = 0;
+    return;
   }
-  for (uint32_t w = t; w < geo.gd.n1; w += stride) bucket.w1[w] = 0;
-  for (uint32_t w = t; w < geo.gd.n2; w += stride) bucket.w2[w] = 0;
-}
-
-// (1)+(2)+(3b): compact first occurrences into uniq (first-occurrence order),
-// misses into miss_list (same order), CSR offsets per request, and move every
-// hit into the current bucket.  Clears on non-current classes, sets on cur.
-__global__ void __launch_bounds__(kEntryThreads) k_dedup_emit(StepParams p) {
-  if (block_skips(p.status)) return;
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   const Flags f = entry_flags(p, e);
   __shared__ uint32_t sf[kEntryThreads / 32], sm[kEntryThreads / 32];
@@ -267,170 +311,86 @@ __global__ void __launch_bounds__(kEntryThreads) k_dedup_emit(StepParams p) {
     bf += sf[w];
     bmiss += sm[w];
   }
-  const uint32_t pos = bf + incf - f.first;   // exclusive: unique rows before e
+  const uint32_t pos = bf + incf - f.first;    // exclusive: unique rows before e
   const uint32_t mpos = bmiss + incm - f.miss; // exclusive: misses before e
   if (e < p.E && (e % p.QK) == 0) p.req_off[e / p.QK] = (int32_t)pos;
   if (!f.first) return;
   p.grp.uniq[pos] = f.a;
   p.addr_row[f.a] = pos;
-  if (f.miss) {
-    p.miss_list[mpos] = f.a;
-    return;
-  }
-  const uint32_t s = p.grp.map[f.a];
-  if (s >= p.geo.S) {
-    latch(p.status, ULA_ERR_INTERNAL);
-    return;
-  }
-  const uint32_t c = class_of(p.grp.stamp[s], p.round, p.geo.B);
-  if (c == p.geo.B + 1) {
-    latch(p.status, ULA_ERR_INTERNAL);
-    return;
-  }
-  if (c != p.cur) {
-    bm_clear(class_bitmap(p.grp, p.geo, c), s);
-    bm_set(class_bitmap(p.grp, p.geo, p.cur), s);
-  }
-  p.grp.stamp[s] = p.round;
+  if (f.miss) p.miss_list[mpos] = f.a;
 }
 
-__global__ void k_entry_rows(StepParams p) {
-  if (*(volatile int *)p.status) return;
-  const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e >= p.E) return;
-  const uint32_t a = p.sel[e];
-  p.entry_row[e] = a == kPad ? -1 : (int32_t)p.addr_row[a];
-}
-
-// ------------------------------------------------------------- selection
-//
-// (4) "the first q set bits" of a sequence of bitmaps taken in a fixed order
-// (step: free, cold, ring oldest -> newest; alloc: free), plus the first K
-// set bits of the host-free bitmap.  Three passes:
-//   count: per 1,024-slot segment, the number of set bits; a superblock whose
-//          level-2 word is zero, or a segment whose level-1 word is zero, is
-//          skipped without touching the level below;
-//   scan:  exclusive prefix over the segments in selection order;
-//   emit:  each non-empty segment below the quota writes its set bits'
-//          slots at their ranks (warp-wide popcount prefix).
-// Grid for count/emit: x = superblock, y = order position (last = host),
-// z = group.  One warp per segment.
-
-__device__ __forceinline__ uint32_t select_quota(const SelectParams &p, const GroupDev &g) {
-  return p.quota == 0xffffffffu ? g.cnt->M : p.quota;
-}
-
-__device__ __forceinline__ bool select_target(const SelectParams &p, const GroupDev &g,
-                                              uint32_t y, Bitmap &bm, uint32_t &nseg,
-                                              uint32_t &n0, uint32_t *&counts, uint32_t *&bases) {
-  const Geometry &geo = p.geo;
-  const uint32_t host_off = (geo.B + 1) * geo.nseg;
-  if (y == p.n_cls) {
-    bm = host_free_bitmap(g);
-    nseg = geo.hseg;
-    n0 = geo.hd.n0;
-    counts = g.seg_count + host_off;
-    bases = g.seg_base + host_off;
-  } else {
-    bm = class_bitmap(g, geo, p.order[y]);
-    nseg = geo.nseg;
-    n0 = geo.gd.n0;
-    counts = g.seg_count + (size_t)y * geo.nseg;
-    bases = g.seg_base + (size_t)y * geo.nseg;
-  }
-  return true;
-}
-
-__global__ void __launch_bounds__(1024) k_select_count(SelectParams p) {
-  if (*(volatile int *)p.status) return;
-  const GroupDev g = p.groups[p.group0 + blockIdx.z];
-  if (select_quota(p, g) == 0) return;
-  Bitmap bm;
-  uint32_t nseg, n0, *counts, *bases;
-  select_target(p, g, blockIdx.y, bm, nseg, n0, counts, bases);
-  const uint32_t sup = blockIdx.x, warp = threadIdx.x >> 5, lane = lane_id();
-  const uint32_t seg = sup * 32 + warp;
-  if (seg >= nseg) return;
-  uint32_t n = 0;
-  const uint32_t s2 = bm.w2[sup];
-  if ((s2 >> warp) & 1u) {
-    const uint32_t s1 = bm.w1[seg];
-    if ((s1 >> lane) & 1u) n = __popc(bm.w0[seg * 32 + lane]);
-  }
-  n = warp_sum(n);
-  if (lane == 0) counts[seg] = n;
-}
-
-// chunked exclusive block scan of vals[0..n) into out[0..n); returns the total
-__device__ uint32_t block_exclusive_scan(const uint32_t *vals, uint32_t *out, uint32_t n) {
-  __shared__ uint32_t ws[32];
-  __shared__ uint32_t total;
-  const uint32_t per = (n + blockDim.x - 1) / blockDim.x;
-  const uint32_t i0 = min(threadIdx.x * per, n), i1 = min(i0 + per, n);
-  uint32_t s = 0;
-  for (uint32_t i = i0; i < i1; ++i) s += vals[i];
-  const uint32_t inc = warp_incl_scan(s);
-  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  const uint32_t nwarps = blockDim.x >> 5;
-  if (lane == 31) ws[warp] = inc;
+// (4) Walk the segment counts of the classes in `ord` for the first `quota` set
+// bits, then the host-free bitmap for the first K = quota - (free slots taken)
+// set bits, and record one work entry per segment that holds some of them.
+// Block-wide (T threads); stops as soon as the quota is met.
+template <int T>
+__device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order &ord,
+                            uint32_t quota, bool is_step, int *status) {
+  __shared__ uint32_t s_nwork;
+  if (threadIdx.x == 0) s_nwork = 0;
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t x = lane < nwarps ? ws[lane] : 0u;
-    const uint32_t y = warp_incl_scan(x);
-    __syncwarp();
-    if (lane < nwarps) ws[lane] = y;
-    if (lane == 31) total = y;
-  }
-  __syncthreads();
-  uint32_t run = (warp ? ws[warp - 1] : 0) + inc - s;
-  for (uint32_t i = i0; i < i1; ++i) {
-    const uint32_t v = vals[i];
-    out[i] = run;
-    run += v;
-  }
-  const uint32_t t = total;
-  __syncthreads();
-  return t;
-}
-
-__global__ void __launch_bounds__(kScanThreads) k_select_scan(SelectParams p) {
-  if (block_skips(p.status)) return;
-  const GroupDev g = p.groups[p.group0 + blockIdx.x];
-  const Geometry &geo = p.geo;
-  const uint32_t quota = select_quota(p, g);
-  if (quota == 0) {
-    if (threadIdx.x == 0) {
-      g.cnt->F = 0;
-      g.cnt->K = 0;
+  uint32_t rem = quota, base = 0, taken_free = 0, taken_cold = 0;
+  for (uint32_t y = 0; y < ord.n_cls && rem > 0; ++y) {
+    const Bitmap bm = class_bitmap(g, geo, ord.cls[y]);
+    uint32_t taken_y = 0;
+    for (uint32_t s0 = 0; s0 < geo.nseg && rem > 0; s0 += T) {
+      const uint32_t seg = s0 + threadIdx.x;
+      const uint32_t v = seg < geo.nseg ? __ldcg(&bm.cnt[seg]) : 0u;
+      uint32_t total, ntake;
+      const uint32_t inc = block_incl_scan<T>(v, &total);
+      const uint32_t excl = inc - v;
+      const uint32_t take = (v > 0 && excl < rem) ? 1u : 0u;
+      const uint32_t tpos = block_incl_scan<T>(take, &ntake);
+      if (take) g.work[s_nwork + tpos - 1] = make_uint4(y, seg, base + excl, v);
+      const uint32_t got = min(total, rem);
+      base += got;
+      rem -= got;
+      taken_y += got;
+      __syncthreads();
+      if (threadIdx.x == 0) s_nwork += ntake;
+      __syncthreads();
     }
-    return;
+    if (ord.cls[y] == geo.B + 1) taken_free += taken_y;
+    else if (ord.cls[y] == geo.B) taken_cold += taken_y;
   }
-  const uint32_t ngpu = p.n_cls * geo.nseg;
-  const uint32_t gpu_total = block_exclusive_scan(g.seg_count, g.seg_base, ngpu);
-  const uint32_t host_off = (geo.B + 1) * geo.nseg;
-  const uint32_t host_total =
-      block_exclusive_scan(g.seg_count + host_off, g.seg_base + host_off, geo.hseg);
-  __syncthreads();  // seg_base of other threads is read below
+  const uint32_t F = taken_free;
+  const uint32_t nwork_gpu = s_nwork;
+  const uint32_t K = (is_step && rem == 0) ? quota - F : (is_step ? 0u : rem);
+  uint32_t hrem = K, hbase = 0;
+  const Bitmap hb = host_free_bitmap(g);
+  for (uint32_t s0 = 0; s0 < geo.hseg && hrem > 0; s0 += T) {
+    const uint32_t seg = s0 + threadIdx.x;
+    const uint32_t v = seg < geo.hseg ? __ldcg(&hb.cnt[seg]) : 0u;
+    uint32_t total, ntake;
+    const uint32_t inc = block_incl_scan<T>(v, &total);
+    const uint32_t excl = inc - v;
+    const uint32_t take = (v > 0 && excl < hrem) ? 1u : 0u;
+    const uint32_t tpos = block_incl_scan<T>(take, &ntake);
+    if (take) g.work[s_nwork + tpos - 1] = make_uint4(kHostPos, seg, hbase + excl, v);
+    const uint32_t got = min(total, hrem);
+    hbase += got;
+    hrem -= got;
+    __syncthreads();
+    if (threadIdx.x == 0) s_nwork += ntake;
+    __syncthreads();
+  }
   if (threadIdx.x != 0) return;
-  const uint32_t free_total = p.n_cls > 1 ? g.seg_base[geo.nseg] : gpu_total;
-  const uint32_t cold_end = p.n_cls > 2 ? g.seg_base[2 * geo.nseg] : gpu_total;
-  const uint32_t F = min(quota, free_total);
-  const uint32_t K = quota - F;
   GroupCounters *c = g.cnt;
-  if (host_total < K || (p.is_step && gpu_total < quota) || free_total != c->free_gpu ||
-      host_total != c->free_host) {
-    latch(p.status, ULA_ERR_INTERNAL);
+  if ((is_step && rem > 0) || hrem > 0) {
+    latch(status, ULA_ERR_INTERNAL);  // the capacity check rules this out
     return;
   }
   c->F = F;
   c->K = K;
-  if (p.is_step) {
-    const uint32_t from_cold = min(quota - F, cold_end - free_total);
+  c->n_work = s_nwork;
+  c->n_work_gpu = nwork_gpu;
+  if (is_step) {
     c->free_gpu -= F;   // F free slots filled
     c->free_host += F;  // K host slots taken, quota host slots released
     c->stat[kStVictFree] += F;
-    c->stat[kStVictCold] += from_cold;
-    c->stat[kStVictRing] += quota - F - from_cold;
+    c->stat[kStVictCold] += taken_cold;
+    c->stat[kStVictRing] += quota - F - taken_cold;
     c->stat[kStWriteback] += K;
     c->stat[kStBytesD2H] += (unsigned long long)K * g.layers * geo.W;
   } else {
@@ -439,32 +399,77 @@ __global__ void __launch_bounds__(kScanThreads) k_select_scan(SelectParams p) {
   }
 }
 
-__global__ void __launch_bounds__(1024) k_select_emit(SelectParams p) {
+// (3b) every hit moves to the current bucket (clears on its old class, sets
+// on cur) and its slot is recorded for the gather; entry rows for every entry.
+// The last block then walks the classes for the M victims.
+__global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
+  if (block_skips(p.status)) return;
+  const GroupDev &g = p.grp;
+  const Geometry &geo = p.geo;
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  const uint32_t U = g.cnt->U;
+  if (i < U) {
+    const uint32_t m = g.map[g.uniq[i]];
+    if (!(m & kHostBit)) {
+      const uint32_t c = m < geo.S ? class_of(g.stamp[m], p.round, geo.B) : geo.B + 1;
+      if (c == geo.B + 1) {
+        latch(p.status, ULA_ERR_INTERNAL);
+      } else {
+        if (c != p.cur) {
+          bm_clear(class_bitmap(g, geo, c), m);
+          bm_set(class_bitmap(g, geo, p.cur), m);
+        }
+        g.stamp[m] = p.round;
+        g.row_slot[i] = m;
+      }
+    }
+  }
+  if (i < p.E) {
+    const uint32_t a = p.sel[i];
+    p.entry_row[i] = a == kPad ? -1 : (int32_t)p.addr_row[a];
+  }
+  if (!last_block(&g.cnt->done[1])) return;
+  select_walk<kEntryThreads>(g, geo, p.order, __ldcg(&g.cnt->M), true, p.status);
+}
+
+// (4) Each work entry's segment: its set bits in ascending order get the ranks
+// [base, base + count); ranks below the quota are written out.  Host entries
+// claim their slots (clears only on the host-free bitmap; GPU classes read only).
+__global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
   if (*(volatile int *)p.status) return;
-  const GroupDev g = p.groups[p.group0 + blockIdx.z];
-  const uint32_t quota = select_quota(p, g);
-  if (quota == 0) return;
-  const bool host = blockIdx.y == p.n_cls;
-  const uint32_t q = host ? g.cnt->K : quota;
-  Bitmap bm;
-  uint32_t nseg, n0, *counts, *bases;
-  select_target(p, g, blockIdx.y, bm, nseg, n0, counts, bases);
-  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  const uint32_t seg = blockIdx.x * 32 + warp;
-  if (seg >= nseg) return;
-  const uint32_t base = bases[seg];
-  if (counts[seg] == 0 || base >= q) return;
-  const uint32_t wi = seg * 32 + lane;
-  uint32_t word = wi < n0 ? bm.w0[wi] : 0u;
-  const uint32_t inc = warp_incl_scan(__popc(word));
-  uint32_t rank = base + inc - __popc(word);
-  uint32_t *dst = host ? g.wb_host : g.victims;
-  while (word && rank < q) {
-    const uint32_t b = __ffs(word) - 1;
-    word &= word - 1;
-    const uint32_t slot = wi * 32 + b;
-    dst[rank++] = slot;
-    if (host) bm_clear(bm, slot);  // claim the write-back target (clears only)
+  const GroupDev g = p.groups[p.group0 + blockIdx.y];
+  const Geometry &geo = p.geo;
+  const GroupCounters *c = g.cnt;
+  const uint32_t n_work = c->n_work;
+  const uint32_t q_gpu = p.quota == 0xffffffffu ? c->M : p.quota;
+  const uint32_t q_host = c->K;
+  const uint32_t lane = lane_id();
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  for (uint32_t i = warp; i < n_work; i += nwarps) {
+    const uint4 e = g.work[i];
+    const bool host = e.x == kHostPos;
+    if (!host && e.x >= p.order.n_cls) {
+      if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
+      continue;
+    }
+    const Bitmap bm = host ? host_free_bitmap(g) : class_bitmap(g, geo, p.order.cls[e.x]);
+    const uint32_t n0 = host ? geo.hd.n0 : geo.gd.n0;
+    const uint32_t q = host ? q_host : q_gpu;
+    uint32_t *dst = host ? g.wb_host : g.victims;
+    const uint32_t seg = e.y;
+    const uint32_t wi = seg * 32 + lane;
+    const uint32_t s1 = bm.w1[seg];  // level-1 summary: which words of the segment hold bits
+    uint32_t word = (((s1 >> lane) & 1u) && wi < n0) ? bm.w0[wi] : 0u;
+    const uint32_t pc = __popc(word);
+    uint32_t rank = e.z + warp_incl_scan(pc) - pc;
+    while (word && rank < q) {
+      const uint32_t b = __ffs(word) - 1;
+      word &= word - 1;
+      const uint32_t slot = wi * 32 + b;
+      dst[rank++] = slot;
+      if (host) bm_clear(bm, slot);  // claim the write-back (or placement) target
+    }
   }
 }
 
@@ -472,10 +477,11 @@ __global__ void __launch_bounds__(1024) k_select_emit(SelectParams p) {
 //
 // (5) per victim i (one warp): write the victim's rows back to its host slot
 // if it holds data, fill miss i's rows from its host slot, then update the map
-// (after this warp's copies), move the slot into the current bucket and
-// release the miss's host slot.  Each lane handles the same 16-byte chunks in
-// the write-back and in the fill, so its read of a chunk precedes its write
-// of the same chunk.  Host memory is reached directly over the host link.
+// (after this warp's copies), move the slot into the current bucket, record
+// the row's slot for the gather and release the miss's host slot.  Each lane
+// handles the same 16-byte chunks in the write-back and in the fill, so its read
+// of a chunk precedes its write of the same chunk.  Host memory is reached
+// directly over the host link.
 constexpr int kMoveUnroll = 6;
 
 __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
@@ -542,6 +548,7 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
         bm_set(class_bitmap(g, geo, p.cur), v);
       }
       g.stamp[v] = p.round;
+      g.row_slot[p.addr_row[a]] = v;
       bm_set(host_free_bitmap(g), hs);
     }
   }
@@ -549,12 +556,12 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
 
 // ------------------------------------------------------------------ gather
 //
-// (6) out[layer][u] = layer `layer` of the slot the committed map gives for
-// uniq[u].  The U rows are spread over all warps (rows_per_warp = ceil(U /
-// warps), at most 32): lanes resolve the warp's slots through the map, then the
-// warp streams the rows' 16-byte chunks, consecutive lanes on consecutive chunks
-// (coalesced within a row; the warp's output rows are contiguous).  Loads are
-// issued kGatherUnroll deep before the stores.
+// (6) out[layer][u] = layer `layer` of the slot that the commit recorded for
+// unique row u (the committed map's entry for uniq[u]).  The U rows are spread
+// over all warps (rows_per_warp = ceil(U / warps), at most 32): lanes read the
+// warp's slots, then the warp streams the rows' 16-byte chunks, consecutive lanes
+// on consecutive chunks (coalesced within a row; the warp's output rows are
+// contiguous).  Loads are issued kGatherUnroll deep before the stores.
 constexpr int kGatherUnroll = 8;
 
 __global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
@@ -577,8 +584,8 @@ __global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
     uint32_t slot = 0;
     bool bad = false;
     if (lane < nrows) {
-      const uint32_t m = g.map[g.uniq[row0 + lane]];
-      bad = (m & kHostBit) || m >= geo.S;
+      const uint32_t m = g.row_slot[row0 + lane];
+      bad = m >= geo.S;
       slot = bad ? 0u : m;
     }
     if (__any_sync(0xffffffffu, bad)) {
@@ -617,6 +624,14 @@ __global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
 }
 
 // ------------------------------------------------------------ alloc / free
+
+// Alloc, per group (one block each): walk the free class for n slots, then the
+// host-free bitmap for the rest.
+__global__ void __launch_bounds__(kScanThreads) k_alloc_select(EmitParams p) {
+  if (block_skips(p.status)) return;
+  const GroupDev g = p.groups[p.group0 + blockIdx.x];
+  select_walk<kScanThreads>(g, p.geo, p.order, p.quota, false, p.status);
+}
 
 // Alloc: address i of the range goes to the i-th selected free GPU slot (the
 // lowest ones, joining the current bucket), the rest to the selected host slots.
@@ -714,31 +729,35 @@ cudaError_t launch_bitmap_fill(Bitmap b, uint32_t nbits, cudaStream_t s) {
 
 cudaError_t launch_dedup(const StepParams &p, cudaStream_t s) {
   const uint32_t nblk = div_up(p.E, kEntryThreads);
-  if (nblk) {
-    k_dedup_stamp<<<nblk, kEntryThreads, 0, s>>>(p);
-    k_dedup_count<<<nblk, kEntryThreads, 0, s>>>(p);
-  }
-  k_dedup_scan<<<1, kScanThreads, 0, s>>>(p, nblk);
+  if (nblk) k_dedup_stamp<<<nblk, kEntryThreads, 0, s>>>(p);
+  k_dedup_count_scan<<<nblk ? nblk : 1, kEntryThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_rotate_mark(const StepParams &p, cudaStream_t s) {
-  const uint32_t rot_blocks = div_up(p.geo.gd.n0, 256);
-  k_rotate<<<rot_blocks ? rot_blocks : 1, 256, 0, s>>>(p);
+cudaError_t launch_rotate_emit(const StepParams &p, cudaStream_t s) {
+  StepParams q = p;
+  q.emit_blocks = div_up(p.E, kEntryThreads);
+  const uint32_t words = p.geo.gd.n0 > p.geo.gd.n1 ? p.geo.gd.n0 : p.geo.gd.n1;
+  uint32_t rot = div_up(words, kEntryThreads * 4);
+  rot = rot ? rot : 1;
+  k_rotate_emit<<<q.emit_blocks + rot, kEntryThreads, 0, s>>>(q);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mark_select(const StepParams &p, cudaStream_t s) {
   const uint32_t nblk = div_up(p.E, kEntryThreads);
-  if (nblk) {
-    k_dedup_emit<<<nblk, kEntryThreads, 0, s>>>(p);
-    k_entry_rows<<<nblk, kEntryThreads, 0, s>>>(p);
-  }
+  k_mark_select<<<nblk ? nblk : 1, kEntryThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(const SelectParams &p, uint32_t n_groups, cudaStream_t s) {
-  const uint32_t nsup = p.geo.nsup > p.geo.hsup ? p.geo.nsup : p.geo.hsup;
-  dim3 grid(nsup ? nsup : 1, p.n_cls + 1, n_groups);
-  k_select_count<<<grid, 1024, 0, s>>>(p);
-  k_select_scan<<<n_groups, kScanThreads, 0, s>>>(p);
-  k_select_emit<<<grid, 1024, 0, s>>>(p);
+cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int blocks, cudaStream_t s) {
+  dim3 grid(blocks > 0 ? blocks : 1, n_groups);
+  k_select_emit<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s) {
+  k_alloc_select<<<n_groups, kScanThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 

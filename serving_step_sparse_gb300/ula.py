@@ -56,7 +56,8 @@ class ula_debug_layout(C.Structure):
 class ula_debug_state(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in (
         "map", "owner", "stamp", "class_bits", "class_sum1", "class_sum2", "host_free_bits",
-        "host_free_sum1", "host_free_sum2", "uniq", "victims", "wb_host")] + \
+        "host_free_sum1", "host_free_sum2", "uniq", "victims", "wb_host", "class_seg_count",
+        "host_seg_count", "row_slot")] + \
         [(n, C.c_uint32) for n in ("round", "cur", "free_gpu", "free_host", "U", "M", "hits",
                                     "victims_free", "writebacks")]
 

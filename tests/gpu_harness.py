@@ -121,6 +121,15 @@ def check_gpu_internal(st: dict, w):
         n1 = (n0 + 31) // 32
         assert np.array_equal(unpack_bits(w1, n0).astype(bool), w0[:n0] != 0)
         assert np.array_equal(unpack_bits(w2, n1).astype(bool), w1[:n1] != 0)
+    # segment counts (set bits per 1,024 slots) agree with the bitmaps
+    for c in range(B + 2):
+        bits = unpack_bits(st["class_bits"][c], S).astype(np.int64)
+        segs = np.add.reduceat(bits, np.arange(0, S, 1024)) if S else np.zeros(0)
+        assert np.array_equal(st["class_seg_count"][c][:len(segs)], segs), f"segment counts {c}"
+    if H:
+        bits = unpack_bits(st["host_free_bits"], H).astype(np.int64)
+        segs = np.add.reduceat(bits, np.arange(0, H, 1024))
+        assert np.array_equal(st["host_seg_count"][:len(segs)], segs), "host segment counts"
     r = st["round"]
     stamp = st["stamp"]
     exp = np.where(stamp == ula.STAMP_FREE, B + 1,

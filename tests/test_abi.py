@@ -52,7 +52,7 @@ def test_binding_struct_sizes_match_header(libpath):
     assert C.sizeof(ula.ula_config) == 4 * (8 + ula.MAX_GROUPS)
     assert C.sizeof(ula.ula_stats) == 8 * 12
     assert C.sizeof(ula.ula_debug_layout) == 4 * 8
-    assert C.sizeof(ula.ula_debug_state) == 8 * 12 + 4 * 9 + 4  # padded to 8
+    assert C.sizeof(ula.ula_debug_state) == 8 * 15 + 4 * 9 + 4  # padded to 8
     src = open(HEADER).read()
     assert "#define ULA_MAX_GROUPS 64" in src and "#define ULA_MAX_BUCKETS 64" in src
     for name, val in (("ULA_ERR_INVALID_ARG", 1), ("ULA_ERR_CAPACITY", 2), ("ULA_ERR_UNMAPPED", 3),
