@@ -33,7 +33,9 @@ namespace ula {
 namespace {
 
 constexpr int kScanThreads = 1024;
-constexpr int kEntryThreads = 256;
+constexpr int kEntryThreads = 1024;  // blocks of the per-entry kernels with block scans
+constexpr int kStampThreads = 256;
+constexpr int kWalkSegs = 4;        // segments per thread per step of the victim walk
 
 __device__ __forceinline__ void latch(int *status, int code) { atomicCAS(status, 0, code); }
 
@@ -119,6 +121,19 @@ __device__ __forceinline__ void bm_clear(Bitmap b, uint32_t bit) {
   const uint32_t old0 = atomicAnd(&b.w0[i0], ~m0);
   if (old0 & m0) atomicSub(&b.cnt[bit >> 10], 1u);
   if (old0 == m0) {  // this clear emptied the word
+    const uint32_t i1 = i0 >> 5;
+    const uint32_t m1 = 1u << (i0 & 31);
+    const uint32_t old1 = atomicAnd(&b.w1[i1], ~m1);
+    if (old1 == m1) atomicAnd(&b.w2[i1 >> 5], ~(1u << (i1 & 31)));
+  }
+}
+
+// Clear the set bits `mask` of level-0 word i0 at once (clear-only phase).
+__device__ __forceinline__ void bm_clear_mask(Bitmap b, uint32_t i0, uint32_t mask) {
+  const uint32_t old0 = atomicAnd(&b.w0[i0], ~mask);
+  const uint32_t cleared = old0 & mask;
+  if (cleared) atomicSub(&b.cnt[i0 >> 5], (uint32_t)__popc(cleared));
+  if (old0 && (old0 & ~mask) == 0) {  // this clear emptied the word
     const uint32_t i1 = i0 >> 5;
     const uint32_t m1 = 1u << (i0 & 31);
     const uint32_t old1 = atomicAnd(&b.w1[i1], ~m1);
@@ -324,6 +339,51 @@ __global__ void __launch_bounds__(kEntryThreads) k_rotate_emit(StepParams p) {
 // bits, then the host-free bitmap for the first K = quota - (free slots taken)
 // set bits, and record one work entry per segment that holds some of them.
 // Block-wide (T threads); stops as soon as the quota is met.
+// One step of the walk over segment counts cnt[s0 .. s0 + T*V): threads take V
+// consecutive segments each; segments holding ranks below `rem` (counted from
+// `base`) become work entries (position y).  Advances base/rem; returns what it took.
+template <int T>
+__device__ __forceinline__ uint32_t walk_chunk(const uint32_t *cnt, uint32_t nseg, uint32_t s0,
+                                               uint32_t y, uint32_t &base, uint32_t &rem,
+                                               uint4 *work, uint32_t *s_nwork) {
+  uint32_t v[kWalkSegs];
+  uint32_t mine = 0;
+  const uint32_t first = s0 + threadIdx.x * kWalkSegs;
+#pragma unroll
+  for (int j = 0; j < kWalkSegs; ++j) {
+    v[j] = first + j < nseg ? __ldcg(&cnt[first + j]) : 0u;
+    mine += v[j];
+  }
+  uint32_t total, ntake;
+  uint32_t excl = block_incl_scan<T>(mine, &total) - mine;
+  uint32_t takes = 0;
+  {  // this thread's segments that hold ranks below rem
+    uint32_t e = excl;
+#pragma unroll
+    for (int j = 0; j < kWalkSegs; ++j) {
+      takes += (v[j] > 0 && e < rem) ? 1u : 0u;
+      e += v[j];
+    }
+  }
+  uint32_t pos = block_incl_scan<T>(takes, &ntake) - takes + *s_nwork;
+#pragma unroll
+  for (int j = 0; j < kWalkSegs; ++j) {
+    if (v[j] > 0 && excl < rem) work[pos++] = make_uint4(y, first + j, base + excl, v[j]);
+    excl += v[j];
+  }
+  const uint32_t got = min(total, rem);
+  base += got;
+  rem -= got;
+  __syncthreads();
+  if (threadIdx.x == 0) *s_nwork += ntake;
+  __syncthreads();
+  return got;
+}
+
+// (4) Walk the segment counts of the classes in `ord` for the first `quota` set
+// bits, then the host-free bitmap for the first K = quota - (free slots taken)
+// set bits, and record one work entry per segment that holds some of them.
+// Block-wide (T threads); stops as soon as the quota is met.
 template <int T>
 __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order &ord,
                             uint32_t quota, bool is_step, int *status) {
@@ -334,23 +394,8 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
   for (uint32_t y = 0; y < ord.n_cls && rem > 0; ++y) {
     const Bitmap bm = class_bitmap(g, geo, ord.cls[y]);
     uint32_t taken_y = 0;
-    for (uint32_t s0 = 0; s0 < geo.nseg && rem > 0; s0 += T) {
-      const uint32_t seg = s0 + threadIdx.x;
-      const uint32_t v = seg < geo.nseg ? __ldcg(&bm.cnt[seg]) : 0u;
-      uint32_t total, ntake;
-      const uint32_t inc = block_incl_scan<T>(v, &total);
-      const uint32_t excl = inc - v;
-      const uint32_t take = (v > 0 && excl < rem) ? 1u : 0u;
-      const uint32_t tpos = block_incl_scan<T>(take, &ntake);
-      if (take) g.work[s_nwork + tpos - 1] = make_uint4(y, seg, base + excl, v);
-      const uint32_t got = min(total, rem);
-      base += got;
-      rem -= got;
-      taken_y += got;
-      __syncthreads();
-      if (threadIdx.x == 0) s_nwork += ntake;
-      __syncthreads();
-    }
+    for (uint32_t s0 = 0; s0 < geo.nseg && rem > 0; s0 += T * kWalkSegs)
+      taken_y += walk_chunk<T>(bm.cnt, geo.nseg, s0, y, base, rem, g.work, &s_nwork);
     if (ord.cls[y] == geo.B + 1) taken_free += taken_y;
     else if (ord.cls[y] == geo.B) taken_cold += taken_y;
   }
@@ -359,22 +404,8 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
   const uint32_t K = (is_step && rem == 0) ? quota - F : (is_step ? 0u : rem);
   uint32_t hrem = K, hbase = 0;
   const Bitmap hb = host_free_bitmap(g);
-  for (uint32_t s0 = 0; s0 < geo.hseg && hrem > 0; s0 += T) {
-    const uint32_t seg = s0 + threadIdx.x;
-    const uint32_t v = seg < geo.hseg ? __ldcg(&hb.cnt[seg]) : 0u;
-    uint32_t total, ntake;
-    const uint32_t inc = block_incl_scan<T>(v, &total);
-    const uint32_t excl = inc - v;
-    const uint32_t take = (v > 0 && excl < hrem) ? 1u : 0u;
-    const uint32_t tpos = block_incl_scan<T>(take, &ntake);
-    if (take) g.work[s_nwork + tpos - 1] = make_uint4(kHostPos, seg, hbase + excl, v);
-    const uint32_t got = min(total, hrem);
-    hbase += got;
-    hrem -= got;
-    __syncthreads();
-    if (threadIdx.x == 0) s_nwork += ntake;
-    __syncthreads();
-  }
+  for (uint32_t s0 = 0; s0 < geo.hseg && hrem > 0; s0 += T * kWalkSegs)
+    walk_chunk<T>(hb.cnt, geo.hseg, s0, kHostPos, hbase, hrem, g.work, &s_nwork);
   if (threadIdx.x != 0) return;
   GroupCounters *c = g.cnt;
   if ((is_step && rem > 0) || hrem > 0) {
@@ -463,13 +494,14 @@ __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
     uint32_t word = (((s1 >> lane) & 1u) && wi < n0) ? bm.w0[wi] : 0u;
     const uint32_t pc = __popc(word);
     uint32_t rank = e.z + warp_incl_scan(pc) - pc;
+    uint32_t taken = 0;
     while (word && rank < q) {
       const uint32_t b = __ffs(word) - 1;
       word &= word - 1;
-      const uint32_t slot = wi * 32 + b;
-      dst[rank++] = slot;
-      if (host) bm_clear(bm, slot);  // claim the write-back (or placement) target
+      taken |= 1u << b;
+      dst[rank++] = wi * 32 + b;
     }
+    if (host && taken) bm_clear_mask(bm, wi, taken);  // claim the write-back targets
   }
 }
 
@@ -729,7 +761,7 @@ cudaError_t launch_bitmap_fill(Bitmap b, uint32_t nbits, cudaStream_t s) {
 
 cudaError_t launch_dedup(const StepParams &p, cudaStream_t s) {
   const uint32_t nblk = div_up(p.E, kEntryThreads);
-  if (nblk) k_dedup_stamp<<<nblk, kEntryThreads, 0, s>>>(p);
+  if (nblk) k_dedup_stamp<<<div_up(p.E, kStampThreads), kStampThreads, 0, s>>>(p);
   k_dedup_count_scan<<<nblk ? nblk : 1, kEntryThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
