@@ -140,12 +140,14 @@ int ula_free(ula_ctx *ctx, uint32_t logical_base, uint32_t n);
  *   (5) write each victim that holds data back to the host pool (the j-th such victim
  *       to the j-th lowest free host slot), fill each miss from its host slot, then
  *       update the map (moves complete before the map changes) and signal,
- *   (6) gather out[j][u] = layer j of unique address u, for every layer of the group:
- *       layer 0 before the call's work joins `stream`, layers 1.. on the context's
- *       low-priority side stream (prefetch).
+ *   (6) gather out[j][u] = layer j of unique address u, for every layer of the group.
+ *       Rows that hit are gathered on the context's low-priority side stream as soon
+ *       as the hits are known (their slots never move in this round); rows that
+ *       missed are written by the fill itself, from the bytes it moves.
  * The work runs on the context's internal highest-priority stream, ordered after
- * everything already enqueued on `stream`; `stream` is made to wait for it (through
- * layer 0), so work the caller enqueues next on `stream` sees layer 0 and the outputs.
+ * everything already enqueued on `stream`; `stream` is made to wait for the commit
+ * and for layer 0, so work the caller enqueues next on `stream` sees layer 0 and the
+ * other outputs; later layers are signalled through layer_ready.
  *   d_sel       : device [n_req][q][k] uint32 logical addresses; ULA_ADDR_PAD = none.
  *   d_out       : device [L_g][out_cap_rows][row_bytes]; rows [0, U) are written.
  *   d_entry_row : device [n_req*q*k] int32: row u of each entry, -1 for pads.
@@ -232,13 +234,14 @@ int ula_debug_inject(ula_ctx *ctx, int code);
  * ula_profile_read sums their durations.  Reading synchronises the context.
  */
 enum {
-  ULA_PHASE_DEDUP = 0,    /* dedup, translate, capacity check */
-  ULA_PHASE_ROTATE_MARK,  /* ring rotation, hit marking, CSR / entry rows */
-  ULA_PHASE_SELECT,       /* victim (or free-slot) selection */
-  ULA_PHASE_MOVE,         /* write-back, fill, map commit */
-  ULA_PHASE_GATHER,       /* one layer's row gather */
-  ULA_PHASE_ALLOC,        /* alloc placement and copy-in */
-  ULA_PHASE_FREE,         /* free */
+  ULA_PHASE_DEDUP = 0,  /* dedup, translate, capacity check */
+  ULA_PHASE_ROTATE,     /* ring rotation + compaction of unique rows and misses */
+  ULA_PHASE_MARK,       /* hit marking, entry rows, victim walk over segment counts */
+  ULA_PHASE_SELECT,     /* victim (or free-slot) index emission */
+  ULA_PHASE_MOVE,       /* write-back, fill (and the missed rows' outputs), map commit */
+  ULA_PHASE_GATHER,     /* one layer's gather of the hit rows */
+  ULA_PHASE_ALLOC,      /* alloc placement and copy-in */
+  ULA_PHASE_FREE,       /* free */
   ULA_PHASE_COUNT
 };
 

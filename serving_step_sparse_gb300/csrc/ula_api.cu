@@ -11,6 +11,7 @@
 // side-stream gathers, so a slot is never refilled while an earlier gather of
 // it is still reading.
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -38,6 +39,7 @@ struct ula_ctx {
   cudaStream_t crit = nullptr;  // internal, highest priority: the step's critical path
   cudaStream_t side = nullptr;  // internal, lowest priority: later-layer gathers
   cudaEvent_t in_evt = nullptr, out_evt = nullptr, commit_evt = nullptr;
+  cudaEvent_t marked_evt = nullptr, hit0_evt = nullptr;
   int move_blocks = 0, gather_blocks = 0;  // persistent grids (resident blocks)
   int emit_blocks = 0;
   cudaEvent_t side_evt[ULA_MAX_GROUPS] = {};
@@ -149,6 +151,19 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kMoveBlocksPerSm = 2;
+
+// blocks per SM from the environment (or `dflt`), clamped to [1, fit]
+int env_blocks(const char *name, int dflt, int fit) {
+  int v = dflt;
+  if (const char *e = std::getenv(name)) {
+    const int x = std::atoi(e);
+    if (x > 0) v = x;
+  }
+  if (v > fit) v = fit;
+  return v < 1 ? 1 : v;
+}
+
 // device-accessible address of a device or pinned host pointer, or nullptr
 void *device_address(const void *p, int device, bool allow_device, bool allow_host) {
   if (!p) return nullptr;
@@ -195,6 +210,8 @@ void destroy_resources(ula_ctx *c) {
   if (c->in_evt) cudaEventDestroy(c->in_evt);
   if (c->out_evt) cudaEventDestroy(c->out_evt);
   if (c->commit_evt) cudaEventDestroy(c->commit_evt);
+  if (c->marked_evt) cudaEventDestroy(c->marked_evt);
+  if (c->hit0_evt) cudaEventDestroy(c->hit0_evt);
   for (uint32_t g = 0; g < ULA_MAX_GROUPS; ++g)
     if (c->side_evt[g]) cudaEventDestroy(c->side_evt[g]);
   for (auto &t : c->prof_pending) {
@@ -242,7 +259,14 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(cudaEventCreateWithFlags(&c->in_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->out_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->commit_evt, cudaEventDisableTiming));
+  ULA_CUDA(cudaEventCreateWithFlags(&c->marked_evt, cudaEventDisableTiming));
+  ULA_CUDA(cudaEventCreateWithFlags(&c->hit0_evt, cudaEventDisableTiming));
   ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks));
+  // The move is bound by the host link and needs few SMs to saturate it; the hit
+  // gathers run beside it.  ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune
+  // the persistent grids (clamped to what fits on an SM).
+  c->move_blocks = env_blocks("ULA_MOVE_BLOCKS_PER_SM", kMoveBlocksPerSm, c->move_blocks);
+  c->gather_blocks = env_blocks("ULA_GATHER_BLOCKS_PER_SM", c->gather_blocks, c->gather_blocks);
   c->move_blocks *= c->sm_count;
   c->gather_blocks *= c->sm_count;
   c->emit_blocks = c->sm_count;
@@ -481,11 +505,29 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   for (uint32_t d = 1; d < B; ++d) p.order.cls[1 + d] = (cur + d) % B;
   // (1)(2) dedup + translate + capacity check
   ULA_CUDA(c->phase(ULA_PHASE_DEDUP, s, E ? 2 : 1, [&] { return launch_dedup(p, s); }));
-  // (3) rotate + compaction; hits into the current bucket, entry rows, victim walk
-  ULA_CUDA(c->phase(ULA_PHASE_ROTATE_MARK, s, 2, [&] {
-    cudaError_t e = launch_rotate_emit(p, s);
-    return e != cudaSuccess ? e : launch_mark_select(p, s);
-  }));
+  // (3a) rotation + compaction of unique rows and misses
+  ULA_CUDA(c->phase(ULA_PHASE_ROTATE, s, 1, [&] { return launch_rotate_emit(p, s); }));
+  // (3b) hits into the current bucket, entry rows; the victim walk
+  ULA_CUDA(c->phase(ULA_PHASE_MARK, s, 1, [&] { return launch_mark_select(p, s); }));
+  const bool gather = out_cap_rows != 0;
+  GatherParams gp{};
+  gp.geo = c->geo;
+  gp.grp = gd;
+  gp.out = static_cast<uint8_t *>(d_out);
+  gp.out_cap = out_cap_rows;
+  gp.status = c->status;
+  if (gather) {
+    // (6) the hit rows, on the prefetch stream, while the misses are being moved:
+    // a hit's slot does not change in its round
+    ULA_CUDA(cudaEventRecord(c->marked_evt, s));
+    ULA_CUDA(cudaStreamWaitEvent(c->side, c->marked_evt, 0));
+    for (uint32_t j = 0; j < gd.layers; ++j) {
+      gp.layer = j;
+      ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, 1,
+                        [&] { return launch_gather(gp, c->gather_blocks, c->side); }));
+      if (j == 0) ULA_CUDA(cudaEventRecord(c->hit0_evt, c->side));
+    }
+  }
   // (4) victims' and write-back slots' indices
   EmitParams ep{};
   ep.geo = c->geo;
@@ -496,42 +538,34 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   ep.status = c->status;
   ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
                     [&] { return launch_select_emit(ep, 1, c->emit_blocks, s); }));
-  // (5) write-back, fill, then map commit
+  // (5) write-back, fill (writing the missed rows' outputs), then map commit
   MoveParams mp{};
   mp.geo = c->geo;
   mp.grp = gd;
   mp.miss_list = c->miss_list;
   mp.addr_row = c->addr_row;
+  mp.out = gather ? static_cast<uint8_t *>(d_out) : nullptr;
+  mp.out_cap = out_cap_rows;
   mp.round = r;
   mp.cur = cur;
   mp.status = c->status;
   ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, 1, [&] { return launch_move(mp, c->move_blocks, s); }));
-  // signal: the commit event; every gather is ordered after it
+  // signal: the commit event; layer j is ready once its hit rows are gathered too
   ULA_CUDA(cudaEventRecord(c->commit_evt, s));
-  // (6) gather: layer 0 now, later layers on the side stream
-  GatherParams gp{};
-  gp.geo = c->geo;
-  gp.grp = gd;
-  gp.out = static_cast<uint8_t *>(d_out);
-  gp.out_cap = out_cap_rows;
-  gp.status = c->status;
-  gp.layer = 0;
-  if (out_cap_rows)
-    ULA_CUDA(c->phase(ULA_PHASE_GATHER, s, 1, [&] { return launch_gather(gp, c->gather_blocks, s); }));
+  if (gather) ULA_CUDA(cudaStreamWaitEvent(s, c->hit0_evt, 0));
   if (layer_ready && layer_ready[0])
     ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[0]), s));
-  if (gd.layers > 1) {
+  if (gather) {
     ULA_CUDA(cudaStreamWaitEvent(c->side, c->commit_evt, 0));
-    for (uint32_t j = 1; j < gd.layers; ++j) {
-      gp.layer = j;
-      if (out_cap_rows)
-        ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, 1,
-                          [&] { return launch_gather(gp, c->gather_blocks, c->side); }));
+    for (uint32_t j = 1; j < gd.layers; ++j)
       if (layer_ready && layer_ready[j])
         ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), c->side));
-    }
     ULA_CUDA(cudaEventRecord(c->side_evt[group], c->side));
     c->side_pending[group] = true;
+  } else {
+    for (uint32_t j = 1; j < gd.layers; ++j)
+      if (layer_ready && layer_ready[j])
+        ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), s));
   }
   ULA_CUDA(c->leave(caller));
   return ULA_OK;

@@ -16,9 +16,9 @@
 //   k_mark_select       (3b) hits move to the current bucket, entry rows; the last
 //                       block walks the segment counts (4) in class order
 //   k_select_emit       (4) the victims' and write-back slots' indices
-//   k_move_commit       (5) write-back, fill, map commit
-// and then k_gather (6), layer 0 on the critical path, the other layers on the
-// prefetch stream.
+//   k_move_commit       (5) write-back, fill, map commit; (6) the missed rows' outputs
+// and k_gather (6) for the rows that hit, on the prefetch stream, concurrent with
+// the selection and the move (hit slots never move in their round).
 //
 // Concurrency discipline for the bitmaps: inside one kernel a given bitmap is
 // either only set or only cleared.  That keeps the summary levels and the
@@ -441,7 +441,9 @@ __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
   const uint32_t U = g.cnt->U;
   if (i < U) {
     const uint32_t m = g.map[g.uniq[i]];
-    if (!(m & kHostBit)) {
+    if (m & kHostBit) {
+      g.row_slot[i] = kNone;  // filled (and its output written) by the move
+    } else {
       const uint32_t c = m < geo.S ? class_of(g.stamp[m], p.round, geo.B) : geo.B + 1;
       if (c == geo.B + 1) {
         latch(p.status, ULA_ERR_INTERNAL);
@@ -526,6 +528,8 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
   const size_t sb = (size_t)g.layers * geo.W;
   const uint32_t nvec = (uint32_t)(sb / 16);
+  const uint32_t CW = geo.W / 16;
+  uint4 *out = reinterpret_cast<uint4 *>(p.out);
   for (uint32_t i = warp; i < M; i += nwarps) {
     const uint32_t v = g.victims[i];
     const uint32_t a = p.miss_list[i];
@@ -534,9 +538,11 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
     const bool owned = i >= F;
     const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
     const uint32_t o = owned && v < geo.S ? g.owner[v] : kNone;
+    const uint32_t row = a < geo.max_logical ? p.addr_row[a] : kNone;
     const bool bad = v >= geo.S || loc == kUnalloc || !(loc & kHostBit) || hs >= geo.H ||
                      (owned && (hd >= geo.H || o >= geo.max_logical)) ||
-                     (!owned && v < geo.S && g.owner[v] != kNone);
+                     (!owned && v < geo.S && g.owner[v] != kNone) ||
+                     (out && row >= p.out_cap);
     if (bad) {
       if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
       continue;
@@ -568,6 +574,16 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
         const uint32_t c = c0 + u * 32 + lane;
         if (c < nvec) gp[c] = fill[u];
       }
+      if (out) {  // (6) for a missed row: its outputs straight from the moved bytes
+#pragma unroll
+        for (int u = 0; u < kMoveUnroll; ++u) {
+          const uint32_t c = c0 + u * 32 + lane;
+          if (c < nvec) {
+            const uint32_t j = c / CW;
+            out[((size_t)j * p.out_cap + row) * CW + (c - j * CW)] = fill[u];
+          }
+        }
+      }
     }
     __syncwarp();
     if (lane == 0) {
@@ -580,7 +596,6 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
         bm_set(class_bitmap(g, geo, p.cur), v);
       }
       g.stamp[v] = p.round;
-      g.row_slot[p.addr_row[a]] = v;
       bm_set(host_free_bitmap(g), hs);
     }
   }
@@ -588,12 +603,14 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
 
 // ------------------------------------------------------------------ gather
 //
-// (6) out[layer][u] = layer `layer` of the slot that the commit recorded for
-// unique row u (the committed map's entry for uniq[u]).  The U rows are spread
-// over all warps (rows_per_warp = ceil(U / warps), at most 32): lanes read the
-// warp's slots, then the warp streams the rows' 16-byte chunks, consecutive lanes
-// on consecutive chunks (coalesced within a row; the warp's output rows are
-// contiguous).  Loads are issued kGatherUnroll deep before the stores.
+// (6) out[layer][u] = layer `layer` of unique row u's slot, for the rows that hit
+// (recorded by the marking; a hit's slot does not change in its round, so this
+// runs while the misses are being moved; missed rows are written by the move).
+// The U rows are spread over all warps (rows_per_warp = ceil(U / warps), at most
+// 32): lanes read the warp's slots, then the warp streams the rows' 16-byte
+// chunks, consecutive lanes on consecutive chunks (coalesced within a row; the
+// warp's output rows are contiguous).  Loads are issued kGatherUnroll deep before
+// the stores.
 constexpr int kGatherUnroll = 8;
 
 __global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
@@ -613,12 +630,12 @@ __global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
   const uint32_t r0 = lane / CW, c0 = lane % CW;  // chunk (row, col) of f = lane
   for (uint32_t row0 = warp * rpw; row0 < U; row0 += nwarps * rpw) {
     const uint32_t nrows = min(rpw, U - row0);
-    uint32_t slot = 0;
+    uint32_t slot = kNone;
     bool bad = false;
     if (lane < nrows) {
       const uint32_t m = g.row_slot[row0 + lane];
-      bad = m >= geo.S;
-      slot = bad ? 0u : m;
+      bad = m != kNone && m >= geo.S;
+      slot = bad ? kNone : m;
     }
     if (__any_sync(0xffffffffu, bad)) {
       if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
@@ -633,7 +650,7 @@ __global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
 #pragma unroll
       for (int u = 0; u < kGatherUnroll; ++u) {
         const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
-        if (f0 + u * 32 + lane < total) v[u] = __ldcs(pool + (size_t)s * sbv + c);
+        if (f0 + u * 32 + lane < total && s != kNone) v[u] = __ldcs(pool + (size_t)s * sbv + c);
         c += 32;
         while (c >= CW) {
           c -= CW;
@@ -644,7 +661,8 @@ __global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
       c = cs;
 #pragma unroll
       for (int u = 0; u < kGatherUnroll; ++u) {
-        if (f0 + u * 32 + lane < total) orow[(size_t)r * CW + c] = v[u];
+        const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
+        if (f0 + u * 32 + lane < total && s != kNone) orow[(size_t)r * CW + c] = v[u];
         c += 32;
         while (c >= CW) {
           c -= CW;

@@ -28,7 +28,7 @@ ERR_TIMEOUT = 5
 ERR_POISONED = 6
 ERR_INTERNAL = 7
 
-PHASES = ["dedup", "rotate_mark", "select", "move", "gather", "alloc", "free"]
+PHASES = ["dedup", "rotate", "mark", "select", "move", "gather", "alloc", "free"]
 NOALLOC_MAX_ENTRIES = 65536
 
 
