@@ -37,7 +37,8 @@ struct ula_ctx {
   int sm_count = 0;
   cudaStream_t home = nullptr;  // the caller's stream given at create (alloc/free order)
   cudaStream_t crit = nullptr;  // internal, highest priority: the step's critical path
-  cudaStream_t side = nullptr;  // internal, lowest priority: later-layer gathers
+  cudaStream_t side = nullptr;  // internal, lowest priority: later layers' hit gathers
+  cudaStream_t first = nullptr; // internal, highest priority: layer 0's hit gather
   cudaEvent_t in_evt = nullptr, out_evt = nullptr, commit_evt = nullptr;
   cudaEvent_t marked_evt = nullptr, hit0_evt = nullptr;
   int move_blocks = 0, gather_blocks = 0;  // persistent grids (resident blocks)
@@ -51,7 +52,7 @@ struct ula_ctx {
   unsigned long long *tbl = nullptr;
   uint32_t *addr_row = nullptr;
   uint2 *blk = nullptr;
-  uint32_t *miss_list = nullptr;
+  uint32_t *miss_list = nullptr, *miss_hs = nullptr, *miss_row = nullptr;
   int *status = nullptr;
   uint32_t decision_cap = 0;
   uint32_t epoch = 0;
@@ -207,6 +208,7 @@ void destroy_resources(ula_ctx *c) {
   c->allocations.clear();
   if (c->side) cudaStreamDestroy(c->side);
   if (c->crit) cudaStreamDestroy(c->crit);
+  if (c->first) cudaStreamDestroy(c->first);
   if (c->in_evt) cudaEventDestroy(c->in_evt);
   if (c->out_evt) cudaEventDestroy(c->out_evt);
   if (c->commit_evt) cudaEventDestroy(c->commit_evt);
@@ -256,6 +258,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest));
   ULA_CUDA(cudaStreamCreateWithPriority(&c->crit, cudaStreamNonBlocking, prio_greatest));
   ULA_CUDA(cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, prio_least));
+  ULA_CUDA(cudaStreamCreateWithPriority(&c->first, cudaStreamNonBlocking, prio_greatest));
   ULA_CUDA(cudaEventCreateWithFlags(&c->in_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->out_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->commit_evt, cudaEventDisableTiming));
@@ -279,6 +282,8 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(c->alloc(&c->addr_row, cfg.max_logical));
   ULA_CUDA(c->alloc(&c->blk, max_blk));
   ULA_CUDA(c->alloc(&c->miss_list, cfg.max_entries));
+  ULA_CUDA(c->alloc(&c->miss_hs, cfg.max_entries));
+  ULA_CUDA(c->alloc(&c->miss_row, cfg.max_entries));
   ULA_CUDA(c->alloc(&c->status, 1));
   ULA_CUDA(c->alloc(&c->cnt_d, G));
   ULA_CUDA(c->alloc(&c->groups_d, G));
@@ -497,6 +502,8 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.addr_row = c->addr_row;
   p.blk = c->blk;
   p.miss_list = c->miss_list;
+  p.miss_hs = c->miss_hs;
+  p.miss_row = c->miss_row;
   p.status = c->status;
   c->inject = 0;
   p.order.n_cls = B + 1;  // victims: free, cold, ring oldest (cur+1) .. newest (cur-1)
@@ -517,15 +524,20 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   gp.out_cap = out_cap_rows;
   gp.status = c->status;
   if (gather) {
-    // (6) the hit rows, on the prefetch stream, while the misses are being moved:
-    // a hit's slot does not change in its round
+    // (6) the hit rows, while the misses are being moved (a hit's slot does not
+    // change in its round): layer 0 on a high-priority stream, the later layers
+    // on the low-priority prefetch stream
     ULA_CUDA(cudaEventRecord(c->marked_evt, s));
+    ULA_CUDA(cudaStreamWaitEvent(c->first, c->marked_evt, 0));
+    gp.layer = 0;
+    ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->first, 1,
+                      [&] { return launch_gather(gp, c->gather_blocks, c->first); }));
+    ULA_CUDA(cudaEventRecord(c->hit0_evt, c->first));
     ULA_CUDA(cudaStreamWaitEvent(c->side, c->marked_evt, 0));
-    for (uint32_t j = 0; j < gd.layers; ++j) {
+    for (uint32_t j = 1; j < gd.layers; ++j) {
       gp.layer = j;
       ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, 1,
                         [&] { return launch_gather(gp, c->gather_blocks, c->side); }));
-      if (j == 0) ULA_CUDA(cudaEventRecord(c->hit0_evt, c->side));
     }
   }
   // (4) victims' and write-back slots' indices
@@ -543,13 +555,14 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   mp.geo = c->geo;
   mp.grp = gd;
   mp.miss_list = c->miss_list;
-  mp.addr_row = c->addr_row;
+  mp.miss_hs = c->miss_hs;
+  mp.miss_row = c->miss_row;
   mp.out = gather ? static_cast<uint8_t *>(d_out) : nullptr;
   mp.out_cap = out_cap_rows;
   mp.round = r;
   mp.cur = cur;
   mp.status = c->status;
-  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, 1, [&] { return launch_move(mp, c->move_blocks, s); }));
+  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, 2, [&] { return launch_move(mp, c->move_blocks, s); }));
   // signal: the commit event; layer j is ready once its hit rows are gathered too
   ULA_CUDA(cudaEventRecord(c->commit_evt, s));
   if (gather) ULA_CUDA(cudaStreamWaitEvent(s, c->hit0_evt, 0));
@@ -579,6 +592,7 @@ static int sync_impl(ula_ctx *c) {
       c->side_pending[g] = false;
     }
   ULA_CUDA(cudaStreamSynchronize(c->crit));
+  ULA_CUDA(cudaStreamSynchronize(c->first));
   ULA_CUDA(cudaStreamSynchronize(c->home));
   return ULA_OK;
 }

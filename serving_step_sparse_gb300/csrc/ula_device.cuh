@@ -134,6 +134,8 @@ struct StepParams {
   uint32_t *addr_row;       // [max_logical]: unique row of an address this step
   uint2 *blk;               // [blocks]: (first occurrences, misses) per block, then offsets
   uint32_t *miss_list;      // [max_entries]: misses in first-occurrence order
+  uint32_t *miss_hs;        // [max_entries]: host slot of miss i
+  uint32_t *miss_row;       // [max_entries]: unique row of miss i
   int *status;              // latched device error (0 = none)
 };
 
@@ -150,8 +152,9 @@ struct EmitParams {
 struct MoveParams {
   Geometry geo;
   GroupDev grp;
-  const uint32_t *miss_list;
-  const uint32_t *addr_row;
+  const uint32_t *miss_list;  // [M] addresses
+  const uint32_t *miss_hs;    // [M] their host slots
+  const uint32_t *miss_row;   // [M] their unique rows
   uint8_t *out;             // [L][out_cap][W]: the missed rows' outputs (NULL: none)
   uint32_t out_cap;
   uint32_t round, cur;
@@ -195,7 +198,7 @@ cudaError_t launch_mark_select(const StepParams &p, cudaStream_t s);
 cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int blocks, cudaStream_t s);
 // alloc: walk of the free class and the host-free bitmap for a quota of n, per group
 cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s);
-cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s);
+cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s);  // copies, then commit
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s);

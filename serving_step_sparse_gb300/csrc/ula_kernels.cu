@@ -7,7 +7,7 @@
 // (bucket ring + cold bucket, rotation by relabelling, victim order, bitmaps
 // with summary levels, parallel hit detection/dedup, move -> map -> signal).
 //
-// One step of one group is six launches on the critical path:
+// One step of one group is seven launches on the critical path:
 //   k_dedup_stamp       (1) every entry bids to be its address's first occurrence
 //   k_dedup_count_scan  (1)(2) per-block counts of first occurrences / misses; the
 //                       last block scans them and runs the capacity check
@@ -16,7 +16,8 @@
 //   k_mark_select       (3b) hits move to the current bucket, entry rows; the last
 //                       block walks the segment counts (4) in class order
 //   k_select_emit       (4) the victims' and write-back slots' indices
-//   k_move_commit       (5) write-back, fill, map commit; (6) the missed rows' outputs
+//   k_move              (5) write-back and fill; (6) the missed rows' outputs
+//   k_commit            (5) map, labels and host slots, after the copies
 // and k_gather (6) for the rows that hit, on the prefetch stream, concurrent with
 // the selection and the move (hit slots never move in their round).
 //
@@ -332,7 +333,11 @@ __global__ void __launch_bounds__(kEntryThreads) k_rotate_emit(StepParams p) {
   if (!f.first) return;
   p.grp.uniq[pos] = f.a;
   p.addr_row[f.a] = pos;
-  if (f.miss) p.miss_list[mpos] = f.a;
+  if (f.miss) {
+    p.miss_list[mpos] = f.a;
+    p.miss_hs[mpos] = p.grp.map[f.a] & kSlotMask;
+    p.miss_row[mpos] = pos;
+  }
 }
 
 // (4) Walk the segment counts of the classes in `ord` for the first `quota` set
@@ -509,16 +514,18 @@ __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
 
 // -------------------------------------------------------- move and commit
 //
-// (5) per victim i (one warp): write the victim's rows back to its host slot
-// if it holds data, fill miss i's rows from its host slot, then update the map
-// (after this warp's copies), move the slot into the current bucket, record
-// the row's slot for the gather and release the miss's host slot.  Each lane
-// handles the same 16-byte chunks in the write-back and in the fill, so its read
-// of a chunk precedes its write of the same chunk.  Host memory is reached
-// directly over the host link.
+// (5) Data first: per victim i (one warp), write the victim's rows back to its
+// host slot if it holds data and fill miss i's rows from its host slot; for the
+// missed row, its outputs are written straight from the moved bytes (6).  Each
+// lane handles the same 16-byte chunks in the write-back and in the fill, so
+// its read of a chunk precedes its write of the same chunk.  Host memory is
+// reached directly over the host link.  The per-victim plan (victim slot, host
+// slots, row) is read up front from arrays filled by the compaction and the
+// selection, so a warp starts its copies after one round of independent loads.
+// Then, in the next kernel, the map and the labels (k_commit).
 constexpr int kMoveUnroll = 6;
 
-__global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
+__global__ void __launch_bounds__(256, 3) k_move(MoveParams p) {
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -532,18 +539,11 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
   uint4 *out = reinterpret_cast<uint4 *>(p.out);
   for (uint32_t i = warp; i < M; i += nwarps) {
     const uint32_t v = g.victims[i];
-    const uint32_t a = p.miss_list[i];
-    const uint32_t loc = a < geo.max_logical ? g.map[a] : kUnalloc;
-    const uint32_t hs = loc & kSlotMask;
+    const uint32_t hs = p.miss_hs[i];
+    const uint32_t row = p.miss_row[i];
     const bool owned = i >= F;
     const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
-    const uint32_t o = owned && v < geo.S ? g.owner[v] : kNone;
-    const uint32_t row = a < geo.max_logical ? p.addr_row[a] : kNone;
-    const bool bad = v >= geo.S || loc == kUnalloc || !(loc & kHostBit) || hs >= geo.H ||
-                     (owned && (hd >= geo.H || o >= geo.max_logical)) ||
-                     (!owned && v < geo.S && g.owner[v] != kNone) ||
-                     (out && row >= p.out_cap);
-    if (bad) {
+    if (v >= geo.S || hs >= geo.H || (owned && hd >= geo.H) || (out && row >= p.out_cap)) {
       if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
       continue;
     }
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
         const uint32_t c = c0 + u * 32 + lane;
         if (c < nvec) gp[c] = fill[u];
       }
-      if (out) {  // (6) for a missed row: its outputs straight from the moved bytes
+      if (out) {  // (6) the missed row's outputs, from the moved bytes
 #pragma unroll
         for (int u = 0; u < kMoveUnroll; ++u) {
           const uint32_t c = c0 + u * 32 + lane;
@@ -585,19 +585,42 @@ __global__ void __launch_bounds__(256, 3) k_move_commit(MoveParams p) {
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      if (owned) g.map[o] = kHostBit | hd;
-      g.map[a] = v;
-      g.owner[v] = a;
-      const uint32_t c = class_of(g.stamp[v], p.round, geo.B);
-      if (c != p.cur) {
-        bm_clear(class_bitmap(g, geo, c), v);
-        bm_set(class_bitmap(g, geo, p.cur), v);
-      }
-      g.stamp[v] = p.round;
-      bm_set(host_free_bitmap(g), hs);
+  }
+}
+
+// (5) Then the map: one thread per victim, after every copy has completed
+// (kernel boundary).  The evicted owner now maps to its host slot, the miss to
+// the victim slot; the slot joins the current bucket (clears on its old class,
+// sets on cur); the miss's host slot is released (sets only on the host-free
+// bitmap).
+__global__ void k_commit(MoveParams p) {
+  if (*(volatile int *)p.status) return;
+  const GroupDev &g = p.grp;
+  const Geometry &geo = p.geo;
+  const uint32_t M = g.cnt->M, F = g.cnt->F;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < M; i += stride) {
+    const uint32_t v = g.victims[i];
+    const uint32_t a = p.miss_list[i];
+    const uint32_t hs = p.miss_hs[i];
+    const bool owned = i >= F;
+    const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
+    const uint32_t o = v < geo.S ? g.owner[v] : kNone;
+    if (v >= geo.S || a >= geo.max_logical || hs >= geo.H ||
+        (owned ? (hd >= geo.H || o >= geo.max_logical) : o != kNone)) {
+      latch(p.status, ULA_ERR_INTERNAL);
+      continue;
     }
+    if (owned) g.map[o] = kHostBit | hd;
+    g.map[a] = v;
+    g.owner[v] = a;
+    const uint32_t c = class_of(g.stamp[v], p.round, geo.B);
+    if (c != p.cur) {
+      bm_clear(class_bitmap(g, geo, c), v);
+      bm_set(class_bitmap(g, geo, p.cur), v);
+    }
+    g.stamp[v] = p.round;
+    bm_set(host_free_bitmap(g), hs);
   }
 }
 
@@ -812,13 +835,14 @@ cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStre
 }
 
 cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm) {
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move_commit, 256, 0);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move, 256, 0);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather, 256, 0);
 }
 
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
-  k_move_commit<<<blocks, 256, 0, s>>>(p);
+  k_move<<<blocks, 256, 0, s>>>(p);
+  k_commit<<<blocks, 256, 0, s>>>(p);  // grid-stride over the victims
   return cudaGetLastError();
 }
 
