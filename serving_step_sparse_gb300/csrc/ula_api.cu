@@ -41,7 +41,7 @@ struct ula_ctx {
   cudaStream_t first = nullptr; // internal, highest priority: layer 0's hit gather
   cudaEvent_t in_evt = nullptr, out_evt = nullptr, commit_evt = nullptr;
   cudaEvent_t marked_evt = nullptr, hit0_evt = nullptr;
-  int move_blocks = 0;  // persistent grid of the move (resident blocks)
+  int move_blocks = 0, gather_blocks = 0;  // persistent grids (resident blocks)
   int emit_blocks = 0;
   cudaEvent_t side_evt[ULA_MAX_GROUPS] = {};
   bool side_pending[ULA_MAX_GROUPS] = {};
@@ -264,12 +264,14 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(cudaEventCreateWithFlags(&c->commit_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->marked_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->hit0_evt, cudaEventDisableTiming));
-  ULA_CUDA(resident_blocks(&c->move_blocks));
+  ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks));
   // The move is bound by the host link and needs few SMs to saturate it; the hit
-  // gathers run beside it.  ULA_MOVE_BLOCKS_PER_SM tunes its persistent grid
-  // (clamped to what fits on an SM).
+  // gathers run beside it.  ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune
+  // the persistent grids (clamped to what fits on an SM).
   c->move_blocks = env_blocks("ULA_MOVE_BLOCKS_PER_SM", kMoveBlocksPerSm, c->move_blocks);
+  c->gather_blocks = env_blocks("ULA_GATHER_BLOCKS_PER_SM", c->gather_blocks, c->gather_blocks);
   c->move_blocks *= c->sm_count;
+  c->gather_blocks *= c->sm_count;
   c->emit_blocks = c->sm_count;
   for (uint32_t g = 0; g < G; ++g)
     ULA_CUDA(cudaEventCreateWithFlags(&c->side_evt[g], cudaEventDisableTiming));
@@ -515,7 +517,6 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   // (3b) hits into the current bucket, entry rows; the victim walk
   ULA_CUDA(c->phase(ULA_PHASE_MARK, s, 1, [&] { return launch_mark_select(p, s); }));
   const bool gather = out_cap_rows != 0;
-  const uint32_t gather_rows = (uint32_t)(E < out_cap_rows ? E : out_cap_rows);  // >= U
   GatherParams gp{};
   gp.geo = c->geo;
   gp.grp = gd;
@@ -530,13 +531,13 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
     ULA_CUDA(cudaStreamWaitEvent(c->first, c->marked_evt, 0));
     gp.layer = 0;
     ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->first, 1,
-                      [&] { return launch_gather(gp, gather_rows, c->first); }));
+                      [&] { return launch_gather(gp, c->gather_blocks, c->first); }));
     ULA_CUDA(cudaEventRecord(c->hit0_evt, c->first));
     ULA_CUDA(cudaStreamWaitEvent(c->side, c->marked_evt, 0));
     for (uint32_t j = 1; j < gd.layers; ++j) {
       gp.layer = j;
       ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, 1,
-                        [&] { return launch_gather(gp, gather_rows, c->side); }));
+                        [&] { return launch_gather(gp, c->gather_blocks, c->side); }));
     }
   }
   // (4) victims' and write-back slots' indices

@@ -199,12 +199,11 @@ cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int block
 // alloc: walk of the free class and the host-free bitmap for a quota of n, per group
 cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s);
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s);  // copies, then commit
-// one block per 64 rows up to max_rows (an upper bound of U known on the host)
-cudaError_t launch_gather(const GatherParams &p, uint32_t max_rows, cudaStream_t s);
+cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s);
 cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);
-// resident 256-thread blocks per SM of the persistent move kernel
-cudaError_t resident_blocks(int *move_per_sm);
+// resident 256-thread blocks per SM of the persistent kernels
+cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm);
 
 }  // namespace ula

@@ -629,66 +629,68 @@ __global__ void k_commit(MoveParams p) {
 // (6) out[layer][u] = layer `layer` of unique row u's slot, for the rows that hit
 // (recorded by the marking; a hit's slot does not change in its round, so this
 // runs while the misses are being moved; missed rows are written by the move).
-// Short blocks, not a persistent grid: each warp takes kGatherRowsPerWarp rows
-// and exits, so the critical path's kernels get SMs as soon as blocks retire.
-// Lanes read the warp's slots, then the warp streams the rows' 16-byte chunks,
-// consecutive lanes on consecutive chunks (coalesced within a row; the warp's
-// output rows are contiguous).  Loads are issued kGatherUnroll deep before the
-// stores.
+// The U rows are spread over all warps (rows_per_warp = ceil(U / warps), at most
+// 32): lanes read the warp's slots, then the warp streams the rows' 16-byte
+// chunks, consecutive lanes on consecutive chunks (coalesced within a row; the
+// warp's output rows are contiguous).  Loads are issued kGatherUnroll deep before
+// the stores.
 constexpr int kGatherUnroll = 8;
-constexpr uint32_t kGatherRowsPerWarp = 8;
-constexpr uint32_t kGatherRowsPerBlock = kGatherRowsPerWarp * 8;  // 256 threads
 
-__global__ void __launch_bounds__(256) k_gather(GatherParams p) {
+__global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
   const uint32_t U = g.cnt->U;
   const uint32_t lane = lane_id();
-  const uint32_t row0 = blockIdx.x * kGatherRowsPerBlock + (threadIdx.x >> 5) * kGatherRowsPerWarp;
-  if (row0 >= U) return;
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
   const uint32_t CW = geo.W / 16;
   const size_t sbv = (size_t)g.layers * CW;  // slot stride in uint4
   const uint4 *pool = reinterpret_cast<const uint4 *>(g.gpu_pool) + (size_t)p.layer * CW;
   uint4 *out = reinterpret_cast<uint4 *>(p.out) + (size_t)p.layer * p.out_cap * CW;
-  const uint32_t nrows = min(kGatherRowsPerWarp, U - row0);
-  uint32_t slot = kNone;
-  bool bad = false;
-  if (lane < nrows) {
-    const uint32_t m = g.row_slot[row0 + lane];
-    bad = m != kNone && m >= geo.S;
-    slot = bad ? kNone : m;
-  }
-  if (__any_sync(0xffffffffu, bad)) {
-    if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
-    return;
-  }
-  const uint32_t total = nrows * CW;
-  uint4 *orow = out + (size_t)row0 * CW;
-  uint32_t r = lane / CW, c = lane % CW;  // chunk (row, col) of f = lane
-  for (uint32_t f0 = 0; f0 < total; f0 += 32 * kGatherUnroll) {
-    uint4 v[kGatherUnroll];
-    const uint32_t rs = r, cs = c;
-#pragma unroll
-    for (int u = 0; u < kGatherUnroll; ++u) {
-      const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
-      if (f0 + u * 32 + lane < total && s != kNone) v[u] = __ldcs(pool + (size_t)s * sbv + c);
-      c += 32;
-      while (c >= CW) {
-        c -= CW;
-        ++r;
-      }
+  uint32_t rpw = (U + nwarps - 1) / nwarps;
+  rpw = rpw < 1 ? 1 : (rpw > 32 ? 32 : rpw);
+  const uint32_t r0 = lane / CW, c0 = lane % CW;  // chunk (row, col) of f = lane
+  for (uint32_t row0 = warp * rpw; row0 < U; row0 += nwarps * rpw) {
+    const uint32_t nrows = min(rpw, U - row0);
+    uint32_t slot = kNone;
+    bool bad = false;
+    if (lane < nrows) {
+      const uint32_t m = g.row_slot[row0 + lane];
+      bad = m != kNone && m >= geo.S;
+      slot = bad ? kNone : m;
     }
-    r = rs;
-    c = cs;
+    if (__any_sync(0xffffffffu, bad)) {
+      if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
+      continue;
+    }
+    const uint32_t total = nrows * CW;
+    uint4 *orow = out + (size_t)row0 * CW;
+    uint32_t r = r0, c = c0;
+    for (uint32_t f0 = 0; f0 < total; f0 += 32 * kGatherUnroll) {
+      uint4 v[kGatherUnroll];
+      const uint32_t rs = r, cs = c;
 #pragma unroll
-    for (int u = 0; u < kGatherUnroll; ++u) {
-      const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
-      if (f0 + u * 32 + lane < total && s != kNone) orow[(size_t)r * CW + c] = v[u];
-      c += 32;
-      while (c >= CW) {
-        c -= CW;
-        ++r;
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
+        if (f0 + u * 32 + lane < total && s != kNone) v[u] = __ldcs(pool + (size_t)s * sbv + c);
+        c += 32;
+        while (c >= CW) {
+          c -= CW;
+          ++r;
+        }
+      }
+      r = rs;
+      c = cs;
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
+        if (f0 + u * 32 + lane < total && s != kNone) orow[(size_t)r * CW + c] = v[u];
+        c += 32;
+        while (c >= CW) {
+          c -= CW;
+          ++r;
+        }
       }
     }
   }
@@ -832,8 +834,10 @@ cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStre
   return cudaGetLastError();
 }
 
-cudaError_t resident_blocks(int *move_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move, 256, 0);
+cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm) {
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move, 256, 0);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather, 256, 0);
 }
 
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
@@ -842,9 +846,8 @@ cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const GatherParams &p, uint32_t max_rows, cudaStream_t s) {
-  const uint32_t blocks = div_up(max_rows, kGatherRowsPerBlock);  // rows beyond U exit at once
-  k_gather<<<blocks ? blocks : 1, 256, 0, s>>>(p);
+cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s) {
+  k_gather<<<blocks, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
