@@ -226,6 +226,12 @@ int ula_debug_export(ula_ctx *ctx, uint32_t group, ula_debug_state *st);
 /* The next ula_step_group latches `code` on the device before it changes anything
  * (host-side fault injection for tests of the error path; no GPU fault). */
 int ula_debug_inject(ula_ctx *ctx, int code);
+/* Re-run the gather of the hit rows of `group`'s last step for one layer into d_out
+ * ([L_g][out_cap_rows][row_bytes], device) on `stream`, changing no state (for timing
+ * the gather kernel on its own).  Valid until the group's slots change again (its next
+ * step, or any alloc/free). */
+int ula_debug_regather(ula_ctx *ctx, uint32_t group, uint32_t layer, void *d_out,
+                       uint32_t out_cap_rows, void *stream);
 
 /* ------------------------------------------------------------ profiling
  * Kernel launches are counted per phase always.  When enabled, every phase

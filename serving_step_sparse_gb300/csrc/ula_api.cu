@@ -728,6 +728,30 @@ int ula_profile_read(ula_ctx *c, ula_profile *out, int reset) {
   return ULA_OK;
 }
 
+int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, void *d_out,
+                       uint32_t out_cap_rows, void *stream) {
+  if (!c || group >= c->cfg.n_groups || !d_out || !aligned16(d_out)) return ULA_ERR_INVALID_ARG;
+  if (c->poisoned) return ULA_ERR_POISONED;
+  const GroupDev &gd = c->groups_h[group];
+  if (layer >= gd.layers || out_cap_rows < 1) return ULA_ERR_INVALID_ARG;
+  ULA_CUDA(c->ensure_device());
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+  ULA_CUDA(c->enter(caller));
+  ULA_CUDA(c->wait_side(c->crit, group));
+  GroupCounters cnt;
+  ULA_CUDA(cudaMemcpy(&cnt, gd.cnt, sizeof(cnt), cudaMemcpyDeviceToHost));
+  if (cnt.U > out_cap_rows) return ULA_ERR_CAPACITY;
+  GatherParams gp{};
+  gp.geo = c->geo;
+  gp.grp = gd;
+  gp.out = static_cast<uint8_t *>(d_out);
+  gp.out_cap = out_cap_rows;
+  gp.layer = layer;
+  gp.status = c->status;
+  ULA_CUDA(launch_gather(gp, c->gather_blocks, caller));
+  return ULA_OK;
+}
+
 int ula_debug_inject(ula_ctx *c, int code) {
   if (!c) return ULA_ERR_INVALID_ARG;
   if (c->poisoned) return ULA_ERR_POISONED;

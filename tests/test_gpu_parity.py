@@ -344,3 +344,28 @@ def test_layer_ready_events_and_side_stream_order():
             apply_events(orc.alloc, orc.free, ev)
     finally:
         gpu.close()
+
+
+def test_regather_reproduces_hit_rows():
+    """ula_debug_regather (used to time the gather alone) writes the same hit rows."""
+    from serving_step_sparse_gb300 import ula
+    w = small("cfg1").replace(steps=5)
+    gpu = GpuRun(w)
+    try:
+        for _ in range(w.steps):
+            gpu.step()
+        for g in range(w.n_groups):
+            st = gpu.cache.export(g)
+            U = st["U"]
+            hit = st["row_slot"][:U] != 0xFFFFFFFF
+            assert hit.sum() == st["hits"]
+            for j in range(w.layers_per_group):
+                buf = torch.zeros_like(gpu.outs[g])
+                ula.ula_debug_regather(gpu.cache.ctx, g, j, buf.data_ptr(), buf.shape[1],
+                                       torch.cuda.current_stream().cuda_stream)
+                torch.cuda.synchronize()
+                got = buf[j, :U].cpu().numpy()[hit]
+                exp = gpu.outs[g][j, :U].cpu().numpy()[hit]
+                assert np.array_equal(got, exp)
+    finally:
+        gpu.close()
