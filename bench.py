@@ -50,6 +50,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--requests", type=int, default=None,
                     help="run the workload's recipe with fewer live requests (profiling cases)")
+    ap.add_argument("--traffic-case", action="store_true",
+                    help="after the warm-up steps, re-gather group 0's hit rows once (layer 0) "
+                         "and print their number: the launch an ncu traffic capture takes")
     return ap.parse_args(argv)
 
 
@@ -262,6 +265,15 @@ def run_gpu(args, rank, world, local):
     for t in range(args.warmup):
         do_step(sel_dev[t], steps[t][1], rows_dev[t])
     st0 = cache.sync()
+    if args.traffic_case:
+        st = cache.export(0)
+        out = cache.out_buffer(0, max(1, st["U"]))
+        ula.ula_debug_regather(cache.ctx, 0, 0, out.data_ptr(), out.shape[1], stream.cuda_stream)
+        torch.cuda.synchronize()
+        print(json.dumps({"traffic_case": {"hit_rows": st["hits"], "unique_rows": st["U"],
+                                           "gather_launches_before": args.warmup * G * L}}))
+        cache.close()
+        sys.exit(0)
     ula.ula_profile_read(cache.ctx, reset=True)
     if world > 1:
         import torch.distributed as dist
