@@ -228,8 +228,9 @@ int ula_debug_export(ula_ctx *ctx, uint32_t group, ula_debug_state *st);
 int ula_debug_inject(ula_ctx *ctx, int code);
 /* Re-run the gather of the hit rows of `group`'s last step for one layer into d_out
  * ([L_g][out_cap_rows][row_bytes], device) on `stream`, changing no state (for timing
- * the gather kernel on its own).  Valid until the group's slots change again (its next
- * step, or any alloc/free). */
+ * the gather kernel on its own).  Launches at once: the caller orders it after the
+ * step (e.g. ula_sync) and before the group's slots change again (its next step, or
+ * any alloc/free).  More rows than out_cap_rows latch ULA_ERR_CAPACITY. */
 int ula_debug_regather(ula_ctx *ctx, uint32_t group, uint32_t layer, void *d_out,
                        uint32_t out_cap_rows, void *stream);
 

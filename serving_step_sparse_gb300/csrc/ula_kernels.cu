@@ -641,6 +641,10 @@ __global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
   const uint32_t U = g.cnt->U;
+  if (U > p.out_cap) {  // only a re-gather into a short buffer can get here
+    if (blockIdx.x == 0 && threadIdx.x == 0) latch(p.status, ULA_ERR_CAPACITY);
+    return;
+  }
   const uint32_t lane = lane_id();
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
