@@ -558,6 +558,10 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   MoveParams mp{};
   mp.geo = c->geo;
   mp.grp = gd;
+  mp.sel = d_sel;
+  mp.entry_row = d_entry_row;
+  mp.addr_row = c->addr_row;
+  mp.E = (uint32_t)E;
   mp.miss_list = c->miss_list;
   mp.miss_hs = c->miss_hs;
   mp.miss_row = c->miss_row;

@@ -152,6 +152,10 @@ struct EmitParams {
 struct MoveParams {
   Geometry geo;
   GroupDev grp;
+  const uint32_t *sel;        // [E] the step's selection (entry rows are written at commit)
+  int32_t *entry_row;         // [E]
+  const uint32_t *addr_row;   // [max_logical]
+  uint32_t E;
   const uint32_t *miss_list;  // [M] addresses
   const uint32_t *miss_hs;    // [M] their host slots
   const uint32_t *miss_row;   // [M] their unique rows

@@ -396,7 +396,9 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
   if (threadIdx.x == 0) s_nwork = 0;
   __syncthreads();
   uint32_t rem = quota, base = 0, taken_free = 0, taken_cold = 0;
+  const uint32_t free_gpu = __ldcg(&g.cnt->free_gpu);
   for (uint32_t y = 0; y < ord.n_cls && rem > 0; ++y) {
+    if (ord.cls[y] == geo.B + 1 && free_gpu == 0) continue;  // no free slot to walk
     const Bitmap bm = class_bitmap(g, geo, ord.cls[y]);
     uint32_t taken_y = 0;
     for (uint32_t s0 = 0; s0 < geo.nseg && rem > 0; s0 += T * kWalkSegs)
@@ -436,8 +438,8 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
 }
 
 // (3b) every hit moves to the current bucket (clears on its old class, sets
-// on cur) and its slot is recorded for the gather; entry rows for every entry.
-// The last block then walks the classes for the M victims.
+// on cur) and its slot is recorded for the gather.  The last block then walks
+// the classes for the M victims.
 __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
   if (block_skips(p.status)) return;
   const GroupDev &g = p.grp;
@@ -461,10 +463,6 @@ __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
         g.row_slot[i] = m;
       }
     }
-  }
-  if (i < p.E) {
-    const uint32_t a = p.sel[i];
-    p.entry_row[i] = a == kPad ? -1 : (int32_t)p.addr_row[a];
   }
   if (!last_block(&g.cnt->done[1])) return;
   select_walk<kEntryThreads>(g, geo, p.order, __ldcg(&g.cnt->M), true, p.status);
@@ -592,13 +590,17 @@ __global__ void __launch_bounds__(256, 3) k_move(MoveParams p) {
 // (kernel boundary).  The evicted owner now maps to its host slot, the miss to
 // the victim slot; the slot joins the current bucket (clears on its old class,
 // sets on cur); the miss's host slot is released (sets only on the host-free
-// bitmap).
+// bitmap).  (1) The idle threads also write every entry's unique row.
 __global__ void k_commit(MoveParams p) {
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
   const uint32_t M = g.cnt->M, F = g.cnt->F;
   const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < p.E; e += stride) {
+    const uint32_t a = p.sel[e];
+    p.entry_row[e] = a == kPad ? -1 : (int32_t)p.addr_row[a];
+  }
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < M; i += stride) {
     const uint32_t v = g.victims[i];
     const uint32_t a = p.miss_list[i];
