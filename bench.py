@@ -399,33 +399,40 @@ def run_gpu(args, rank, world, local):
 
 def isolated_gather(cache, ula, torch, dev, stream, W, reps=20):
     """The gather kernel alone: re-gather group 0's last hit rows (layer 0), L2 flushed
-    between launches, CUDA events on the launching stream."""
+    between launches, CUDA events on the launching stream; with the step's grid and
+    with every block that fits on the SMs."""
     st = cache.export(0)
     hits = st["hits"]
     out = cache.out_buffer(0, max(1, st["U"]))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ms = []
-    for i in range(reps + 2):
-        flush.zero_()
-        e0.record(stream)
-        ula.ula_debug_regather(cache.ctx, 0, 0, out.data_ptr(), out.shape[1], stream.cuda_stream)
-        e1.record(stream)
-        e1.synchronize()
-        if i >= 2:
-            ms.append(e0.elapsed_time(e1))
-    avg = sum(ms) / len(ms)
-    ach = hits * 2 * W / (avg / 1e3) / 1e9
     peak, _ = measured_peaks()
-    return {"achieved": round(ach, 1), "frac": round(ach / peak, 4), "avg_launch_us": round(avg * 1e3, 2),
-            "rows_per_launch": hits, "launches": reps, "l2": "flushed (512 MB write) before each launch"}
+    res = {}
+    for name, bps in (("step_grid", 0), ("full_grid", 64)):
+        ms = []
+        for i in range(reps + 2):
+            flush.zero_()
+            e0.record(stream)
+            ula.ula_debug_regather(cache.ctx, 0, 0, out.data_ptr(), out.shape[1], stream.cuda_stream,
+                                   blocks_per_sm=bps)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 2:
+                ms.append(e0.elapsed_time(e1))
+        avg = sum(ms) / len(ms)
+        ach = hits * 2 * W / (avg / 1e3) / 1e9
+        res[name] = {"achieved": round(ach, 1), "frac": round(ach / peak, 4),
+                     "avg_launch_us": round(avg * 1e3, 2)}
+    res.update({"rows_per_launch": hits, "launches": reps,
+                "l2": "flushed (512 MB write) before each launch"})
+    return res
 
 
 # Traffic measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for the gather
 # kernel, per gathered row, together with the hash of the kernel source it was taken on.
 # Reported only while the source is unchanged.
-GATHER_TRAFFIC = {"source_sha256": "32f06d249c9371f39b5ebe54a6269c58598ebde92e40be77ed40fa4e78bb9701",
-                  "bytes_per_row": 18763776 / 24255}  # 24,255 hit rows, 12-request case
+GATHER_TRAFFIC = {"source_sha256": "b7c34a4ff5061c2704b6946e1f6c033d17420a452692fa1e0be2f2b1d24c6572",
+                  "bytes_per_row": 18764288 / 24255}  # 24,255 hit rows, 12-request case
 
 
 def traffic_per_launch(rows_per_launch):

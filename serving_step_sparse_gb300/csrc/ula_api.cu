@@ -42,6 +42,7 @@ struct ula_ctx {
   cudaEvent_t in_evt = nullptr, out_evt = nullptr, commit_evt = nullptr;
   cudaEvent_t marked_evt = nullptr, hit0_evt = nullptr;
   int move_blocks = 0, gather_blocks = 0;  // persistent grids (resident blocks)
+  int gather_fit_per_sm = 0;
   int emit_blocks = 0;
   cudaEvent_t side_evt[ULA_MAX_GROUPS] = {};
   bool side_pending[ULA_MAX_GROUPS] = {};
@@ -269,6 +270,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(cudaEventCreateWithFlags(&c->marked_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->hit0_evt, cudaEventDisableTiming));
   ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks));
+  c->gather_fit_per_sm = c->gather_blocks;
   // The move is bound by the host link and needs few SMs to saturate it; the hit
   // gathers run beside it.  ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune
   // the persistent grids (clamped to what fits on an SM).
@@ -737,7 +739,7 @@ int ula_profile_read(ula_ctx *c, ula_profile *out, int reset) {
 }
 
 int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, void *d_out,
-                       uint32_t out_cap_rows, void *stream) {
+                       uint32_t out_cap_rows, uint32_t blocks_per_sm, void *stream) {
   if (!c || group >= c->cfg.n_groups || !d_out || !aligned16(d_out)) return ULA_ERR_INVALID_ARG;
   if (c->poisoned) return ULA_ERR_POISONED;
   const GroupDev &gd = c->groups_h[group];
@@ -751,7 +753,12 @@ int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, void *d_out,
   gp.out_cap = out_cap_rows;
   gp.layer = layer;
   gp.status = c->status;
-  ULA_CUDA(launch_gather(gp, c->gather_blocks, caller));
+  int blocks = c->gather_blocks;
+  if (blocks_per_sm) {
+    const int fit = c->gather_fit_per_sm;
+    blocks = c->sm_count * ((int)blocks_per_sm < fit ? (int)blocks_per_sm : fit);
+  }
+  ULA_CUDA(launch_gather(gp, blocks, caller));
   return ULA_OK;
 }
 

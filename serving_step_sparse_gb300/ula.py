@@ -100,7 +100,7 @@ def _load():
     lib.ula_profile_enable.restype = i32
     lib.ula_profile_read.argtypes = [p, C.POINTER(ula_profile), i32]
     lib.ula_profile_read.restype = i32
-    lib.ula_debug_regather.argtypes = [p, u32, u32, p, u32, p]
+    lib.ula_debug_regather.argtypes = [p, u32, u32, p, u32, u32, p]
     lib.ula_debug_regather.restype = i32
     lib.ula_dedup_noalloc.argtypes = [p, u32, p, p, p, p]
     lib.ula_dedup_noalloc.restype = i32
@@ -198,8 +198,8 @@ def ula_debug_inject(ctx: int, code: int) -> None:
 
 
 def ula_debug_regather(ctx: int, group: int, layer: int, d_out: int, out_cap_rows: int,
-                       stream) -> None:
-    _check(lib.ula_debug_regather(ctx, group, layer, d_out, out_cap_rows, stream),
+                       stream, blocks_per_sm: int = 0) -> None:
+    _check(lib.ula_debug_regather(ctx, group, layer, d_out, out_cap_rows, blocks_per_sm, stream),
            "ula_debug_regather")
 
 

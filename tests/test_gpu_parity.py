@@ -362,7 +362,8 @@ def test_regather_reproduces_hit_rows():
             for j in range(w.layers_per_group):
                 buf = torch.zeros_like(gpu.outs[g])
                 ula.ula_debug_regather(gpu.cache.ctx, g, j, buf.data_ptr(), buf.shape[1],
-                                       torch.cuda.current_stream().cuda_stream)
+                                       torch.cuda.current_stream().cuda_stream,
+                                       blocks_per_sm=2 if j % 2 else 0)
                 torch.cuda.synchronize()
                 got = buf[j, :U].cpu().numpy()[hit]
                 exp = gpu.outs[g][j, :U].cpu().numpy()[hit]
