@@ -34,6 +34,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, INVALID_ARG, CAPACITY, UNMAPPED, INTERNAL = 0, 1, 2, 3, 7
+BYPASS = 1  # overflow bypass flag
 FREE, COLD = -1, -2
 TIER_UNALLOCATED, TIER_GPU, TIER_HOST = 0, 1, 2
 
@@ -54,6 +55,8 @@ def _configure(l):
     p, u32, i32 = C.c_void_p, C.c_uint32, C.c_int
     l.orc_create.argtypes = [u32, u32, p, u32, u32, u32, u32]
     l.orc_create.restype = p
+    l.orc_create2.argtypes = [u32, u32, p, u32, u32, u32, u32, u32]
+    l.orc_create2.restype = p
     l.orc_destroy.argtypes = [p]
     l.orc_alloc.argtypes = [p, u32, p, p]
     l.orc_alloc.restype = i32
@@ -110,7 +113,7 @@ class Oracle:
     """PB-LRU residency oracle: same calls as the library, semantically."""
 
     def __init__(self, row_bytes, layers_per_group, gpu_slots, host_slots, ring_buckets,
-                 max_logical, _lib=None):
+                 max_logical, _lib=None, bypass=False):
         self._l = _lib if _lib is not None else lib()
         self.row_bytes = int(row_bytes)
         self.layers = [int(x) for x in layers_per_group]
@@ -118,8 +121,13 @@ class Oracle:
         self.S, self.H, self.B = int(gpu_slots), int(host_slots), int(ring_buckets)
         self.max_logical = int(max_logical)
         L = np.array(self.layers, dtype=np.uint32)
-        self._h = self._l.orc_create(self.row_bytes, self.G, _ptr(L), self.S, self.H, self.B,
-                                   self.max_logical)
+        self.bypass = bool(bypass)
+        if self.bypass:
+            self._h = self._l.orc_create2(self.row_bytes, self.G, _ptr(L), self.S, self.H,
+                                          self.B, self.max_logical, BYPASS)
+        else:
+            self._h = self._l.orc_create(self.row_bytes, self.G, _ptr(L), self.S, self.H,
+                                         self.B, self.max_logical)
         if not self._h:
             raise ValueError("bad oracle configuration")
 
@@ -155,13 +163,13 @@ class Oracle:
         out = np.zeros((self.layers[g], cap, self.row_bytes), dtype=np.uint8)
         entry_row = np.empty(sel.size, dtype=np.int32)
         req_off = np.empty(R + 1, dtype=np.int32)
-        cnt = np.zeros(8, dtype=np.uint64)
+        cnt = np.zeros(9, dtype=np.uint64)
         rc = self._l.orc_step_group(self._h, g, _ptr(sel), R, Q, K, _ptr(out), cap,
                                   _ptr(entry_row), _ptr(req_off), _ptr(cnt))
         if rc:
             raise OracleError(rc, f"step_group({g})")
         keys = ["uniq", "hits", "misses", "victims_free", "victims_cold", "victims_ring",
-                "writebacks", "rows_gathered"]
+                "writebacks", "rows_gathered", "bypassed"]
         return {"out": out, "entry_row": entry_row, "req_off": req_off,
                 "counters": {k: int(v) for k, v in zip(keys, cnt)}}
 

@@ -39,7 +39,12 @@
 //     address fails with UNMAPPED before any state changes;
 //   * alloc hands out logical bases monotonically, places each new address
 //     in the lowest free GPU slot (joining the current bucket), else the
-//     lowest free host slot, and never evicts; free releases both tiers.
+//     lowest free host slot, and never evicts; free releases both tiers;
+//   * with the overflow bypass enabled (an extension, not on the pages), a
+//     step with more misses than can be made resident moves only the first
+//     M' = min(M, S - hits, free GPU + free host slots) misses; each later
+//     miss is gathered straight from its host slot into the output and stays
+//     on the host.
 
 #include <algorithm>
 #include <cstdint>
@@ -91,10 +96,13 @@ struct Group {
   std::vector<uint32_t> last_victims;   // victim i paired with miss i
   std::vector<uint32_t> last_wb_host;   // host slot of the j-th write-back
   std::vector<int> last_victim_class;   // class each victim was taken from
+  size_t last_bypassed = 0;             // misses served from the host pool directly
 };
 
+constexpr uint32_t kFlagBypass = 1u;  // overflow bypass (same bit as the library's flag)
+
 struct Oracle {
-  uint32_t row_bytes = 0, n_groups = 0, S = 0, H = 0, B = 0, max_logical = 0;
+  uint32_t row_bytes = 0, n_groups = 0, S = 0, H = 0, B = 0, max_logical = 0, flags = 0;
   uint32_t next_logical = 0;
   std::vector<uint8_t> live;  // [max_logical]
   std::vector<Group> groups;
@@ -119,10 +127,11 @@ void move_to_current_bucket(Group &g, uint32_t s) {
 
 extern "C" {
 
-void *orc_create(uint32_t row_bytes, uint32_t n_groups, const uint32_t *layers, uint32_t S,
-                 uint32_t H, uint32_t B, uint32_t max_logical) {
+void *orc_create2(uint32_t row_bytes, uint32_t n_groups, const uint32_t *layers, uint32_t S,
+                  uint32_t H, uint32_t B, uint32_t max_logical, uint32_t flags) {
   if (!row_bytes || !n_groups || !layers || !S || !B || !max_logical) return nullptr;
   Oracle *o = new Oracle;
+  o->flags = flags;
   o->row_bytes = row_bytes;
   o->n_groups = n_groups;
   o->S = S;
@@ -146,6 +155,11 @@ void *orc_create(uint32_t row_bytes, uint32_t n_groups, const uint32_t *layers, 
     g.host_pool.assign((size_t)H * o->slot_bytes(g), 0);
   }
   return o;
+}
+
+void *orc_create(uint32_t row_bytes, uint32_t n_groups, const uint32_t *layers, uint32_t S,
+                 uint32_t H, uint32_t B, uint32_t max_logical) {
+  return orc_create2(row_bytes, n_groups, layers, S, H, B, max_logical, 0);
 }
 
 void orc_destroy(void *h) { delete static_cast<Oracle *>(h); }
@@ -211,8 +225,8 @@ int orc_free(void *h, uint32_t base, uint32_t n) {
   return kOk;
 }
 
-// counters (optional, [8]): uniq, hits, misses, victims from free, from cold,
-// from the ring, write-backs, rows gathered.
+// counters (optional, [9]): uniq, hits, misses, victims from free, from cold,
+// from the ring, write-backs, rows gathered, misses bypassed.
 int orc_step_group(void *h, uint32_t gi, const uint32_t *sel, uint32_t n_req, uint32_t q,
                    uint32_t k, uint8_t *out, uint32_t out_cap, int32_t *entry_row,
                    int32_t *req_off, uint64_t *counters) {
@@ -242,20 +256,26 @@ int orc_step_group(void *h, uint32_t gi, const uint32_t *sel, uint32_t n_req, ui
   req_off[n_req] = (int32_t)uniq.size();
 
   // (2) translate through the map: GPU-resident = hit, host-resident = miss.
-  std::vector<uint32_t> misses;
+  std::vector<uint32_t> misses, bypassed;
   size_t hits = 0;
   for (uint32_t a : uniq) {
     if (g.where[a].tier == kOnGpu) ++hits;
     else misses.push_back(a);
   }
-  const size_t M = misses.size();
-
   // capacity: victims come from everything but the current bucket, which
   // after marking holds exactly the hits; write-backs need free host slots.
   const size_t free_gpu = g.free_slots.size();
+  const size_t can_place = std::min((size_t)o->S - hits, free_gpu + g.host_free.size());
+  if (uniq.size() > out_cap) return kCapacity;
+  if (misses.size() > can_place) {
+    if (!(o->flags & kFlagBypass)) return kCapacity;
+    // bypass: only the first can_place misses become resident; the rest are
+    // gathered from the host pool below and stay where they are
+    bypassed.assign(misses.begin() + can_place, misses.end());
+    misses.resize(can_place);
+  }
+  const size_t M = misses.size();
   const size_t writebacks_needed = M > free_gpu ? M - free_gpu : 0;
-  if (M > (size_t)o->S - hits || writebacks_needed > g.host_free.size() || uniq.size() > out_cap)
-    return kCapacity;
 
   for (size_t e = 0; e < E; ++e) entry_row[e] = sel[e] == kPad ? -1 : row_of[sel[e]];
 
@@ -332,22 +352,25 @@ int orc_step_group(void *h, uint32_t gi, const uint32_t *sel, uint32_t n_req, ui
   for (uint32_t j = 0; j < g.layers; ++j)
     for (size_t u = 0; u < uniq.size(); ++u) {
       const Location loc = g.where[uniq[u]];
+      const std::vector<uint8_t> &pool = loc.tier == kOnGpu ? g.gpu_pool : g.host_pool;  // host: bypassed
       std::memcpy(out + ((size_t)j * out_cap + u) * o->row_bytes,
-                  &g.gpu_pool[(size_t)loc.slot * sb + (size_t)j * o->row_bytes], o->row_bytes);
+                  &pool[(size_t)loc.slot * sb + (size_t)j * o->row_bytes], o->row_bytes);
     }
 
   g.last_victims = victims;
   g.last_wb_host = wb_host;
   g.last_victim_class = victim_class;
+  g.last_bypassed = bypassed.size();
   if (counters) {
     counters[0] = uniq.size();
     counters[1] = hits;
-    counters[2] = M;
+    counters[2] = M + bypassed.size();
     counters[3] = n_free;
     counters[4] = n_cold;
     counters[5] = n_ring;
     counters[6] = wb;
     counters[7] = (uint64_t)uniq.size() * g.layers;
+    counters[8] = bypassed.size();
   }
   return kOk;
 }

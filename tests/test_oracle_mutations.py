@@ -29,8 +29,10 @@ MUTATIONS = [
     ("evicted owner's map not updated", "      g.where[prev_owner] = Location{kOnHost, hs};\n", ""),
     ("misses paired in reverse", "    const uint32_t a = misses[i];", "    const uint32_t a = misses[M - 1 - i];"),
     ("rotation skips a bucket", "  g.cur = (g.cur + 1) % o->B;", "  g.cur = (g.cur + 2) % o->B;"),
-    ("gather always reads layer 0", "&g.gpu_pool[(size_t)loc.slot * sb + (size_t)j * o->row_bytes]",
-     "&g.gpu_pool[(size_t)loc.slot * sb + (size_t)0 * o->row_bytes]"),
+    ("gather always reads layer 0", "&pool[(size_t)loc.slot * sb + (size_t)j * o->row_bytes]",
+     "&pool[(size_t)loc.slot * sb + (size_t)0 * o->row_bytes]"),
+    ("bypass keeps the last misses instead of the first", "    misses.resize(can_place);",
+     "    misses.erase(misses.begin(), misses.end() - can_place);"),
     ("miss host slots never released", "  for (uint32_t hs : released_host) {\n    g.host_free.insert(hs);", "  for (uint32_t hs : released_host) {\n"),
     ("alloc takes highest free slot", "      if (!g.free_slots.empty()) {  // lowest free GPU slot; a prefill write counts as an access\n        uint32_t s = *g.free_slots.begin();",
      "      if (!g.free_slots.empty()) {\n        uint32_t s = *g.free_slots.rbegin();"),
@@ -43,6 +45,8 @@ MUTATIONS = [
 
 def _fast_pins():
     pins.test_worked_example_golden()
+    for seed in range(0, 80, 9):
+        pins.test_overflow_bypass_matches_timestamp_model(seed)
     for seed in range(0, 120, 7):
         pins.test_with_folds_matches_timestamp_model(seed)
     for seed in range(0, 60, 9):

@@ -110,8 +110,8 @@ class BruteForce:
     round-granular LRU: free ascending, then occupied slots by (last round, slot).
     """
 
-    def __init__(self, S, H, B, lru=False):
-        self.S, self.H, self.B, self.lru = S, H, B, lru
+    def __init__(self, S, H, B, lru=False, bypass=False):
+        self.S, self.H, self.B, self.lru, self.bypass = S, H, B, lru, bypass
         self.loc = {}          # addr -> ("G"|"H", slot)
         self.owner = {}        # GPU slot -> addr
         self.host_owner = {}   # host slot -> addr
@@ -159,6 +159,13 @@ class BruteForce:
             if self.loc[a][0] == "G":
                 self.last[self.loc[a][1]] = self.round
         misses = [a for a in uniq if self.loc[a][0] == "H"]
+        hits = len(uniq) - len(misses)
+        free_gpu = self.S - len(self.owner)
+        free_host = self.H - len(self.host_owner)
+        can_place = min(self.S - hits, free_gpu + free_host)
+        if len(misses) > can_place:
+            assert self.bypass, "capacity exceeded without the bypass"
+            misses = misses[:can_place]  # the rest are read from the host pool in place
         victims = self.order()[:len(misses)]
         assert len(victims) == len(misses)
         owned = [v for v in victims if v in self.owner]
@@ -179,10 +186,10 @@ class BruteForce:
         return victims, wb
 
 
-def _random_trace(rng, S, H, B, rounds, lru, n0):
+def _random_trace(rng, S, H, B, rounds, lru, n0, bypass=False, max_pick=None):
     """Random tiny trace: selections with repeats and pads, allocs and frees between steps."""
-    o = Oracle(ID_ROW_BYTES, [1], S, H, B, 4096)
-    bf = BruteForce(S, H, B, lru=lru)
+    o = Oracle(ID_ROW_BYTES, [1], S, H, B, 4096, bypass=bypass)
+    bf = BruteForce(S, H, B, lru=lru, bypass=bypass)
     live = []
     assert o.alloc(n0, _id_row_buf(0, n0)) == bf.alloc(n0)
     live += list(range(n0))
@@ -199,7 +206,7 @@ def _random_trace(rng, S, H, B, rounds, lru, n0):
                 base = bf.alloc(n)
                 assert o.alloc(n, _id_row_buf(base, n)) == base
                 live += list(range(base, base + n))
-        k = rng.randint(1, min(S, 6))
+        k = rng.randint(1, max_pick if max_pick else min(S, 6))
         picks = rng.sample(live, min(k, len(live)))
         flat = []
         for a in picks:  # duplicates and pads inside the selection
@@ -241,6 +248,34 @@ def test_with_folds_matches_timestamp_model(seed):
     B = rng.randint(2, 5)
     _random_trace(rng, S=S, H=64, B=B, rounds=rng.randint(10, 120), lru=False,
                   n0=rng.randint(S, S + 24))
+
+
+@pytest.mark.parametrize("seed", range(80))
+def test_overflow_bypass_matches_timestamp_model(seed):
+    """Selections larger than the pool: the first S - hits misses become resident,
+    the rest are gathered from the host pool in place (the gathered ids are checked
+    inside _random_trace)."""
+    rng = random.Random(5000 + seed)
+    S = rng.randint(2, 10)
+    B = rng.randint(2, 5)
+    _random_trace(rng, S=S, H=rng.choice([16, 64]), B=B, rounds=rng.randint(10, 60), lru=False,
+                  n0=rng.randint(S, S + 12), bypass=True, max_pick=2 * S + 3)
+
+
+def test_overflow_without_bypass_is_an_error():
+    o = Oracle(ID_ROW_BYTES, [1], 4, 16, 3, 64)
+    o.alloc(10, _id_row_buf(0, 10))
+    with pytest.raises(OracleError) as ei:
+        o.step_group(0, np.arange(6, dtype=np.uint32).reshape(1, 1, 6))
+    assert ei.value.code == CAPACITY
+    ob = Oracle(ID_ROW_BYTES, [1], 4, 16, 3, 64, bypass=True)
+    ob.alloc(10, _id_row_buf(0, 10))
+    res = ob.step_group(0, np.arange(10, dtype=np.uint32).reshape(1, 1, 10))
+    c = res["counters"]
+    # slots 0..3 hold addresses 0..3 (hits); no slot is left for the 6 misses
+    assert c["hits"] == 4 and c["misses"] == 6 and c["bypassed"] == 6
+    got = res["out"][0, :10].view(np.uint32)[:, 0]
+    assert got.tolist() == list(range(10))
 
 
 def test_textbook_lru_differs_once_folds_happen():
