@@ -239,7 +239,8 @@ def run_gpu(args, rank, world, local):
     link = host_link_peaks(torch)
     cache = UlaCache(row_bytes=W, layers_per_group=[L] * G, gpu_slots=w.gpu_slots,
                      host_slots=w.host_slots, ring_buckets=w.ring_buckets,
-                     max_logical=w.max_logical, max_entries=E, device=dev, stream=stream)
+                     max_logical=w.max_logical, max_entries=E, device=dev, stream=stream,
+                     bypass_overflow=w.bypass)
     trace = stage_initial(cache, w, synth, torch)
     n_value, n_prof = args.steps, min(args.profile_steps, args.steps)
     n_e2e = 0 if args.no_e2e else args.steps

@@ -68,8 +68,15 @@ typedef struct ula_config {
   uint32_t ring_buckets;     /* B: ring buckets per group, including the current one (1..64) */
   uint32_t max_logical;      /* logical addresses live in [0, max_logical) (1 .. 2^31-1) */
   uint32_t max_entries;      /* largest n_req*q*k of one ula_step_group call */
-  uint32_t flags;            /* reserved, must be 0 */
+  uint32_t flags;            /* ULA_FLAG_* below; other bits must be 0 */
 } ula_config;
+
+/* Overflow bypass (an extension; the pages have no counterpart).  Without it, a step
+ * whose misses cannot all be made resident fails with ULA_ERR_CAPACITY.  With it, the
+ * first M' = min(misses, S - hits, free GPU + free host slots) misses (in dedup order)
+ * are moved as usual and every later miss is gathered straight from its host slot into
+ * the output: it stays on the host and nothing else changes for it. */
+#define ULA_FLAG_BYPASS_OVERFLOW 1u
 
 /* Counters accumulated since ula_create, summed over groups. */
 typedef struct ula_stats {
@@ -83,8 +90,9 @@ typedef struct ula_stats {
   uint64_t victims_ring;   /* victims taken from ring buckets */
   uint64_t writebacks;     /* victims that held data and were written back */
   uint64_t rows_gathered;  /* (address, layer) rows written to gather outputs */
-  uint64_t bytes_h2d;      /* fill bytes moved host -> GPU */
+  uint64_t bytes_h2d;      /* fill (and bypass) bytes moved host -> GPU */
   uint64_t bytes_d2h;      /* write-back bytes moved GPU -> host */
+  uint64_t bypassed;       /* misses gathered from the host pool in place (overflow bypass) */
 } ula_stats;
 
 /*
@@ -158,8 +166,8 @@ int ula_free(ula_ctx *ctx, uint32_t logical_base, uint32_t n);
  *   stream      : the caller's stream; the step is ordered after every earlier call on
  *                 this context.  Returns without waiting for the device.
  * Device-detected errors (latched, returned by ula_sync, nothing changed by the step):
- * UNMAPPED (an address >= max_logical or not allocated), CAPACITY (misses > S - hits,
- * write-backs > free host slots, or U > out_cap_rows).
+ * UNMAPPED (an address >= max_logical or not allocated), CAPACITY (misses > S - hits or
+ * write-backs > free host slots, unless ULA_FLAG_BYPASS_OVERFLOW; or U > out_cap_rows).
  * Host-detected: INVALID_ARG (group out of range, n_req*q*k > max_entries, NULL buffers).
  */
 int ula_step_group(ula_ctx *ctx, uint32_t group, const uint32_t *d_sel, uint32_t n_req,

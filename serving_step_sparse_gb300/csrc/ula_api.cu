@@ -204,7 +204,7 @@ int validate_config(const ula_config *c) {
     return ULA_ERR_INVALID_ARG;
   if (c->ring_buckets == 0 || c->ring_buckets > ULA_MAX_BUCKETS) return ULA_ERR_INVALID_ARG;
   if (c->max_logical == 0 || c->max_logical > kSlotMask) return ULA_ERR_INVALID_ARG;
-  if (c->max_entries == 0 || c->flags != 0) return ULA_ERR_INVALID_ARG;
+  if (c->max_entries == 0 || (c->flags & ~ULA_FLAG_BYPASS_OVERFLOW) != 0) return ULA_ERR_INVALID_ARG;
   return ULA_OK;
 }
 
@@ -240,6 +240,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   geo.B = B;
   geo.W = cfg.row_bytes;
   geo.max_logical = cfg.max_logical;
+  geo.bypass = (cfg.flags & ULA_FLAG_BYPASS_OVERFLOW) ? 1u : 0u;
   geo.gd = dims_for(S);
   geo.hd = dims_for(H);
   geo.nseg = geo.gd.n1;
@@ -618,9 +619,9 @@ int ula_sync(ula_ctx *c, ula_stats *stats) {
     std::vector<GroupCounters> h(c->cfg.n_groups);
     ULA_CUDA(cudaMemcpy(h.data(), c->cnt_d, sizeof(GroupCounters) * h.size(),
                         cudaMemcpyDeviceToHost));
-    unsigned long long acc[12] = {};
+    unsigned long long acc[kStCount] = {};
     for (const GroupCounters &x : h)
-      for (int i = 0; i < 12; ++i) acc[i] += x.stat[i];
+      for (int i = 0; i < kStCount; ++i) acc[i] += x.stat[i];
     stats->steps = acc[kStSteps];
     stats->entries = acc[kStEntries];
     stats->uniq = acc[kStUniq];
@@ -633,6 +634,7 @@ int ula_sync(ula_ctx *c, ula_stats *stats) {
     stats->rows_gathered = acc[kStRows];
     stats->bytes_h2d = acc[kStBytesH2D];
     stats->bytes_d2h = acc[kStBytesD2H];
+    stats->bypassed = acc[kStBypassed];
   }
   if (st) {
     c->poisoned = st;

@@ -51,15 +51,16 @@ struct GroupCounters {
   uint32_t U, M, hits; // last step: unique addresses, misses, hits
   uint32_t F;          // last step: victims taken from free slots (alloc: GPU placements)
   uint32_t K;          // last step: write-backs (alloc: host placements)
+  uint32_t Mx;         // last step: misses gathered from the host pool in place (bypass)
   uint32_t n_work;     // selection work entries (GPU classes, then host)
   uint32_t n_work_gpu; // of which on GPU-slot classes
   uint32_t done[3];    // "last block" tickets of the multi-block kernels
-  unsigned long long stat[12];  // ula_stats order
+  unsigned long long stat[13];  // ula_stats order
 };
 
 enum StatIdx {
   kStSteps = 0, kStEntries, kStUniq, kStHits, kStMisses, kStVictFree, kStVictCold,
-  kStVictRing, kStWriteback, kStRows, kStBytesH2D, kStBytesD2H
+  kStVictRing, kStWriteback, kStRows, kStBytesH2D, kStBytesD2H, kStBypassed, kStCount
 };
 
 // Everything one group owns on the device.
@@ -87,6 +88,7 @@ struct GroupDev {
 struct Geometry {
   uint32_t S, H, B, W;   // GPU slots, host slots, ring buckets, row bytes
   uint32_t max_logical;
+  uint32_t bypass;       // ULA_FLAG_BYPASS_OVERFLOW set
   Dims gd, hd;           // bitmap dims for GPU-slot and host-slot bitmaps
   uint32_t nseg, hseg;   // segments (= level-1 words) per bitmap
 };

@@ -250,14 +250,17 @@ __global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p
   if (p.E == 0)
     for (uint32_t r = threadIdx.x; r <= p.n_req; r += blockDim.x) p.req_off[r] = 0;
   if (threadIdx.x == 0) {
-    const uint32_t U = runf, M = runm, hits = U - M;
-    const bool ok = U <= p.out_cap && (uint64_t)M + hits <= p.geo.S &&
-                    (uint64_t)M <= (uint64_t)c->free_gpu + c->free_host;
+    const uint32_t U = runf, Mall = runm, hits = U - Mall;
+    const uint64_t can_place = min((uint64_t)p.geo.S - hits,
+                                   (uint64_t)c->free_gpu + c->free_host);
+    const uint32_t M = (uint32_t)min((uint64_t)Mall, can_place);  // misses made resident
+    const bool ok = U <= p.out_cap && (M == Mall || p.geo.bypass);
     if (!ok) {
       latch(p.status, ULA_ERR_CAPACITY);
     } else {
       c->U = U;
       c->M = M;
+      c->Mx = Mall - M;
       c->hits = hits;
       c->F = 0;
       c->K = 0;
@@ -269,9 +272,10 @@ __global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p
       c->stat[kStEntries] += p.E;
       c->stat[kStUniq] += U;
       c->stat[kStHits] += hits;
-      c->stat[kStMisses] += M;
+      c->stat[kStMisses] += Mall;
+      c->stat[kStBypassed] += Mall - M;
       c->stat[kStRows] += (unsigned long long)U * p.grp.layers;
-      c->stat[kStBytesH2D] += (unsigned long long)M * sb;
+      c->stat[kStBytesH2D] += (unsigned long long)Mall * sb;
     }
   }
 }
@@ -527,7 +531,7 @@ __global__ void __launch_bounds__(256, 3) k_move(MoveParams p) {
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
-  const uint32_t M = g.cnt->M, F = g.cnt->F;
+  const uint32_t M = g.cnt->M, F = g.cnt->F, Mx = g.cnt->Mx;
   const uint32_t lane = lane_id();
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -535,6 +539,33 @@ __global__ void __launch_bounds__(256, 3) k_move(MoveParams p) {
   const uint32_t nvec = (uint32_t)(sb / 16);
   const uint32_t CW = geo.W / 16;
   uint4 *out = reinterpret_cast<uint4 *>(p.out);
+  // overflow bypass: misses [M, M + Mx) are copied from their host slots to the
+  // output only (they stay on the host)
+  for (uint32_t i = M + warp; i < M + Mx; i += nwarps) {
+    const uint32_t hs = p.miss_hs[i];
+    const uint32_t row = p.miss_row[i];
+    if (!out || hs >= geo.H || row >= p.out_cap) {
+      if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
+      continue;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(g.host_pool + (size_t)hs * sb);
+    for (uint32_t c0 = 0; c0 < nvec; c0 += 32 * kMoveUnroll) {
+      uint4 v[kMoveUnroll];
+#pragma unroll
+      for (int u = 0; u < kMoveUnroll; ++u) {
+        const uint32_t c = c0 + u * 32 + lane;
+        if (c < nvec) v[u] = src[c];
+      }
+#pragma unroll
+      for (int u = 0; u < kMoveUnroll; ++u) {
+        const uint32_t c = c0 + u * 32 + lane;
+        if (c < nvec) {
+          const uint32_t j = c / CW;
+          out[((size_t)j * p.out_cap + row) * CW + (c - j * CW)] = v[u];
+        }
+      }
+    }
+  }
   for (uint32_t i = warp; i < M; i += nwarps) {
     const uint32_t v = g.victims[i];
     const uint32_t hs = p.miss_hs[i];

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libula.so")
 MAX_GROUPS = 64
 MAX_BUCKETS = 64
 ADDR_PAD = 0xFFFFFFFF
+FLAG_BYPASS_OVERFLOW = 1
 MAP_UNALLOCATED = 0xFFFFFFFF
 MAP_HOST = 0x80000000
 STAMP_FREE = 0xFFFFFFFF
@@ -42,7 +43,7 @@ class ula_config(C.Structure):
 class ula_stats(C.Structure):
     _fields_ = [(n, C.c_uint64) for n in (
         "steps", "entries", "uniq", "hits", "misses", "victims_free", "victims_cold",
-        "victims_ring", "writebacks", "rows_gathered", "bytes_h2d", "bytes_d2h")]
+        "victims_ring", "writebacks", "rows_gathered", "bytes_h2d", "bytes_d2h", "bypassed")]
 
     def as_dict(self):
         return {n: int(getattr(self, n)) for n, _ in self._fields_}

@@ -49,6 +49,7 @@ class Workload:
     ring_buckets: int = 8       # B ring buckets (+ one cold bucket)
     row_bytes: int = 656        # 512 e4m3 latent + 4 fp32 scales + 64 bf16 rope
     pad_prob: float = 0.0       # fraction of entries replaced by the pad marker (edge tests)
+    bypass: bool = False        # overflow bypass: misses beyond the pool are read in place
     _cache: dict = field(default_factory=dict, compare=False, hash=False, repr=False)
 
     @property
@@ -139,6 +140,15 @@ WORKLOADS = {
         n_live=192, n_total=256, ctx_min=16384, ctx_max=16384, n_groups=2, layers_per_group=4,
         q=1, k=2048, window=512, keep=0.5, fresh="zipf", zipf_s=1.1, steps=256,
         turnover_period=4, gpu_frac=0.1),
+    # The low-overlap stress as literally stated: all 256 requests at once.  One step
+    # selects 524,288 rows against 419,430 GPU slots, so it needs the overflow bypass.
+    "cfg4_literal": Workload(
+        name="cfg4_literal", seed=4,
+        description=("low overlap, literal: 256 requests x 16K ctx all at once, 2 groups x 4 "
+                     "layers, top-2,048, overlap 0.5 + Zipf(1.1), GPU pool 10%, overflow bypass"),
+        n_live=256, ctx_min=16384, ctx_max=16384, n_groups=2, layers_per_group=4,
+        q=1, k=2048, window=512, keep=0.5, fresh="zipf", zipf_s=1.1, steps=256,
+        gpu_frac=0.1, bypass=True),
 }
 
 
@@ -157,6 +167,7 @@ def small(name: str, **kw) -> Workload:
         "cfg3": dict(n_live=4, ctx_min=4096, ctx_max=4096, k=256, window=64, steps=48),
         "cfg4": dict(n_live=12, n_total=20, ctx_min=2048, ctx_max=2048, k=256, window=64,
                      steps=40, turnover_period=4),
+        "cfg4_literal": dict(n_live=20, ctx_min=2048, ctx_max=2048, k=256, window=64, steps=40),
     }[name]
     shrink.update(kw)
     return w.replace(name=name + "_small", description=w.description + " (reduced)", **shrink)

@@ -21,7 +21,7 @@ class GpuRun:
         self.cache = UlaCache(row_bytes=w.row_bytes, layers_per_group=[L] * G,
                               gpu_slots=w.gpu_slots, host_slots=w.host_slots,
                               ring_buckets=w.ring_buckets, max_logical=w.max_logical,
-                              max_entries=w.entries_per_step)
+                              max_entries=w.entries_per_step, bypass_overflow=w.bypass)
         self.cap = out_cap if out_cap is not None else w.entries_per_step
         self.outs = [self.cache.out_buffer(g, self.cap) for g in range(G)]
         E = w.entries_per_step

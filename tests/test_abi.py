@@ -50,7 +50,7 @@ def test_binding_struct_sizes_match_header(libpath):
     from serving_step_sparse_gb300 import ula
     # ula_config: 9 uint32 + 64 layer counts
     assert C.sizeof(ula.ula_config) == 4 * (8 + ula.MAX_GROUPS)
-    assert C.sizeof(ula.ula_stats) == 8 * 12
+    assert C.sizeof(ula.ula_stats) == 8 * 13
     assert C.sizeof(ula.ula_debug_layout) == 4 * 8
     assert C.sizeof(ula.ula_debug_state) == 8 * 15 + 4 * 9 + 4  # padded to 8
     src = open(HEADER).read()

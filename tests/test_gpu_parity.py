@@ -78,11 +78,13 @@ def test_parity_cfg0_full():
     assert stats["steps"] == 64 and stats["misses"] > 0 and stats["hits"] > 0
 
 
-@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3", "cfg4"])
+@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3", "cfg4", "cfg4_literal"])
 def test_parity_small(name):
     w = small(name)
     stats = run_parity(w, w.steps)
     assert stats["misses"] > 0
+    if w.bypass:
+        assert stats["bypassed"] > 0  # the literal recipe overflows the pool every step
 
 
 def test_parity_cfg1_full():
@@ -91,7 +93,8 @@ def test_parity_cfg1_full():
     assert stats["steps"] == w.steps * w.n_groups and stats["writebacks"] > 0
 
 
-@pytest.mark.parametrize("name,steps", [("cfg2", 12), ("cfg3", 12), ("cfg4", 13)])
+@pytest.mark.parametrize("name,steps", [("cfg2", 12), ("cfg3", 12), ("cfg4", 13),
+                                        ("cfg4_literal", 6)])
 def test_parity_full_size_sampled(name, steps):
     """Full-size workloads: state compared every step, gathered bytes sampled."""
     w = WORKLOADS[name]
