@@ -15,7 +15,7 @@ commit, gather of all layers) plus the step's appended-token alloc.
               measured pinned copy bandwidth
   cpu_baseline : the CPU oracle on a bounded sample of the same workload (1 core)
 
---impl reference times the CPU oracle alone (the reference arm of this build).
+--impl reference times the CPU oracle alone (the reference arm).
 Multi-GPU (torchrun, N > 1): independent replicas, one per GPU; value = all ranks'
 rows / the slowest rank's time.
 """
@@ -430,16 +430,25 @@ def isolated_gather(cache, ula, torch, dev, stream, W, reps=20):
 
 
 # Traffic measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for the gather
-# kernel, per gathered row, together with the hash of the kernel source it was taken on.
-# Reported only while the source is unchanged.
-GATHER_TRAFFIC = {"source_sha256": "b7c34a4ff5061c2704b6946e1f6c033d17420a452692fa1e0be2f2b1d24c6572",
+# kernel, per gathered row, together with the hash of the gather kernel's source (its
+# launch-shape defaults and its body) it was taken on.  Reported only while that source
+# is unchanged.
+GATHER_TRAFFIC = {"source_sha256": "a6288ae84402ae80b9d46626a8a480242be96917a72437429e06bba4c06d9586",
                   "bytes_per_row": 18764288 / 24255}  # 24,255 hit rows, 12-request case
 
 
-def traffic_per_launch(rows_per_launch):
+def gather_source_sha256() -> str:
     src = os.path.join(ROOT, "serving_step_sparse_gb300", "csrc", "ula_kernels.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if GATHER_TRAFFIC["source_sha256"] != sha or GATHER_TRAFFIC["bytes_per_row"] is None:
+    lines = open(src).read().splitlines()
+    keep = [ln for ln in lines if ln.startswith("#define ULA_GATHER_")]
+    start = next(i for i, ln in enumerate(lines) if ln.startswith("constexpr int kGatherUnroll"))
+    end = next(i for i in range(start, len(lines)) if lines[i] == "}")
+    keep += lines[start:end + 1]
+    return hashlib.sha256("\n".join(keep).encode()).hexdigest()
+
+
+def traffic_per_launch(rows_per_launch):
+    if GATHER_TRAFFIC["source_sha256"] != gather_source_sha256():
         return None
     return round(GATHER_TRAFFIC["bytes_per_row"] * rows_per_launch)
 

@@ -241,8 +241,8 @@ int ula_debug_inject(ula_ctx *ctx, int code);
  * any alloc/free).  More rows than out_cap_rows latch ULA_ERR_CAPACITY. */
 int ula_debug_regather(ula_ctx *ctx, uint32_t group, uint32_t layer, void *d_out,
                        uint32_t out_cap_rows, uint32_t blocks_per_sm, void *stream);
-/* blocks_per_sm: 0 = the grid the step uses; otherwise that many 256-thread blocks per
- * SM (at most what fits). */
+/* blocks_per_sm: 0 = the grid the step uses; otherwise that many blocks per SM (at most
+ * what fits). */
 
 /* ------------------------------------------------------------ profiling
  * Kernel launches are counted per phase always.  When enabled, every phase

@@ -38,6 +38,24 @@ constexpr int kEntryThreads = 1024;  // blocks of the per-entry kernels with blo
 constexpr int kStampThreads = 256;
 constexpr int kWalkSegs = 4;        // segments per thread per step of the victim walk
 
+// Launch shapes of the two persistent copy kernels (build-time tunables).
+#ifndef ULA_GATHER_THREADS
+#define ULA_GATHER_THREADS 256
+#endif
+#ifndef ULA_GATHER_MINBLOCKS
+#define ULA_GATHER_MINBLOCKS 4
+#endif
+#ifndef ULA_GATHER_UNROLL
+#define ULA_GATHER_UNROLL 8
+#endif
+#ifndef ULA_MOVE_MINBLOCKS
+#define ULA_MOVE_MINBLOCKS 3
+#endif
+#ifndef ULA_MOVE_UNROLL
+#define ULA_MOVE_UNROLL 6
+#endif
+constexpr int kGatherThreads = ULA_GATHER_THREADS;
+
 __device__ __forceinline__ void latch(int *status, int code) { atomicCAS(status, 0, code); }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
@@ -525,9 +543,9 @@ __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
 // slots, row) is read up front from arrays filled by the compaction and the
 // selection, so a warp starts its copies after one round of independent loads.
 // Then, in the next kernel, the map and the labels (k_commit).
-constexpr int kMoveUnroll = 6;
+constexpr int kMoveUnroll = ULA_MOVE_UNROLL;
 
-__global__ void __launch_bounds__(256, 3) k_move(MoveParams p) {
+__global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) {
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -667,9 +685,9 @@ __global__ void k_commit(MoveParams p) {
 // chunks, consecutive lanes on consecutive chunks (coalesced within a row; the
 // warp's output rows are contiguous).  Loads are issued kGatherUnroll deep before
 // the stores.
-constexpr int kGatherUnroll = 8;
+constexpr int kGatherUnroll = ULA_GATHER_UNROLL;
 
-__global__ void __launch_bounds__(256, 4) k_gather(GatherParams p) {
+__global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather(GatherParams p) {
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -874,7 +892,7 @@ cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStre
 cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move, 256, 0);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather, 256, 0);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather, kGatherThreads, 0);
 }
 
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
@@ -884,7 +902,7 @@ cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
 }
 
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s) {
-  k_gather<<<blocks, 256, 0, s>>>(p);
+  k_gather<<<blocks, kGatherThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
