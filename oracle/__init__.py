@@ -17,7 +17,12 @@ Parity status of each part (pins live in ``tests/test_oracle_pins.py``):
       happen; brute-force timestamp characterisation with folds; a hand-worked
       example)
   write-back host slots -- pinned (brute force from the exported state)
-  exact-LRU hit rate companion -- parity unpinned (reported only)
+  timestamps (round of each slot's last access) -- pinned (brute force)
+  exact-LRU mode (flag EXACT_LRU: timestamps + oldest-first victims) -- pinned
+      (brute-force timestamp LRU on random tiny traces, with and without the
+      overflow bypass)
+  exact-LRU hit-rate companion (ExactLru) -- pinned through the exact-LRU mode
+      (same hits on the same trace)
 """
 from __future__ import annotations
 
@@ -34,7 +39,8 @@ _lock = threading.Lock()
 _lib = None
 
 OK, INVALID_ARG, CAPACITY, UNMAPPED, INTERNAL = 0, 1, 2, 3, 7
-BYPASS = 1  # overflow bypass flag
+BYPASS = 1     # overflow bypass flag
+EXACT_LRU = 2  # exact LRU in place of PB-LRU
 FREE, COLD = -1, -2
 TIER_UNALLOCATED, TIER_GPU, TIER_HOST = 0, 1, 2
 
@@ -67,6 +73,7 @@ def _configure(l):
     l.orc_last_decisions.argtypes = [p, u32, p, p, p, p]
     l.orc_last_decisions.restype = u32
     l.orc_export.argtypes = [p, u32, p, p, p, p, p, p, p]
+    l.orc_export_stamps.argtypes = [p, u32, p, p]
     l.orc_gpu_pool.argtypes = [p, u32]
     l.orc_gpu_pool.restype = p
     l.orc_host_pool.argtypes = [p, u32]
@@ -110,10 +117,10 @@ class OracleError(RuntimeError):
 
 
 class Oracle:
-    """PB-LRU residency oracle: same calls as the library, semantically."""
+    """Residency oracle (PB-LRU, or exact LRU): same calls as the library, semantically."""
 
     def __init__(self, row_bytes, layers_per_group, gpu_slots, host_slots, ring_buckets,
-                 max_logical, _lib=None, bypass=False):
+                 max_logical, _lib=None, bypass=False, exact_lru=False):
         self._l = _lib if _lib is not None else lib()
         self.row_bytes = int(row_bytes)
         self.layers = [int(x) for x in layers_per_group]
@@ -122,9 +129,11 @@ class Oracle:
         self.max_logical = int(max_logical)
         L = np.array(self.layers, dtype=np.uint32)
         self.bypass = bool(bypass)
-        if self.bypass:
+        self.exact_lru = bool(exact_lru)
+        flags = (BYPASS if self.bypass else 0) | (EXACT_LRU if self.exact_lru else 0)
+        if flags:
             self._h = self._l.orc_create2(self.row_bytes, self.G, _ptr(L), self.S, self.H,
-                                          self.B, self.max_logical, BYPASS)
+                                          self.B, self.max_logical, flags)
         else:
             self._h = self._l.orc_create(self.row_bytes, self.G, _ptr(L), self.S, self.H,
                                          self.B, self.max_logical)
@@ -195,6 +204,13 @@ class Oracle:
         return {"tier": tier, "slot": slot, "cls": cls, "owner": owner,
                 "host_free": host_free[:self.H], "host_owner": host_owner[:self.H],
                 "cur": cur.value}
+
+    def stamps(self, g: int):
+        """(timestamp per GPU slot: round of its last access, 0xFFFFFFFF if free; rounds so far)."""
+        st = np.empty(self.S, dtype=np.uint32)
+        r = C.c_uint32(0)
+        self._l.orc_export_stamps(self._h, g, _ptr(st), C.byref(r))
+        return st, r.value
 
     def gpu_pool(self, g: int) -> np.ndarray:
         n = self.S * self.layers[g] * self.row_bytes

@@ -44,7 +44,15 @@
 //     step with more misses than can be made resident moves only the first
 //     M' = min(M, S - hits, free GPU + free host slots) misses; each later
 //     miss is gathered straight from its host slot into the output and stays
-//     on the host.
+//     on the host;
+//   * exact LRU (the baseline policy of §3's first paragraph, selectable in
+//     place of PB-LRU): every GPU slot keeps a timestamp, the round of its
+//     last access (a hit, a fill, or an alloc placement, which counts in the
+//     latest round); victims are the free slots, lowest first, then the
+//     occupied slots in ascending (timestamp, slot) order.  A slot accessed in
+//     the current round is never chosen.  There are no buckets: every
+//     occupied slot carries the one label "cold".  Everything else (pairing,
+//     write-back slots, capacity, bypass, move -> map -> signal) is as above.
 
 #include <algorithm>
 #include <cstdint>
@@ -83,6 +91,9 @@ struct Group {
   uint32_t layers = 0;
   std::vector<Location> where;          // [max_logical]: the logical-to-physical map
   std::vector<int> cls;                 // [S]: kFree, kCold or a ring bucket index
+  std::vector<uint32_t> stamp;          // [S]: round of the last access, kNone if free
+  std::set<std::pair<uint32_t, uint32_t>> by_age;  // exact LRU: (stamp, slot) of occupied slots
+  uint32_t round = 0;                   // scheduling rounds (step calls) so far
   std::vector<uint32_t> owner;          // [S]: logical address held, or kNone
   std::set<uint32_t> free_slots;        // GPU slots holding nothing
   std::set<uint32_t> cold;              // the cold bucket
@@ -99,7 +110,8 @@ struct Group {
   size_t last_bypassed = 0;             // misses served from the host pool directly
 };
 
-constexpr uint32_t kFlagBypass = 1u;  // overflow bypass (same bit as the library's flag)
+constexpr uint32_t kFlagBypass = 1u;    // overflow bypass (same bits as the library's flags)
+constexpr uint32_t kFlagExactLru = 2u;  // exact LRU in place of PB-LRU
 
 struct Oracle {
   uint32_t row_bytes = 0, n_groups = 0, S = 0, H = 0, B = 0, max_logical = 0, flags = 0;
@@ -108,6 +120,7 @@ struct Oracle {
   std::vector<Group> groups;
 
   size_t slot_bytes(const Group &g) const { return (size_t)g.layers * row_bytes; }
+  bool exact() const { return (flags & kFlagExactLru) != 0; }
 };
 
 void remove_from_class(Group &g, uint32_t s) {
@@ -123,6 +136,32 @@ void move_to_current_bucket(Group &g, uint32_t s) {
   g.cls[s] = (int)g.cur;
 }
 
+// Slot s is accessed in the current round: PB-LRU moves it into the current
+// bucket; exact LRU renews its timestamp (it joins, or stays in, the one
+// occupied class).
+void touch(const Oracle &o, Group &g, uint32_t s) {
+  if (o.exact()) {
+    if (g.cls[s] != kFree) g.by_age.erase({g.stamp[s], s});
+    remove_from_class(g, s);
+    g.cold.insert(s);
+    g.cls[s] = kCold;
+    g.by_age.insert({g.round, s});
+  } else {
+    move_to_current_bucket(g, s);
+  }
+  g.stamp[s] = g.round;
+}
+
+// Slot s gives up its data and becomes free.
+void release_slot(Group &g, uint32_t s) {
+  if (g.cls[s] != kFree) g.by_age.erase({g.stamp[s], s});
+  remove_from_class(g, s);
+  g.free_slots.insert(s);
+  g.cls[s] = kFree;
+  g.owner[s] = kNone;
+  g.stamp[s] = kNone;
+}
+
 }  // namespace
 
 extern "C" {
@@ -130,6 +169,7 @@ extern "C" {
 void *orc_create2(uint32_t row_bytes, uint32_t n_groups, const uint32_t *layers, uint32_t S,
                   uint32_t H, uint32_t B, uint32_t max_logical, uint32_t flags) {
   if (!row_bytes || !n_groups || !layers || !S || !B || !max_logical) return nullptr;
+  if (flags & ~(kFlagBypass | kFlagExactLru)) return nullptr;
   Oracle *o = new Oracle;
   o->flags = flags;
   o->row_bytes = row_bytes;
@@ -145,6 +185,7 @@ void *orc_create2(uint32_t row_bytes, uint32_t n_groups, const uint32_t *layers,
     g.layers = layers[gi];
     g.where.assign(max_logical, Location{});
     g.cls.assign(S, kFree);
+    g.stamp.assign(S, kNone);
     g.owner.assign(S, kNone);
     for (uint32_t s = 0; s < S; ++s) g.free_slots.insert(s);
     g.ring.assign(B, std::set<uint32_t>{});
@@ -180,7 +221,7 @@ int orc_alloc(void *h, uint32_t n, const uint8_t *rows, uint32_t *base_out) {
       const uint8_t *src = rows + group_off + (size_t)i * sb;
       if (!g.free_slots.empty()) {  // lowest free GPU slot; a prefill write counts as an access
         uint32_t s = *g.free_slots.begin();
-        move_to_current_bucket(g, s);
+        touch(*o, g, s);
         g.owner[s] = a;
         g.where[a] = Location{kOnGpu, s};
         std::memcpy(&g.gpu_pool[(size_t)s * sb], src, sb);
@@ -210,10 +251,7 @@ int orc_free(void *h, uint32_t base, uint32_t n) {
       const uint32_t a = base + i;
       Location loc = g.where[a];
       if (loc.tier == kOnGpu) {
-        remove_from_class(g, loc.slot);
-        g.free_slots.insert(loc.slot);
-        g.cls[loc.slot] = kFree;
-        g.owner[loc.slot] = kNone;
+        release_slot(g, loc.slot);
       } else {
         g.host_free.insert(loc.slot);
         g.host_owner[loc.slot] = kNone;
@@ -279,18 +317,23 @@ int orc_step_group(void *h, uint32_t gi, const uint32_t *sel, uint32_t n_req, ui
 
   for (size_t e = 0; e < E; ++e) entry_row[e] = sel[e] == kPad ? -1 : row_of[sel[e]];
 
-  // (3a) rotate: the current bucket advances one position; what is left in the
-  //      bucket about to be reused is folded into the cold bucket.
+  // (3a) a new round.  PB-LRU: the current bucket advances one position; what
+  //      is left in the bucket about to be reused is folded into the cold bucket.
+  //      (Exact LRU has no buckets; its ring stays empty.)
+  g.round++;
   g.cur = (g.cur + 1) % o->B;
-  for (uint32_t s : g.ring[g.cur]) {
-    g.cold.insert(s);
-    g.cls[s] = kCold;
+  if (!o->exact()) {
+    for (uint32_t s : g.ring[g.cur]) {
+      g.cold.insert(s);
+      g.cls[s] = kCold;
+    }
+    g.ring[g.cur].clear();
   }
-  g.ring[g.cur].clear();
 
-  // (3b) hits: the slot moves into the current bucket.
+  // (3b) hits: the slot is accessed in this round (PB-LRU: it moves into the
+  //      current bucket; exact LRU: its timestamp becomes this round).
   for (uint32_t a : uniq)
-    if (g.where[a].tier == kOnGpu) move_to_current_bucket(g, g.where[a].slot);
+    if (g.where[a].tier == kOnGpu) touch(*o, g, g.where[a].slot);
 
   // (4) victims: free slots, then the cold bucket, then the ring from oldest
   //     (cur+1) to newest (cur-1); never the current bucket; lowest slot first.
@@ -304,8 +347,18 @@ int orc_step_group(void *h, uint32_t gi, const uint32_t *sel, uint32_t n_req, ui
     }
   };
   take(g.free_slots, kFree);
-  take(g.cold, kCold);
-  for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));
+  if (o->exact()) {
+    // exact LRU: the oldest timestamp first, ties to the lowest slot; a slot
+    // stamped in this round (a hit) is never taken
+    for (const auto &ts : g.by_age) {
+      if (victims.size() == M || ts.first == g.round) break;
+      victims.push_back(ts.second);
+      victim_class.push_back(kCold);
+    }
+  } else {
+    take(g.cold, kCold);
+    for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));
+  }
 
   if (victims.size() != M) return kInternal;
 
@@ -340,7 +393,7 @@ int orc_step_group(void *h, uint32_t gi, const uint32_t *sel, uint32_t n_req, ui
     std::memcpy(&g.gpu_pool[(size_t)v * sb], &g.host_pool[(size_t)src_host * sb], sb);
     g.where[a] = Location{kOnGpu, v};
     g.owner[v] = a;
-    move_to_current_bucket(g, v);
+    touch(*o, g, v);
     released_host.push_back(src_host);
   }
   for (uint32_t hs : released_host) {
@@ -404,6 +457,15 @@ void orc_export(void *h, uint32_t gi, uint8_t *tier, uint32_t *slot, int32_t *cl
   }
   if (host_owner) std::copy(g.host_owner.begin(), g.host_owner.end(), host_owner);
   if (cur) *cur = g.cur;
+}
+
+// Timestamps of group gi's GPU slots ([S]: round of the last access, kNone if
+// free) and its round count.
+void orc_export_stamps(void *h, uint32_t gi, uint32_t *stamp, uint32_t *round) {
+  Oracle *o = static_cast<Oracle *>(h);
+  const Group &g = o->groups[gi];
+  if (stamp) std::copy(g.stamp.begin(), g.stamp.end(), stamp);
+  if (round) *round = g.round;
 }
 
 const uint8_t *orc_gpu_pool(void *h, uint32_t gi) {

@@ -50,6 +50,7 @@ class Workload:
     row_bytes: int = 656        # 512 e4m3 latent + 4 fp32 scales + 64 bf16 rope
     pad_prob: float = 0.0       # fraction of entries replaced by the pad marker (edge tests)
     bypass: bool = False        # overflow bypass: misses beyond the pool are read in place
+    exact_lru: bool = False     # exact LRU (timestamp per slot) in place of PB-LRU
     _cache: dict = field(default_factory=dict, compare=False, hash=False, repr=False)
 
     @property
@@ -108,7 +109,8 @@ class Workload:
                 "layers_per_group": self.layers_per_group, "top_k": self.k,
                 "query_tokens": self.q, "gpu_slots": self.gpu_slots,
                 "host_slots": self.host_slots, "ring_buckets": self.ring_buckets,
-                "row_bytes": self.row_bytes, "trace_steps": self.steps, "seed": self.seed}
+                "row_bytes": self.row_bytes, "trace_steps": self.steps, "seed": self.seed,
+                "policy": "exact LRU" if self.exact_lru else "PB-LRU"}
 
 
 WORKLOADS = {

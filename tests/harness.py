@@ -39,7 +39,7 @@ def alloc_rows(w, addr0: int, n: int, mode: str) -> np.ndarray:
 def make_oracle(w, mode: str = "bytes") -> Oracle:
     W = w.row_bytes if mode == "bytes" else ID_ROW_BYTES
     return Oracle(W, [w.layers_per_group] * w.n_groups, w.gpu_slots, w.host_slots,
-                  w.ring_buckets, w.max_logical, bypass=w.bypass)
+                  w.ring_buckets, w.max_logical, bypass=w.bypass, exact_lru=w.exact_lru)
 
 
 def initial_allocs(w, trace):

@@ -21,8 +21,8 @@ MUTATIONS = [
     ("ring newest first", "take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));",
      "take(g.ring[(g.cur + o->B - d) % o->B], (int)((g.cur + o->B - d) % o->B));"),
     ("no fold into cold", "for (uint32_t s : g.ring[g.cur]) {", "for (uint32_t s : std::set<uint32_t>{}) {"),
-    ("cold after ring", "  take(g.cold, kCold);\n  for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));",
-     "  for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));\n  take(g.cold, kCold);"),
+    ("cold after ring", "    take(g.cold, kCold);\n    for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));",
+     "    for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));\n    take(g.cold, kCold);"),
     ("highest slot first", "    for (uint32_t s : from) {", "    for (auto it = from.rbegin(); it != from.rend(); ++it) { uint32_t s = *it;"),
     ("write-back to highest free host slot", "  for (uint32_t hs : g.host_free) {\n    if (wb_host.size()",
      "  for (auto it = g.host_free.rbegin(); it != g.host_free.rend(); ++it) { uint32_t hs = *it;\n    if (wb_host.size()"),
@@ -36,10 +36,18 @@ MUTATIONS = [
     ("miss host slots never released", "  for (uint32_t hs : released_host) {\n    g.host_free.insert(hs);", "  for (uint32_t hs : released_host) {\n"),
     ("alloc takes highest free slot", "      if (!g.free_slots.empty()) {  // lowest free GPU slot; a prefill write counts as an access\n        uint32_t s = *g.free_slots.begin();",
      "      if (!g.free_slots.empty()) {\n        uint32_t s = *g.free_slots.rbegin();"),
-    ("hits not moved to the current bucket", "    if (g.where[a].tier == kOnGpu) move_to_current_bucket(g, g.where[a].slot);", "    (void)a;"),
+    ("hits not marked as accessed", "    if (g.where[a].tier == kOnGpu) touch(*o, g, g.where[a].slot);", "    (void)a;"),
     ("write-back skipped (data lost)", "      std::memcpy(&g.host_pool[(size_t)hs * sb], &g.gpu_pool[(size_t)v * sb], sb);\n", ""),
     ("fill skipped", "    std::memcpy(&g.gpu_pool[(size_t)v * sb], &g.host_pool[(size_t)src_host * sb], sb);\n    g.where[a]",
      "    g.where[a]"),
+    ("exact LRU: occupied slots taken in slot order, not oldest first",
+     "    for (const auto &ts : g.by_age) {\n      if (victims.size() == M || ts.first == g.round) break;\n      victims.push_back(ts.second);",
+     "    for (uint32_t sl : g.cold) {\n      if (victims.size() == M) break;\n      if (g.stamp[sl] == g.round) continue;\n      victims.push_back(sl);"),
+    ("exact LRU: an access renews the timestamp but not the age order",
+     "    g.by_age.insert({g.round, s});\n  } else {",
+     "    g.by_age.insert({g.stamp[s] == kNone ? g.round : g.stamp[s], s});\n  } else {"),
+    ("timestamps of alloc placements one round late", "  g.stamp[s] = g.round;\n}",
+     "  g.stamp[s] = g.round + (g.owner[s] == kNone ? 1u : 0u);\n}"),
 ]
 
 
@@ -51,6 +59,10 @@ def _fast_pins():
         pins.test_with_folds_matches_timestamp_model(seed)
     for seed in range(0, 60, 9):
         pins.test_no_fold_equals_round_lru(seed)
+    for seed in range(0, 120, 7):
+        pins.test_exact_lru_matches_timestamp_model(seed)
+    for seed in range(0, 40, 5):
+        pins.test_exact_lru_bypass_matches_timestamp_model(seed)
     pins.test_rotation_only_relabels()
     pins.test_errors_leave_state_untouched()
     pins.test_alloc_placement_and_free()

@@ -7,6 +7,9 @@ reasoning fix -- independent of the oracle's own code:
   LRU with the lowest slot first inside a round;
 * with folds, a brute-force model written from per-slot timestamps (a slot is cold
   iff its last access is at least B rounds old) instead of bucket sets;
+* the exact-LRU mode (§3's baseline policy: a timestamp per slot, the oldest
+  evicted first) against the same brute force's round-granular LRU order, for any
+  number of ring buckets, and the per-slot timestamps against the brute force's;
 * the gathered rows against the generator's closed form (byte for byte);
 * invariants: never both tiers (§2), slot ownership, class partition, the
   current round's slots never evicted (§3), rotation changes labels only (§3),
@@ -186,9 +189,10 @@ class BruteForce:
         return victims, wb
 
 
-def _random_trace(rng, S, H, B, rounds, lru, n0, bypass=False, max_pick=None):
-    """Random tiny trace: selections with repeats and pads, allocs and frees between steps."""
-    o = Oracle(ID_ROW_BYTES, [1], S, H, B, 4096, bypass=bypass)
+def _random_trace(rng, S, H, B, rounds, lru, n0, bypass=False, max_pick=None, exact=False):
+    """Random tiny trace: selections with repeats and pads, allocs and frees between steps.
+    exact: the oracle runs its exact-LRU mode (checked against lru=True)."""
+    o = Oracle(ID_ROW_BYTES, [1], S, H, B, 4096, bypass=bypass, exact_lru=exact)
     bf = BruteForce(S, H, B, lru=lru, bypass=bypass)
     live = []
     assert o.alloc(n0, _id_row_buf(0, n0)) == bf.alloc(n0)
@@ -226,6 +230,9 @@ def _random_trace(rng, S, H, B, rounds, lru, n0, bypass=False, max_pick=None):
         st = o.export(0)
         for a, (t, s) in bf.loc.items():
             assert st["tier"][a] == (TIER_GPU if t == "G" else TIER_HOST) and st["slot"][a] == s
+        stamp, rounds_done = o.stamps(0)
+        assert rounds_done == bf.round
+        assert stamp.tolist() == [bf.last.get(x, 0xFFFFFFFF) for x in range(S)]
         got = res["out"][0, :res["req_off"][-1]].view(np.uint32)[:, 0]
         assert got.tolist() == list(dict.fromkeys(a for a in flat if a != synth.PAD))
     return o
@@ -260,6 +267,25 @@ def test_overflow_bypass_matches_timestamp_model(seed):
     B = rng.randint(2, 5)
     _random_trace(rng, S=S, H=rng.choice([16, 64]), B=B, rounds=rng.randint(10, 60), lru=False,
                   n0=rng.randint(S, S + 12), bypass=True, max_pick=2 * S + 3)
+
+
+@pytest.mark.parametrize("seed", range(120))
+def test_exact_lru_matches_timestamp_model(seed):
+    """Exact LRU: free slots ascending, then occupied slots by (last round, slot),
+    whatever the ring size (B is ignored by the policy)."""
+    rng = random.Random(9000 + seed)
+    S = rng.randint(2, 16)
+    B = rng.randint(1, 5)
+    _random_trace(rng, S=S, H=64, B=B, rounds=rng.randint(10, 120), lru=True,
+                  n0=rng.randint(S, S + 24), exact=True)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_exact_lru_bypass_matches_timestamp_model(seed):
+    rng = random.Random(12000 + seed)
+    S = rng.randint(2, 10)
+    _random_trace(rng, S=S, H=rng.choice([16, 64]), B=rng.randint(1, 4), rounds=rng.randint(10, 60),
+                  lru=True, n0=rng.randint(S, S + 12), bypass=True, max_pick=2 * S + 3, exact=True)
 
 
 def test_overflow_without_bypass_is_an_error():
@@ -445,6 +471,47 @@ def test_alloc_placement_and_free():
     for j in range(3):
         ids = res["out"][j, :2].view(np.uint32)
         assert ids[:, 0].tolist() == [8, 0] and (ids[:, 1] == (1 << 16 | j)).all()
+
+
+class _WithCompanion(OracleRun):
+    """An oracle replay with the exact-LRU hit-rate companion stepped beside it."""
+
+    def __init__(self, w):
+        self.lru = ExactLru(w.n_groups, w.gpu_slots, w.max_logical)
+        super().__init__(w, mode="id")
+
+    def alloc(self, expect_base, n):
+        assert self.lru.alloc(n) == expect_base
+        return super().alloc(expect_base, n)
+
+    def free(self, base, n):
+        self.lru.free(base, n)
+        super().free(base, n)
+
+    def step(self):
+        from tests.harness import apply_events
+        sel, ev = self.trace.step()
+        res = [self.o.step_group(g, sel[g]) for g in range(self.w.n_groups)]
+        for g in range(self.w.n_groups):
+            self.lru.step_group(g, sel[g])
+        apply_events(self.alloc, self.free, ev)
+        return sel, ev, res
+
+
+@pytest.mark.parametrize("name", ["cfg1", "cfg4"])
+def test_exact_lru_companion_agrees_with_exact_mode(name):
+    """The hit-rate companion and the oracle's exact-LRU mode are the same policy:
+    same hits and unique rows on the same trace (turnover included)."""
+    w = small(name).replace(steps=20, exact_lru=True)
+    run = _WithCompanion(w)
+    uniq = hits = 0
+    for _ in range(w.steps):
+        sel, ev, res = run.step()
+        for g in range(w.n_groups):
+            uniq += res[g]["counters"]["uniq"]
+            hits += res[g]["counters"]["hits"]
+    assert int(run.lru.acc[0]) == uniq and int(run.lru.acc[1]) == hits
+    assert 0 < hits < uniq
 
 
 def test_exact_lru_companion_sanity():
