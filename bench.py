@@ -44,6 +44,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="cfg2")
+    ap.add_argument("--policy", choices=["pblru", "exact"], default="pblru",
+                    help="replacement policy: PB-LRU, or exact LRU (timestamp scan)")
     ap.add_argument("--profile-steps", type=int, default=60)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -240,7 +242,7 @@ def run_gpu(args, rank, world, local):
     cache = UlaCache(row_bytes=W, layers_per_group=[L] * G, gpu_slots=w.gpu_slots,
                      host_slots=w.host_slots, ring_buckets=w.ring_buckets,
                      max_logical=w.max_logical, max_entries=E, device=dev, stream=stream,
-                     bypass_overflow=w.bypass)
+                     bypass_overflow=w.bypass, exact_lru=w.exact_lru)
     trace = stage_initial(cache, w, synth, torch)
     n_value, n_prof = args.steps, min(args.profile_steps, args.steps)
     n_e2e = 0 if args.no_e2e else args.steps
@@ -455,11 +457,11 @@ def traffic_per_launch(rows_per_launch):
 
 # ------------------------------------------------------------- CPU oracle arm
 
-def cpu_sample_workload(name):
+def cpu_sample_workload(name, exact=False):
     from synth.configs import WORKLOADS
     w = WORKLOADS[name]
     n = min(4, w.n_live)
-    kw = dict(n_live=n, name=w.name + "_cpu_sample",
+    kw = dict(n_live=n, name=w.name + "_cpu_sample", exact_lru=exact,
               description=w.description + f" (first {n} requests)")
     if w.n_total is not None:
         kw["n_total"] = n
@@ -467,15 +469,16 @@ def cpu_sample_workload(name):
     return w.replace(**kw)
 
 
-def run_oracle(name, warmup, steps=None, seconds=None):
-    """The oracle as it stands, single-threaded, on a bounded sample of the workload."""
+def run_oracle(name, warmup, steps=None, seconds=None, exact=False):
+    """The oracle as it stands, single-threaded, on a bounded sample of the workload
+    (exact: its exact-LRU mode)."""
     import numpy as np
 
     import synth
     from oracle import ExactLru
     from tests.harness import OracleRun, apply_events
 
-    w = cpu_sample_workload(name)
+    w = cpu_sample_workload(name, exact)
     run = OracleRun(w, "bytes")
     lru = ExactLru(w.n_groups, w.gpu_slots, w.max_logical)
     for b, n in [(int(b), int(c)) for b, c in zip(*run.trace.initial()[1::-1])]:
@@ -485,6 +488,8 @@ def run_oracle(name, warmup, steps=None, seconds=None):
     n_done = 0
     limit = steps if steps is not None else 10 ** 9
     while n_done < warmup + limit:
+        if n_done == warmup:
+            lru.acc[:] = 0  # hit rates over the timed steps only
         sel, ev = run.trace.step()
         t0 = time.perf_counter()
         res = [run.o.step_group(g, sel[g]) for g in range(w.n_groups)]
@@ -509,7 +514,8 @@ def run_oracle(name, warmup, steps=None, seconds=None):
             "sample": (f"{w.description}: {w.n_live} requests, S={w.gpu_slots}, "
                        f"H={w.host_slots}, {timed_steps} decode steps after {warmup} warm-up, "
                        f"656-byte rows moved, single-threaded"),
-            "pblru_hit_rate": hits / max(1, uniq), "exact_lru_hit_rate": lru.hit_rate}
+            "policy": "exact LRU" if exact else "PB-LRU",
+            "hit_rate": hits / max(1, uniq), "exact_lru_hit_rate": lru.hit_rate}
 
 
 # -------------------------------------------------------------------- main
@@ -517,6 +523,9 @@ def run_oracle(name, warmup, steps=None, seconds=None):
 def workload_for(args):
     from synth.configs import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.policy == "exact":
+        w = w.replace(exact_lru=True, name=w.name + "_exact",
+                      description=w.description + " (exact LRU)")
     if args.requests is not None and args.requests != w.n_live:
         w = w.replace(n_live=args.requests, name=f"{w.name}_r{args.requests}",
                       description=w.description + f" (recipe with {args.requests} requests)")
@@ -536,7 +545,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        cb = run_oracle(args.workload, args.warmup, steps=args.steps)
+        cb = run_oracle(args.workload, args.warmup, steps=args.steps, exact=w.exact_lru)
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "rows/s",
                 "n_gpus": args.gpus, "steps": cb["steps"], "warmup": args.warmup,
                 "ms_per_step": round(cb["seconds"] / max(1, cb["steps"]) * 1e3, 3),
@@ -563,11 +572,16 @@ def main(argv=None):
                 "config": config, "roofline": r["roofline"], "host_link": r["host_link"],
                 "gpu_launches": r["launches"], "clocks": r["clocks"],
                 "phases_ms_per_step": r["phases"],
-                "pblru_hit_rate": r["stats"]["hits"] / max(1, r["stats"]["uniq"])}
+                "scheduling_ms_per_step": round(sum(r["phases"].get(k, 0.0)
+                                                    for k in ("rotate", "mark", "select")), 4),
+                "metadata_ms_per_step": round(sum(r["phases"].get(k, 0.0)
+                                                  for k in ("dedup", "rotate", "mark", "select")), 4),
+                "hit_rate": r["stats"]["hits"] / max(1, r["stats"]["uniq"])}
         if r["e2e"] is not None:
             line["e2e"] = r["e2e"]
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = run_oracle(args.workload, 2, seconds=args.cpu_seconds)
+            line["cpu_baseline"] = run_oracle(args.workload, 2, seconds=args.cpu_seconds,
+                                              exact=w.exact_lru)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

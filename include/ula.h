@@ -78,6 +78,20 @@ typedef struct ula_config {
  * the output: it stays on the host and nothing else changes for it. */
 #define ULA_FLAG_BYPASS_OVERFLOW 1u
 
+/* Exact LRU in place of PB-LRU: the baseline replacement policy that §3 "PB-LRU" sets
+ * PB-LRU against (a timestamp per slot, victims found by scanning the whole pool).
+ * Every GPU slot keeps the round of its last access (a hit, a fill, or an alloc
+ * placement, which counts in the latest round); victims are the free slots, lowest
+ * first, then the occupied slots in ascending (timestamp, slot) order, found by a
+ * scan of all S timestamps (a radix select of the oldest, then a stable sort of the
+ * chosen ones).  A slot accessed in the current round is never chosen.  There are no
+ * ring buckets: every occupied slot carries the cold label (diagnostics), and the
+ * victims_cold counter counts the occupied slots taken.  Pairing, write-back slots,
+ * capacity, the bypass and the move -> map -> signal order are as for PB-LRU.  The
+ * scan runs as one cooperative launch whose grid-wide barriers are bounded waits: a
+ * wait that expires latches ULA_ERR_TIMEOUT. */
+#define ULA_FLAG_EXACT_LRU 2u
+
 /* Counters accumulated since ula_create, summed over groups. */
 typedef struct ula_stats {
   uint64_t steps;          /* ula_step_group calls completed */

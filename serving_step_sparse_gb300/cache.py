@@ -73,7 +73,7 @@ class UlaCache:
     def __init__(self, *, row_bytes: int, layers_per_group, gpu_slots: int, host_slots: int,
                  ring_buckets: int, max_logical: int, max_entries: int, device="cuda",
                  stream: torch.cuda.Stream | None = None, huge_host_pages: bool = True,
-                 bypass_overflow: bool = False):
+                 bypass_overflow: bool = False, exact_lru: bool = False):
         self.device = torch.device(device)
         self.W = int(row_bytes)
         self.layers = [int(x) for x in layers_per_group]
@@ -88,7 +88,8 @@ class UlaCache:
         self.host_pools = [b.tensor for b in self._host_bufs] if self.H else None
         cfg = ula.make_config(self.W, self.layers, self.S, self.H, self.B, self.max_logical,
                               self.max_entries,
-                              ula.FLAG_BYPASS_OVERFLOW if bypass_overflow else 0)
+                              (ula.FLAG_BYPASS_OVERFLOW if bypass_overflow else 0)
+                              | (ula.FLAG_EXACT_LRU if exact_lru else 0))
         with torch.cuda.device(self.device):
             self.ctx = ula.ula_create(cfg, [p.data_ptr() for p in self.gpu_pools],
                                       [p.data_ptr() for p in self.host_pools] if self.H else None,

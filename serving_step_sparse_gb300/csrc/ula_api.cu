@@ -54,6 +54,8 @@ struct ula_ctx {
   uint32_t *addr_row = nullptr;
   uint2 *blk = nullptr;
   uint32_t *miss_list = nullptr, *miss_hs = nullptr, *miss_row = nullptr;
+  LruScratch lru{};     // exact LRU's scan scratch (ULA_FLAG_EXACT_LRU only)
+  int lru_blocks = 0;   // its cooperative grid
   int *status = nullptr;
   uint32_t decision_cap = 0;
   uint32_t epoch = 0;
@@ -204,7 +206,8 @@ int validate_config(const ula_config *c) {
     return ULA_ERR_INVALID_ARG;
   if (c->ring_buckets == 0 || c->ring_buckets > ULA_MAX_BUCKETS) return ULA_ERR_INVALID_ARG;
   if (c->max_logical == 0 || c->max_logical > kSlotMask) return ULA_ERR_INVALID_ARG;
-  if (c->max_entries == 0 || (c->flags & ~ULA_FLAG_BYPASS_OVERFLOW) != 0) return ULA_ERR_INVALID_ARG;
+  if (c->max_entries == 0) return ULA_ERR_INVALID_ARG;
+  if ((c->flags & ~(ULA_FLAG_BYPASS_OVERFLOW | ULA_FLAG_EXACT_LRU)) != 0) return ULA_ERR_INVALID_ARG;
   return ULA_OK;
 }
 
@@ -241,6 +244,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   geo.W = cfg.row_bytes;
   geo.max_logical = cfg.max_logical;
   geo.bypass = (cfg.flags & ULA_FLAG_BYPASS_OVERFLOW) ? 1u : 0u;
+  geo.exact = (cfg.flags & ULA_FLAG_EXACT_LRU) ? 1u : 0u;
   geo.gd = dims_for(S);
   geo.hd = dims_for(H);
   geo.nseg = geo.gd.n1;
@@ -295,6 +299,20 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(c->alloc(&c->cnt_d, G));
   ULA_CUDA(c->alloc(&c->groups_d, G));
   cudaStream_t s = c->home;
+  if (geo.exact) {  // one cooperative block per SM (it must fit beside the gathers)
+    int per_sm = 0;
+    ULA_CUDA(lru_resident_blocks(&per_sm));
+    if (per_sm < 1) return ULA_ERR_CUDA;
+    c->lru_blocks = c->sm_count;
+    const size_t nb = (size_t)c->lru_blocks;
+    ULA_CUDA(c->alloc(&c->lru.blk, 2 * nb));
+    ULA_CUDA(c->alloc(&c->lru.hist, (size_t)kLruSelectPasses * kLruBins));
+    ULA_CUDA(c->alloc(&c->lru.table, kSortBins * nb + kSortBins));
+    ULA_CUDA(c->alloc(&c->lru.list[0], cfg.max_entries));
+    ULA_CUDA(c->alloc(&c->lru.list[1], cfg.max_entries));
+    ULA_CUDA(c->alloc(&c->lru.bar, 2));
+    ULA_CUDA(cudaMemsetAsync(c->lru.bar, 0, 2 * sizeof(uint32_t), s));
+  }
   ULA_CUDA(cudaMemsetAsync(c->tbl, 0, sizeof(unsigned long long) * cfg.max_logical, s));
   ULA_CUDA(cudaMemsetAsync(c->status, 0, sizeof(int), s));
 
@@ -517,6 +535,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.order.cls[0] = B + 1;
   p.order.cls[1] = B;
   for (uint32_t d = 1; d < B; ++d) p.order.cls[1 + d] = (cur + d) % B;
+  if (c->geo.exact) p.order.n_cls = 1;  // exact LRU walks the free slots; the scan does the rest
   // (1)(2) dedup + translate + capacity check
   ULA_CUDA(c->phase(ULA_PHASE_DEDUP, s, E ? 2 : 1, [&] { return launch_dedup(p, s); }));
   // (3a) rotation + compaction of unique rows and misses
@@ -555,8 +574,17 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   ep.order = p.order;
   ep.quota = 0xffffffffu;
   ep.status = c->status;
-  ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
-                    [&] { return launch_select_emit(ep, 1, c->emit_blocks, s); }));
+  LruParams lp{};
+  lp.geo = c->geo;
+  lp.grp = gd;
+  lp.sc = c->lru;
+  lp.round = r;
+  lp.status = c->status;
+  ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, c->geo.exact ? 2 : 1, [&] {
+    cudaError_t e = launch_select_emit(ep, 1, c->emit_blocks, s);
+    if (e == cudaSuccess && c->geo.exact) e = launch_lru_select(lp, c->lru_blocks, s);
+    return e;
+  }));
   // (5) write-back, fill (writing the missed rows' outputs), then map commit
   MoveParams mp{};
   mp.geo = c->geo;

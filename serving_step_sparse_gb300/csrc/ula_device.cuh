@@ -89,6 +89,7 @@ struct Geometry {
   uint32_t S, H, B, W;   // GPU slots, host slots, ring buckets, row bytes
   uint32_t max_logical;
   uint32_t bypass;       // ULA_FLAG_BYPASS_OVERFLOW set
+  uint32_t exact;        // ULA_FLAG_EXACT_LRU set: occupied slots all in class B, no ring
   Dims gd, hd;           // bitmap dims for GPU-slot and host-slot bitmaps
   uint32_t nseg, hseg;   // segments (= level-1 words) per bitmap
 };
@@ -167,6 +168,30 @@ struct MoveParams {
   int *status;
 };
 
+// Exact-LRU victim scan (one cooperative launch per step).
+constexpr int kLruThreads = 512;
+constexpr int kLruDigit = 11;                    // bits per radix-select digit
+constexpr uint32_t kLruBins = 1u << kLruDigit;
+constexpr int kLruSelectPasses = 3;              // 32-bit keys: 11 + 11 + 10 bits
+constexpr uint32_t kSortBins = 256;              // 8-bit digits of the stable sort
+
+struct LruScratch {
+  uint4 *blk;          // [2][grid]: per block (min stamp, max stamp, candidates), then
+                       // (slots below, at the threshold)
+  uint32_t *hist;      // [kLruSelectPasses][kLruBins]
+  uint32_t *table;     // [kSortBins][grid] digit counts of a sort pass, then [kSortBins] totals
+  uint2 *list[2];      // [max_entries]: (stamp - oldest, slot) of the chosen slots
+  uint32_t *bar;       // [2]: grid barrier arrivals, generation
+};
+
+struct LruParams {
+  Geometry geo;
+  GroupDev grp;
+  LruScratch sc;
+  uint32_t round;
+  int *status;
+};
+
 struct GatherParams {
   Geometry geo;
   GroupDev grp;
@@ -206,6 +231,10 @@ cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int block
 cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s);
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s);  // copies, then commit
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
+// exact LRU: victims [F, M) by a scan of the slot timestamps (cooperative launch of
+// `blocks` co-resident blocks)
+cudaError_t launch_lru_select(const LruParams &p, int blocks, cudaStream_t s);
+cudaError_t lru_resident_blocks(int *per_sm);
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s);
 cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);

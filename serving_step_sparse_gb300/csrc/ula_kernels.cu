@@ -168,6 +168,18 @@ __device__ __forceinline__ uint32_t class_of(uint32_t stamp, uint32_t round, uin
   return stamp % B;
 }
 
+// The class of a slot under the configured policy: exact LRU keeps every
+// occupied slot in the one class B (its order lives in the stamps alone).
+__device__ __forceinline__ uint32_t slot_class(const Geometry &geo, uint32_t stamp, uint32_t round) {
+  if (geo.exact) return stamp == kNone ? geo.B + 1 : geo.B;
+  return class_of(stamp, round, geo.B);
+}
+
+// The class a slot joins when it is accessed in the round whose bucket is `cur`.
+__device__ __forceinline__ uint32_t access_class(const Geometry &geo, uint32_t cur) {
+  return geo.exact ? geo.B : cur;
+}
+
 // ------------------------------------------------------------------ init
 
 // all of [0, nbits) set, with exact summaries and segment counts
@@ -307,6 +319,7 @@ __global__ void __launch_bounds__(kEntryThreads) k_rotate_emit(StepParams p) {
   if (block_skips(p.status)) return;
   const Geometry &geo = p.geo;
   if (blockIdx.x >= p.emit_blocks) {
+    if (geo.exact) return;  // no ring under exact LRU
     const Bitmap bucket = class_bitmap(p.grp, geo, p.cur);
     const Bitmap cold = class_bitmap(p.grp, geo, geo.B);
     const uint32_t nthr = (gridDim.x - p.emit_blocks) * blockDim.x;
@@ -408,12 +421,15 @@ __device__ __forceinline__ uint32_t walk_chunk(const uint32_t *cnt, uint32_t nse
 }
 
 // (4) Walk the segment counts of the classes in `ord` for the first `quota` set
-// bits, then the host-free bitmap for the first K = quota - (free slots taken)
-// set bits, and record one work entry per segment that holds some of them.
-// Block-wide (T threads); stops as soon as the quota is met.
+// bits, then the host-free bitmap for the first K = total - (free slots taken)
+// set bits (a step's victims that hold data; alloc: what the GPU walk lacked),
+// and record one work entry per segment that holds some of them.  Block-wide (T
+// threads); stops as soon as the quota is met.  A step walks for quota = total
+// victims under PB-LRU; under exact LRU it walks the free class only, for
+// quota = min(total, free slots), and the scan picks the rest.
 template <int T>
 __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order &ord,
-                            uint32_t quota, bool is_step, int *status) {
+                            uint32_t quota, uint32_t total, bool is_step, int *status) {
   __shared__ uint32_t s_nwork;
   if (threadIdx.x == 0) s_nwork = 0;
   __syncthreads();
@@ -430,7 +446,7 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
   }
   const uint32_t F = taken_free;
   const uint32_t nwork_gpu = s_nwork;
-  const uint32_t K = (is_step && rem == 0) ? quota - F : (is_step ? 0u : rem);
+  const uint32_t K = (is_step && rem == 0) ? total - F : (is_step ? 0u : rem);
   uint32_t hrem = K, hbase = 0;
   const Bitmap hb = host_free_bitmap(g);
   for (uint32_t s0 = 0; s0 < geo.hseg && hrem > 0; s0 += T * kWalkSegs)
@@ -449,8 +465,12 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
     c->free_gpu -= F;   // F free slots filled
     c->free_host += F;  // K host slots taken, quota host slots released
     c->stat[kStVictFree] += F;
-    c->stat[kStVictCold] += taken_cold;
-    c->stat[kStVictRing] += quota - F - taken_cold;
+    if (geo.exact) {
+      c->stat[kStVictCold] += total - F;  // occupied slots (the scan's victims)
+    } else {
+      c->stat[kStVictCold] += taken_cold;
+      c->stat[kStVictRing] += quota - F - taken_cold;
+    }
     c->stat[kStWriteback] += K;
     c->stat[kStBytesD2H] += (unsigned long long)K * g.layers * geo.W;
   } else {
@@ -460,8 +480,9 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
 }
 
 // (3b) every hit moves to the current bucket (clears on its old class, sets
-// on cur) and its slot is recorded for the gather.  The last block then walks
-// the classes for the M victims.
+// on cur) and its slot is recorded for the gather; under exact LRU only its
+// timestamp changes.  The last block then walks the classes for the M victims
+// (exact LRU: the free class only).
 __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
   if (block_skips(p.status)) return;
   const GroupDev &g = p.grp;
@@ -473,13 +494,14 @@ __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
     if (m & kHostBit) {
       g.row_slot[i] = kNone;  // filled (and its output written) by the move
     } else {
-      const uint32_t c = m < geo.S ? class_of(g.stamp[m], p.round, geo.B) : geo.B + 1;
+      const uint32_t c = m < geo.S ? slot_class(geo, g.stamp[m], p.round) : geo.B + 1;
+      const uint32_t to = access_class(geo, p.cur);
       if (c == geo.B + 1) {
         latch(p.status, ULA_ERR_INTERNAL);
       } else {
-        if (c != p.cur) {
+        if (c != to) {
           bm_clear(class_bitmap(g, geo, c), m);
-          bm_set(class_bitmap(g, geo, p.cur), m);
+          bm_set(class_bitmap(g, geo, to), m);
         }
         g.stamp[m] = p.round;
         g.row_slot[i] = m;
@@ -487,7 +509,9 @@ __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
     }
   }
   if (!last_block(&g.cnt->done[1])) return;
-  select_walk<kEntryThreads>(g, geo, p.order, __ldcg(&g.cnt->M), true, p.status);
+  const uint32_t M = __ldcg(&g.cnt->M);
+  const uint32_t quota = geo.exact ? min(M, __ldcg(&g.cnt->free_gpu)) : M;
+  select_walk<kEntryThreads>(g, geo, p.order, quota, M, true, p.status);
 }
 
 // (4) Each work entry's segment: its set bits in ascending order get the ranks
@@ -499,7 +523,7 @@ __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
   const Geometry &geo = p.geo;
   const GroupCounters *c = g.cnt;
   const uint32_t n_work = c->n_work;
-  const uint32_t q_gpu = p.quota == 0xffffffffu ? c->M : p.quota;
+  const uint32_t q_gpu = p.quota == 0xffffffffu ? (geo.exact ? c->F : c->M) : p.quota;
   const uint32_t q_host = c->K;
   const uint32_t lane = lane_id();
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -665,10 +689,11 @@ __global__ void k_commit(MoveParams p) {
     if (owned) g.map[o] = kHostBit | hd;
     g.map[a] = v;
     g.owner[v] = a;
-    const uint32_t c = class_of(g.stamp[v], p.round, geo.B);
-    if (c != p.cur) {
+    const uint32_t c = slot_class(geo, g.stamp[v], p.round);
+    const uint32_t to = access_class(geo, p.cur);
+    if (c != to) {
       bm_clear(class_bitmap(g, geo, c), v);
-      bm_set(class_bitmap(g, geo, p.cur), v);
+      bm_set(class_bitmap(g, geo, to), v);
     }
     g.stamp[v] = p.round;
     bm_set(host_free_bitmap(g), hs);
@@ -751,6 +776,365 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
   }
 }
 
+// ------------------------------------------------------------- exact LRU
+//
+// Exact LRU's victims beyond the free slots (§3 "PB-LRU", first paragraph: a
+// timestamp per slot, victims found by scanning the whole pool): the Q = M - F
+// occupied slots with the smallest (timestamp, slot) among those not accessed
+// in this round, in that order, written to victims[F + rank].  One cooperative
+// launch of co-resident blocks; its phases are separated by grid-wide barriers:
+//   1. scan: oldest and newest candidate timestamp, number of candidates;
+//   2. radix select on key = timestamp - oldest, 11-bit digits from the top:
+//      the threshold timestamp T, and how many slots stamped T are taken (the
+//      lowest ones);
+//   3. stable compaction, in slot order, of the chosen slots;
+//   4. stable LSD radix sort of the chosen (key, slot) pairs on the key's 8-bit
+//      digits; the last pass writes the victims.
+
+constexpr uint32_t kBarrierSpins = 1u << 22;  // polls of ~128 ns: about half a second
+
+__device__ __forceinline__ uint32_t ld_acquire(const void *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid-wide barrier of a cooperative launch (all blocks co-resident).  Bounded:
+// a block that polls more than kBarrierSpins times latches ULA_ERR_TIMEOUT; a
+// block that sees an error latched stops waiting.  Returns false (in every
+// thread of the block) when the grid must give up.
+__device__ __forceinline__ bool grid_sync(uint32_t *bar, int *status) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const uint32_t gen = ld_acquire(&bar[1]);
+    __threadfence();
+    if (atomicAdd(&bar[0], 1u) == gridDim.x - 1) {
+      atomicExch(&bar[0], 0u);
+      __threadfence();
+      atomicAdd(&bar[1], 1u);
+    } else {
+      uint32_t spins = 0;
+      while (ld_acquire(&bar[1]) == gen) {
+        if (ld_acquire(status) != 0) {
+          ok = 0;
+          break;
+        }
+        if (++spins > kBarrierSpins) {
+          latch(status, ULA_ERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(128);
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+template <typename Op>
+__device__ __forceinline__ uint32_t block_reduce(uint32_t v, Op op, uint32_t ident) {
+  __shared__ uint32_t ws[kLruThreads / 32];
+  __shared__ uint32_t res;
+#pragma unroll
+  for (int d = 16; d; d >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, d));
+  if (lane_id() == 0) ws[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    uint32_t x = threadIdx.x < kLruThreads / 32 ? ws[threadIdx.x] : ident;
+#pragma unroll
+    for (int d = 16; d; d >>= 1) x = op(x, __shfl_xor_sync(0xffffffffu, x, d));
+    if (threadIdx.x == 0) res = x;
+  }
+  __syncthreads();
+  const uint32_t r = res;
+  __syncthreads();
+  return r;
+}
+
+struct OpMin {
+  __device__ uint32_t operator()(uint32_t a, uint32_t b) const { return a < b ? a : b; }
+};
+struct OpMax {
+  __device__ uint32_t operator()(uint32_t a, uint32_t b) const { return a > b ? a : b; }
+};
+struct OpAdd {
+  __device__ uint32_t operator()(uint32_t a, uint32_t b) const { return a + b; }
+};
+
+// Four consecutive stamps [i, i+4) (i a multiple of 4); those at or past `end` read
+// as kNone (never a candidate).
+__device__ __forceinline__ uint4 load4(const uint32_t *stamp, uint32_t i, uint32_t end) {
+  if (i + 4 <= end) return __ldcg(reinterpret_cast<const uint4 *>(stamp + i));
+  uint4 v = make_uint4(kNone, kNone, kNone, kNone);
+  if (i < end) v.x = __ldcg(stamp + i);
+  if (i + 1 < end) v.y = __ldcg(stamp + i + 1);
+  if (i + 2 < end) v.z = __ldcg(stamp + i + 2);
+  return v;
+}
+
+// (512 threads at <= 40 registers: it fits on an SM beside the gathers.)
+__global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
+  __shared__ uint32_t s_hist[kLruBins];
+  __shared__ uint32_t s_wcnt[kLruThreads / 32][kSortBins];
+  __shared__ uint32_t s_off[kSortBins];
+  __shared__ uint32_t s_pick[2];
+  if (ld_acquire(p.status) != 0) return;
+  const GroupDev &g = p.grp;
+  const uint32_t M = __ldcg(&g.cnt->M), F = __ldcg(&g.cnt->F);
+  if (M <= F) return;  // no occupied slot is needed
+  const uint32_t Q = M - F, r = p.round, S = p.geo.S;
+  const uint32_t G = gridDim.x, b = blockIdx.x, t = threadIdx.x;
+  const uint32_t tid = b * kLruThreads + t, nthr = G * kLruThreads;
+  const uint32_t *stamp = g.stamp;
+  const uint32_t S4 = (S + 3) / 4;  // groups of four stamps
+  uint32_t *victims = g.victims;
+  LruScratch sc = p.sc;
+
+  // ---- 1. oldest / newest candidate timestamp and the candidates' count.
+  // A candidate is an occupied slot not accessed in this round (stamp < r; a
+  // free slot's stamp is kNone).
+  uint32_t lo = kNone, hi = 0, cnt = 0;
+  for (uint32_t q = tid; q < S4; q += nthr) {
+    const uint4 v = load4(stamp, 4 * q, S);
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (x[j] < r) {
+        lo = min(lo, x[j]);
+        hi = max(hi, x[j]);
+        ++cnt;
+      }
+  }
+  lo = block_reduce(lo, OpMin(), kNone);
+  hi = block_reduce(hi, OpMax(), 0u);
+  cnt = block_reduce(cnt, OpAdd(), 0u);
+  if (t == 0) sc.blk[b] = make_uint4(lo, hi, cnt, 0);
+  for (uint32_t i = tid; i < kLruSelectPasses * kLruBins; i += nthr) sc.hist[i] = 0;
+  if (!grid_sync(sc.bar, p.status)) return;
+  lo = kNone;
+  hi = 0;
+  cnt = 0;
+  for (uint32_t j = t; j < G; j += kLruThreads) {
+    const uint4 v = __ldcg(&sc.blk[j]);
+    lo = min(lo, v.x);
+    hi = max(hi, v.y);
+    cnt += v.z;
+  }
+  lo = block_reduce(lo, OpMin(), kNone);
+  hi = block_reduce(hi, OpMax(), 0u);
+  cnt = block_reduce(cnt, OpAdd(), 0u);
+  if (cnt < Q) {  // the capacity check rules this out (same values in every block)
+    if (b == 0 && t == 0) latch(p.status, ULA_ERR_INTERNAL);
+    return;
+  }
+
+  // ---- 2. radix select: the Q-th smallest key, digit by digit from the top
+  const uint32_t span = hi - lo;
+  const int nbits = span ? 32 - __clz(span) : 0;
+  uint32_t prefix = 0, rem = Q;  // rem: how many still to take at or above the prefix
+  int done = 0;
+  for (int pass = 0; done < nbits; ++pass) {
+    const int width = min(kLruDigit, nbits - done);
+    const int shift = nbits - done - width;
+    const uint32_t nb = 1u << width, mask = nb - 1;
+    for (uint32_t i = t; i < nb; i += kLruThreads) s_hist[i] = 0;
+    __syncthreads();
+    for (uint32_t q = tid; q < S4; q += nthr) {
+      const uint4 v = load4(stamp, 4 * q, S);
+      const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (x[j] < r) {
+          const uint32_t key = x[j] - lo;
+          if (((unsigned long long)key >> (shift + width)) == prefix)
+            atomicAdd(&s_hist[(key >> shift) & mask], 1u);
+        }
+    }
+    __syncthreads();
+    uint32_t *gh = sc.hist + (size_t)pass * kLruBins;
+    for (uint32_t i = t; i < nb; i += kLruThreads)
+      if (s_hist[i]) atomicAdd(&gh[i], s_hist[i]);
+    if (!grid_sync(sc.bar, p.status)) return;
+    // every block finds the same digit: the first whose running count reaches rem
+    uint32_t c4[4], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t bin = 4 * t + j;
+      c4[j] = bin < nb ? __ldcg(&gh[bin]) : 0u;
+      sum += c4[j];
+    }
+    uint32_t tot;
+    const uint32_t excl = block_incl_scan<kLruThreads>(sum, &tot) - sum;
+    if (tot < rem) {
+      if (b == 0 && t == 0) latch(p.status, ULA_ERR_INTERNAL);
+      return;
+    }
+    if (excl < rem && rem <= excl + sum) {
+      uint32_t acc = excl;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (acc + c4[j] >= rem) {
+          s_pick[0] = 4 * t + j;
+          s_pick[1] = acc;
+          break;
+        }
+        acc += c4[j];
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << width) | s_pick[0];
+    rem -= s_pick[1];
+    done += width;
+    __syncthreads();
+  }
+  const uint32_t T = lo + prefix;  // threshold timestamp
+  const uint32_t need = rem;       // slots stamped T that are taken, lowest first
+
+  // ---- 3. stable compaction in slot order: stamp < T, or stamp == T among the
+  // first `need` such slots.  Block b owns slots [s0, s1), four per thread per chunk.
+  const uint32_t per = (((S + G - 1) / G) + 3) & ~3u;
+  const uint32_t s0 = min(S, b * per), s1 = min(S, s0 + per);
+  uint32_t n_lt = 0, n_eq = 0;
+  for (uint32_t base = s0; base < s1; base += 4 * kLruThreads) {
+    const uint4 v = load4(stamp, base + 4 * t, s1);
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      n_lt += x[j] < T;
+      n_eq += x[j] == T;
+    }
+  }
+  n_lt = block_reduce(n_lt, OpAdd(), 0u);
+  n_eq = block_reduce(n_eq, OpAdd(), 0u);
+  if (t == 0) sc.blk[G + b] = make_uint4(n_lt, n_eq, 0, 0);  // (phase 1 used blk[0, G))
+  if (!grid_sync(sc.bar, p.status)) return;
+  uint32_t run_lt = 0, run_eq = 0;  // slots below / at the threshold before this block
+  for (uint32_t j = t; j < b; j += kLruThreads) {
+    const uint4 v = __ldcg(&sc.blk[G + j]);
+    run_lt += v.x;
+    run_eq += v.y;
+  }
+  run_lt = block_reduce(run_lt, OpAdd(), 0u);
+  run_eq = block_reduce(run_eq, OpAdd(), 0u);
+  for (uint32_t base = s0; base < s1; base += 4 * kLruThreads) {
+    const uint32_t i = base + 4 * t;
+    const uint4 v = load4(stamp, i, s1);
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+    uint32_t mine = 0;  // (below << 16) | at, this thread's four slots
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mine += ((x[j] < T) << 16) | (x[j] == T);
+    uint32_t tot;
+    uint32_t before = block_incl_scan<kLruThreads>(mine, &tot) - mine;
+    uint32_t lt_before = run_lt + (before >> 16), eq_before = run_eq + (before & 0xffffu);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool is_lt = x[j] < T, is_eq = x[j] == T;
+      if (is_lt || (is_eq && eq_before < need)) {
+        const uint32_t pos = lt_before + min(eq_before, need);
+        if (pos < Q) sc.list[0][pos] = make_uint2(x[j] - lo, i + j);
+        else latch(p.status, ULA_ERR_INTERNAL);
+      }
+      lt_before += is_lt;
+      eq_before += is_eq;
+    }
+    run_lt += tot >> 16;
+    run_eq += tot & 0xffffu;
+  }
+  if (!grid_sync(sc.bar, p.status)) return;
+
+  // ---- 4. order the chosen slots by (timestamp, slot): the list is in slot
+  // order, so a stable sort on the key is enough
+  const uint32_t kmax = T - lo;
+  const int sbits = kmax ? 32 - __clz(kmax) : 0;
+  const int spasses = (sbits + 7) / 8;
+  if (spasses == 0) {  // one timestamp: slot order is the order
+    for (uint32_t i = tid; i < Q; i += nthr) victims[F + i] = __ldcg(&sc.list[0][i]).y;
+    return;
+  }
+  const uint32_t chunk = (Q + G - 1) / G;
+  const uint32_t c0 = min(Q, b * chunk), c1 = min(Q, c0 + chunk);
+  const uint32_t warp = t >> 5, lane = lane_id();
+  uint2 *src = sc.list[0], *dst = sc.list[1];
+  for (int ps = 0; ps < spasses; ++ps) {
+    const int shift = 8 * ps;
+    const bool last = ps == spasses - 1;
+    // (a) this block's digit counts, stored digit-major: table[d][b]
+    for (uint32_t i = t; i < kSortBins; i += kLruThreads) s_hist[i] = 0;
+    __syncthreads();
+    for (uint32_t i = c0 + t; i < c1; i += kLruThreads)
+      atomicAdd(&s_hist[(__ldcg(&src[i]).x >> shift) & 0xffu], 1u);
+    __syncthreads();
+    for (uint32_t d = t; d < kSortBins; d += kLruThreads) sc.table[(size_t)d * G + b] = s_hist[d];
+    if (!grid_sync(sc.bar, p.status)) return;
+    // (b) per digit (blocks take digits in turn): exclusive prefix over blocks in
+    // place; the digit's total goes to table[256 * G + d]
+    for (uint32_t d = b; d < kSortBins; d += G) {
+      uint32_t *col = sc.table + (size_t)d * G;
+      uint32_t run = 0;
+      for (uint32_t j0 = 0; j0 < G; j0 += kLruThreads) {
+        const uint32_t j = j0 + t;
+        const uint32_t v = j < G ? __ldcg(&col[j]) : 0u;
+        uint32_t tot;
+        const uint32_t inc = block_incl_scan<kLruThreads>(v, &tot);
+        if (j < G) col[j] = run + inc - v;
+        run += tot;
+      }
+      if (t == 0) sc.table[(size_t)kSortBins * G + d] = run;
+    }
+    if (!grid_sync(sc.bar, p.status)) return;
+    // (c) this block's start for each digit
+    {
+      const uint32_t v = t < kSortBins ? __ldcg(&sc.table[(size_t)kSortBins * G + t]) : 0u;
+      uint32_t tot;
+      const uint32_t inc = block_incl_scan<kLruThreads>(v, &tot);
+      if (t < kSortBins) s_off[t] = inc - v + __ldcg(&sc.table[(size_t)t * G + b]);
+    }
+    __syncthreads();
+    // (d) stable scatter, a tile of kLruThreads elements at a time
+    for (uint32_t base = c0; base < c1; base += kLruThreads) {
+      const uint32_t i = base + t;
+      const bool valid = i < c1;
+      uint2 e = make_uint2(0, 0);
+      uint32_t d = kSortBins;  // invalid lanes form their own group
+      if (valid) {
+        e = __ldcg(&src[i]);
+        d = (e.x >> shift) & 0xffu;
+      }
+      for (uint32_t k = t; k < (kLruThreads / 32) * kSortBins; k += kLruThreads)
+        (&s_wcnt[0][0])[k] = 0;
+      __syncthreads();
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      const uint32_t lrank = __popc(peers & ((1u << lane) - 1u));
+      if (valid && lrank == 0) s_wcnt[warp][d] = __popc(peers);
+      __syncthreads();
+      if (valid) {
+        uint32_t rank = s_off[d] + lrank;
+        for (uint32_t w = 0; w < warp; ++w) rank += s_wcnt[w][d];
+        if (rank >= Q) latch(p.status, ULA_ERR_INTERNAL);
+        else if (last) victims[F + rank] = e.y;
+        else dst[rank] = e;
+      }
+      __syncthreads();
+      if (t < kSortBins) {
+        uint32_t add = 0;
+        for (uint32_t w = 0; w < kLruThreads / 32; ++w) add += s_wcnt[w][t];
+        s_off[t] += add;
+      }
+      __syncthreads();
+    }
+    if (last) break;
+    if (!grid_sync(sc.bar, p.status)) return;
+    uint2 *tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+}
+
 // ------------------------------------------------------------ alloc / free
 
 // Alloc, per group (one block each): walk the free class for n slots, then the
@@ -758,7 +1142,7 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
 __global__ void __launch_bounds__(kScanThreads) k_alloc_select(EmitParams p) {
   if (block_skips(p.status)) return;
   const GroupDev g = p.groups[p.group0 + blockIdx.x];
-  select_walk<kScanThreads>(g, p.geo, p.order, p.quota, false, p.status);
+  select_walk<kScanThreads>(g, p.geo, p.order, p.quota, p.quota, false, p.status);
 }
 
 // Alloc: address i of the range goes to the i-th selected free GPU slot (the
@@ -793,7 +1177,7 @@ __global__ void __launch_bounds__(256) k_alloc_place(AllocParams p) {
         g.owner[slot] = a;
         g.stamp[slot] = round;
         bm_clear(class_bitmap(g, geo, geo.B + 1), slot);
-        bm_set(class_bitmap(g, geo, cur), slot);
+        bm_set(class_bitmap(g, geo, access_class(geo, cur)), slot);
       } else {
         g.map[a] = kHostBit | slot;
       }
@@ -828,7 +1212,7 @@ __global__ void k_free(FreeParams p) {
       latch(p.status, ULA_ERR_INTERNAL);
       return;
     }
-    const uint32_t c = class_of(g.stamp[m], p.round[gi], geo.B);
+    const uint32_t c = slot_class(geo, g.stamp[m], p.round[gi]);
     if (c == geo.B + 1) {
       latch(p.status, ULA_ERR_INTERNAL);
       return;
@@ -866,9 +1250,9 @@ cudaError_t launch_rotate_emit(const StepParams &p, cudaStream_t s) {
   StepParams q = p;
   q.emit_blocks = div_up(p.E, kEntryThreads);
   const uint32_t words = p.geo.gd.n0 > p.geo.gd.n1 ? p.geo.gd.n0 : p.geo.gd.n1;
-  uint32_t rot = div_up(words, kEntryThreads * 4);
-  rot = rot ? rot : 1;
-  k_rotate_emit<<<q.emit_blocks + rot, kEntryThreads, 0, s>>>(q);
+  uint32_t rot = p.geo.exact ? 0u : div_up(words, kEntryThreads * 4);
+  const uint32_t grid = q.emit_blocks + rot;
+  k_rotate_emit<<<grid ? grid : 1, kEntryThreads, 0, s>>>(q);
   return cudaGetLastError();
 }
 
@@ -899,6 +1283,17 @@ cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
   k_move<<<blocks, 256, 0, s>>>(p);
   k_commit<<<blocks, 256, 0, s>>>(p);  // grid-stride over the victims
   return cudaGetLastError();
+}
+
+cudaError_t lru_resident_blocks(int *per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, k_lru_select, kLruThreads, 0);
+}
+
+cudaError_t launch_lru_select(const LruParams &p, int blocks, cudaStream_t s) {
+  LruParams q = p;
+  void *args[] = {&q};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(k_lru_select), dim3(blocks),
+                                     dim3(kLruThreads), args, 0, s);
 }
 
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s) {

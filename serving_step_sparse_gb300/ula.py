@@ -16,6 +16,7 @@ MAX_GROUPS = 64
 MAX_BUCKETS = 64
 ADDR_PAD = 0xFFFFFFFF
 FLAG_BYPASS_OVERFLOW = 1
+FLAG_EXACT_LRU = 2
 MAP_UNALLOCATED = 0xFFFFFFFF
 MAP_HOST = 0x80000000
 STAMP_FREE = 0xFFFFFFFF

@@ -21,7 +21,8 @@ class GpuRun:
         self.cache = UlaCache(row_bytes=w.row_bytes, layers_per_group=[L] * G,
                               gpu_slots=w.gpu_slots, host_slots=w.host_slots,
                               ring_buckets=w.ring_buckets, max_logical=w.max_logical,
-                              max_entries=w.entries_per_step, bypass_overflow=w.bypass)
+                              max_entries=w.entries_per_step, bypass_overflow=w.bypass,
+                              exact_lru=w.exact_lru)
         self.cap = out_cap if out_cap is not None else w.entries_per_step
         self.outs = [self.cache.out_buffer(g, self.cap) for g in range(G)]
         E = w.entries_per_step
@@ -103,7 +104,8 @@ def gpu_state_in_oracle_terms(st: dict, w) -> dict:
     hosted = np.nonzero(tier == TIER_HOST)[0]
     host_owner[slot[hosted]] = hosted
     return {"tier": tier, "slot": slot, "cls": cls, "owner": st["owner"].copy(),
-            "host_free": host_free, "host_owner": host_owner, "cur": st["cur"]}
+            "host_free": host_free, "host_owner": host_owner, "cur": st["cur"],
+            "stamp": st["stamp"].copy(), "round": st["round"]}
 
 
 def check_gpu_internal(st: dict, w):
@@ -132,8 +134,11 @@ def check_gpu_internal(st: dict, w):
         assert np.array_equal(st["host_seg_count"][:len(segs)], segs), "host segment counts"
     r = st["round"]
     stamp = st["stamp"]
-    exp = np.where(stamp == ula.STAMP_FREE, B + 1,
-                   np.where((np.uint32(r) - stamp).astype(np.uint32) >= B, B, stamp % B))
+    if w.exact_lru:  # one class of occupied slots, no ring
+        exp = np.where(stamp == ula.STAMP_FREE, B + 1, B)
+    else:
+        exp = np.where(stamp == ula.STAMP_FREE, B + 1,
+                       np.where((np.uint32(r) - stamp).astype(np.uint32) >= B, B, stamp % B))
     bits = np.stack([unpack_bits(st["class_bits"][c], S) for c in range(B + 2)])
     assert np.array_equal(bits.argmax(axis=0), exp), "stamps agree with class bitmaps"
     assert st["free_gpu"] == int(bits[B + 1].sum())
@@ -141,8 +146,12 @@ def check_gpu_internal(st: dict, w):
         assert st["free_host"] == int(unpack_bits(st["host_free_bits"], H).sum())
 
 
-def compare_states(gpu_o: dict, orc: dict, where: str):
-    for k in ("tier", "slot", "cls", "owner", "host_free", "host_owner"):
+def compare_states(gpu_o: dict, orc: dict, where: str, stamps=None):
+    """stamps: the oracle's (timestamps, rounds) of the group, compared when given."""
+    if stamps is not None:
+        orc = dict(orc, stamp=stamps[0])
+        assert gpu_o["round"] == stamps[1], where
+    for k in ("tier", "slot", "cls", "owner", "host_free", "host_owner") + (("stamp",) if stamps is not None else ()):
         a, b = gpu_o[k], orc[k]
         if not np.array_equal(a, b):
             idx = np.nonzero(a != b)[0][:8]

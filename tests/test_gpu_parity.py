@@ -30,7 +30,7 @@ def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2
     try:
         for g in range(w.n_groups):  # initial placement
             compare_states(gpu_state_in_oracle_terms(gpu.cache.export(g), w), orc.o.export(g),
-                           f"initial g{g}")
+                           f"initial g{g}", orc.o.stamps(g))
         for t in range(steps):
             sel, ev = gpu.trace.step()
             gpu.run_groups(sel)
@@ -59,7 +59,7 @@ def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2
                     check_gpu_internal(st, w)
                     go = gpu_state_in_oracle_terms(st, w)
                     oo = orc.o.export(g)
-                    compare_states(go, oo, where)
+                    compare_states(go, oo, where, orc.o.stamps(g))
                     v, vc, wb = orc.o.last_decisions(g)
                     assert st["M"] == len(v) and st["writebacks"] == len(wb), where
                     assert np.array_equal(st["victims"][:len(v)], v), f"{where}: victims"
@@ -124,12 +124,14 @@ def test_everything_fits_on_gpu_no_host_pool():
     assert stats["misses"] == 0 and stats["writebacks"] == 0
 
 
-def _direct(S=64, H=256, B=3, layers=(1, 3), W=16, max_logical=512, max_entries=64):
+def _direct(S=64, H=256, B=3, layers=(1, 3), W=16, max_logical=512, max_entries=64,
+            exact=False):
     from serving_step_sparse_gb300.cache import UlaCache
     from oracle import Oracle
     c = UlaCache(row_bytes=W, layers_per_group=list(layers), gpu_slots=S, host_slots=H,
-                 ring_buckets=B, max_logical=max_logical, max_entries=max_entries)
-    o = Oracle(W, list(layers), S, H, B, max_logical)
+                 ring_buckets=B, max_logical=max_logical, max_entries=max_entries,
+                 exact_lru=exact)
+    o = Oracle(W, list(layers), S, H, B, max_logical, exact_lru=exact)
     return c, o
 
 
@@ -191,13 +193,82 @@ def test_mixed_layers_duplicates_across_requests_and_empty_steps():
         c.close()
 
 
+# ----------------------------------------------------------------- exact LRU
+
+@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3", "cfg4", "cfg4_literal"])
+def test_exact_lru_parity_small(name):
+    w = small(name).replace(exact_lru=True)
+    stats = run_parity(w, w.steps)
+    assert stats["misses"] > 0 and stats["victims_cold"] > 0 and stats["victims_ring"] == 0
+
+
+@pytest.mark.parametrize("name,steps", [("cfg2", 8), ("cfg3", 8), ("cfg4_literal", 4)])
+def test_exact_lru_full_size_sampled(name, steps):
+    w = WORKLOADS[name].replace(exact_lru=True)
+    stats = run_parity(w, steps, mode="id", state_every=1, out_every=10**9, sample_rows=4096)
+    assert stats["steps"] == steps * w.n_groups
+
+
+def test_exact_lru_wide_timestamp_spread():
+    """Timestamps thousands of rounds apart: a two-digit radix select and a two-pass
+    sort of the chosen slots (their keys span more than 256 rounds)."""
+    from tests.gpu_harness import gpu_state_in_oracle_terms
+    layers, W, S, H, B = (1,), 16, 64, 512, 8
+    c, o = _direct(S=S, H=H, B=B, layers=layers, W=W, max_logical=1024, max_entries=64,
+                   exact=True)
+    try:
+        n = 400
+        rows = _rows(layers, 0, n, W)
+        assert c.alloc(n, torch.from_numpy(rows).pin_memory()) == 0 and o.alloc(n, rows) == 0
+        c.sync()
+        hot = np.arange(0, 16, dtype=np.uint32)           # touched every round
+        warm = np.arange(16, 40, dtype=np.uint32)         # one touched every 120 rounds
+        cold = np.arange(64, n, dtype=np.uint32)          # on the host, pulled in bursts
+        rng = np.random.default_rng(5)
+        rounds = 3200
+        bursts = 0
+        wide = []  # (candidate timestamp span, chosen victims' timestamp span) per burst
+        for step in range(rounds):
+            sel = [hot]
+            if step % 120 == 0:
+                sel.append(warm[(step // 120) % len(warm):][:1])
+            if step in (1500, 2600, 3100, 3199):
+                sel.append(rng.choice(cold, 20, replace=False).astype(np.uint32))
+                bursts += 1
+            flat = np.concatenate(sel)
+            if step in (1500, 2600, 3100, 3199) or step % 400 == 0:
+                before, _ = o.stamps(0)
+                _step_both(c, o, 0, flat.reshape(1, 1, -1))
+                go = gpu_state_in_oracle_terms(c.export(0), _W(S, H, B))
+                compare_states(go, o.export(0), f"round {step}", o.stamps(0))
+                v, vc, wb = o.last_decisions(0)
+                st = c.export(0)
+                assert np.array_equal(st["victims"][:len(v)], v), f"round {step}: victims"
+                if len(v):
+                    occ = before[before != 0xFFFFFFFF]
+                    wide.append((int(occ.max() - occ.min()),
+                                 int(before[v].max()) - int(before[v].min())))
+            else:  # quick rounds: GPU and oracle step, outputs not compared
+                sd = torch.from_numpy(flat.view(np.int32).copy()).cuda()
+                out = c.out_buffer(0, flat.size)
+                er = torch.empty(flat.size, dtype=torch.int32, device="cuda")
+                ro = torch.empty(2, dtype=torch.int32, device="cuda")
+                c.step_group(0, sd.view(1, 1, -1), out, er, ro)
+                o.step_group(0, flat.reshape(1, 1, -1))
+        assert bursts == 4 and o.stamps(0)[1] == rounds
+        assert any(a >= 2048 and b >= 256 for a, b in wide), wide
+        c.sync()
+    finally:
+        c.close()
+
+
 def _export_all(c, G, S, H, B):
     from tests.gpu_harness import gpu_state_in_oracle_terms
     return [gpu_state_in_oracle_terms(c.export(g), _W(S, H, B)) for g in range(G)]
 
 
 def _same(a, b):
-    return all(all(np.array_equal(x[k], y[k]) for k in x) for x, y in zip(a, b))
+    return all(all(np.array_equal(x[k], y[k]) for k in x if k in y) for x, y in zip(a, b))
 
 
 @pytest.mark.parametrize("case", ["capacity", "unmapped", "out_cap", "inject"])
