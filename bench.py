@@ -50,6 +50,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--pool-frac", type=float, default=None,
+                    help="GPU pool as a fraction of the history (policy comparisons)")
     ap.add_argument("--requests", type=int, default=None,
                     help="run the workload's recipe with fewer live requests (profiling cases)")
     ap.add_argument("--traffic-case", action="store_true",
@@ -526,6 +528,10 @@ def workload_for(args):
     if args.policy == "exact":
         w = w.replace(exact_lru=True, name=w.name + "_exact",
                       description=w.description + " (exact LRU)")
+    if args.pool_frac is not None:
+        w = w.replace(gpu_frac=args.pool_frac, gpu_slots_explicit=None, host_slots_explicit=None,
+                      name=w.name + f"_pool{args.pool_frac:g}",
+                      description=w.description + f" (GPU pool {args.pool_frac:g} of history)")
     if args.requests is not None and args.requests != w.n_live:
         w = w.replace(n_live=args.requests, name=f"{w.name}_r{args.requests}",
                       description=w.description + f" (recipe with {args.requests} requests)")

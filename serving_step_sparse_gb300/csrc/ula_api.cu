@@ -310,8 +310,13 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
     ULA_CUDA(c->alloc(&c->lru.table, kSortBins * nb + kSortBins));
     ULA_CUDA(c->alloc(&c->lru.list[0], cfg.max_entries));
     ULA_CUDA(c->alloc(&c->lru.list[1], cfg.max_entries));
-    ULA_CUDA(c->alloc(&c->lru.bar, 2));
-    ULA_CUDA(cudaMemsetAsync(c->lru.bar, 0, 2 * sizeof(uint32_t), s));
+    ULA_CUDA(c->alloc(&c->lru.bar, 3));
+    c->lru.per = (uint32_t)((((uint64_t)S + nb - 1) / nb + 3) & ~3ull);
+    ULA_CUDA(c->alloc(&c->lru.rows, (size_t)kLruBins * nb));
+    ULA_CUDA(c->alloc(&c->lru.totals, 2 * kLruBins));
+    ULA_CUDA(cudaMemsetAsync(c->lru.totals, 0, 2 * kLruBins * sizeof(uint32_t), s));
+    ULA_CUDA(c->alloc(&c->lru.blist, (size_t)c->lru.per * nb));
+    ULA_CUDA(cudaMemsetAsync(c->lru.bar, 0, 3 * sizeof(uint32_t), s));
   }
   ULA_CUDA(cudaMemsetAsync(c->tbl, 0, sizeof(unsigned long long) * cfg.max_logical, s));
   ULA_CUDA(cudaMemsetAsync(c->status, 0, sizeof(int), s));
@@ -542,6 +547,18 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   ULA_CUDA(c->phase(ULA_PHASE_ROTATE, s, 1, [&] { return launch_rotate_emit(p, s); }));
   // (3b) hits into the current bucket, entry rows; the victim walk
   ULA_CUDA(c->phase(ULA_PHASE_MARK, s, 1, [&] { return launch_mark_select(p, s); }));
+  if (c->geo.exact) {
+    // (4) exact LRU: the timestamp scan, before the hit gathers are released (its
+    // grid-wide phases run several times slower beside them)
+    LruParams lp{};
+    lp.geo = c->geo;
+    lp.grp = gd;
+    lp.sc = c->lru;
+    lp.round = r;
+    lp.status = c->status;
+    ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
+                      [&] { return launch_lru_select(lp, c->lru_blocks, s); }));
+  }
   const bool gather = out_cap_rows != 0;
   GatherParams gp{};
   gp.geo = c->geo;
@@ -574,17 +591,8 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   ep.order = p.order;
   ep.quota = 0xffffffffu;
   ep.status = c->status;
-  LruParams lp{};
-  lp.geo = c->geo;
-  lp.grp = gd;
-  lp.sc = c->lru;
-  lp.round = r;
-  lp.status = c->status;
-  ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, c->geo.exact ? 2 : 1, [&] {
-    cudaError_t e = launch_select_emit(ep, 1, c->emit_blocks, s);
-    if (e == cudaSuccess && c->geo.exact) e = launch_lru_select(lp, c->lru_blocks, s);
-    return e;
-  }));
+  ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
+                    [&] { return launch_select_emit(ep, 1, c->emit_blocks, s); }));
   // (5) write-back, fill (writing the missed rows' outputs), then map commit
   MoveParams mp{};
   mp.geo = c->geo;

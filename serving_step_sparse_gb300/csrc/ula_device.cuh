@@ -55,6 +55,7 @@ struct GroupCounters {
   uint32_t n_work;     // selection work entries (GPU classes, then host)
   uint32_t n_work_gpu; // of which on GPU-slot classes
   uint32_t done[3];    // "last block" tickets of the multi-block kernels
+  uint32_t lru_lo;     // exact LRU: a lower bound of every occupied slot's stamp
   unsigned long long stat[13];  // ula_stats order
 };
 
@@ -181,7 +182,12 @@ struct LruScratch {
   uint32_t *hist;      // [kLruSelectPasses][kLruBins]
   uint32_t *table;     // [kSortBins][grid] digit counts of a sort pass, then [kSortBins] totals
   uint2 *list[2];      // [max_entries]: (stamp - oldest, slot) of the chosen slots
-  uint32_t *bar;       // [2]: grid barrier arrivals, generation
+  uint32_t *bar;       // [3]: grid barrier arrivals, generation; totals buffer parity
+  // fast path
+  uint32_t *rows;      // [grid][kLruBins]: per-block key counts
+  uint32_t *totals;    // [2][kLruBins]: the pool's key counts (one buffer per launch parity)
+  uint2 *blist;        // [grid][per]: each block's chosen (key, slot), slot order
+  uint32_t per;        // slots per block (a multiple of 4)
 };
 
 struct LruParams {

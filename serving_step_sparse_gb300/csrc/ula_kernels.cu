@@ -792,6 +792,8 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
 //      digits; the last pass writes the victims.
 
 constexpr uint32_t kBarrierSpins = 1u << 22;  // polls of ~128 ns: about half a second
+constexpr int kLruRegChunks = 4;  // chunks of 4 * kLruThreads stamps a block keeps in registers
+constexpr int kLruColLoads = 5;   // per-block counts a lane loads at once (5 * 32 >= 152 blocks)
 
 __device__ __forceinline__ uint32_t ld_acquire(const void *p) {
   uint32_t v;
@@ -826,7 +828,7 @@ __device__ __forceinline__ bool grid_sync(uint32_t *bar, int *status) {
           ok = 0;
           break;
         }
-        __nanosleep(128);
+        if (spins > 256) __nanosleep(128);  // poll tightly at first
       }
     }
     __threadfence();
@@ -877,23 +879,30 @@ __device__ __forceinline__ uint4 load4(const uint32_t *stamp, uint32_t i, uint32
   return v;
 }
 
-// (512 threads at <= 40 registers: it fits on an SM beside the gathers.)
-__global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
-  __shared__ uint32_t s_hist[kLruBins];
-  __shared__ uint32_t s_wcnt[kLruThreads / 32][kSortBins];
-  __shared__ uint32_t s_off[kSortBins];
-  __shared__ uint32_t s_pick[2];
-  if (ld_acquire(p.status) != 0) return;
+// Shared memory of the exact-LRU kernel.
+struct LruSmem {
+  uint32_t hist[kLruBins];
+  uint32_t wcnt[kLruThreads / 32][kSortBins];
+  uint32_t off[kSortBins];
+  uint32_t pick[2];
+};
+
+// The general path: the exact oldest timestamp first (a scan), then a radix select
+// over all 32 bits of key = stamp - oldest, a stable compaction and a stable LSD
+// sort.  Returns the threshold timestamp T, or kNone when the grid gives up.
+__device__ uint32_t lru_general(const LruParams &p, LruSmem &sm, uint32_t Q, uint32_t F) {
+  uint32_t *s_hist = sm.hist;
+  uint32_t(*s_wcnt)[kSortBins] = sm.wcnt;
+  uint32_t *s_off = sm.off;
+  uint32_t *s_pick = sm.pick;
   const GroupDev &g = p.grp;
-  const uint32_t M = __ldcg(&g.cnt->M), F = __ldcg(&g.cnt->F);
-  if (M <= F) return;  // no occupied slot is needed
-  const uint32_t Q = M - F, r = p.round, S = p.geo.S;
+  const uint32_t r = p.round, S = p.geo.S;
   const uint32_t G = gridDim.x, b = blockIdx.x, t = threadIdx.x;
   const uint32_t tid = b * kLruThreads + t, nthr = G * kLruThreads;
   const uint32_t *stamp = g.stamp;
   const uint32_t S4 = (S + 3) / 4;  // groups of four stamps
   uint32_t *victims = g.victims;
-  LruScratch sc = p.sc;
+  const LruScratch &sc = p.sc;
 
   // ---- 1. oldest / newest candidate timestamp and the candidates' count.
   // A candidate is an occupied slot not accessed in this round (stamp < r; a
@@ -915,7 +924,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
   cnt = block_reduce(cnt, OpAdd(), 0u);
   if (t == 0) sc.blk[b] = make_uint4(lo, hi, cnt, 0);
   for (uint32_t i = tid; i < kLruSelectPasses * kLruBins; i += nthr) sc.hist[i] = 0;
-  if (!grid_sync(sc.bar, p.status)) return;
+  if (!grid_sync(sc.bar, p.status)) return kNone;
   lo = kNone;
   hi = 0;
   cnt = 0;
@@ -930,7 +939,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
   cnt = block_reduce(cnt, OpAdd(), 0u);
   if (cnt < Q) {  // the capacity check rules this out (same values in every block)
     if (b == 0 && t == 0) latch(p.status, ULA_ERR_INTERNAL);
-    return;
+    return kNone;
   }
 
   // ---- 2. radix select: the Q-th smallest key, digit by digit from the top
@@ -959,7 +968,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
     uint32_t *gh = sc.hist + (size_t)pass * kLruBins;
     for (uint32_t i = t; i < nb; i += kLruThreads)
       if (s_hist[i]) atomicAdd(&gh[i], s_hist[i]);
-    if (!grid_sync(sc.bar, p.status)) return;
+    if (!grid_sync(sc.bar, p.status)) return kNone;
     // every block finds the same digit: the first whose running count reaches rem
     uint32_t c4[4], sum = 0;
 #pragma unroll
@@ -972,7 +981,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
     const uint32_t excl = block_incl_scan<kLruThreads>(sum, &tot) - sum;
     if (tot < rem) {
       if (b == 0 && t == 0) latch(p.status, ULA_ERR_INTERNAL);
-      return;
+      return kNone;
     }
     if (excl < rem && rem <= excl + sum) {
       uint32_t acc = excl;
@@ -1012,7 +1021,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
   n_lt = block_reduce(n_lt, OpAdd(), 0u);
   n_eq = block_reduce(n_eq, OpAdd(), 0u);
   if (t == 0) sc.blk[G + b] = make_uint4(n_lt, n_eq, 0, 0);  // (phase 1 used blk[0, G))
-  if (!grid_sync(sc.bar, p.status)) return;
+  if (!grid_sync(sc.bar, p.status)) return kNone;
   uint32_t run_lt = 0, run_eq = 0;  // slots below / at the threshold before this block
   for (uint32_t j = t; j < b; j += kLruThreads) {
     const uint4 v = __ldcg(&sc.blk[G + j]);
@@ -1045,7 +1054,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
     run_lt += tot >> 16;
     run_eq += tot & 0xffffu;
   }
-  if (!grid_sync(sc.bar, p.status)) return;
+  if (!grid_sync(sc.bar, p.status)) return kNone;
 
   // ---- 4. order the chosen slots by (timestamp, slot): the list is in slot
   // order, so a stable sort on the key is enough
@@ -1054,7 +1063,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
   const int spasses = (sbits + 7) / 8;
   if (spasses == 0) {  // one timestamp: slot order is the order
     for (uint32_t i = tid; i < Q; i += nthr) victims[F + i] = __ldcg(&sc.list[0][i]).y;
-    return;
+    return T;
   }
   const uint32_t chunk = (Q + G - 1) / G;
   const uint32_t c0 = min(Q, b * chunk), c1 = min(Q, c0 + chunk);
@@ -1070,7 +1079,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
       atomicAdd(&s_hist[(__ldcg(&src[i]).x >> shift) & 0xffu], 1u);
     __syncthreads();
     for (uint32_t d = t; d < kSortBins; d += kLruThreads) sc.table[(size_t)d * G + b] = s_hist[d];
-    if (!grid_sync(sc.bar, p.status)) return;
+    if (!grid_sync(sc.bar, p.status)) return kNone;
     // (b) per digit (blocks take digits in turn): exclusive prefix over blocks in
     // place; the digit's total goes to table[256 * G + d]
     for (uint32_t d = b; d < kSortBins; d += G) {
@@ -1086,7 +1095,7 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
       }
       if (t == 0) sc.table[(size_t)kSortBins * G + d] = run;
     }
-    if (!grid_sync(sc.bar, p.status)) return;
+    if (!grid_sync(sc.bar, p.status)) return kNone;
     // (c) this block's start for each digit
     {
       const uint32_t v = t < kSortBins ? __ldcg(&sc.table[(size_t)kSortBins * G + t]) : 0u;
@@ -1128,11 +1137,272 @@ __global__ void __launch_bounds__(kLruThreads, 3) k_lru_select(LruParams p) {
       __syncthreads();
     }
     if (last) break;
-    if (!grid_sync(sc.bar, p.status)) return;
+    if (!grid_sync(sc.bar, p.status)) return kNone;
     uint2 *tmp = src;
     src = dst;
     dst = tmp;
   }
+  return T;
+}
+
+// (512 threads at <= 64 registers: it fits on an SM beside the gathers.)
+//
+// The fast path, taken when the Q oldest candidates are stamped within the
+// window [lo, lo + nb - 2] of nb <= kLruBins rounds, lo being a lower bound of
+// every candidate's stamp kept from the previous scan (the threshold T of a scan
+// bounds the stamps left: every older one was chosen and refilled, and stamps
+// only grow).  One grid-wide barrier:
+//   A. every block histograms key = min(stamp - lo, nb - 1) over its own
+//      contiguous slot range (kept in shared memory), publishes the row and adds
+//      it to the pool's totals;
+//   C. every block: running totals, the first key dT whose running total reaches
+//      Q (T = lo + dT) and how many slots stamped T are taken (need); then, for
+//      keys <= dT, how many slots of each lie in earlier blocks;
+//   D. every block that holds chosen slots lists them in slot order;
+//   E. one warp per block ranks them: rank = (candidates with a smaller key) +
+//      (same key in earlier blocks) + (same key earlier in this block).
+// The totals are accumulated in one of two buffers while the other is cleared
+// for the next launch.  Otherwise the general path (lru_general) runs.
+__global__ void __launch_bounds__(kLruThreads, 2) k_lru_select(LruParams p) {
+  __shared__ LruSmem sm;
+  __shared__ uint32_t s_own[kLruBins];  // this block's histogram
+  if (ld_acquire(p.status) != 0) return;
+  const GroupDev &g = p.grp;
+  const uint32_t M = __ldcg(&g.cnt->M), F = __ldcg(&g.cnt->F);
+  if (M <= F) return;  // no occupied slot is needed
+  const uint32_t Q = M - F, r = p.round, S = p.geo.S;
+  const uint32_t G = gridDim.x, b = blockIdx.x, t = threadIdx.x;
+  const uint32_t lane = lane_id(), warp = t >> 5;
+  const uint32_t *stamp = g.stamp;
+  const LruScratch &sc = p.sc;
+  const uint32_t lo = __ldcg(&g.cnt->lru_lo);
+  const uint32_t par = ld_acquire(&sc.bar[2]) & 1u;
+  uint32_t *totals = sc.totals + par * kLruBins;
+  const uint32_t per = sc.per;
+  const uint32_t s0 = min(S, b * per), s1 = min(S, s0 + per);
+  // keys 0 .. r-1-lo; nb bins, the last one also collecting every older-than-window key
+  const uint32_t span = r - lo;  // >= 1 (lo <= every candidate's stamp < r)
+  uint32_t nb = kLruBins;
+  if (span < kLruBins) {
+    nb = 2;
+    while (nb <= span) nb <<= 1;
+  }
+
+  // ---- A. the block's histogram.  When the block's range fits in kLruRegChunks
+  // chunks (the same for every block), its stamps are loaded once, all at once, and
+  // kept in registers for phase D.
+  const bool in_regs = per <= kLruRegChunks * 4 * kLruThreads;
+  uint4 sv[kLruRegChunks];
+  if (in_regs) {
+#pragma unroll
+    for (int c = 0; c < kLruRegChunks; ++c) sv[c] = load4(stamp, s0 + (c * kLruThreads + t) * 4, s1);
+  }
+  for (uint32_t k = t; k < nb; k += kLruThreads) s_own[k] = 0;
+  __syncthreads();
+  bool bad = false;
+  auto hist4 = [&](const uint4 v) {
+    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool cand = x[j] < r;
+      bad |= cand && x[j] < lo;
+      const uint32_t key = cand ? min(x[j] - lo, nb - 1) : kNone;
+      const uint32_t peers = __match_any_sync(0xffffffffu, key);
+      if (cand && lane == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&s_own[key], __popc(peers));
+    }
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int c = 0; c < kLruRegChunks; ++c) hist4(sv[c]);
+  } else {
+    for (uint32_t base = s0; base < s1; base += 4 * kLruThreads) hist4(load4(stamp, base + 4 * t, s1));
+  }
+  if (bad) latch(p.status, ULA_ERR_INTERNAL);  // a stamp below the bound: the grid gives up
+  __syncthreads();
+  uint32_t *row = sc.rows + (size_t)b * kLruBins;
+  for (uint32_t k = t; k < nb; k += kLruThreads) {
+    const uint32_t v = s_own[k];
+    row[k] = v;
+    if (v) atomicAdd(&totals[k], v);
+  }
+  uint32_t *other = sc.totals + (par ^ 1u) * kLruBins;  // cleared for the next launch
+  for (uint32_t k = b * kLruThreads + t; k < kLruBins; k += G * kLruThreads) other[k] = 0;
+  if (!grid_sync(sc.bar, p.status)) return;
+  if (b == 0 && t == 0) atomicXor(&sc.bar[2], 1u);  // every block has read the parity
+
+  // ---- C. running totals (sm.hist[k]: candidates with a key below k) and the threshold
+  uint32_t c4[4], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t k = 4 * t + j;
+    c4[j] = k < nb ? __ldcg(&totals[k]) : 0u;
+    sum += c4[j];
+  }
+  uint32_t tot;
+  const uint32_t excl = block_incl_scan<kLruThreads>(sum, &tot) - sum;
+  {
+    uint32_t acc = excl;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      sm.hist[4 * t + j] = acc;
+      if (acc < Q && Q <= acc + c4[j]) {
+        sm.pick[0] = 4 * t + j;
+        sm.pick[1] = acc;
+      }
+      acc += c4[j];
+    }
+  }
+  __syncthreads();
+  if (tot < Q) {  // the capacity check rules this out (same in every block)
+    if (b == 0 && t == 0) latch(p.status, ULA_ERR_INTERNAL);
+    return;
+  }
+  uint32_t T;
+  if (sm.hist[nb - 1] < Q) {  // the window holds fewer than Q candidates
+    T = lru_general(p, sm, Q, F);
+  } else {
+    const uint32_t dT = sm.pick[0], need = Q - sm.pick[1];
+    // slots of each key <= dT in earlier blocks (sm.off is too small for many keys:
+    // use the per-warp table's storage, kLruThreads/32 * kSortBins >= kLruBins words)
+    uint32_t *pre = &sm.wcnt[0][0];
+    for (uint32_t k = warp; k <= dT; k += kLruThreads / 32) {
+      uint32_t acc = 0;
+      for (uint32_t j0 = 0; j0 < b; j0 += 32 * kLruColLoads) {
+        uint32_t v[kLruColLoads];
+#pragma unroll
+        for (int u = 0; u < kLruColLoads; ++u) {
+          const uint32_t j = j0 + 32 * u + lane;
+          v[u] = j < b ? __ldcg(&sc.rows[(size_t)j * kLruBins + k]) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kLruColLoads; ++u) acc += v[u];
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) pre[k] = acc;
+    }
+    __syncthreads();
+    const uint32_t eq_prefix = pre[dT];
+    const uint32_t cap = need > eq_prefix ? need - eq_prefix : 0u;
+    uint32_t mine_lt = 0;
+    for (uint32_t k = t; k < dT; k += kLruThreads) mine_lt += s_own[k];
+    const uint32_t n_b = block_reduce(mine_lt, OpAdd(), 0u) + min(s_own[dT], cap);
+
+    if (n_b) {
+      // ---- D. the block's chosen slots in slot order: key < dT, or key == dT
+      // within the first `need` of the pool (eq_prefix of them lie in earlier blocks)
+      uint2 *blist = sc.blist + (size_t)b * per;
+      auto take = [&](const uint32_t i, const uint32_t *key, uint32_t lt_b, uint32_t eq_b) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const bool is_lt = key[j] < dT, is_eq = key[j] == dT;
+          if (is_lt || (is_eq && eq_b < cap)) {
+            const uint32_t pos = lt_b + min(eq_b, cap);
+            if (pos < per) blist[pos] = make_uint2(key[j], i + j);
+            else latch(p.status, ULA_ERR_INTERNAL);
+          }
+          lt_b += is_lt;
+          eq_b += is_eq;
+        }
+      };
+      auto keys4 = [&](const uint4 v, uint32_t *key) {
+        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+        uint32_t m = 0;  // (below << 16) | at
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          key[j] = x[j] < r ? min(x[j] - lo, nb - 1) : kNone;
+          m += ((uint32_t)(key[j] < dT) << 16) | (uint32_t)(key[j] == dT);
+        }
+        return m;
+      };
+      if (in_regs) {
+        // Piece (c, w) = the 128 slots warp w holds of chunk c; pieces in slot order
+        // are c-major.  Warp-level counts, one table of piece totals, one barrier.
+        uint32_t *ptot = sm.off;  // [kLruRegChunks * 16] packed piece totals
+        uint32_t key[kLruRegChunks][4], incl[kLruRegChunks], mine[kLruRegChunks];
+#pragma unroll
+        for (int c = 0; c < kLruRegChunks; ++c) {
+          mine[c] = keys4(sv[c], key[c]);
+          incl[c] = warp_incl_scan(mine[c]);
+          if (lane == 31) ptot[c * (kLruThreads / 32) + warp] = incl[c];
+        }
+        __syncthreads();
+        // exclusive prefix of all pieces: lane l holds pieces 2l and 2l + 1
+        const uint32_t a0 = ptot[2 * lane], a1 = ptot[2 * lane + 1];
+        const uint32_t pin = warp_incl_scan(a0 + a1);
+#pragma unroll
+        for (int c = 0; c < kLruRegChunks; ++c) {
+          const uint32_t pc = c * (kLruThreads / 32) + warp;  // this warp's piece
+          const uint32_t owner = __shfl_sync(0xffffffffu, pin - a0 - a1, pc >> 1);
+          const uint32_t a_even = __shfl_sync(0xffffffffu, a0, pc >> 1);
+          const uint32_t pbase = owner + ((pc & 1u) ? a_even : 0u);
+          const uint32_t before = pbase + incl[c] - mine[c];
+          take(s0 + (c * kLruThreads + t) * 4, key[c], before >> 16, before & 0xffffu);
+        }
+      } else {
+        uint32_t run_lt = 0, run_eq = 0;
+        for (uint32_t base = s0; base < s1; base += 4 * kLruThreads) {
+          uint32_t key[4];
+          const uint32_t m = keys4(load4(stamp, base + 4 * t, s1), key);
+          uint32_t ctot;
+          const uint32_t before = block_incl_scan<kLruThreads>(m, &ctot) - m;
+          take(base + 4 * t, key, run_lt + (before >> 16), run_eq + (before & 0xffffu));
+          run_lt += ctot >> 16;
+          run_eq += ctot & 0xffffu;
+        }
+      }
+
+      // ---- E. ranks; sm.hist[k] becomes the first rank of key k in this block
+      for (uint32_t k = t; k <= dT; k += kLruThreads) sm.hist[k] += pre[k];
+      __syncthreads();
+      if (dT < kSortBins) {  // tiles of kLruThreads list entries, per-warp key counts
+        uint32_t(*wc)[kSortBins] = sm.wcnt;  // (pre is no longer needed)
+        for (uint32_t i0 = 0; i0 < n_b; i0 += kLruThreads) {
+          const uint32_t i = i0 + t;
+          const bool valid = i < n_b;
+          const uint2 e = valid ? blist[i] : make_uint2(kSortBins, 0u);
+          for (uint32_t k = t; k < (kLruThreads / 32) * (dT + 1); k += kLruThreads)
+            wc[k / (dT + 1)][k % (dT + 1)] = 0;
+          __syncthreads();
+          const uint32_t peers = __match_any_sync(0xffffffffu, e.x);
+          const uint32_t lrank = __popc(peers & ((1u << lane) - 1u));
+          if (valid && lrank == 0) wc[warp][e.x] = __popc(peers);
+          __syncthreads();
+          if (valid) {
+            uint32_t rank = sm.hist[e.x] + lrank;
+            for (uint32_t w = 0; w < warp; ++w) rank += wc[w][e.x];
+            if (rank < Q) g.victims[F + rank] = e.y;
+            else latch(p.status, ULA_ERR_INTERNAL);
+          }
+          __syncthreads();
+          for (uint32_t k = t; k <= dT; k += kLruThreads) {
+            uint32_t add = 0;
+            for (uint32_t w = 0; w < kLruThreads / 32; ++w) add += wc[w][k];
+            sm.hist[k] += add;
+          }
+          __syncthreads();
+        }
+      } else if (warp == 0) {  // many keys: one warp, in order
+        for (uint32_t i0 = 0; i0 < n_b; i0 += 32) {
+          const uint32_t i = i0 + lane;
+          const bool valid = i < n_b;
+          const uint2 e = valid ? blist[i] : make_uint2(kNone, 0u);
+          const uint32_t peers = __match_any_sync(0xffffffffu, e.x);
+          const uint32_t lrank = __popc(peers & ((1u << lane) - 1u));
+          const uint32_t rank = valid ? sm.hist[e.x] + lrank : 0u;
+          __syncwarp();
+          if (valid && lrank == 0) sm.hist[e.x] += __popc(peers);
+          __syncwarp();
+          if (valid) {
+            if (rank < Q) g.victims[F + rank] = e.y;
+            else latch(p.status, ULA_ERR_INTERNAL);
+          }
+        }
+      }
+    }
+    T = lo + dT;
+  }
+  // the threshold bounds every stamp left for the next scan
+  if (T != kNone && b == 0 && t == 0) g.cnt->lru_lo = T;
 }
 
 // ------------------------------------------------------------ alloc / free

@@ -93,7 +93,7 @@ class Workload:
     def host_slots(self) -> int:
         if self.host_slots_explicit is not None:
             return self.host_slots_explicit
-        return self.max_live_history - self.gpu_slots + self.entries_per_step
+        return max(0, self.max_live_history - self.gpu_slots + self.entries_per_step)
 
     @property
     def max_logical(self) -> int:

@@ -262,6 +262,52 @@ def test_exact_lru_wide_timestamp_spread():
         c.close()
 
 
+def test_exact_lru_general_path_when_the_window_runs_short():
+    """The fast scan bins timestamps within 2,047 rounds of a lower bound kept from the
+    previous scan; when fewer than Q candidates lie in that window (a few slots left
+    untouched for thousands of rounds, the rest recent) the general path runs: an exact
+    oldest-stamp scan, a 32-bit radix select and a stable sort."""
+    from tests.gpu_harness import gpu_state_in_oracle_terms
+    layers, W, S, H, B = (1,), 16, 64, 512, 8
+    c, o = _direct(S=S, H=H, B=B, layers=layers, W=W, max_logical=1024, max_entries=64,
+                   exact=True)
+    try:
+        n = 300
+        rows = _rows(layers, 0, n, W)
+        assert c.alloc(n, torch.from_numpy(rows).pin_memory()) == 0 and o.alloc(n, rows) == 0
+        c.sync()
+        rng = np.random.default_rng(8)
+        bursts = [(2600, 20), (2601, 3), (5000, 40)]
+        for step in range(5001):
+            if step < 2100:
+                flat = np.array([60, 61, 62, 63], dtype=np.uint32)  # resident, always hits
+            else:  # touch 5..63 a few at a time; 0..4 stay at their first stamp
+                flat = np.unique(np.concatenate([[60, 61, 62, 63],
+                                                 rng.choice(np.arange(5, 64), 3, replace=False)]))
+                flat = flat.astype(np.uint32)
+            burst = dict(bursts).get(step)
+            if burst:
+                flat = np.concatenate([flat, rng.choice(np.arange(64, n), burst, replace=False)
+                                       .astype(np.uint32)])
+                flat = np.unique(flat).astype(np.uint32)
+                _step_both(c, o, 0, flat.reshape(1, 1, -1))
+                go = gpu_state_in_oracle_terms(c.export(0), _W(S, H, B))
+                compare_states(go, o.export(0), f"round {step}", o.stamps(0))
+                v, vc, wb = o.last_decisions(0)
+                assert np.array_equal(c.export(0)["victims"][:len(v)], v), f"round {step}"
+            else:
+                sd = torch.from_numpy(flat.view(np.int32).copy()).cuda()
+                out = c.out_buffer(0, flat.size)
+                er = torch.empty(flat.size, dtype=torch.int32, device="cuda")
+                ro = torch.empty(2, dtype=torch.int32, device="cuda")
+                c.step_group(0, sd.view(1, 1, -1), out, er, ro)
+                o.step_group(0, flat.reshape(1, 1, -1))
+        st = c.sync()
+        assert st["victims_cold"] > 0
+    finally:
+        c.close()
+
+
 def _export_all(c, G, S, H, B):
     from tests.gpu_harness import gpu_state_in_oracle_terms
     return [gpu_state_in_oracle_terms(c.export(g), _W(S, H, B)) for g in range(G)]
