@@ -43,7 +43,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="cfg2")
+    ap.add_argument("--workload", default="longdoc")
     ap.add_argument("--policy", choices=["pblru", "exact"], default="pblru",
                     help="replacement policy: PB-LRU, or exact LRU (timestamp scan)")
     ap.add_argument("--profile-steps", type=int, default=60)

@@ -246,8 +246,13 @@ typedef struct ula_debug_state {
 int ula_debug_layout_get(const ula_ctx *ctx, ula_debug_layout *out);
 int ula_debug_export(ula_ctx *ctx, uint32_t group, ula_debug_state *st);
 /* The next ula_step_group latches `code` on the device before it changes anything
- * (host-side fault injection for tests of the error path; no GPU fault). */
+ * (host-side fault injection for tests of the error path; no GPU fault).  With
+ * code ULA_DEBUG_STALL_SCAN_BARRIER instead, in the next step's exact-LRU scan one
+ * block never arrives at the first grid-wide barrier: the other blocks wait out
+ * their bound (about one second), latch ULA_ERR_TIMEOUT and return (a test of the
+ * bounded wait; nothing hangs). */
 int ula_debug_inject(ula_ctx *ctx, int code);
+#define ULA_DEBUG_STALL_SCAN_BARRIER 0x100
 /* Re-run the gather of the hit rows of `group`'s last step for one layer into d_out
  * ([L_g][out_cap_rows][row_bytes], device) on `stream`, changing no state (for timing
  * the gather kernel on its own).  Launches at once: the caller orders it after the

@@ -525,7 +525,8 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.round = r;
   p.cur = cur;
   p.out_cap = out_cap_rows;
-  p.inject = c->inject;
+  const bool stall = c->inject == ULA_DEBUG_STALL_SCAN_BARRIER;
+  p.inject = stall ? 0 : c->inject;
   p.entry_row = d_entry_row;
   p.req_off = d_req_off;
   p.tbl = c->tbl;
@@ -555,6 +556,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
     lp.grp = gd;
     lp.sc = c->lru;
     lp.round = r;
+    lp.stall = stall ? 1 : 0;
     lp.status = c->status;
     ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
                       [&] { return launch_lru_select(lp, c->lru_blocks, s); }));

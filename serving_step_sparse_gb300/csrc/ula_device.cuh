@@ -195,6 +195,7 @@ struct LruParams {
   GroupDev grp;
   LruScratch sc;
   uint32_t round;
+  int stall;             // test hook: block 0 skips the first grid barrier
   int *status;
 };
 

@@ -791,7 +791,7 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
 //   4. stable LSD radix sort of the chosen (key, slot) pairs on the key's 8-bit
 //      digits; the last pass writes the victims.
 
-constexpr uint32_t kBarrierSpins = 1u << 22;  // polls of ~128 ns: about half a second
+constexpr unsigned long long kBarrierNs = 1000000000ull;  // a barrier wait gives up after 1 s
 constexpr int kLruRegChunks = 4;  // chunks of 4 * kLruThreads stamps a block keeps in registers
 constexpr int kLruColLoads = 5;   // per-block counts a lane loads at once (5 * 32 >= 152 blocks)
 
@@ -801,34 +801,43 @@ __device__ __forceinline__ uint32_t ld_acquire(const void *p) {
   return v;
 }
 
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long v;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v));
+  return v;
+}
+
 // Grid-wide barrier of a cooperative launch (all blocks co-resident).  Bounded:
-// a block that polls more than kBarrierSpins times latches ULA_ERR_TIMEOUT; a
-// block that sees an error latched stops waiting.  Returns false (in every
-// thread of the block) when the grid must give up.
-__device__ __forceinline__ bool grid_sync(uint32_t *bar, int *status) {
+// a block that has waited kBarrierNs latches ULA_ERR_TIMEOUT; a block that sees
+// an error latched stops waiting.  Returns false (in every thread of the block)
+// when the grid must give up.  skip (test hook): this block does not arrive.
+__device__ __forceinline__ bool grid_sync(uint32_t *bar, int *status, bool skip = false) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
     const uint32_t gen = ld_acquire(&bar[1]);
     __threadfence();
-    if (atomicAdd(&bar[0], 1u) == gridDim.x - 1) {
+    if (skip) {
+      ok = 0;
+    } else if (atomicAdd(&bar[0], 1u) == gridDim.x - 1) {
       atomicExch(&bar[0], 0u);
       __threadfence();
       atomicAdd(&bar[1], 1u);
     } else {
+      const unsigned long long t0 = global_ns();
       uint32_t spins = 0;
       while (ld_acquire(&bar[1]) == gen) {
         if (ld_acquire(status) != 0) {
           ok = 0;
           break;
         }
-        if (++spins > kBarrierSpins) {
+        if (global_ns() - t0 > kBarrierNs) {
           latch(status, ULA_ERR_TIMEOUT);
           ok = 0;
           break;
         }
-        if (spins > 256) __nanosleep(128);  // poll tightly at first
+        if (++spins > 256) __nanosleep(128);  // poll tightly at first
       }
     }
     __threadfence();
@@ -1227,7 +1236,7 @@ __global__ void __launch_bounds__(kLruThreads, 2) k_lru_select(LruParams p) {
   }
   uint32_t *other = sc.totals + (par ^ 1u) * kLruBins;  // cleared for the next launch
   for (uint32_t k = b * kLruThreads + t; k < kLruBins; k += G * kLruThreads) other[k] = 0;
-  if (!grid_sync(sc.bar, p.status)) return;
+  if (!grid_sync(sc.bar, p.status, p.stall && b == 0)) return;
   if (b == 0 && t == 0) atomicXor(&sc.bar[2], 1u);  // every block has read the parity
 
   // ---- C. running totals (sm.hist[k]: candidates with a key below k) and the threshold

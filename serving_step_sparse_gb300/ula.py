@@ -27,6 +27,7 @@ ERR_CAPACITY = 2
 ERR_UNMAPPED = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
+DEBUG_STALL_SCAN_BARRIER = 0x100  # ula_debug_inject: the next exact-LRU scan waits out its barrier bound
 ERR_POISONED = 6
 ERR_INTERNAL = 7
 

@@ -114,29 +114,29 @@ class Workload:
 
 
 WORKLOADS = {
-    "cfg0": Workload(
-        name="cfg0", seed=0,
+    "tiny_1x4k": Workload(
+        name="tiny_1x4k", seed=0,
         description="1 request x 4,096 ctx, 1 group x 4 layers, top-256, GPU pool 2,048 slots",
         n_live=1, ctx_min=4096, ctx_max=4096, n_groups=1, layers_per_group=4, q=1, k=256,
         window=64, keep=0.85, steps=64, gpu_slots_explicit=2048, host_slots_explicit=4096),
-    "cfg1": Workload(
-        name="cfg1", seed=1,
+    "batch8_32k": Workload(
+        name="batch8_32k", seed=1,
         description="8 requests x 32K ctx, 4 groups x 3 layers, top-2,048, GPU pool 40% of history",
         n_live=8, ctx_min=32768, ctx_max=32768, n_groups=4, layers_per_group=3, q=1, k=2048,
         window=512, keep=0.9, steps=256, gpu_frac=0.4),
-    "cfg2": Workload(
-        name="cfg2", seed=2,
+    "longdoc": Workload(
+        name="longdoc", seed=2,
         description=("long-document summary: 32 requests x 64K-128K ctx (+<=1,024 appended), "
                      "4 groups x 4 layers, top-2,048 x 3 query tokens, GPU pool 30% of history"),
         n_live=32, ctx_min=65536, ctx_max=131072, n_groups=4, layers_per_group=4, q=3, k=2048,
         window=512, keep=0.9, steps=512, append_max=3, append_cap=1024, gpu_frac=0.3),
-    "cfg3": Workload(
-        name="cfg3", seed=3,
+    "low_evict": Workload(
+        name="low_evict", seed=3,
         description="low eviction: 16 requests x 64K ctx, 4 groups x 4 layers, top-2,048, GPU pool 95%",
         n_live=16, ctx_min=65536, ctx_max=65536, n_groups=4, layers_per_group=4, q=1, k=2048,
         window=512, keep=0.95, steps=512, gpu_frac=0.95),
-    "cfg4": Workload(
-        name="cfg4", seed=4,
+    "low_overlap": Workload(
+        name="low_overlap", seed=4,
         description=("low overlap: 256 requests x 16K ctx (192 live, turnover every 4 steps), "
                      "2 groups x 4 layers, top-2,048, overlap 0.5 + Zipf(1.1), GPU pool 10%"),
         n_live=192, n_total=256, ctx_min=16384, ctx_max=16384, n_groups=2, layers_per_group=4,
@@ -144,8 +144,8 @@ WORKLOADS = {
         turnover_period=4, gpu_frac=0.1),
     # The low-overlap stress as literally stated: all 256 requests at once.  One step
     # selects 524,288 rows against 419,430 GPU slots, so it needs the overflow bypass.
-    "cfg4_literal": Workload(
-        name="cfg4_literal", seed=4,
+    "low_overlap_256": Workload(
+        name="low_overlap_256", seed=4,
         description=("low overlap, literal: 256 requests x 16K ctx all at once, 2 groups x 4 "
                      "layers, top-2,048, overlap 0.5 + Zipf(1.1), GPU pool 10%, overflow bypass"),
         n_live=256, ctx_min=16384, ctx_max=16384, n_groups=2, layers_per_group=4,
@@ -162,14 +162,14 @@ def small(name: str, **kw) -> Workload:
     """A reduced copy of a workload (same recipe, smaller sizes) for full-state parity tests."""
     w = WORKLOADS[name]
     shrink = {
-        "cfg0": dict(),
-        "cfg1": dict(n_live=4, ctx_min=4096, ctx_max=4096, k=256, window=64, steps=48),
-        "cfg2": dict(n_live=6, ctx_min=3000, ctx_max=6000, k=256, window=64, steps=40,
+        "tiny_1x4k": dict(),
+        "batch8_32k": dict(n_live=4, ctx_min=4096, ctx_max=4096, k=256, window=64, steps=48),
+        "longdoc": dict(n_live=6, ctx_min=3000, ctx_max=6000, k=256, window=64, steps=40,
                      append_cap=64),
-        "cfg3": dict(n_live=4, ctx_min=4096, ctx_max=4096, k=256, window=64, steps=48),
-        "cfg4": dict(n_live=12, n_total=20, ctx_min=2048, ctx_max=2048, k=256, window=64,
+        "low_evict": dict(n_live=4, ctx_min=4096, ctx_max=4096, k=256, window=64, steps=48),
+        "low_overlap": dict(n_live=12, n_total=20, ctx_min=2048, ctx_max=2048, k=256, window=64,
                      steps=40, turnover_period=4),
-        "cfg4_literal": dict(n_live=20, ctx_min=2048, ctx_max=2048, k=256, window=64, steps=40),
+        "low_overlap_256": dict(n_live=20, ctx_min=2048, ctx_max=2048, k=256, window=64, steps=40),
     }[name]
     shrink.update(kw)
     return w.replace(name=name + "_small", description=w.description + " (reduced)", **shrink)

@@ -73,12 +73,12 @@ def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2
         gpu.close()
 
 
-def test_parity_cfg0_full():
-    stats = run_parity(WORKLOADS["cfg0"], WORKLOADS["cfg0"].steps)
+def test_parity_tiny_1x4k_full():
+    stats = run_parity(WORKLOADS["tiny_1x4k"], WORKLOADS["tiny_1x4k"].steps)
     assert stats["steps"] == 64 and stats["misses"] > 0 and stats["hits"] > 0
 
 
-@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3", "cfg4", "cfg4_literal"])
+@pytest.mark.parametrize("name", ["batch8_32k", "longdoc", "low_evict", "low_overlap", "low_overlap_256"])
 def test_parity_small(name):
     w = small(name)
     stats = run_parity(w, w.steps)
@@ -87,14 +87,14 @@ def test_parity_small(name):
         assert stats["bypassed"] > 0  # the literal recipe overflows the pool every step
 
 
-def test_parity_cfg1_full():
-    w = WORKLOADS["cfg1"]
+def test_parity_batch8_32k_full():
+    w = WORKLOADS["batch8_32k"]
     stats = run_parity(w, w.steps, mode="bytes", state_every=4, out_every=16)
     assert stats["steps"] == w.steps * w.n_groups and stats["writebacks"] > 0
 
 
-@pytest.mark.parametrize("name,steps", [("cfg2", 12), ("cfg3", 12), ("cfg4", 13),
-                                        ("cfg4_literal", 6)])
+@pytest.mark.parametrize("name,steps", [("longdoc", 12), ("low_evict", 12), ("low_overlap", 13),
+                                        ("low_overlap_256", 6)])
 def test_parity_full_size_sampled(name, steps):
     """Full-size workloads: state compared every step, gathered bytes sampled."""
     w = WORKLOADS[name]
@@ -106,7 +106,7 @@ def test_parity_full_size_sampled(name, steps):
 
 def test_pads_and_ragged_sizes():
     # ragged: S, H not multiples of 32 or 1,024; E not a multiple of the block size
-    w = WORKLOADS["cfg0"].replace(pad_prob=0.1, gpu_slots_explicit=1000 + 7,
+    w = WORKLOADS["tiny_1x4k"].replace(pad_prob=0.1, gpu_slots_explicit=1000 + 7,
                                   host_slots_explicit=3400 + 13, k=250, window=50, steps=32)
     assert w.gpu_slots + w.host_slots >= w.max_live_history + w.entries_per_step
     run_parity(w, w.steps)
@@ -114,12 +114,12 @@ def test_pads_and_ragged_sizes():
 
 @pytest.mark.parametrize("B", [1, 2, 3])
 def test_small_rings(B):
-    w = small("cfg1").replace(ring_buckets=B, steps=24)
+    w = small("batch8_32k").replace(ring_buckets=B, steps=24)
     run_parity(w, w.steps)
 
 
 def test_everything_fits_on_gpu_no_host_pool():
-    w = WORKLOADS["cfg0"].replace(gpu_slots_explicit=4096, host_slots_explicit=0, steps=16)
+    w = WORKLOADS["tiny_1x4k"].replace(gpu_slots_explicit=4096, host_slots_explicit=0, steps=16)
     stats = run_parity(w, w.steps)
     assert stats["misses"] == 0 and stats["writebacks"] == 0
 
@@ -195,14 +195,14 @@ def test_mixed_layers_duplicates_across_requests_and_empty_steps():
 
 # ----------------------------------------------------------------- exact LRU
 
-@pytest.mark.parametrize("name", ["cfg1", "cfg2", "cfg3", "cfg4", "cfg4_literal"])
+@pytest.mark.parametrize("name", ["batch8_32k", "longdoc", "low_evict", "low_overlap", "low_overlap_256"])
 def test_exact_lru_parity_small(name):
     w = small(name).replace(exact_lru=True)
     stats = run_parity(w, w.steps)
     assert stats["misses"] > 0 and stats["victims_cold"] > 0 and stats["victims_ring"] == 0
 
 
-@pytest.mark.parametrize("name,steps", [("cfg2", 8), ("cfg3", 8), ("cfg4_literal", 4)])
+@pytest.mark.parametrize("name,steps", [("longdoc", 8), ("low_evict", 8), ("low_overlap_256", 4)])
 def test_exact_lru_full_size_sampled(name, steps):
     w = WORKLOADS[name].replace(exact_lru=True)
     stats = run_parity(w, steps, mode="id", state_every=1, out_every=10**9, sample_rows=4096)
@@ -306,6 +306,41 @@ def test_exact_lru_general_path_when_the_window_runs_short():
         assert st["victims_cold"] > 0
     finally:
         c.close()
+
+
+def test_exact_lru_barrier_wait_is_bounded():
+    """A block that never arrives at the scan's grid-wide barrier (test hook): the
+    others give up after their bound, the step reports ULA_ERR_TIMEOUT and the
+    context refuses further work; the GPU stays usable."""
+    import time
+    from serving_step_sparse_gb300 import ula
+    layers, W, S, H, B = (1,), 16, 64, 512, 4
+    c, o = _direct(S=S, H=H, B=B, layers=layers, W=W, max_logical=1024, max_entries=64,
+                   exact=True)
+    try:
+        n = 200
+        rows = _rows(layers, 0, n, W)
+        assert c.alloc(n, torch.from_numpy(rows).pin_memory()) == 0
+        c.sync()
+        sel = np.arange(100, 120, dtype=np.uint32).reshape(1, 1, -1)  # 20 misses, no free slot
+        out = c.out_buffer(0, 20)
+        er = torch.empty(20, dtype=torch.int32, device="cuda")
+        ro = torch.empty(2, dtype=torch.int32, device="cuda")
+        sd = torch.from_numpy(sel.view(np.int32).copy()).cuda()
+        ula.ula_debug_inject(c.ctx, ula.DEBUG_STALL_SCAN_BARRIER)
+        t0 = time.monotonic()
+        c.step_group(0, sd, out, er, ro)
+        with pytest.raises(ula.UlaError) as ei:
+            c.sync()
+        assert ei.value.code == ula.ERR_TIMEOUT
+        assert time.monotonic() - t0 < 20.0
+        with pytest.raises(ula.UlaError) as ei:
+            c.step_group(0, sd, out, er, ro)
+        assert ei.value.code == ula.ERR_POISONED
+    finally:
+        c.close()
+    x = torch.ones(1 << 20, device="cuda")  # the device still runs work
+    assert float(x.sum()) == float(1 << 20)
 
 
 def _export_all(c, G, S, H, B):
@@ -434,7 +469,7 @@ def test_config_and_pool_validation():
 def test_layer_ready_events_and_side_stream_order():
     """Layer j's event completes after its rows are written; a consumer waiting on
     each event (on another stream) reads the right bytes."""
-    w = small("cfg1").replace(steps=6)
+    w = small("batch8_32k").replace(steps=6)
     gpu = GpuRun(w)
     orc = OracleRun(w, "bytes")
     consumer = torch.cuda.Stream()
@@ -469,7 +504,7 @@ def test_layer_ready_events_and_side_stream_order():
 def test_regather_reproduces_hit_rows():
     """ula_debug_regather (used to time the gather alone) writes the same hit rows."""
     from serving_step_sparse_gb300 import ula
-    w = small("cfg1").replace(steps=5)
+    w = small("batch8_32k").replace(steps=5)
     gpu = GpuRun(w)
     try:
         for _ in range(w.steps):

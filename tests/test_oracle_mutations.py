@@ -66,8 +66,8 @@ def _fast_pins():
     pins.test_rotation_only_relabels()
     pins.test_errors_leave_state_untouched()
     pins.test_alloc_placement_and_free()
-    pins.test_workload_closed_forms_and_invariants("cfg0")
-    pins.test_workload_closed_forms_and_invariants("cfg2")
+    pins.test_workload_closed_forms_and_invariants("tiny_1x4k")
+    pins.test_workload_closed_forms_and_invariants("longdoc")
 
 
 def test_unmutated_source_passes():

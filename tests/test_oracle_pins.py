@@ -323,9 +323,9 @@ def test_textbook_lru_differs_once_folds_happen():
 
 # ----------------------------------------------------- workload-level pins
 
-@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "cfg3", "cfg4"])
+@pytest.mark.parametrize("name", ["tiny_1x4k", "batch8_32k", "longdoc", "low_evict", "low_overlap"])
 def test_workload_closed_forms_and_invariants(name):
-    w = WORKLOADS["cfg0"] if name == "cfg0" else small(name)
+    w = WORKLOADS["tiny_1x4k"] if name == "tiny_1x4k" else small(name)
     w = w.replace(steps=min(w.steps, 24))
     run = OracleRun(w, mode="bytes")
     for t in range(w.steps):
@@ -355,7 +355,7 @@ def test_workload_closed_forms_and_invariants(name):
 
 
 def test_current_round_never_evicted_and_all_selected_resident():
-    w = small("cfg4").replace(steps=16)
+    w = small("low_overlap").replace(steps=16)
     run = OracleRun(w, mode="id")
     for _ in range(w.steps):
         sel_all, ev = run.trace.step()
@@ -386,7 +386,7 @@ def test_current_round_never_evicted_and_all_selected_resident():
 
 def test_rotation_only_relabels():
     """A step whose selection is all hits moves no data and changes no map entry."""
-    w = WORKLOADS["cfg0"]
+    w = WORKLOADS["tiny_1x4k"]
     run = OracleRun(w, mode="bytes")
     st0 = run.o.export(0)
     gp0 = run.o.gpu_pool(0).copy()
@@ -409,7 +409,7 @@ def _state_equal(a, b):
 
 
 def test_errors_leave_state_untouched():
-    w = WORKLOADS["cfg0"]
+    w = WORKLOADS["tiny_1x4k"]
     run = OracleRun(w, mode="bytes")
     for _ in range(3):
         run.step()
@@ -498,7 +498,7 @@ class _WithCompanion(OracleRun):
         return sel, ev, res
 
 
-@pytest.mark.parametrize("name", ["cfg1", "cfg4"])
+@pytest.mark.parametrize("name", ["batch8_32k", "low_overlap"])
 def test_exact_lru_companion_agrees_with_exact_mode(name):
     """The hit-rate companion and the oracle's exact-LRU mode are the same policy:
     same hits and unique rows on the same trace (turnover included)."""

@@ -39,7 +39,7 @@ def test_noalloc_dedup_matches_step_group(pads):
     from tests.gpu_harness import GpuRun
     from tests.harness import apply_events
 
-    w = small("cfg2").replace(pad_prob=pads, steps=3)  # 3 query tokens: duplicates across them
+    w = small("longdoc").replace(pad_prob=pads, steps=3)  # 3 query tokens: duplicates across them
     assert w.entries_per_step <= ula.NOALLOC_MAX_ENTRIES
     gpu = GpuRun(w)
     stream = torch.cuda.Stream()
