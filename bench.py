@@ -50,6 +50,11 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layer-signal", action="store_true",
+                    help="layer-major fill with a device flag per layer (reports how early "
+                         "each layer is ready)")
+    ap.add_argument("--latency-steps", type=int, default=20,
+                    help="steps of the per-layer ready-time pass (synchronised per step)")
     ap.add_argument("--pool-frac", type=float, default=None,
                     help="GPU pool as a fraction of the history (policy comparisons)")
     ap.add_argument("--requests", type=int, default=None,
@@ -244,16 +249,18 @@ def run_gpu(args, rank, world, local):
     cache = UlaCache(row_bytes=W, layers_per_group=[L] * G, gpu_slots=w.gpu_slots,
                      host_slots=w.host_slots, ring_buckets=w.ring_buckets,
                      max_logical=w.max_logical, max_entries=E, device=dev, stream=stream,
-                     bypass_overflow=w.bypass, exact_lru=w.exact_lru)
+                     bypass_overflow=w.bypass, exact_lru=w.exact_lru,
+                     layer_signal=args.layer_signal)
     trace = stage_initial(cache, w, synth, torch)
     n_value, n_prof = args.steps, min(args.profile_steps, args.steps)
+    n_lat = min(args.latency_steps, args.steps)
     n_e2e = 0 if args.no_e2e else args.steps
-    steps = gen_steps(trace, w, args.warmup + n_value + n_prof + n_e2e, synth, np)
+    steps = gen_steps(trace, w, args.warmup + n_value + n_prof + n_lat + n_e2e, synth, np)
     outs = [cache.out_buffer(g, E) for g in range(G)]
     entry_row = [torch.empty(E, dtype=torch.int32, device=dev) for _ in range(G)]
     req_off = [torch.empty(R + 1, dtype=torch.int32, device=dev) for _ in range(G)]
-    # device-resident inputs for the value and profiled passes
-    n_dev = args.warmup + n_value + n_prof
+    # device-resident inputs for the value, profiled and latency passes
+    n_dev = args.warmup + n_value + n_prof + n_lat
     sel_dev = torch.from_numpy(np.stack([s[0] for s in steps[:n_dev]]).view(np.int32)).to(dev)
     rows_dev = [torch.from_numpy(s[2].reshape(-1)).to(dev) if s[2] is not None else None
                 for s in steps[:n_dev]]
@@ -310,11 +317,44 @@ def run_gpu(args, rank, world, local):
     # ---- profiled pass: per-launch gather / move durations on their own streams
     ula.ula_profile_enable(cache.ctx, True)
     st2a = cache.sync()
-    for t in range(args.warmup + n_value, n_dev):
+    for t in range(args.warmup + n_value, args.warmup + n_value + n_prof):
         do_step(sel_dev[t], steps[t][1], rows_dev[t])
     st2 = cache.sync()
     prof = ula.ula_profile_read(cache.ctx, reset=True)
     ula.ula_profile_enable(cache.ctx, False)
+
+    # ---- per-layer ready times (one step at a time): from the group call to its
+    # layer_ready events (CUDA events on the caller's stream side), and, with the
+    # layer signal, to each layer's device flag (globaltimer in the kernels)
+    ev_ms = [[] for _ in range(L)]
+    flag_ms = [[] for _ in range(L)]
+    t0_ev = torch.cuda.Event(enable_timing=True)
+    lr_ev = [torch.cuda.Event(enable_timing=True) for _ in range(L)]
+    for t in range(n_dev - n_lat, n_dev):
+        sel_t, ev, rows_t = sel_dev[t], steps[t][1], rows_dev[t]
+        for g in range(G):
+            torch.cuda.synchronize()
+            t0_ev.record(stream)
+            cache.step_group(g, sel_t[g], outs[g], entry_row[g], req_off[g], layer_ready=lr_ev)
+            cache.sync()
+            torch.cuda.synchronize()
+            for j in range(L):
+                ev_ms[j].append(t0_ev.elapsed_time(lr_ev[j]))
+            if args.layer_signal:
+                ns = ula.ula_debug_layer_times(cache.ctx, g, L)
+                for j in range(L):
+                    flag_ms[j].append((int(ns[j]) - int(ns[L])) / 1e6)
+        if ev["append_n"]:
+            got = cache.alloc(ev["append_n"], rows_t)
+            assert got == ev["append_base"]
+    cache.sync()
+    layer_ready = {"layer_ready_event_ms": [round(float(np.median(x)), 4) for x in ev_ms],
+                   "how": "median over groups and steps; one group call at a time, from an "
+                          "event recorded before the call to its layer_ready events"}
+    if args.layer_signal:
+        layer_ready["layer_flag_ms"] = [round(float(np.median(x)), 4) for x in flag_ms]
+        layer_ready["flag_how"] = ("device globaltimer from the step's first kernel to the "
+                                   "store of each layer's flag")
 
     # ---- e2e: host buffers through the C ABI
     e2e = None
@@ -391,6 +431,7 @@ def run_gpu(args, rank, world, local):
     res = {
         "rows": agg["rows"], "value_ms": agg["value_ms"], "launches": launches,
         "roofline": roof, "host_link": host, "clocks": clk, "phases": phases, "e2e": e2e,
+        "layer_ready": layer_ready,
         "setup_s": setup_s, "stats": {k: st1[k] - st0[k] for k in st1},
     }
     if e2e is not None:
@@ -544,6 +585,8 @@ def main(argv=None):
     w = workload_for(args)
     config = dict(w.summary())
     config["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    if args.layer_signal:
+        config["layer_signal"] = True
     config["l2"] = ("inputs larger than L2: GPU pool "
                     f"{w.gpu_slots * w.n_groups * w.layers_per_group * w.row_bytes / 1e9:.1f} GB, "
                     "rows gathered at random slots")
@@ -578,6 +621,7 @@ def main(argv=None):
                 "config": config, "roofline": r["roofline"], "host_link": r["host_link"],
                 "gpu_launches": r["launches"], "clocks": r["clocks"],
                 "phases_ms_per_step": r["phases"],
+                "layer_ready": r["layer_ready"],
                 "scheduling_ms_per_step": round(sum(r["phases"].get(k, 0.0)
                                                     for k in ("rotate", "mark", "select")), 4),
                 "metadata_ms_per_step": round(sum(r["phases"].get(k, 0.0)

@@ -92,6 +92,24 @@ typedef struct ula_config {
  * wait that expires latches ULA_ERR_TIMEOUT. */
 #define ULA_FLAG_EXACT_LRU 2u
 
+/* Per-layer signal (§2 "two more details": the current layer computes while later
+ * layers' data arrives; §3: data first, then the signal).  The fill runs layer by
+ * layer (layer 0 of every miss, then layer 1, ...), and as soon as out[j] holds every
+ * unique row of the step (hit rows gathered, missed rows filled) the library stores
+ * the step's round number into the group's device flag j (a release store).  A
+ * consumer kernel on any stream may then start on layer j while later layers are
+ * still moving: it polls the flag with acquire loads until it equals the round that
+ * ula_layer_signal reports, with a bound of its own.  layer_ready events are still
+ * recorded.  The map commit follows the last layer, as without the flag. */
+#define ULA_FLAG_LAYER_SIGNAL 4u
+
+/* ULA_FLAG_LAYER_SIGNAL: *d_flags receives the device address of group `group`'s
+ * flags (uint32 [L_g], owned by the context, valid until ula_destroy); *round receives
+ * the round number of the group's most recently issued ula_step_group (rounds count
+ * from 1; 0 before the first step).  Layer j of that step's output is complete once
+ * flag j equals *round.  INVALID_ARG without the flag or for a bad group. */
+int ula_layer_signal(ula_ctx *ctx, uint32_t group, const uint32_t **d_flags, uint32_t *round);
+
 /* Counters accumulated since ula_create, summed over groups. */
 typedef struct ula_stats {
   uint64_t steps;          /* ula_step_group calls completed */
@@ -253,6 +271,11 @@ int ula_debug_export(ula_ctx *ctx, uint32_t group, ula_debug_state *st);
  * bounded wait; nothing hangs). */
 int ula_debug_inject(ula_ctx *ctx, int code);
 #define ULA_DEBUG_STALL_SCAN_BARRIER 0x100
+/* ULA_FLAG_LAYER_SIGNAL: waits for the context's work (like ula_sync, without its
+ * error check), then copies group `group`'s signal times into ns (host, [L_g + 1]):
+ * ns[j] = device globaltimer (ns) when layer j's flag was set in the last step,
+ * ns[L_g] = when that step started.  For measuring how early each layer is ready. */
+int ula_debug_layer_times(ula_ctx *ctx, uint32_t group, unsigned long long *ns);
 /* Re-run the gather of the hit rows of `group`'s last step for one layer into d_out
  * ([L_g][out_cap_rows][row_bytes], device) on `stream`, changing no state (for timing
  * the gather kernel on its own).  Launches at once: the caller orders it after the

@@ -73,7 +73,8 @@ class UlaCache:
     def __init__(self, *, row_bytes: int, layers_per_group, gpu_slots: int, host_slots: int,
                  ring_buckets: int, max_logical: int, max_entries: int, device="cuda",
                  stream: torch.cuda.Stream | None = None, huge_host_pages: bool = True,
-                 bypass_overflow: bool = False, exact_lru: bool = False):
+                 bypass_overflow: bool = False, exact_lru: bool = False,
+                 layer_signal: bool = False):
         self.device = torch.device(device)
         self.W = int(row_bytes)
         self.layers = [int(x) for x in layers_per_group]
@@ -89,7 +90,8 @@ class UlaCache:
         cfg = ula.make_config(self.W, self.layers, self.S, self.H, self.B, self.max_logical,
                               self.max_entries,
                               (ula.FLAG_BYPASS_OVERFLOW if bypass_overflow else 0)
-                              | (ula.FLAG_EXACT_LRU if exact_lru else 0))
+                              | (ula.FLAG_EXACT_LRU if exact_lru else 0)
+                              | (ula.FLAG_LAYER_SIGNAL if layer_signal else 0))
         with torch.cuda.device(self.device):
             self.ctx = ula.ula_create(cfg, [p.data_ptr() for p in self.gpu_pools],
                                       [p.data_ptr() for p in self.host_pools] if self.H else None,
@@ -121,6 +123,10 @@ class UlaCache:
             ev = [e.cuda_event for e in layer_ready]
         ula.ula_step_group(self.ctx, g, _u32(sel), R, Q, K, out.data_ptr(), cap,
                            _u32(entry_row), _u32(req_off), ev, s.cuda_stream)
+
+    def layer_signal(self, g: int) -> tuple[int, int]:
+        """(device address of group g's uint32 layer flags, round of its last step)."""
+        return ula.ula_layer_signal(self.ctx, g)
 
     def sync(self) -> dict:
         return ula.ula_sync(self.ctx)

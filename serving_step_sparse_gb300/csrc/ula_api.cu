@@ -207,7 +207,8 @@ int validate_config(const ula_config *c) {
   if (c->ring_buckets == 0 || c->ring_buckets > ULA_MAX_BUCKETS) return ULA_ERR_INVALID_ARG;
   if (c->max_logical == 0 || c->max_logical > kSlotMask) return ULA_ERR_INVALID_ARG;
   if (c->max_entries == 0) return ULA_ERR_INVALID_ARG;
-  if ((c->flags & ~(ULA_FLAG_BYPASS_OVERFLOW | ULA_FLAG_EXACT_LRU)) != 0) return ULA_ERR_INVALID_ARG;
+  if ((c->flags & ~(ULA_FLAG_BYPASS_OVERFLOW | ULA_FLAG_EXACT_LRU | ULA_FLAG_LAYER_SIGNAL)) != 0)
+    return ULA_ERR_INVALID_ARG;
   return ULA_OK;
 }
 
@@ -245,6 +246,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   geo.max_logical = cfg.max_logical;
   geo.bypass = (cfg.flags & ULA_FLAG_BYPASS_OVERFLOW) ? 1u : 0u;
   geo.exact = (cfg.flags & ULA_FLAG_EXACT_LRU) ? 1u : 0u;
+  geo.signal = (cfg.flags & ULA_FLAG_LAYER_SIGNAL) ? 1u : 0u;
   geo.gd = dims_for(S);
   geo.hd = dims_for(H);
   geo.nseg = geo.gd.n1;
@@ -348,6 +350,19 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
     ULA_CUDA(c->alloc(&d.wb_host, c->decision_cap));
     ULA_CUDA(c->alloc(&d.work, work_len));
     d.cnt = c->cnt_d + g;
+    if (geo.signal) {
+      const uint32_t L = d.layers;
+      ULA_CUDA(c->alloc(&d.layer_flag, L));
+      ULA_CUDA(c->alloc(&d.layer_cnt, L));
+      ULA_CUDA(c->alloc(&d.move_done, L + 1));  // [L]: the chunk dispenser
+      ULA_CUDA(c->alloc(&d.gather_done, L));
+      ULA_CUDA(c->alloc(&d.layer_ns, L + 1));
+      ULA_CUDA(cudaMemsetAsync(d.layer_flag, 0, sizeof(uint32_t) * L, s));
+      ULA_CUDA(cudaMemsetAsync(d.layer_cnt, 0, sizeof(uint32_t) * L, s));
+      ULA_CUDA(cudaMemsetAsync(d.move_done, 0, sizeof(uint32_t) * (L + 1), s));
+      ULA_CUDA(cudaMemsetAsync(d.gather_done, 0, sizeof(uint32_t) * L, s));
+      ULA_CUDA(cudaMemsetAsync(d.layer_ns, 0, sizeof(unsigned long long) * (L + 1), s));
+    }
     ULA_CUDA(cudaMemsetAsync(d.map, 0xff, sizeof(uint32_t) * cfg.max_logical, s));
     ULA_CUDA(cudaMemsetAsync(d.owner, 0xff, sizeof(uint32_t) * S, s));
     ULA_CUDA(cudaMemsetAsync(d.stamp, 0xff, sizeof(uint32_t) * S, s));
@@ -567,6 +582,8 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   gp.grp = gd;
   gp.out = static_cast<uint8_t *>(d_out);
   gp.out_cap = out_cap_rows;
+  gp.signal = c->geo.signal;
+  gp.round = r;
   gp.status = c->status;
   if (gather) {
     // (6) the hit rows, while the misses are being moved (a hit's slot does not
@@ -799,6 +816,25 @@ int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, void *d_out,
     blocks = c->sm_count * ((int)blocks_per_sm < fit ? (int)blocks_per_sm : fit);
   }
   ULA_CUDA(launch_gather(gp, blocks, caller));
+  return ULA_OK;
+}
+
+int ula_layer_signal(ula_ctx *c, uint32_t group, const uint32_t **d_flags, uint32_t *round) {
+  if (!c || !d_flags || !round || !c->geo.signal || group >= c->cfg.n_groups)
+    return ULA_ERR_INVALID_ARG;
+  *d_flags = c->groups_h[group].layer_flag;
+  *round = c->round[group];
+  return ULA_OK;
+}
+
+int ula_debug_layer_times(ula_ctx *c, uint32_t group, unsigned long long *ns) {
+  if (!c || !ns || !c->geo.signal || group >= c->cfg.n_groups) return ULA_ERR_INVALID_ARG;
+  if (c->poisoned) return ULA_ERR_POISONED;
+  int rc = sync_impl(c);
+  if (rc) return rc;
+  const GroupDev &d = c->groups_h[group];
+  ULA_CUDA(cudaMemcpy(ns, d.layer_ns, sizeof(unsigned long long) * (d.layers + 1),
+                      cudaMemcpyDeviceToHost));
   return ULA_OK;
 }
 

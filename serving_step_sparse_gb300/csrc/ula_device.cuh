@@ -82,6 +82,12 @@ struct GroupDev {
   uint32_t *wb_host;   // [decision_cap]: host slot of write-back j (alloc: host slots)
   uint4 *work;         // [(B+1)*nseg + hseg]: (order position, segment, first rank, count)
   GroupCounters *cnt;
+  // per-layer signal (ULA_FLAG_LAYER_SIGNAL only; NULL otherwise)
+  uint32_t *layer_flag;  // [L]: round whose output of layer j is complete
+  uint32_t *layer_cnt;   // [L]: contributions to layer j's signal in this step
+  uint32_t *move_done;   // [L + 1]: chunks of layer j moved in this step; [L]: dispenser
+  uint32_t *gather_done; // [L]: gather blocks done with layer j in this step
+  unsigned long long *layer_ns;  // [L + 1]: globaltimer at each signal; [L]: step start
   uint32_t layers;     // L_g
   uint32_t pad;
 };
@@ -91,6 +97,7 @@ struct Geometry {
   uint32_t max_logical;
   uint32_t bypass;       // ULA_FLAG_BYPASS_OVERFLOW set
   uint32_t exact;        // ULA_FLAG_EXACT_LRU set: occupied slots all in class B, no ring
+  uint32_t signal;       // ULA_FLAG_LAYER_SIGNAL set: layer-major fill and per-layer flags
   Dims gd, hd;           // bitmap dims for GPU-slot and host-slot bitmaps
   uint32_t nseg, hseg;   // segments (= level-1 words) per bitmap
 };
@@ -205,6 +212,8 @@ struct GatherParams {
   uint8_t *out;             // [L][out_cap][W]
   uint32_t out_cap;
   uint32_t layer;
+  uint32_t signal;          // contributes to the layer's signal (a step's gather)
+  uint32_t round;
   int *status;
 };
 

@@ -58,6 +58,29 @@ constexpr int kGatherThreads = ULA_GATHER_THREADS;
 
 __device__ __forceinline__ void latch(int *status, int code) { atomicCAS(status, 0, code); }
 
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long v;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v));
+  return v;
+}
+
+__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// One contribution to layer j's signal (the move's, or the hit gather's): the
+// last of `needed` stores the round into the layer's flag, after a fence that
+// orders every output write of the contributors before it.
+__device__ void layer_contrib(const GroupDev &g, uint32_t j, uint32_t needed, uint32_t round) {
+  __threadfence();
+  if (atomicAdd(&g.layer_cnt[j], 1u) == needed - 1) {
+    g.layer_cnt[j] = 0;
+    g.layer_ns[j] = global_ns();
+    __threadfence();
+    st_release(&g.layer_flag[j], round);
+  }
+}
+
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
@@ -214,6 +237,7 @@ __global__ void k_dedup_stamp(StepParams p) {
   if (*(volatile int *)p.status) return;
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   if (p.inject && e == 0) latch(p.status, p.inject);
+  if (p.geo.signal && e == 0) p.grp.layer_ns[p.grp.layers] = global_ns();  // step start
   if (e >= p.E) return;
   const uint32_t a = p.sel[e];
   if (a == kPad) return;
@@ -245,6 +269,8 @@ __device__ __forceinline__ Flags entry_flags(const StepParams &p, uint32_t e) {
 // state changes before it passes.
 __global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p) {
   if (block_skips(p.status)) return;
+  if (p.geo.signal && p.E == 0 && blockIdx.x == 0 && threadIdx.x == 0)
+    p.grp.layer_ns[p.grp.layers] = global_ns();  // step start (no entries: no stamp kernel)
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   const Flags f = entry_flags(p, e);
   __shared__ uint32_t sf[kEntryThreads / 32], sm[kEntryThreads / 32];
@@ -296,6 +322,7 @@ __global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p
       c->K = 0;
       c->n_work = 0;
       c->n_work_gpu = 0;
+      if (p.geo.signal) p.grp.move_done[p.grp.layers] = 0;  // the layer-major move's dispenser
       p.req_off[p.n_req] = (int32_t)U;
       const unsigned long long sb = (unsigned long long)p.grp.layers * p.geo.W;
       c->stat[kStSteps] += 1;
@@ -659,6 +686,102 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) 
   }
 }
 
+// (5) With the per-layer signal: the same moves, layer by layer.  The chunks of
+// every layer (16 bytes each, CW per row; layer 0 of every miss and every bypassed
+// miss first, then layer 1, ...) are handed out in order, kMoveBatch at a time, from
+// a counter, so the chunks of layer j are all taken before any of layer j + 1 and
+// layer j completes soon after its last batch was taken.  Inside a batch
+// consecutive lanes take consecutive chunks; a lane reads the victim's chunk
+// (write-back) and the miss's chunk (fill) before it writes either, so each chunk
+// leaves before the new one lands.  Completed chunks are counted per layer; the
+// warp that completes layer j gives the move's contribution to the layer's signal.
+constexpr int kMoveLayerUnroll = 4;
+constexpr uint32_t kMoveBatch = 32 * kMoveLayerUnroll * 2;
+
+__global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move_layers(MoveParams p) {
+  if (*(volatile int *)p.status) return;
+  const GroupDev &g = p.grp;
+  const Geometry &geo = p.geo;
+  const uint32_t M = g.cnt->M, F = g.cnt->F, Mx = g.cnt->Mx;
+  const uint32_t L = g.layers;
+  const uint32_t CW = geo.W / 16;
+  const size_t sb = (size_t)L * geo.W;
+  const uint32_t lane = lane_id();
+  const uint32_t per_layer = (M + Mx) * CW;  // chunks of one layer
+  const uint32_t total = per_layer * L;
+  const uint32_t needed = p.out ? 2u : 1u;
+  uint4 *out = reinterpret_cast<uint4 *>(p.out);
+  if (per_layer == 0) {  // nothing to move: the move's contribution to every layer
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      for (uint32_t j = 0; j < L; ++j) layer_contrib(g, j, needed, p.round);
+    return;
+  }
+  uint32_t *next = &g.move_done[L];  // the dispenser (reset before the step's move)
+  for (;;) {
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(next, kMoveBatch);
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (base >= total) break;
+    const uint32_t end = min(base + kMoveBatch, total);
+    for (uint32_t c0 = base + lane; c0 < end; c0 += 32 * kMoveLayerUnroll) {
+      uint4 fill[kMoveLayerUnroll], back[kMoveLayerUnroll];
+      uint32_t vs[kMoveLayerUnroll], hds[kMoveLayerUnroll], rows[kMoveLayerUnroll],
+          offs[kMoveLayerUnroll], js[kMoveLayerUnroll];
+#pragma unroll
+      for (int u = 0; u < kMoveLayerUnroll; ++u) {
+        vs[u] = hds[u] = rows[u] = kNone;
+        offs[u] = js[u] = 0;
+        const uint32_t c = c0 + u * 32;
+        if (c >= end) continue;
+        const uint32_t j = c / per_layer, cc = c - j * per_layer;
+        const uint32_t i = cc / CW, k = cc - i * CW;
+        const uint32_t hs = p.miss_hs[i], row = p.miss_row[i];
+        if (hs >= geo.H || (out && row >= p.out_cap) || (i >= M && !out)) {
+          latch(p.status, ULA_ERR_INTERNAL);
+          continue;
+        }
+        uint32_t v = kNone, hd = kNone;
+        if (i < M) {  // resident miss: the victim slot, and its write-back target if it holds data
+          v = g.victims[i];
+          if (i >= F) hd = g.wb_host[i - F];
+          if (v >= geo.S || (i >= F && hd >= geo.H)) {
+            latch(p.status, ULA_ERR_INTERNAL);
+            continue;
+          }
+        }
+        const uint32_t off = j * geo.W + 16 * k;  // byte offset inside a slot
+        js[u] = j;
+        offs[u] = off;
+        vs[u] = v;
+        hds[u] = hd;
+        rows[u] = out ? row : kNone;
+        fill[u] = *reinterpret_cast<const uint4 *>(g.host_pool + (size_t)hs * sb + off);
+        if (hd != kNone) back[u] = *reinterpret_cast<const uint4 *>(g.gpu_pool + (size_t)v * sb + off);
+      }
+#pragma unroll
+      for (int u = 0; u < kMoveLayerUnroll; ++u) {
+        if (hds[u] != kNone)
+          *reinterpret_cast<uint4 *>(g.host_pool + (size_t)hds[u] * sb + offs[u]) = back[u];
+        if (vs[u] != kNone)
+          *reinterpret_cast<uint4 *>(g.gpu_pool + (size_t)vs[u] * sb + offs[u]) = fill[u];
+        if (rows[u] != kNone)
+          out[((size_t)js[u] * p.out_cap + rows[u]) * CW + (offs[u] - js[u] * geo.W) / 16] = fill[u];
+      }
+    }
+    __threadfence();  // every lane's writes of the batch before its count
+    __syncwarp();
+    if (lane == 0) {
+      for (uint32_t j = base / per_layer; j <= (end - 1) / per_layer; ++j) {
+        const uint32_t n = min(end, (j + 1) * per_layer) - max(base, j * per_layer);
+        if (atomicAdd(&g.move_done[j], n) + n == per_layer) {
+          g.move_done[j] = 0;
+          layer_contrib(g, j, needed, p.round);
+        }
+      }
+    }
+  }
+}
+
 // (5) Then the map: one thread per victim, after every copy has completed
 // (kernel boundary).  The evicted owner now maps to its host slot, the miss to
 // the victim slot; the slot joins the current bucket (clears on its old class,
@@ -774,6 +897,12 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
       }
     }
   }
+  // per-layer signal: the hit rows of this layer are one of its two contributions
+  if (p.signal) {
+    __threadfence();  // every thread's output writes before the block's ticket
+    if (last_block(&g.gather_done[p.layer]) && threadIdx.x == 0)
+      layer_contrib(g, p.layer, 2u, p.round);
+  }
 }
 
 // ------------------------------------------------------------- exact LRU
@@ -798,12 +927,6 @@ constexpr int kLruColLoads = 5;   // per-block counts a lane loads at once (5 * 
 __device__ __forceinline__ uint32_t ld_acquire(const void *p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long v;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v));
   return v;
 }
 
@@ -1559,7 +1682,8 @@ cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm) {
 }
 
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
-  k_move<<<blocks, 256, 0, s>>>(p);
+  if (p.geo.signal) k_move_layers<<<blocks, 256, 0, s>>>(p);
+  else k_move<<<blocks, 256, 0, s>>>(p);
   k_commit<<<blocks, 256, 0, s>>>(p);  // grid-stride over the victims
   return cudaGetLastError();
 }

@@ -17,6 +17,7 @@ MAX_BUCKETS = 64
 ADDR_PAD = 0xFFFFFFFF
 FLAG_BYPASS_OVERFLOW = 1
 FLAG_EXACT_LRU = 2
+FLAG_LAYER_SIGNAL = 4
 MAP_UNALLOCATED = 0xFFFFFFFF
 MAP_HOST = 0x80000000
 STAMP_FREE = 0xFFFFFFFF
@@ -107,6 +108,10 @@ def _load():
     lib.ula_debug_regather.restype = i32
     lib.ula_dedup_noalloc.argtypes = [p, u32, p, p, p, p]
     lib.ula_dedup_noalloc.restype = i32
+    lib.ula_layer_signal.argtypes = [p, u32, C.POINTER(p), C.POINTER(u32)]
+    lib.ula_layer_signal.restype = i32
+    lib.ula_debug_layer_times.argtypes = [p, u32, p]
+    lib.ula_debug_layer_times.restype = i32
     return lib
 
 
@@ -194,6 +199,21 @@ def ula_debug_layout_get(ctx: int) -> ula_debug_layout:
 def ula_debug_export(ctx: int, group: int, st: ula_debug_state) -> ula_debug_state:
     _check(lib.ula_debug_export(ctx, group, C.byref(st)), "ula_debug_export")
     return st
+
+
+def ula_layer_signal(ctx: int, group: int) -> tuple[int, int]:
+    """(device address of the group's layer flags, round of its last issued step)."""
+    ptr, rnd = C.c_void_p(), C.c_uint32()
+    _check(lib.ula_layer_signal(ctx, group, C.byref(ptr), C.byref(rnd)), "ula_layer_signal")
+    return ptr.value or 0, rnd.value
+
+
+def ula_debug_layer_times(ctx: int, group: int, layers: int):
+    """[L + 1] globaltimer ns: when each layer's flag was set, then the step's start."""
+    import numpy as np
+    ns = np.zeros(layers + 1, dtype=np.uint64)
+    _check(lib.ula_debug_layer_times(ctx, group, ns.ctypes.data), "ula_debug_layer_times")
+    return ns
 
 
 def ula_debug_inject(ctx: int, code: int) -> None:

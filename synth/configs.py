@@ -51,6 +51,7 @@ class Workload:
     pad_prob: float = 0.0       # fraction of entries replaced by the pad marker (edge tests)
     bypass: bool = False        # overflow bypass: misses beyond the pool are read in place
     exact_lru: bool = False     # exact LRU (timestamp per slot) in place of PB-LRU
+    layer_signal: bool = False  # layer-major fill with a device flag per layer
     _cache: dict = field(default_factory=dict, compare=False, hash=False, repr=False)
 
     @property

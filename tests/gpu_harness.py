@@ -22,7 +22,7 @@ class GpuRun:
                               gpu_slots=w.gpu_slots, host_slots=w.host_slots,
                               ring_buckets=w.ring_buckets, max_logical=w.max_logical,
                               max_entries=w.entries_per_step, bypass_overflow=w.bypass,
-                              exact_lru=w.exact_lru)
+                              exact_lru=w.exact_lru, layer_signal=w.layer_signal)
         self.cap = out_cap if out_cap is not None else w.entries_per_step
         self.outs = [self.cache.out_buffer(g, self.cap) for g in range(G)]
         E = w.entries_per_step
@@ -82,6 +82,25 @@ class GpuRun:
         if full_out:
             res["out"] = self.outs[g][:, :U].cpu().numpy()
         return res
+
+
+class _DeviceWords:
+    """A device array the library owns, seen through the CUDA array interface."""
+
+    def __init__(self, ptr: int, n: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (ptr, False),
+                                         "version": 2}
+
+
+def check_layer_signal(cache, g: int, layers: int, where: str):
+    """After a synced step: every layer flag holds the step's round, and each flag was
+    set after the step started."""
+    ptr, rnd = cache.layer_signal(g)
+    flags = torch.as_tensor(_DeviceWords(ptr, layers), device=cache.device).cpu().numpy()
+    assert (flags.view(np.uint32) == rnd).all(), f"{where}: flags {flags.tolist()} round {rnd}"
+    ns = ula.ula_debug_layer_times(cache.ctx, g, layers)
+    assert (ns[:layers] >= ns[layers]).all() and ns[layers] > 0, f"{where}: signal times {ns}"
+    return ns
 
 
 def unpack_bits(words: np.ndarray, nbits: int) -> np.ndarray:

@@ -19,8 +19,8 @@ from tests.harness import OracleRun, check_invariants, check_step_outputs
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from tests.gpu_harness import (GpuRun, check_gpu_internal, compare_states, expand_id_rows,
-                                   gpu_state_in_oracle_terms)
+    from tests.gpu_harness import (GpuRun, check_gpu_internal, check_layer_signal, compare_states,
+                                   expand_id_rows, gpu_state_in_oracle_terms)
 
 
 def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2048, seed=0):
@@ -54,6 +54,8 @@ def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2
                         else:
                             exp = expand_id_rows(ro["out"][j, rows], w.seed, g, j, w.row_bytes)
                         assert np.array_equal(got, exp), f"{where}: gathered bytes layer {j}"
+                if w.layer_signal:
+                    check_layer_signal(gpu.cache, g, w.layers_per_group, where)
                 if t % state_every == 0 or t == steps - 1:
                     st = gpu.cache.export(g)
                     check_gpu_internal(st, w)
@@ -191,6 +193,29 @@ def test_mixed_layers_duplicates_across_requests_and_empty_steps():
                 compare_states(go, o.export(gg), f"step {step} g{gg}")
     finally:
         c.close()
+
+
+# --------------------------------------------------------- per-layer signal
+
+@pytest.mark.parametrize("name", ["tiny_1x4k", "batch8_32k", "longdoc", "low_overlap",
+                                  "low_overlap_256"])
+def test_layer_signal_parity_small(name):
+    """Layer-major fill with per-layer flags: outputs and state bit-exact with the
+    oracle, every flag at the step's round after the step."""
+    w = (WORKLOADS[name] if name == "tiny_1x4k" else small(name)).replace(layer_signal=True)
+    stats = run_parity(w, min(w.steps, 24))
+    assert stats["misses"] > 0
+
+
+@pytest.mark.parametrize("name,steps", [("longdoc", 6), ("low_overlap_256", 4)])
+def test_layer_signal_full_size_sampled(name, steps):
+    w = WORKLOADS[name].replace(layer_signal=True)
+    run_parity(w, steps, mode="id", state_every=1, out_every=10**9, sample_rows=4096)
+
+
+def test_layer_signal_with_exact_lru():
+    w = small("low_evict").replace(layer_signal=True, exact_lru=True, steps=24)
+    run_parity(w, w.steps)
 
 
 # ----------------------------------------------------------------- exact LRU
