@@ -276,6 +276,16 @@ int ula_debug_inject(ula_ctx *ctx, int code);
  * ns[j] = device globaltimer (ns) when layer j's flag was set in the last step,
  * ns[L_g] = when that step started.  For measuring how early each layer is ready. */
 int ula_debug_layer_times(ula_ctx *ctx, uint32_t group, unsigned long long *ns);
+/* ULA_FLAG_LAYER_SIGNAL: a model consumer of one layer.  Launches at once on `stream`
+ * one block that polls group `group`'s flag `layer` with acquire loads until it equals
+ * `round` (bounded: 1 s), then reads out[layer][0, n_rows) (d_out as given to the step,
+ * [L_g][out_cap_rows][row_bytes]) and writes into d_result (device, u64 [3]): the
+ * globaltimer when it saw the flag, the wrapping sum of the rows' 32-bit words, and a
+ * status (0, or ULA_ERR_TIMEOUT when the bound expired).  It changes no state; it
+ * shows what a consumer on another stream does while later layers are still moving. */
+int ula_debug_consume(ula_ctx *ctx, uint32_t group, uint32_t layer, uint32_t round,
+                      const void *d_out, uint32_t out_cap_rows, uint32_t n_rows,
+                      unsigned long long *d_result, void *stream);
 /* Re-run the gather of the hit rows of `group`'s last step for one layer into d_out
  * ([L_g][out_cap_rows][row_bytes], device) on `stream`, changing no state (for timing
  * the gather kernel on its own).  Launches at once: the caller orders it after the

@@ -838,6 +838,20 @@ int ula_debug_layer_times(ula_ctx *c, uint32_t group, unsigned long long *ns) {
   return ULA_OK;
 }
 
+int ula_debug_consume(ula_ctx *c, uint32_t group, uint32_t layer, uint32_t round,
+                      const void *d_out, uint32_t out_cap_rows, uint32_t n_rows,
+                      unsigned long long *d_result, void *stream) {
+  if (!c || !c->geo.signal || group >= c->cfg.n_groups || !d_result) return ULA_ERR_INVALID_ARG;
+  const GroupDev &d = c->groups_h[group];
+  if (layer >= d.layers || n_rows > out_cap_rows || (n_rows && !d_out)) return ULA_ERR_INVALID_ARG;
+  if (c->poisoned) return ULA_ERR_POISONED;
+  ULA_CUDA(c->ensure_device());
+  ULA_CUDA(launch_consume(d.layer_flag + layer, round, static_cast<const uint8_t *>(d_out),
+                          out_cap_rows, layer, n_rows, c->cfg.row_bytes, d_result,
+                          static_cast<cudaStream_t>(stream)));
+  return ULA_OK;
+}
+
 int ula_debug_inject(ula_ctx *c, int code) {
   if (!c) return ULA_ERR_INVALID_ARG;
   if (c->poisoned) return ULA_ERR_POISONED;

@@ -251,6 +251,10 @@ cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
 // `blocks` co-resident blocks)
 cudaError_t launch_lru_select(const LruParams &p, int blocks, cudaStream_t s);
 cudaError_t lru_resident_blocks(int *per_sm);
+// a model consumer of one layer (diagnostics): waits for the layer's flag, sums the rows
+cudaError_t launch_consume(const uint32_t *flag, uint32_t round, const uint8_t *out,
+                           uint32_t out_cap, uint32_t layer, uint32_t n_rows, uint32_t W,
+                           unsigned long long *result, cudaStream_t s);
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s);
 cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);

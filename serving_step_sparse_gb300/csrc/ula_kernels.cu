@@ -696,7 +696,10 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) 
 // leaves before the new one lands.  Completed chunks are counted per layer; the
 // warp that completes layer j gives the move's contribution to the layer's signal.
 constexpr int kMoveLayerUnroll = 4;
-constexpr uint32_t kMoveBatch = 32 * kMoveLayerUnroll * 2;
+#ifndef ULA_MOVE_BATCH
+#define ULA_MOVE_BATCH (32 * 4 * 2)
+#endif
+constexpr uint32_t kMoveBatch = ULA_MOVE_BATCH;  // chunks handed out at a time (a multiple of 32)
 
 __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move_layers(MoveParams p) {
   if (*(volatile int *)p.status) return;
@@ -1628,6 +1631,51 @@ __global__ void k_free(FreeParams p) {
   g.map[a] = kUnalloc;
 }
 
+// A model consumer of one layer: one block polls the layer's flag (acquire) until
+// it holds the round, bounded by kBarrierNs, then sums the layer's rows.
+__global__ void k_consume(const uint32_t *flag, uint32_t round, const uint8_t *out,
+                          uint32_t out_cap, uint32_t layer, uint32_t n_rows, uint32_t W,
+                          unsigned long long *result) {
+  __shared__ int s_ok;
+  __shared__ unsigned long long s_seen;
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = global_ns();
+    int ok = 1;
+    while (ld_acquire(flag) != round) {
+      if (global_ns() - t0 > kBarrierNs) {
+        ok = 0;
+        break;
+      }
+    }
+    s_ok = ok;
+    s_seen = global_ns();
+  }
+  __syncthreads();
+  if (!s_ok) {
+    if (threadIdx.x == 0) {
+      result[0] = s_seen;
+      result[1] = 0;
+      result[2] = ULA_ERR_TIMEOUT;
+    }
+    return;
+  }
+  const uint32_t *words = reinterpret_cast<const uint32_t *>(out + (size_t)layer * out_cap * W);
+  const size_t n = (size_t)n_rows * W / 4;
+  uint32_t sum = 0;
+  for (size_t i = threadIdx.x; i < n; i += blockDim.x) sum += __ldcg(&words[i]);
+  sum = warp_sum(sum);
+  __shared__ uint32_t ws[32];
+  if (lane_id() == 0) ws[threadIdx.x >> 5] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t tot = 0;
+    for (uint32_t w = 0; w < blockDim.x / 32; ++w) tot += ws[w];
+    result[0] = s_seen;
+    result[1] = tot;
+    result[2] = 0;
+  }
+}
+
 inline uint32_t div_up(uint64_t a, uint64_t b) { return (uint32_t)((a + b - 1) / b); }
 
 }  // namespace
@@ -1685,6 +1733,13 @@ cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
   if (p.geo.signal) k_move_layers<<<blocks, 256, 0, s>>>(p);
   else k_move<<<blocks, 256, 0, s>>>(p);
   k_commit<<<blocks, 256, 0, s>>>(p);  // grid-stride over the victims
+  return cudaGetLastError();
+}
+
+cudaError_t launch_consume(const uint32_t *flag, uint32_t round, const uint8_t *out,
+                           uint32_t out_cap, uint32_t layer, uint32_t n_rows, uint32_t W,
+                           unsigned long long *result, cudaStream_t s) {
+  k_consume<<<1, 256, 0, s>>>(flag, round, out, out_cap, layer, n_rows, W, result);
   return cudaGetLastError();
 }
 

@@ -112,6 +112,8 @@ def _load():
     lib.ula_layer_signal.restype = i32
     lib.ula_debug_layer_times.argtypes = [p, u32, p]
     lib.ula_debug_layer_times.restype = i32
+    lib.ula_debug_consume.argtypes = [p, u32, u32, u32, p, u32, u32, p, p]
+    lib.ula_debug_consume.restype = i32
     return lib
 
 
@@ -214,6 +216,12 @@ def ula_debug_layer_times(ctx: int, group: int, layers: int):
     ns = np.zeros(layers + 1, dtype=np.uint64)
     _check(lib.ula_debug_layer_times(ctx, group, ns.ctypes.data), "ula_debug_layer_times")
     return ns
+
+
+def ula_debug_consume(ctx: int, group: int, layer: int, round_: int, d_out: int,
+                      out_cap_rows: int, n_rows: int, d_result: int, stream) -> None:
+    _check(lib.ula_debug_consume(ctx, group, layer, round_, d_out, out_cap_rows, n_rows,
+                                 d_result, stream), "ula_debug_consume")
 
 
 def ula_debug_inject(ctx: int, code: int) -> None:

@@ -213,6 +213,50 @@ def test_layer_signal_full_size_sampled(name, steps):
     run_parity(w, steps, mode="id", state_every=1, out_every=10**9, sample_rows=4096)
 
 
+def test_layer_signal_consumers_on_another_stream():
+    """Model consumers of every layer, launched on another stream right after each
+    group call and before any synchronisation, each wait for their layer's flag and
+    read exactly the oracle's rows for that layer."""
+    from serving_step_sparse_gb300 import ula
+    from tests.harness import apply_events
+    w = WORKLOADS["batch8_32k"].replace(layer_signal=True, steps=10)
+    gpu = GpuRun(w)
+    orc = OracleRun(w, "bytes")
+    L = w.layers_per_group
+    side = torch.cuda.Stream()
+    res = torch.zeros((w.n_groups, L, 3), dtype=torch.int64, device="cuda")
+    early = total = 0
+    try:
+        for t in range(w.steps):
+            sel, ev = gpu.trace.step()
+            gpu.sel_d.copy_(torch.from_numpy(np.ascontiguousarray(sel).view(np.int32)))
+            for g in range(w.n_groups):
+                gpu.cache.step_group(g, gpu.sel_d[g], gpu.outs[g], gpu.entry_row[g], gpu.req_off[g])
+                _, rnd = gpu.cache.layer_signal(g)
+                ro = orc.o.step_group(g, sel[g])
+                U = int(ro["req_off"][-1])
+                for j in range(L):
+                    ula.ula_debug_consume(gpu.cache.ctx, g, j, rnd, gpu.outs[g].data_ptr(),
+                                          gpu.cap, U, res[g, j].data_ptr(), side.cuda_stream)
+                exp = [int(ro["out"][j, :U].view(np.uint32).sum(dtype=np.uint64) & 0xFFFFFFFF)
+                       for j in range(L)]
+                torch.cuda.synchronize()
+                gpu.cache.sync()
+                r = res[g].cpu().numpy().astype(np.uint64)
+                ns = ula.ula_debug_layer_times(gpu.cache.ctx, g, L)
+                for j in range(L):
+                    assert r[j, 2] == 0, f"step {t} group {g} layer {j}: consumer timed out"
+                    assert int(r[j, 1]) == exp[j], f"step {t} group {g} layer {j}: checksum"
+                    assert r[j, 0] >= ns[j]  # it saw the flag after the flag was set
+                total += 1
+                early += int(r[0, 0] < ns[L - 1])  # layer 0 read before the last layer landed
+            apply_events(gpu.alloc, gpu.free, ev)
+            apply_events(orc.alloc, orc.free, ev)
+        print(f"layer-0 consumer started before the last layer was signalled in {early}/{total}")
+    finally:
+        gpu.close()
+
+
 def test_layer_signal_with_exact_lru():
     w = small("low_evict").replace(layer_signal=True, exact_lru=True, steps=24)
     run_parity(w, w.steps)
