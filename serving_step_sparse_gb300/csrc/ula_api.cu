@@ -346,6 +346,8 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
     ULA_CUDA(c->alloc(&d.hfc, geo.hd.n1));
     ULA_CUDA(c->alloc(&d.uniq, cfg.max_entries));
     ULA_CUDA(c->alloc(&d.row_slot, cfg.max_entries));
+    ULA_CUDA(c->alloc(&d.hitbits, geo.gd.n0));
+    ULA_CUDA(cudaMemsetAsync(d.hitbits, 0, sizeof(uint32_t) * geo.gd.n0, s));
     ULA_CUDA(c->alloc(&d.victims, c->decision_cap));
     ULA_CUDA(c->alloc(&d.wb_host, c->decision_cap));
     ULA_CUDA(c->alloc(&d.work, work_len));

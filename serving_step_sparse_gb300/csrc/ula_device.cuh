@@ -78,6 +78,7 @@ struct GroupDev {
   uint8_t *host_pool;  // [H][L][W], pinned host memory (device pointer)
   uint32_t *uniq;      // [max_entries]: this group's unique addresses of its last step
   uint32_t *row_slot;  // [max_entries]: GPU slot of unique row u if it hit, kNone if it missed
+  uint32_t *hitbits;   // [n0]: slots hit in this step (PB-LRU marking), cleared by the marking
   uint32_t *victims;   // [decision_cap]: victim i serves miss i (alloc: GPU slots)
   uint32_t *wb_host;   // [decision_cap]: host slot of write-back j (alloc: host slots)
   uint4 *work;         // [(B+1)*nseg + hseg]: (order position, segment, first rank, count)

@@ -37,6 +37,7 @@ constexpr int kScanThreads = 1024;
 constexpr int kEntryThreads = 1024;  // blocks of the per-entry kernels with block scans
 constexpr int kStampThreads = 256;
 constexpr int kWalkSegs = 4;        // segments per thread per step of the victim walk
+constexpr int kMarkClasses = 8;     // class words a marking warp loads at once
 
 // Launch shapes of the two persistent copy kernels (build-time tunables).
 #ifndef ULA_GATHER_THREADS
@@ -249,16 +250,17 @@ __global__ void k_dedup_stamp(StepParams p) {
 }
 
 struct Flags {
-  uint32_t a, first, miss;
+  uint32_t a, first, miss, m;  // m: the map entry of a first occurrence
 };
 
 __device__ __forceinline__ Flags entry_flags(const StepParams &p, uint32_t e) {
-  Flags f{kPad, 0, 0};
+  Flags f{kPad, 0, 0, kNone};
   if (e < p.E) {
     f.a = p.sel[e];
     if (f.a != kPad && p.tbl[f.a] == first_key(p.epoch, e)) {
       f.first = 1;
-      f.miss = (p.grp.map[f.a] & kHostBit) ? 1u : 0u;  // (2) translate
+      f.m = p.grp.map[f.a];
+      f.miss = (f.m & kHostBit) ? 1u : 0u;  // (2) translate
     }
   }
   return f;
@@ -397,8 +399,17 @@ __global__ void __launch_bounds__(kEntryThreads) k_rotate_emit(StepParams p) {
   p.addr_row[f.a] = pos;
   if (f.miss) {
     p.miss_list[mpos] = f.a;
-    p.miss_hs[mpos] = p.grp.map[f.a] & kSlotMask;
+    p.miss_hs[mpos] = f.m & kSlotMask;
     p.miss_row[mpos] = pos;
+    p.grp.row_slot[pos] = kNone;  // filled (and its output written) by the move
+  } else if (f.m >= geo.S) {
+    latch(p.status, ULA_ERR_INTERNAL);
+  } else {
+    // (3b) a hit: its slot for the gather, its access in this round, and (PB-LRU)
+    // its bit in the step's hit map, which the marking applies to the labels
+    p.grp.row_slot[pos] = f.m;
+    p.grp.stamp[f.m] = p.round;
+    if (!geo.exact) atomicOr(&p.grp.hitbits[f.m >> 5], 1u << (f.m & 31));
   }
 }
 
@@ -506,32 +517,63 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
   }
 }
 
-// (3b) every hit moves to the current bucket (clears on its old class, sets
-// on cur) and its slot is recorded for the gather; under exact LRU only its
-// timestamp changes.  The last block then walks the classes for the M victims
-// (exact LRU: the free class only).
+// (3b) Every hit moves to the current bucket (labels only), applied word by word:
+// one warp per segment takes the step's hit map for its 32 words and, class by
+// class, clears the hit bits on every other class and sets them on the current
+// bucket, then rewrites the segment's count and level-1 word (the warp owns both
+// for every class) and flips the level-2 bit if the segment's emptiness changed.
+// The hit map is cleared on the way.  (Exact LRU: hits only restamp, done by the
+// compaction.)  The last block then walks the classes for the M victims (exact
+// LRU: the free class only).
 __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
   if (block_skips(p.status)) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
-  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
-  const uint32_t U = g.cnt->U;
-  if (i < U) {
-    const uint32_t m = g.map[g.uniq[i]];
-    if (m & kHostBit) {
-      g.row_slot[i] = kNone;  // filled (and its output written) by the move
-    } else {
-      const uint32_t c = m < geo.S ? slot_class(geo, g.stamp[m], p.round) : geo.B + 1;
-      const uint32_t to = access_class(geo, p.cur);
-      if (c == geo.B + 1) {
-        latch(p.status, ULA_ERR_INTERNAL);
-      } else {
-        if (c != to) {
-          bm_clear(class_bitmap(g, geo, c), m);
-          bm_set(class_bitmap(g, geo, to), m);
+  if (!geo.exact) {
+    const uint32_t lane = lane_id();
+    const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (uint32_t sg = warp; sg < geo.nseg; sg += nwarps) {
+      const uint32_t w = sg * 32 + lane;
+      const bool valid = w < geo.gd.n0;
+      const uint32_t hw = valid ? g.hitbits[w] : 0u;
+      if (!__any_sync(0xffffffffu, hw != 0)) continue;
+      if (hw) g.hitbits[w] = 0;
+      for (uint32_t c0 = 0; c0 < geo.B + 2; c0 += kMarkClasses) {
+        uint32_t xs[kMarkClasses];
+#pragma unroll
+        for (int u = 0; u < kMarkClasses; ++u) {  // the classes' words, loaded at once
+          const uint32_t c = c0 + u;
+          xs[u] = valid && c < geo.B + 2 ? class_bitmap(g, geo, c).w0[w] : 0u;
         }
-        g.stamp[m] = p.round;
-        g.row_slot[i] = m;
+#pragma unroll
+        for (int u = 0; u < kMarkClasses; ++u) {
+          const uint32_t c = c0 + u;
+          if (c >= geo.B + 2) break;
+          const Bitmap bm = class_bitmap(g, geo, c);
+          const uint32_t x = xs[u];
+          if (c == geo.B + 1) {  // a hit's slot is never free
+            if (x & hw) latch(p.status, ULA_ERR_INTERNAL);
+            continue;
+          }
+          const uint32_t nx = c == p.cur ? (x | hw) : (x & ~hw);
+          if (!__any_sync(0xffffffffu, nx != x)) continue;
+          if (nx != x) bm.w0[w] = nx;
+          int d = (int)__popc(nx) - (int)__popc(x);
+#pragma unroll
+          for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+          const uint32_t nz = __ballot_sync(0xffffffffu, nx != 0);
+          if (lane == 0) {
+            bm.cnt[sg] += (uint32_t)d;
+            const uint32_t old1 = bm.w1[sg];
+            if (nz != old1) {
+              bm.w1[sg] = nz;
+              const uint32_t bit = 1u << (sg & 31);
+              if (old1 == 0) atomicOr(&bm.w2[sg >> 5], bit);       // segment became non-empty
+              else if (nz == 0) atomicAnd(&bm.w2[sg >> 5], ~bit);  // segment became empty
+            }
+          }
+        }
       }
     }
   }
@@ -1707,7 +1749,8 @@ cudaError_t launch_rotate_emit(const StepParams &p, cudaStream_t s) {
 }
 
 cudaError_t launch_mark_select(const StepParams &p, cudaStream_t s) {
-  const uint32_t nblk = div_up(p.E, kEntryThreads);
+  // one warp per segment of the class bitmaps (the marking), at least one block (the walk)
+  const uint32_t nblk = div_up(p.geo.nseg, kEntryThreads / 32);
   k_mark_select<<<nblk ? nblk : 1, kEntryThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
