@@ -59,6 +59,14 @@ constexpr int kGatherThreads = ULA_GATHER_THREADS;
 
 __device__ __forceinline__ void latch(int *status, int code) { atomicCAS(status, 0, code); }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may be scheduled before the previous kernel on its stream has
+// finished; pdl_wait() returns once that kernel has completed and its writes are
+// visible (at once for an ordinary launch), and pdl_launch() lets the next kernel
+// be scheduled as soon as every block of this one has issued it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long v;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(v));
@@ -235,6 +243,7 @@ __device__ __forceinline__ unsigned long long first_key(uint32_t epoch, uint32_t
 // (1) every entry proposes itself as its address's first occurrence; the
 // largest key of this epoch = the smallest entry index wins.
 __global__ void k_dedup_stamp(StepParams p) {
+  pdl_launch();
   if (*(volatile int *)p.status) return;
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   if (p.inject && e == 0) latch(p.status, p.inject);
@@ -270,6 +279,8 @@ __device__ __forceinline__ Flags entry_flags(const StepParams &p, uint32_t e) {
 // into exclusive offsets, totals U and M, and runs the capacity check -- no
 // state changes before it passes.
 __global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p) {
+  pdl_wait();
+  pdl_launch();
   if (block_skips(p.status)) return;
   if (p.geo.signal && p.E == 0 && blockIdx.x == 0 && threadIdx.x == 0)
     p.grp.layer_ns[p.grp.layers] = global_ns();  // step start (no entries: no stamp kernel)
@@ -345,6 +356,8 @@ __global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p
 // rotation -- the current bucket advances to `cur` and what is left in it folds
 // into the cold bucket (sets on cold, clears on the reused bucket; labels only).
 __global__ void __launch_bounds__(kEntryThreads) k_rotate_emit(StepParams p) {
+  pdl_wait();
+  pdl_launch();
   if (block_skips(p.status)) return;
   const Geometry &geo = p.geo;
   if (blockIdx.x >= p.emit_blocks) {
@@ -526,6 +539,8 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
 // compaction.)  The last block then walks the classes for the M victims (exact
 // LRU: the free class only).
 __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
+  pdl_wait();
+  pdl_launch();
   if (block_skips(p.status)) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -587,6 +602,8 @@ __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
 // [base, base + count); ranks below the quota are written out.  Host entries
 // claim their slots (clears only on the host-free bitmap; GPU classes read only).
 __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
+  pdl_wait();
+  pdl_launch();
   if (*(volatile int *)p.status) return;
   const GroupDev g = p.groups[p.group0 + blockIdx.y];
   const Geometry &geo = p.geo;
@@ -639,6 +656,7 @@ __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
 constexpr int kMoveUnroll = ULA_MOVE_UNROLL;
 
 __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) {
+  pdl_wait();  // (no early trigger: the commit's blocks would hold SM room for the whole move)
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -744,6 +762,7 @@ constexpr int kMoveLayerUnroll = 4;
 constexpr uint32_t kMoveBatch = ULA_MOVE_BATCH;  // chunks handed out at a time (a multiple of 32)
 
 __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move_layers(MoveParams p) {
+  pdl_wait();
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -833,6 +852,7 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move_layers(MovePar
 // sets on cur); the miss's host slot is released (sets only on the host-free
 // bitmap).  (1) The idle threads also write every entry's unique row.
 __global__ void k_commit(MoveParams p) {
+  pdl_wait();
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -1720,6 +1740,23 @@ __global__ void k_consume(const uint32_t *flag, uint32_t round, const uint8_t *o
 
 inline uint32_t div_up(uint64_t a, uint64_t b) { return (uint32_t)((a + b - 1) / b); }
 
+// A launch that may start while the previous kernel on the stream finishes (the
+// kernel calls pdl_wait() before it reads anything that kernel wrote).
+template <typename P>
+cudaError_t launch_dependent(void (*kernel)(P), dim3 grid, dim3 block, cudaStream_t s, const P &p) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 }  // namespace
 
 // --------------------------------------------------------------- launchers
@@ -1734,8 +1771,7 @@ cudaError_t launch_bitmap_fill(Bitmap b, uint32_t nbits, cudaStream_t s) {
 cudaError_t launch_dedup(const StepParams &p, cudaStream_t s) {
   const uint32_t nblk = div_up(p.E, kEntryThreads);
   if (nblk) k_dedup_stamp<<<div_up(p.E, kStampThreads), kStampThreads, 0, s>>>(p);
-  k_dedup_count_scan<<<nblk ? nblk : 1, kEntryThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(k_dedup_count_scan, dim3(nblk ? nblk : 1), dim3(kEntryThreads), s, p);
 }
 
 cudaError_t launch_rotate_emit(const StepParams &p, cudaStream_t s) {
@@ -1744,21 +1780,17 @@ cudaError_t launch_rotate_emit(const StepParams &p, cudaStream_t s) {
   const uint32_t words = p.geo.gd.n0 > p.geo.gd.n1 ? p.geo.gd.n0 : p.geo.gd.n1;
   uint32_t rot = p.geo.exact ? 0u : div_up(words, kEntryThreads * 4);
   const uint32_t grid = q.emit_blocks + rot;
-  k_rotate_emit<<<grid ? grid : 1, kEntryThreads, 0, s>>>(q);
-  return cudaGetLastError();
+  return launch_dependent(k_rotate_emit, dim3(grid ? grid : 1), dim3(kEntryThreads), s, q);
 }
 
 cudaError_t launch_mark_select(const StepParams &p, cudaStream_t s) {
   // one warp per segment of the class bitmaps (the marking), at least one block (the walk)
   const uint32_t nblk = div_up(p.geo.nseg, kEntryThreads / 32);
-  k_mark_select<<<nblk ? nblk : 1, kEntryThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(k_mark_select, dim3(nblk ? nblk : 1), dim3(kEntryThreads), s, p);
 }
 
 cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int blocks, cudaStream_t s) {
-  dim3 grid(blocks > 0 ? blocks : 1, n_groups);
-  k_select_emit<<<grid, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(k_select_emit, dim3(blocks > 0 ? blocks : 1, n_groups), dim3(256), s, p);
 }
 
 cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s) {
@@ -1773,10 +1805,10 @@ cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm) {
 }
 
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
-  if (p.geo.signal) k_move_layers<<<blocks, 256, 0, s>>>(p);
-  else k_move<<<blocks, 256, 0, s>>>(p);
-  k_commit<<<blocks, 256, 0, s>>>(p);  // grid-stride over the victims
-  return cudaGetLastError();
+  cudaError_t e = launch_dependent(p.geo.signal ? k_move_layers : k_move, dim3(blocks), dim3(256),
+                                   s, p);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(k_commit, dim3(blocks), dim3(256), s, p);  // grid-stride over the victims
 }
 
 cudaError_t launch_consume(const uint32_t *flag, uint32_t round, const uint8_t *out,
