@@ -87,6 +87,19 @@ def _configure(l):
     l.orc_lru_free.restype = i32
     l.orc_lru_step.argtypes = [p, u32, p, C.c_size_t, p]
     l.orc_lru_step.restype = i32
+    l.orc_tp_create.argtypes = [u32, u32, p, u32, u32, u32, u32, u32, u32]
+    l.orc_tp_create.restype = p
+    l.orc_tp_destroy.argtypes = [p]
+    l.orc_tp_alloc.argtypes = [p, u32, p, p]
+    l.orc_tp_alloc.restype = i32
+    l.orc_tp_free.argtypes = [p, u32, u32]
+    l.orc_tp_free.restype = i32
+    l.orc_tp_step_group.argtypes = [p, u32, p, u32, u32, u32, p, p, u32, p, p, p, p, p]
+    l.orc_tp_step_group.restype = i32
+    l.orc_tp_buffer.argtypes = [p, u32, u32, p, p, p, p, p]
+    l.orc_tp_buffer.restype = u32
+    l.orc_tp_partition.argtypes = [p, u32]
+    l.orc_tp_partition.restype = p
     return l
 
 
@@ -223,6 +236,109 @@ class Oracle:
             return np.zeros((0, self.layers[g], self.row_bytes), dtype=np.uint8)
         buf = (C.c_uint8 * n).from_address(self._l.orc_host_pool(self._h, g))
         return np.frombuffer(buf, dtype=np.uint8).reshape(self.H, self.layers[g], self.row_bytes)
+
+
+class OracleTP:
+    """TP mode emulated: P partitions (DP residency over t mod P) and, per rank and
+    group, a local buffer of remote rows."""
+
+    KEYS = ["uniq", "hits", "misses", "victims_free", "victims_cold", "victims_ring",
+            "writebacks", "rows_gathered", "bypassed"]
+
+    def __init__(self, row_bytes, layers_per_group, parts, gpu_slots, host_slots, ring_buckets,
+                 max_logical, buffer_slots, _lib=None):
+        self._l = _lib if _lib is not None else lib()
+        self.row_bytes = int(row_bytes)
+        self.layers = [int(x) for x in layers_per_group]
+        self.G, self.P = len(self.layers), int(parts)
+        self.S, self.H, self.B = int(gpu_slots), int(host_slots), int(ring_buckets)
+        self.max_logical, self.slots = int(max_logical), int(buffer_slots)
+        L = np.array(self.layers, dtype=np.uint32)
+        self._h = self._l.orc_tp_create(self.row_bytes, self.G, _ptr(L), self.P, self.S, self.H,
+                                        self.B, self.max_logical, self.slots)
+        if not self._h:
+            raise ValueError("bad TP oracle configuration")
+        self._keep = L
+
+    def close(self):
+        if self._h:
+            self._l.orc_tp_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def alloc(self, n: int, rows: np.ndarray | None) -> int:
+        """rows: per group, [n][L_g][row_bytes] in global address order."""
+        base = C.c_uint32(0)
+        if rows is not None:
+            rows = np.ascontiguousarray(rows, dtype=np.uint8)
+        rc = self._l.orc_tp_alloc(self._h, n, _ptr(rows), C.byref(base))
+        if rc:
+            raise OracleError(rc, "tp alloc")
+        return base.value
+
+    def free(self, base: int, n: int):
+        rc = self._l.orc_tp_free(self._h, base, n)
+        if rc:
+            raise OracleError(rc, "tp free")
+
+    def step_group(self, g: int, sel: np.ndarray, out_cap: int | None = None):
+        """Per rank r: res[r]["local"] (partition r's DP step on the entries it owns) and
+        res[r]["remote"] (rank r's buffer on the entries it does not own), each a dict of
+        out [L][cap][W], entry_row, req_off, counters."""
+        sel = np.ascontiguousarray(sel, dtype=np.uint32)
+        R, Q, K = sel.shape
+        cap = int(out_cap if out_cap is not None else max(1, sel.size))
+        L, P = self.layers[g], self.P
+        mk = lambda: {"out": np.zeros((L, cap, self.row_bytes), dtype=np.uint8),
+                      "entry_row": np.empty(sel.size, dtype=np.int32),
+                      "req_off": np.empty(R + 1, dtype=np.int32)}
+        loc, rem = [mk() for _ in range(P)], [mk() for _ in range(P)]
+        arr = lambda xs, k: (C.c_void_p * P)(*[x[k].ctypes.data for x in xs])
+        cnt = np.zeros((P, 2, 9), dtype=np.uint64)
+        rc = self._l.orc_tp_step_group(self._h, g, _ptr(sel), R, Q, K, arr(loc, "out"),
+                                       arr(rem, "out"), cap, arr(loc, "entry_row"),
+                                       arr(loc, "req_off"), arr(rem, "entry_row"),
+                                       arr(rem, "req_off"), _ptr(cnt))
+        if rc:
+            raise OracleError(rc, f"tp step_group({g})")
+        res = []
+        for r in range(P):
+            loc[r]["counters"] = dict(zip(self.KEYS, map(int, cnt[r, 0])))
+            rem[r]["counters"] = dict(zip(self.KEYS, map(int, cnt[r, 1])))
+            res.append({"local": loc[r], "remote": rem[r]})
+        return res
+
+    def buffer(self, r: int, g: int):
+        where = np.empty(self.max_logical, dtype=np.int64)
+        owner = np.empty(self.slots, dtype=np.uint32)
+        cls = np.empty(self.slots, dtype=np.int32)
+        victims = np.empty(max(1, self.slots), dtype=np.uint32)
+        cur = C.c_uint32(0)
+        n = self._l.orc_tp_buffer(self._h, r, g, _ptr(where), _ptr(owner), _ptr(cls), C.byref(cur),
+                                  _ptr(victims))
+        return {"where": where, "owner": owner, "cls": cls, "cur": cur.value,
+                "victims": victims[:n].copy()}
+
+    def partition(self, p: int) -> "Oracle":
+        """A non-owning view of partition p (its export and pools)."""
+        o = _PartitionView.__new__(_PartitionView)
+        o._l, o._h = self._l, self._l.orc_tp_partition(self._h, p)
+        o.row_bytes, o.layers, o.G = self.row_bytes, self.layers, self.G
+        o.S, o.H, o.B = self.S, self.H, self.B
+        o.max_logical = (self.max_logical + self.P - 1) // self.P
+        o.bypass = o.exact_lru = False
+        o._owner = self  # keeps the TP oracle alive while the view is used
+        return o
+
+
+class _PartitionView(Oracle):
+    """A partition of an OracleTP, seen as a DP oracle; it does not own the handle."""
+
+    def close(self):
+        self._h = None
+
+    __del__ = close
 
 
 class ExactLru:

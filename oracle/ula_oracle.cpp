@@ -45,6 +45,11 @@
 //     M' = min(M, S - hits, free GPU + free host slots) misses; each later
 //     miss is gathered straight from its host slot into the output and stays
 //     on the host;
+//   * TP mode (emulated, orc_tp_*): address t belongs to partition t mod P, a
+//     DP residency over local ids t / P; each rank keeps per group a local
+//     buffer of remote rows (PB-LRU over its own slots and ring, victims'
+//     copies dropped, misses fetched from the owner's GPU slot after the
+//     owner's step);
 //   * exact LRU (the baseline policy of §3's first paragraph, selectable in
 //     place of PB-LRU): every GPU slot keeps a timestamp, the round of its
 //     last access (a hit, a fill, or an alloc placement, which counts in the
@@ -598,5 +603,294 @@ int orc_lru_step(void *h, uint32_t gi, const uint32_t *sel, size_t n_entries, ui
   acc[1] += hits;
   return kOk;
 }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// TP mode, emulated (§2 "Unified logical addresses", TP paragraph): address t
+// belongs to partition t mod P (P partitions stand in for P GPUs).  Each
+// partition is a DP residency (the code above) over its own addresses, with
+// local ids t / P.  Each rank r keeps, per group, a local buffer of recently
+// selected remote rows (t mod P != r): PB-LRU over the buffer's own slots and
+// ring, a victim's copy is dropped (the owner keeps the entry), and a missing
+// row is fetched from its owner's GPU slot, where the owner's step has just made
+// it resident.
+
+namespace {
+struct Buffer {  // one rank's local buffer for one group
+  uint32_t layers = 0;
+  std::vector<int64_t> where;            // [max_logical]: buffer slot, or -1
+  std::vector<int> cls;                  // [slots]
+  std::vector<uint32_t> owner;           // [slots]
+  std::set<uint32_t> free_slots, cold;
+  std::vector<std::set<uint32_t>> ring;  // [B]
+  uint32_t cur = 0;
+  std::vector<uint8_t> pool;             // [slots][layers][row_bytes]
+  std::vector<uint32_t> last_victims;
+};
+
+struct Tp {
+  uint32_t P = 0, slots = 0, row_bytes = 0, n_groups = 0, max_logical = 0, B = 0;
+  std::vector<uint32_t> layers;
+  std::vector<Oracle *> parts;              // [P]
+  std::vector<std::vector<Buffer>> buf;     // [P ranks][G]
+  uint32_t next_logical = 0;
+};
+
+void buffer_to_current(Buffer &b, uint32_t s) {
+  int c = b.cls[s];
+  if (c == kFree) b.free_slots.erase(s);
+  else if (c == kCold) b.cold.erase(s);
+  else b.ring[(size_t)c].erase(s);
+  b.ring[b.cur].insert(s);
+  b.cls[s] = (int)b.cur;
+}
+
+// The rows of partition p among global addresses [base, base + n), per group, as
+// the partition's alloc wants them (its local ids are consecutive).
+std::vector<uint8_t> partition_rows(const Tp &t, uint32_t p, uint32_t base, uint32_t n,
+                                    const uint8_t *rows, uint32_t *n_p) {
+  std::vector<uint8_t> out;
+  uint32_t cnt = 0;
+  for (uint32_t a = base; a < base + n; ++a)
+    if (a % t.P == p) ++cnt;
+  size_t group_off = 0;
+  for (uint32_t g = 0; g < t.n_groups; ++g) {
+    const size_t sb = (size_t)t.layers[g] * t.row_bytes;
+    for (uint32_t a = base; a < base + n; ++a)
+      if (a % t.P == p) {
+        const uint8_t *src = rows + group_off + (size_t)(a - base) * sb;
+        out.insert(out.end(), src, src + sb);
+      }
+    group_off += (size_t)n * sb;
+  }
+  *n_p = cnt;
+  return out;
+}
+}  // namespace
+
+extern "C" {
+
+void *orc_tp_create(uint32_t row_bytes, uint32_t n_groups, const uint32_t *layers, uint32_t P,
+                    uint32_t S, uint32_t H, uint32_t B, uint32_t max_logical, uint32_t slots) {
+  if (!P || !slots || !max_logical) return nullptr;
+  Tp *t = new Tp;
+  t->P = P;
+  t->slots = slots;
+  t->row_bytes = row_bytes;
+  t->n_groups = n_groups;
+  t->max_logical = max_logical;
+  t->B = B;
+  t->layers.assign(layers, layers + n_groups);
+  const uint32_t local_max = (max_logical + P - 1) / P;
+  for (uint32_t p = 0; p < P; ++p) {
+    void *o = orc_create2(row_bytes, n_groups, layers, S, H, B, local_max, 0);
+    if (!o) {
+      for (Oracle *x : t->parts) delete x;
+      delete t;
+      return nullptr;
+    }
+    t->parts.push_back(static_cast<Oracle *>(o));
+  }
+  t->buf.resize(P);
+  for (uint32_t r = 0; r < P; ++r) {
+    t->buf[r].resize(n_groups);
+    for (uint32_t g = 0; g < n_groups; ++g) {
+      Buffer &b = t->buf[r][g];
+      b.layers = layers[g];
+      b.where.assign(max_logical, -1);
+      b.cls.assign(slots, kFree);
+      b.owner.assign(slots, kNone);
+      for (uint32_t s = 0; s < slots; ++s) b.free_slots.insert(s);
+      b.ring.assign(B, std::set<uint32_t>{});
+      b.pool.assign((size_t)slots * layers[g] * row_bytes, 0);
+    }
+  }
+  return t;
+}
+
+void orc_tp_destroy(void *h) {
+  Tp *t = static_cast<Tp *>(h);
+  for (Oracle *o : t->parts) delete o;
+  delete t;
+}
+
+// rows: per group, [n][layers_g][row_bytes] in global address order.
+int orc_tp_alloc(void *h, uint32_t n, const uint8_t *rows, uint32_t *base_out) {
+  Tp *t = static_cast<Tp *>(h);
+  if (!base_out || (n && !rows)) return kInvalidArg;
+  if ((uint64_t)t->next_logical + n > t->max_logical) return kCapacity;
+  const uint32_t base = t->next_logical;
+  for (uint32_t p = 0; p < t->P; ++p) {
+    uint32_t n_p = 0;
+    std::vector<uint8_t> r = partition_rows(*t, p, base, n, rows, &n_p);
+    uint32_t local_base = 0;
+    const int rc = orc_alloc(t->parts[p], n_p, n_p ? r.data() : nullptr, &local_base);
+    if (rc) return rc;  // (earlier partitions keep their part: TP errors are not atomic)
+  }
+  t->next_logical = base + n;
+  *base_out = base;
+  return kOk;
+}
+
+int orc_tp_free(void *h, uint32_t base, uint32_t n) {
+  Tp *t = static_cast<Tp *>(h);
+  if ((uint64_t)base + n > t->max_logical) return kInvalidArg;
+  for (uint32_t p = 0; p < t->P; ++p) {
+    // partition p's addresses in the range are consecutive local ids
+    uint32_t first = base, cnt = 0;
+    while (first < base + n && first % t->P != p) ++first;
+    for (uint32_t a = first; a < base + n; a += t->P) ++cnt;
+    if (cnt) {
+      const int rc = orc_free(t->parts[p], first / t->P, cnt);
+      if (rc) return rc;
+    }
+  }
+  for (auto &per_rank : t->buf)  // buffered copies of freed addresses are dropped
+    for (Buffer &b : per_rank)
+      for (uint32_t a = base; a < base + n; ++a)
+        if (b.where[a] >= 0) {
+          const uint32_t s = (uint32_t)b.where[a];
+          int c = b.cls[s];
+          if (c == kCold) b.cold.erase(s);
+          else if (c != kFree) b.ring[(size_t)c].erase(s);
+          b.free_slots.insert(s);
+          b.cls[s] = kFree;
+          b.owner[s] = kNone;
+          b.where[a] = -1;
+        }
+  return kOk;
+}
+
+// One TP step of group gi.  For partition (and rank) r: local_out[r], local_entry_row[r],
+// local_req_off[r] are partition r's DP step on the entries it owns (the others as pads,
+// addresses as local ids); remote_out[r], remote_entry_row[r], remote_req_off[r] are rank
+// r's buffer step on the entries it does not own.  counters (optional) [P][2][9]: the DP
+// counters of partition r, then the buffer's (uniq, hits, misses, victims from free, cold,
+// ring, 0, rows gathered, 0).
+int orc_tp_step_group(void *h, uint32_t gi, const uint32_t *sel, uint32_t n_req, uint32_t q,
+                      uint32_t k, uint8_t *const *local_out, uint8_t *const *remote_out,
+                      uint32_t out_cap, int32_t *const *local_entry_row,
+                      int32_t *const *local_req_off, int32_t *const *remote_entry_row,
+                      int32_t *const *remote_req_off, uint64_t *counters) {
+  Tp *t = static_cast<Tp *>(h);
+  if (gi >= t->n_groups) return kInvalidArg;
+  const size_t E = (size_t)n_req * q * k;
+  const uint32_t P = t->P;
+  // (1) every partition steps on the entries it owns
+  std::vector<uint32_t> part_sel(E);
+  for (uint32_t p = 0; p < P; ++p) {
+    for (size_t e = 0; e < E; ++e)
+      part_sel[e] = (sel[e] != kPad && sel[e] % P == p) ? sel[e] / P : kPad;
+    const int rc = orc_step_group(t->parts[p], gi, part_sel.data(), n_req, q, k, local_out[p],
+                                  out_cap, local_entry_row[p], local_req_off[p],
+                                  counters ? counters + (size_t)p * 18 : nullptr);
+    if (rc) return rc;
+  }
+  // (2) every rank's buffer takes the entries it does not own
+  for (uint32_t r = 0; r < P; ++r) {
+    Buffer &b = t->buf[r][gi];
+    const size_t sb = (size_t)b.layers * t->row_bytes;
+    std::vector<uint32_t> uniq;
+    std::unordered_map<uint32_t, int32_t> row_of;
+    int32_t *er = remote_entry_row[r];
+    int32_t *ro = remote_req_off[r];
+    for (uint32_t rq = 0; rq < n_req; ++rq) {
+      ro[rq] = (int32_t)uniq.size();
+      for (size_t e = (size_t)rq * q * k; e < (size_t)(rq + 1) * q * k; ++e) {
+        const uint32_t a = sel[e];
+        if (a == kPad || a % P == r) continue;
+        if (row_of.find(a) == row_of.end()) {
+          row_of.emplace(a, (int32_t)uniq.size());
+          uniq.push_back(a);
+        }
+      }
+    }
+    ro[n_req] = (int32_t)uniq.size();
+    for (size_t e = 0; e < E; ++e)
+      er[e] = (sel[e] == kPad || sel[e] % P == r) ? -1 : row_of[sel[e]];
+    std::vector<uint32_t> misses;
+    size_t hits = 0;
+    for (uint32_t a : uniq) {
+      if (b.where[a] >= 0) ++hits;
+      else misses.push_back(a);
+    }
+    if (uniq.size() > out_cap || misses.size() > t->slots - hits) return kCapacity;
+    // rotate, then hits into the current bucket
+    b.cur = (b.cur + 1) % t->B;
+    for (uint32_t s : b.ring[b.cur]) {
+      b.cold.insert(s);
+      b.cls[s] = kCold;
+    }
+    b.ring[b.cur].clear();
+    for (uint32_t a : uniq)
+      if (b.where[a] >= 0) buffer_to_current(b, (uint32_t)b.where[a]);
+    // victims: free, cold, ring oldest -> newest, lowest slot first
+    std::vector<uint32_t> victims;
+    std::vector<int> vcls;
+    auto take = [&](const std::set<uint32_t> &from, int label) {
+      for (uint32_t s : from) {
+        if (victims.size() == misses.size()) return;
+        victims.push_back(s);
+        vcls.push_back(label);
+      }
+    };
+    take(b.free_slots, kFree);
+    take(b.cold, kCold);
+    for (uint32_t d = 1; d < t->B; ++d) take(b.ring[(b.cur + d) % t->B], (int)((b.cur + d) % t->B));
+    if (victims.size() != misses.size()) return kInternal;
+    uint64_t n_free = 0, n_cold = 0;
+    for (size_t i = 0; i < misses.size(); ++i) {
+      const uint32_t v = victims[i], a = misses[i];
+      if (vcls[i] == kFree) ++n_free;
+      else if (vcls[i] == kCold) ++n_cold;
+      if (b.owner[v] != kNone) b.where[b.owner[v]] = -1;  // the copy is dropped
+      // fetch from the owner partition's GPU slot (resident after its step)
+      const Oracle *o = t->parts[a % P];
+      const Group &og = o->groups[gi];
+      const Location loc = og.where[a / P];
+      if (loc.tier != kOnGpu) return kInternal;
+      std::memcpy(&b.pool[(size_t)v * sb], &og.gpu_pool[(size_t)loc.slot * sb], sb);
+      b.where[a] = v;
+      b.owner[v] = a;
+      buffer_to_current(b, v);
+    }
+    b.last_victims = victims;
+    for (uint32_t j = 0; j < b.layers; ++j)
+      for (size_t u = 0; u < uniq.size(); ++u)
+        std::memcpy(remote_out[r] + ((size_t)j * out_cap + u) * t->row_bytes,
+                    &b.pool[(size_t)b.where[uniq[u]] * sb + (size_t)j * t->row_bytes], t->row_bytes);
+    if (counters) {
+      uint64_t *c = counters + (size_t)r * 18 + 9;
+      c[0] = uniq.size();
+      c[1] = hits;
+      c[2] = misses.size();
+      c[3] = n_free;
+      c[4] = n_cold;
+      c[5] = misses.size() - n_free - n_cold;
+      c[6] = 0;
+      c[7] = (uint64_t)uniq.size() * b.layers;
+      c[8] = 0;
+    }
+  }
+  return kOk;
+}
+
+// Rank r's buffer of group gi: where [max_logical] (slot or -1), owner/cls [slots], cur;
+// returns the number of victims of its last step (copied to victims if given).
+uint32_t orc_tp_buffer(void *h, uint32_t r, uint32_t gi, int64_t *where, uint32_t *owner,
+                       int32_t *cls, uint32_t *cur, uint32_t *victims) {
+  Tp *t = static_cast<Tp *>(h);
+  const Buffer &b = t->buf[r][gi];
+  if (where) std::copy(b.where.begin(), b.where.end(), where);
+  if (owner) std::copy(b.owner.begin(), b.owner.end(), owner);
+  if (cls) std::copy(b.cls.begin(), b.cls.end(), cls);
+  if (cur) *cur = b.cur;
+  if (victims) std::copy(b.last_victims.begin(), b.last_victims.end(), victims);
+  return (uint32_t)b.last_victims.size();
+}
+
+// Partition p's oracle handle (for its export / pools).
+void *orc_tp_partition(void *h, uint32_t p) { return static_cast<Tp *>(h)->parts[p]; }
 
 }  // extern "C"

@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_tp as tp_pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ula_oracle.cpp")
 
@@ -23,7 +24,8 @@ MUTATIONS = [
     ("no fold into cold", "for (uint32_t s : g.ring[g.cur]) {", "for (uint32_t s : std::set<uint32_t>{}) {"),
     ("cold after ring", "    take(g.cold, kCold);\n    for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));",
      "    for (uint32_t d = 1; d < o->B; ++d) take(g.ring[(g.cur + d) % o->B], (int)((g.cur + d) % o->B));\n    take(g.cold, kCold);"),
-    ("highest slot first", "    for (uint32_t s : from) {", "    for (auto it = from.rbegin(); it != from.rend(); ++it) { uint32_t s = *it;"),
+    ("highest slot first", "    for (uint32_t s : from) {\n      if (victims.size() == M) return;",
+     "    for (auto it = from.rbegin(); it != from.rend(); ++it) { uint32_t s = *it;\n      if (victims.size() == M) return;"),
     ("write-back to highest free host slot", "  for (uint32_t hs : g.host_free) {\n    if (wb_host.size()",
      "  for (auto it = g.host_free.rbegin(); it != g.host_free.rend(); ++it) { uint32_t hs = *it;\n    if (wb_host.size()"),
     ("evicted owner's map not updated", "      g.where[prev_owner] = Location{kOnHost, hs};\n", ""),
@@ -48,6 +50,11 @@ MUTATIONS = [
      "    g.by_age.insert({g.stamp[s] == kNone ? g.round : g.stamp[s], s});\n  } else {"),
     ("timestamps of alloc placements one round late", "  g.stamp[s] = g.round;\n}",
      "  g.stamp[s] = g.round + (g.owner[s] == kNone ? 1u : 0u);\n}"),
+    ("TP buffer: ring newest first", "take(b.ring[(b.cur + d) % t->B], (int)((b.cur + d) % t->B));",
+     "take(b.ring[(b.cur + t->B - d) % t->B], (int)((b.cur + t->B - d) % t->B));"),
+    ("TP buffer: evicted copy still mapped", "      if (b.owner[v] != kNone) b.where[b.owner[v]] = -1;  // the copy is dropped\n", ""),
+    ("TP fetch from the neighbouring partition", "      const Oracle *o = t->parts[a % P];",
+     "      const Oracle *o = t->parts[(a + 1) % P];"),
 ]
 
 
@@ -63,6 +70,9 @@ def _fast_pins():
         pins.test_exact_lru_matches_timestamp_model(seed)
     for seed in range(0, 40, 5):
         pins.test_exact_lru_bypass_matches_timestamp_model(seed)
+    for seed in range(0, 60, 6):
+        tp_pins.test_tp_buffer_matches_timestamp_model(seed)
+    tp_pins.test_tp_one_partition_is_the_dp_oracle()
     pins.test_rotation_only_relabels()
     pins.test_errors_leave_state_untouched()
     pins.test_alloc_placement_and_free()
