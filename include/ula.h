@@ -350,6 +350,59 @@ int ula_profile_read(ula_ctx *ctx, ula_profile *out, int reset);
 int ula_dedup_noalloc(const uint32_t *d_sel, uint32_t n, uint32_t *d_uniq,
                       int32_t *d_entry_row, uint32_t *d_n_uniq, void *stream);
 
+/*
+ * TP mode, emulated on one GPU (§2 "Unified logical addresses", TP paragraph): the
+ * pools of P GPUs form one distributed address space in which logical address t
+ * lives on "GPU" t mod P; each computing GPU keeps a local buffer of recently
+ * selected KV from the others.  Here P partitions of this GPU stand in for the P
+ * GPUs: partition p is a DP residency context (everything above) over local ids
+ * t / P with its own GPU and host pools, and rank r's local buffer (per group) holds
+ * copies of remote rows (t mod P != r) in buffer_slots slots under PB-LRU, evicted
+ * copies dropped (the owner keeps the entry); a missing row is fetched from its
+ * owner partition's GPU slot, where the owner's step has just made it resident (the
+ * cross-GPU copy of TP mode, here a copy inside HBM).  Limits: 1 <= P <= 8; TP with
+ * ULA_FLAG_LAYER_SIGNAL or ULA_FLAG_EXACT_LRU is not supported (INVALID_ARG).
+ *
+ * ula_tp_create -- cfg: per partition (gpu_slots, host_slots per partition; max_logical
+ *   and max_entries global).  gpu_pools, host_pools: host arrays [P * G] (partition-
+ *   major) of pools as for ula_create; buffer_pools: [P * G] device pools of
+ *   [buffer_slots][L_g][row_bytes] (rank-major).  stream: the home stream.  Creates
+ *   2P contexts and 2P streams; the pools stay caller-owned.
+ * ula_tp_alloc -- rows: per group [n][L_g][row_bytes] for global addresses
+ *   [base, base + n), device-accessible; each partition takes its every-P-th rows.
+ *   Not atomic across partitions: an error can leave earlier partitions allocated.
+ * ula_tp_free -- frees the range in every partition and drops every buffered copy.
+ * ula_tp_step_group -- one TP step of `group` for the whole selection d_sel (device
+ *   [n_req][q][k], global addresses): partition p runs a DP step on the entries it owns
+ *   (others as pads, addresses as local ids), writing d_local_out[p] (rows of its own
+ *   addresses, first-occurrence order), d_local_entry_row[p], d_local_req_off[p]; then
+ *   rank r's buffer takes the entries it does not own, writing d_remote_out[r],
+ *   d_remote_entry_row[r], d_remote_req_off[r] (as for ula_step_group; -1 for pads and
+ *   for the other side's entries).  Host arrays of P device pointers each; all outputs
+ *   [L_g][out_cap_rows][row_bytes].  The partitions run concurrently on their own
+ *   streams, the buffers after all of them; `stream` continues after everything.
+ *   Device errors latch in the context that met them and are returned by ula_tp_sync.
+ * ula_tp_sync -- waits for every context; stats (optional, host [2P]): partition
+ *   p's counters at [p], rank r's buffer counters at [P + r] (bytes_h2d = fetched bytes).
+ * ula_tp_context -- the context of partition `index` (kind 0) or of rank `index`'s
+ *   buffer (kind 1), for the diagnostics above; owned by the TP object.
+ */
+typedef struct ula_tp ula_tp;
+int ula_tp_create(const ula_config *cfg, uint32_t parts, uint32_t buffer_slots,
+                  void *const *gpu_pools, void *const *host_pools, void *const *buffer_pools,
+                  void *stream, ula_tp **out);
+int ula_tp_alloc(ula_tp *tp, uint32_t n, const void *rows, uint32_t *logical_base);
+int ula_tp_free(ula_tp *tp, uint32_t base, uint32_t n);
+int ula_tp_step_group(ula_tp *tp, uint32_t group, const uint32_t *d_sel, uint32_t n_req,
+                      uint32_t q, uint32_t k, void *const *d_local_out,
+                      void *const *d_remote_out, uint32_t out_cap_rows,
+                      int32_t *const *d_local_entry_row, int32_t *const *d_local_req_off,
+                      int32_t *const *d_remote_entry_row, int32_t *const *d_remote_req_off,
+                      void *stream);
+int ula_tp_sync(ula_tp *tp, ula_stats *stats);
+ula_ctx *ula_tp_context(ula_tp *tp, int kind, uint32_t index);
+int ula_tp_destroy(ula_tp *tp);
+
 #ifdef __cplusplus
 }
 #endif

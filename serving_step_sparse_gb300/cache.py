@@ -181,3 +181,98 @@ class UlaCache:
 
     def inject(self, code: int):
         ula.ula_debug_inject(self.ctx, code)
+
+
+class _ContextView(UlaCache):
+    """A context owned by a UlaTP, with UlaCache's diagnostics (export); not owned."""
+
+    def __init__(self, ctx: int, gpu_slots: int, host_slots: int, max_logical: int,
+                 max_entries: int, layers, row_bytes: int, ring_buckets: int, device):
+        self.ctx = ctx
+        self.S, self.H, self.B = gpu_slots, host_slots, ring_buckets
+        self.max_logical, self.max_entries = max_logical, max_entries
+        self.layers, self.W, self.G = list(layers), row_bytes, len(layers)
+        self.device = device
+        self._host_bufs = []
+        self.layout = ula.ula_debug_layout_get(ctx)
+
+    def close(self):
+        self.ctx = None
+
+
+class UlaTP:
+    """TP mode emulated on one GPU: P partitions (address t on partition t mod P), each a
+    DP residency with its own GPU and pinned host pools, and per rank a local buffer of
+    remote rows (buffer_slots slots per group) filled from the owners' GPU pools."""
+
+    def __init__(self, *, row_bytes: int, layers_per_group, parts: int, gpu_slots: int,
+                 host_slots: int, ring_buckets: int, max_logical: int, max_entries: int,
+                 buffer_slots: int, device="cuda", stream: torch.cuda.Stream | None = None,
+                 huge_host_pages: bool = True):
+        self.device = torch.device(device)
+        self.W, self.layers, self.P = int(row_bytes), [int(x) for x in layers_per_group], int(parts)
+        self.G = len(self.layers)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        P, S, H = self.P, int(gpu_slots), int(host_slots)
+        self.gpu_pools = [torch.empty(S * L * self.W, dtype=torch.uint8, device=self.device)
+                          for _ in range(P) for L in self.layers]
+        self._host_bufs = ([PinnedHostBuffer(H * L * self.W, huge_host_pages)
+                            for _ in range(P) for L in self.layers] if H else [])
+        self.buffer_pools = [torch.empty(int(buffer_slots) * L * self.W, dtype=torch.uint8,
+                                         device=self.device)
+                             for _ in range(P) for L in self.layers]
+        cfg = ula.make_config(self.W, self.layers, S, H, int(ring_buckets), int(max_logical),
+                              int(max_entries), 0)
+        with torch.cuda.device(self.device):
+            self.tp = ula.ula_tp_create(cfg, P, int(buffer_slots),
+                                        [t.data_ptr() for t in self.gpu_pools],
+                                        [b.tensor.data_ptr() for b in self._host_bufs] if H else None,
+                                        [t.data_ptr() for t in self.buffer_pools],
+                                        self.stream.cuda_stream)
+        local_max = (int(max_logical) + P - 1) // P
+        self.parts = [_ContextView(ula.ula_tp_context(self.tp, 0, p), S, H, local_max,
+                                   int(max_entries), self.layers, self.W, int(ring_buckets),
+                                   self.device) for p in range(P)]
+        self.buffers = [_ContextView(ula.ula_tp_context(self.tp, 1, r), int(buffer_slots), 0,
+                                     int(max_logical), int(max_entries), self.layers, self.W,
+                                     int(ring_buckets), self.device) for r in range(P)]
+
+    def alloc(self, n: int, rows: torch.Tensor) -> int:
+        """rows: pinned host or device uint8, per group [n][L_g][W] in global order."""
+        return ula.ula_tp_alloc(self.tp, n, rows.data_ptr())
+
+    def free(self, base: int, n: int):
+        ula.ula_tp_free(self.tp, base, n)
+
+    def step_group(self, g: int, sel: torch.Tensor, local_out, remote_out, local_entry_row,
+                   local_req_off, remote_entry_row, remote_req_off):
+        """sel: device int32 view of uint32 [R][Q][k]; the rest: lists of P device tensors."""
+        R, Q, K = sel.shape
+        cap = local_out[0].shape[1]
+        ula.ula_tp_step_group(self.tp, g, sel.data_ptr(), R, Q, K,
+                              [t.data_ptr() for t in local_out], [t.data_ptr() for t in remote_out],
+                              cap, [t.data_ptr() for t in local_entry_row],
+                              [t.data_ptr() for t in local_req_off],
+                              [t.data_ptr() for t in remote_entry_row],
+                              [t.data_ptr() for t in remote_req_off], self.stream.cuda_stream)
+
+    def sync(self) -> list:
+        """[2P] counter dicts: partitions, then the ranks' buffers."""
+        return ula.ula_tp_sync(self.tp, self.P)
+
+    def out_buffer(self, g: int, cap: int) -> torch.Tensor:
+        return torch.empty((self.layers[g], cap, self.W), dtype=torch.uint8, device=self.device)
+
+    def close(self):
+        if getattr(self, "tp", None):
+            ula.ula_tp_destroy(self.tp)
+            self.tp = None
+        for b in getattr(self, "_host_bufs", []):
+            b.close()
+        self._host_bufs = []
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

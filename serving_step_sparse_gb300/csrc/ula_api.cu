@@ -22,6 +22,9 @@ using namespace ula;
 namespace {
 
 constexpr uint32_t kAllocChunk = 65536;
+// Internal: a TP rank's local buffer (misses fetched from the owner partitions,
+// evicted copies dropped).  Not accepted by the public ula_create.
+constexpr uint32_t kFlagCacheInternal = 1u << 31;
 
 #define ULA_CUDA(call)                      \
   do {                                      \
@@ -54,6 +57,7 @@ struct ula_ctx {
   uint32_t *addr_row = nullptr;
   uint2 *blk = nullptr;
   uint32_t *miss_list = nullptr, *miss_hs = nullptr, *miss_row = nullptr;
+  TpSource tp_src[ULA_MAX_GROUPS] = {};  // TP local buffer: the owner partitions per group
   LruScratch lru{};     // exact LRU's scan scratch (ULA_FLAG_EXACT_LRU only)
   int lru_blocks = 0;   // its cooperative grid
   int *status = nullptr;
@@ -247,6 +251,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   geo.bypass = (cfg.flags & ULA_FLAG_BYPASS_OVERFLOW) ? 1u : 0u;
   geo.exact = (cfg.flags & ULA_FLAG_EXACT_LRU) ? 1u : 0u;
   geo.signal = (cfg.flags & ULA_FLAG_LAYER_SIGNAL) ? 1u : 0u;
+  geo.cache = (cfg.flags & kFlagCacheInternal) ? 1u : 0u;
   geo.gd = dims_for(S);
   geo.hd = dims_for(H);
   geo.nseg = geo.gd.n1;
@@ -405,14 +410,16 @@ const char *ula_error_string(int code) {
   }
 }
 
-int ula_create(const ula_config *cfg, void *const *gpu_pools, void *const *host_pools,
-               void *stream, ula_ctx **out) {
+// internal_flags: kFlagCacheInternal for a TP rank's local buffer
+static int create_ctx(const ula_config *cfg, void *const *gpu_pools, void *const *host_pools,
+                      void *stream, uint32_t internal_flags, ula_ctx **out) {
   if (!out) return ULA_ERR_INVALID_ARG;
   *out = nullptr;
   int rc = validate_config(cfg);
   if (rc) return rc;
   ula_ctx *c = new ula_ctx;
   c->cfg = *cfg;
+  c->cfg.flags |= internal_flags;
   c->home = static_cast<cudaStream_t>(stream);
   rc = create_impl(c, gpu_pools, host_pools);
   if (rc) {
@@ -425,7 +432,16 @@ int ula_create(const ula_config *cfg, void *const *gpu_pools, void *const *host_
   return ULA_OK;
 }
 
-int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) {
+int ula_create(const ula_config *cfg, void *const *gpu_pools, void *const *host_pools,
+               void *stream, ula_ctx **out) {
+  return create_ctx(cfg, gpu_pools, host_pools, stream, 0, out);
+}
+
+// rows: per group, `total` rows [total][L_g][W]; address i of this call is row
+// phase + i * stride (stride 1, phase 0 for ula_alloc; a TP partition takes every
+// P-th row of the TP call's range).
+static int alloc_impl(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base,
+                      uint32_t total, uint32_t phase, uint32_t stride) {
   if (!c || !logical_base) return ULA_ERR_INVALID_ARG;
   if (c->poisoned) return ULA_ERR_POISONED;
   const ula_config &cfg = c->cfg;
@@ -463,10 +479,11 @@ int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) 
     unsigned long long acc = 0;
     for (uint32_t g = 0; g < cfg.n_groups; ++g) {
       const unsigned long long sb = (unsigned long long)cfg.layers_per_group[g] * cfg.row_bytes;
-      ap.group_off[g] = acc + (unsigned long long)off * sb;
+      ap.group_off[g] = acc + ((unsigned long long)phase + (unsigned long long)off * stride) * sb;
       ap.round[g] = c->round[g];
-      acc += (unsigned long long)n * sb;
+      acc += (unsigned long long)total * sb;
     }
+    ap.row_stride = stride;
     ap.base = base + off;
     ap.n = m;
     ap.status = c->status;
@@ -480,12 +497,21 @@ int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) 
   return ULA_OK;
 }
 
-int ula_free(ula_ctx *c, uint32_t base, uint32_t n) {
+int ula_alloc(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logical_base) {
+  return alloc_impl(c, n, rows, logical_base, n, 0, 1);
+}
+
+// drop: a TP local buffer forgets any copies of [base, base + n) (no live check)
+static int free_impl(ula_ctx *c, uint32_t base, uint32_t n, bool drop) {
   if (!c) return ULA_ERR_INVALID_ARG;
   if (c->poisoned) return ULA_ERR_POISONED;
-  if ((uint64_t)base + n > c->next_logical) return ULA_ERR_INVALID_ARG;
-  for (uint32_t i = 0; i < n; ++i)
-    if (!c->live[base + i]) return ULA_ERR_INVALID_ARG;
+  if (!drop) {
+    if ((uint64_t)base + n > c->next_logical) return ULA_ERR_INVALID_ARG;
+    for (uint32_t i = 0; i < n; ++i)
+      if (!c->live[base + i]) return ULA_ERR_INVALID_ARG;
+  } else if ((uint64_t)base + n > c->cfg.max_logical) {
+    return ULA_ERR_INVALID_ARG;
+  }
   if (n == 0) return ULA_OK;
   ULA_CUDA(c->ensure_device());
   cudaStream_t s = c->crit;
@@ -500,10 +526,14 @@ int ula_free(ula_ctx *c, uint32_t base, uint32_t n) {
   fp.status = c->status;
   ULA_CUDA(c->phase(ULA_PHASE_FREE, s, 1, [&] { return launch_free(fp, c->cfg.n_groups, s); }));
   ULA_CUDA(c->leave(c->home));
-  for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 0;
-  c->live_count -= n;
+  if (!drop) {
+    for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 0;
+    c->live_count -= n;
+  }
   return ULA_OK;
 }
+
+int ula_free(ula_ctx *c, uint32_t base, uint32_t n) { return free_impl(c, base, n, false); }
 
 int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n_req, uint32_t q,
                    uint32_t k, void *d_out, uint32_t out_cap_rows, int32_t *d_entry_row,
@@ -552,6 +582,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.miss_list = c->miss_list;
   p.miss_hs = c->miss_hs;
   p.miss_row = c->miss_row;
+  p.src = c->tp_src[group];
   p.status = c->status;
   c->inject = 0;
   p.order.n_cls = B + 1;  // victims: free, cold, ring oldest (cur+1) .. newest (cur-1)
@@ -629,6 +660,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   mp.out_cap = out_cap_rows;
   mp.round = r;
   mp.cur = cur;
+  mp.src = c->tp_src[group];
   mp.status = c->status;
   ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, 2, [&] { return launch_move(mp, c->move_blocks, s); }));
   // signal: the commit event; layer j is ready once its hit rows are gathered too
@@ -858,6 +890,202 @@ int ula_debug_inject(ula_ctx *c, int code) {
   if (!c) return ULA_ERR_INVALID_ARG;
   if (c->poisoned) return ULA_ERR_POISONED;
   c->inject = code;
+  return ULA_OK;
+}
+
+
+// ------------------------------------------------------------------ TP mode
+
+struct ula_tp {
+  uint32_t P = 0, G = 0;
+  ula_config cfg{};
+  std::vector<ula_ctx *> parts, bufs;
+  std::vector<cudaStream_t> ps, bs;
+  std::vector<cudaEvent_t> pdone, bdone;
+  cudaEvent_t split_evt = nullptr;
+  uint32_t *sel = nullptr;  // [2P][max_entries]: partitions' entries, then buffers'
+  uint32_t next_logical = 0;
+};
+
+static void tp_release(ula_tp *t) {
+  for (ula_ctx *c : t->parts) ula_destroy(c);
+  for (ula_ctx *c : t->bufs) ula_destroy(c);
+  for (cudaStream_t s : t->ps) cudaStreamDestroy(s);
+  for (cudaStream_t s : t->bs) cudaStreamDestroy(s);
+  for (cudaEvent_t e : t->pdone) cudaEventDestroy(e);
+  for (cudaEvent_t e : t->bdone) cudaEventDestroy(e);
+  if (t->split_evt) cudaEventDestroy(t->split_evt);
+  if (t->sel) cudaFree(t->sel);
+  delete t;
+}
+
+int ula_tp_create(const ula_config *cfg, uint32_t parts, uint32_t buffer_slots,
+                  void *const *gpu_pools, void *const *host_pools, void *const *buffer_pools,
+                  void *stream, ula_tp **out) {
+  if (!out || !cfg || parts == 0 || parts > kMaxParts || buffer_slots == 0 || !gpu_pools ||
+      !buffer_pools)
+    return ULA_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (cfg->flags & (ULA_FLAG_LAYER_SIGNAL | ULA_FLAG_EXACT_LRU)) return ULA_ERR_INVALID_ARG;
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  ula_tp *t = new ula_tp;
+  t->P = parts;
+  t->G = cfg->n_groups;
+  t->cfg = *cfg;
+  const uint32_t G = t->G;
+  ula_config pc = *cfg;  // a partition: local ids
+  pc.max_logical = (cfg->max_logical + parts - 1) / parts;
+  ula_config bc = *cfg;  // a buffer: global addresses, no host pool
+  bc.gpu_slots = buffer_slots;
+  bc.host_slots = 0;
+  bc.flags = 0;
+  for (uint32_t p = 0; p < parts && !rc; ++p) {
+    ula_ctx *c = nullptr;
+    rc = create_ctx(&pc, gpu_pools + (size_t)p * G, host_pools ? host_pools + (size_t)p * G : nullptr,
+                    stream, 0, &c);
+    if (!rc) t->parts.push_back(c);
+  }
+  for (uint32_t r = 0; r < parts && !rc; ++r) {
+    ula_ctx *c = nullptr;
+    rc = create_ctx(&bc, buffer_pools + (size_t)r * G, nullptr, stream, kFlagCacheInternal, &c);
+    if (!rc) t->bufs.push_back(c);
+  }
+  cudaError_t e = cudaSuccess;
+  for (uint32_t p = 0; p < parts && !rc && e == cudaSuccess; ++p) {
+    cudaStream_t a = nullptr, b = nullptr;
+    cudaEvent_t x = nullptr, y = nullptr;
+    e = cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking);
+    if (e == cudaSuccess) t->ps.push_back(a), e = cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking);
+    if (e == cudaSuccess) t->bs.push_back(b), e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming);
+    if (e == cudaSuccess) t->pdone.push_back(x), e = cudaEventCreateWithFlags(&y, cudaEventDisableTiming);
+    if (e == cudaSuccess) t->bdone.push_back(y);
+  }
+  if (!rc && e == cudaSuccess) e = cudaEventCreateWithFlags(&t->split_evt, cudaEventDisableTiming);
+  if (!rc && e == cudaSuccess)
+    e = cudaMalloc(&t->sel, sizeof(uint32_t) * 2 * (size_t)parts * cfg->max_entries);
+  if (!rc && e != cudaSuccess) rc = ULA_ERR_CUDA;
+  if (!rc) {  // every buffer fetches from the partitions' maps and GPU pools
+    for (ula_ctx *b : t->bufs)
+      for (uint32_t g = 0; g < G; ++g) {
+        TpSource &src = b->tp_src[g];
+        src.P = parts;
+        src.S = cfg->gpu_slots;
+        for (uint32_t p = 0; p < parts; ++p) {
+          src.map[p] = t->parts[p]->groups_h[g].map;
+          src.pool[p] = t->parts[p]->groups_h[g].gpu_pool;
+        }
+      }
+  }
+  if (rc) {
+    cudaDeviceSynchronize();
+    tp_release(t);
+    return rc;
+  }
+  *out = t;
+  return ULA_OK;
+}
+
+int ula_tp_alloc(ula_tp *t, uint32_t n, const void *rows, uint32_t *logical_base) {
+  if (!t || !logical_base) return ULA_ERR_INVALID_ARG;
+  if ((uint64_t)t->next_logical + n > t->cfg.max_logical) return ULA_ERR_CAPACITY;
+  const uint32_t base = t->next_logical;
+  for (uint32_t p = 0; p < t->P; ++p) {
+    uint32_t first = base;
+    while (first < base + n && first % t->P != p) ++first;
+    const uint32_t cnt = first < base + n ? (base + n - first + t->P - 1) / t->P : 0;
+    uint32_t lb = 0;
+    const int rc = alloc_impl(t->parts[p], cnt, rows, &lb, n, first - base, t->P);
+    if (rc) return rc;
+    if (cnt && lb != first / t->P) return ULA_ERR_INTERNAL;
+  }
+  t->next_logical = base + n;
+  *logical_base = base;
+  return ULA_OK;
+}
+
+int ula_tp_free(ula_tp *t, uint32_t base, uint32_t n) {
+  if (!t || (uint64_t)base + n > t->next_logical) return ULA_ERR_INVALID_ARG;
+  for (uint32_t p = 0; p < t->P; ++p) {
+    uint32_t first = base;
+    while (first < base + n && first % t->P != p) ++first;
+    const uint32_t cnt = first < base + n ? (base + n - first + t->P - 1) / t->P : 0;
+    if (cnt) {
+      const int rc = free_impl(t->parts[p], first / t->P, cnt, false);
+      if (rc) return rc;
+    }
+  }
+  for (ula_ctx *b : t->bufs) {
+    const int rc = free_impl(b, base, n, true);
+    if (rc) return rc;
+  }
+  return ULA_OK;
+}
+
+int ula_tp_step_group(ula_tp *t, uint32_t group, const uint32_t *d_sel, uint32_t n_req,
+                      uint32_t q, uint32_t k, void *const *d_local_out,
+                      void *const *d_remote_out, uint32_t out_cap_rows,
+                      int32_t *const *d_local_entry_row, int32_t *const *d_local_req_off,
+                      int32_t *const *d_remote_entry_row, int32_t *const *d_remote_req_off,
+                      void *stream) {
+  if (!t || group >= t->G || !d_local_out || !d_remote_out || !d_local_entry_row ||
+      !d_local_req_off || !d_remote_entry_row || !d_remote_req_off)
+    return ULA_ERR_INVALID_ARG;
+  const uint64_t E = (uint64_t)n_req * q * k;
+  if (E > t->cfg.max_entries || (E && !d_sel)) return ULA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint32_t P = t->P, stride = t->cfg.max_entries;
+  uint32_t *part_sel = t->sel, *buf_sel = t->sel + (size_t)P * stride;
+  ula_ctx *c0 = t->parts[0];
+  ula_ctx *c = c0;  // (for ULA_CUDA's error path)
+  ULA_CUDA(launch_tp_split(d_sel, (uint32_t)E, P, part_sel, buf_sel, stride, s));
+  ULA_CUDA(cudaEventRecord(t->split_evt, s));
+  for (uint32_t p = 0; p < P; ++p) {  // the partitions, concurrently
+    c = t->parts[p];
+    ULA_CUDA(cudaStreamWaitEvent(t->ps[p], t->split_evt, 0));
+    const int rc = ula_step_group(c, group, part_sel + (size_t)p * stride, n_req, q, k,
+                                  d_local_out[p], out_cap_rows, d_local_entry_row[p],
+                                  d_local_req_off[p], nullptr, t->ps[p]);
+    if (rc) return rc;
+    ULA_CUDA(c->wait_side(t->ps[p], group));  // the later layers' gathers too
+    ULA_CUDA(cudaEventRecord(t->pdone[p], t->ps[p]));
+  }
+  for (uint32_t r = 0; r < P; ++r) {  // then every rank's buffer fetches from them
+    c = t->bufs[r];
+    for (uint32_t p = 0; p < P; ++p) ULA_CUDA(cudaStreamWaitEvent(t->bs[r], t->pdone[p], 0));
+    const int rc = ula_step_group(c, group, buf_sel + (size_t)r * stride, n_req, q, k,
+                                  d_remote_out[r], out_cap_rows, d_remote_entry_row[r],
+                                  d_remote_req_off[r], nullptr, t->bs[r]);
+    if (rc) return rc;
+    ULA_CUDA(c->wait_side(t->bs[r], group));
+    ULA_CUDA(cudaEventRecord(t->bdone[r], t->bs[r]));
+  }
+  c = c0;
+  for (uint32_t r = 0; r < P; ++r) ULA_CUDA(cudaStreamWaitEvent(s, t->bdone[r], 0));
+  return ULA_OK;
+}
+
+int ula_tp_sync(ula_tp *t, ula_stats *stats) {
+  if (!t) return ULA_ERR_INVALID_ARG;
+  int first = ULA_OK;
+  for (uint32_t i = 0; i < 2 * t->P; ++i) {
+    ula_ctx *c = i < t->P ? t->parts[i] : t->bufs[i - t->P];
+    const int rc = ula_sync(c, stats ? stats + i : nullptr);
+    if (rc && !first) first = rc;
+  }
+  return first;
+}
+
+ula_ctx *ula_tp_context(ula_tp *t, int kind, uint32_t index) {
+  if (!t || index >= t->P || (kind != 0 && kind != 1)) return nullptr;
+  return kind == 0 ? t->parts[index] : t->bufs[index];
+}
+
+int ula_tp_destroy(ula_tp *t) {
+  if (!t) return ULA_ERR_INVALID_ARG;
+  for (ula_ctx *c : t->parts) sync_impl(c);
+  for (ula_ctx *c : t->bufs) sync_impl(c);
+  tp_release(t);
   return ULA_OK;
 }
 

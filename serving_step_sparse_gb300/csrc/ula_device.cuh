@@ -99,6 +99,8 @@ struct Geometry {
   uint32_t bypass;       // ULA_FLAG_BYPASS_OVERFLOW set
   uint32_t exact;        // ULA_FLAG_EXACT_LRU set: occupied slots all in class B, no ring
   uint32_t signal;       // ULA_FLAG_LAYER_SIGNAL set: layer-major fill and per-layer flags
+  uint32_t cache;        // TP local buffer: misses are fetched from the owner partitions,
+                         // evicted copies are dropped (no host pool, no write-back)
   Dims gd, hd;           // bitmap dims for GPU-slot and host-slot bitmaps
   uint32_t nseg, hseg;   // segments (= level-1 words) per bitmap
 };
@@ -127,6 +129,17 @@ struct Order {
   uint32_t cls[ULA_MAX_BUCKETS + 2];
 };
 
+// TP mode: where a local buffer fetches a missing row (cache mode).  Address t
+// lives in partition t % P at local id t / P; map[p] and pool[p] are that
+// partition's map and GPU pool for the group being stepped.
+constexpr uint32_t kMaxParts = 8;
+constexpr uint32_t kSrcShift = 29;  // a cache miss's source: partition << 29 | slot
+struct TpSource {
+  uint32_t P, S;  // partitions, GPU slots per partition
+  const uint32_t *map[kMaxParts];
+  const uint8_t *pool[kMaxParts];
+};
+
 // Parameters of the per-step kernels of one group.
 struct StepParams {
   Geometry geo;
@@ -148,6 +161,7 @@ struct StepParams {
   uint32_t *miss_list;      // [max_entries]: misses in first-occurrence order
   uint32_t *miss_hs;        // [max_entries]: host slot of miss i
   uint32_t *miss_row;       // [max_entries]: unique row of miss i
+  TpSource src;             // cache mode: the owner partitions
   int *status;              // latched device error (0 = none)
 };
 
@@ -174,6 +188,7 @@ struct MoveParams {
   uint8_t *out;             // [L][out_cap][W]: the missed rows' outputs (NULL: none)
   uint32_t out_cap;
   uint32_t round, cur;
+  TpSource src;               // cache mode: the owner partitions' GPU pools
   int *status;
 };
 
@@ -223,6 +238,7 @@ struct AllocParams {
   const GroupDev *groups;
   const uint8_t *rows;      // device-accessible
   unsigned long long group_off[ULA_MAX_GROUPS];  // byte offset of group g's rows
+  uint32_t row_stride;      // address i of the range is row i * row_stride (TP partitions)
   uint32_t round[ULA_MAX_GROUPS];
   uint32_t base, n;
   int *status;
@@ -252,6 +268,10 @@ cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
 // `blocks` co-resident blocks)
 cudaError_t launch_lru_select(const LruParams &p, int blocks, cudaStream_t s);
 cudaError_t lru_resident_blocks(int *per_sm);
+// TP mode: part_sel[p * stride + e] = the entry as partition p sees it (a local id, or
+// a pad if p does not own it), buf_sel[r * stride + e] = the entry if rank r does not own it
+cudaError_t launch_tp_split(const uint32_t *sel, uint32_t E, uint32_t P, uint32_t *part_sel,
+                            uint32_t *buf_sel, uint32_t stride, cudaStream_t s);
 // a model consumer of one layer (diagnostics): waits for the layer's flag, sums the rows
 cudaError_t launch_consume(const uint32_t *flag, uint32_t round, const uint8_t *out,
                            uint32_t out_cap, uint32_t layer, uint32_t n_rows, uint32_t W,

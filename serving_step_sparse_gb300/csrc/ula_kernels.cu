@@ -251,7 +251,8 @@ __global__ void k_dedup_stamp(StepParams p) {
   if (e >= p.E) return;
   const uint32_t a = p.sel[e];
   if (a == kPad) return;
-  if (a >= p.geo.max_logical || p.grp.map[a] == kUnalloc) {
+  // (a local buffer holds copies: an address it does not hold is a miss, not an error)
+  if (a >= p.geo.max_logical || (!p.geo.cache && p.grp.map[a] == kUnalloc)) {
     latch(p.status, ULA_ERR_UNMAPPED);
     return;
   }
@@ -269,7 +270,7 @@ __device__ __forceinline__ Flags entry_flags(const StepParams &p, uint32_t e) {
     if (f.a != kPad && p.tbl[f.a] == first_key(p.epoch, e)) {
       f.first = 1;
       f.m = p.grp.map[f.a];
-      f.miss = (f.m & kHostBit) ? 1u : 0u;  // (2) translate
+      f.miss = (p.geo.cache ? f.m == kUnalloc : (f.m & kHostBit) != 0) ? 1u : 0u;  // (2) translate
     }
   }
   return f;
@@ -320,8 +321,9 @@ __global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p
     for (uint32_t r = threadIdx.x; r <= p.n_req; r += blockDim.x) p.req_off[r] = 0;
   if (threadIdx.x == 0) {
     const uint32_t U = runf, Mall = runm, hits = U - Mall;
-    const uint64_t can_place = min((uint64_t)p.geo.S - hits,
-                                   (uint64_t)c->free_gpu + c->free_host);
+    const uint64_t can_place =
+        p.geo.cache ? (uint64_t)p.geo.S - hits  // a buffer drops its victims' copies
+                    : min((uint64_t)p.geo.S - hits, (uint64_t)c->free_gpu + c->free_host);
     const uint32_t M = (uint32_t)min((uint64_t)Mall, can_place);  // misses made resident
     const bool ok = U <= p.out_cap && (M == Mall || p.geo.bypass);
     if (!ok) {
@@ -412,7 +414,14 @@ __global__ void __launch_bounds__(kEntryThreads) k_rotate_emit(StepParams p) {
   p.addr_row[f.a] = pos;
   if (f.miss) {
     p.miss_list[mpos] = f.a;
-    p.miss_hs[mpos] = f.m & kSlotMask;
+    if (p.geo.cache) {  // the owner partition's GPU slot (resident after the owner's step)
+      const uint32_t part = f.a % p.src.P;
+      const uint32_t om = part < kMaxParts ? p.src.map[part][f.a / p.src.P] : kNone;
+      if ((om & kHostBit) || om >= (1u << kSrcShift)) latch(p.status, ULA_ERR_INTERNAL);
+      p.miss_hs[mpos] = (part << kSrcShift) | (om & ((1u << kSrcShift) - 1u));
+    } else {
+      p.miss_hs[mpos] = f.m & kSlotMask;
+    }
     p.miss_row[mpos] = pos;
     p.grp.row_slot[pos] = kNone;  // filled (and its output written) by the move
   } else if (f.m >= geo.S) {
@@ -497,7 +506,8 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
   }
   const uint32_t F = taken_free;
   const uint32_t nwork_gpu = s_nwork;
-  const uint32_t K = (is_step && rem == 0) ? total - F : (is_step ? 0u : rem);
+  // (a local buffer writes nothing back: its victims' copies are dropped)
+  const uint32_t K = geo.cache ? 0u : (is_step && rem == 0) ? total - F : (is_step ? 0u : rem);
   uint32_t hrem = K, hbase = 0;
   const Bitmap hb = host_free_bitmap(g);
   for (uint32_t s0 = 0; s0 < geo.hseg && hrem > 0; s0 += T * kWalkSegs)
@@ -514,7 +524,7 @@ __device__ void select_walk(const GroupDev &g, const Geometry &geo, const Order 
   c->n_work_gpu = nwork_gpu;
   if (is_step) {
     c->free_gpu -= F;   // F free slots filled
-    c->free_host += F;  // K host slots taken, quota host slots released
+    if (!geo.cache) c->free_host += F;  // K host slots taken, quota host slots released
     c->stat[kStVictFree] += F;
     if (geo.exact) {
       c->stat[kStVictCold] += total - F;  // occupied slots (the scan's victims)
@@ -699,14 +709,18 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) 
     const uint32_t v = g.victims[i];
     const uint32_t hs = p.miss_hs[i];
     const uint32_t row = p.miss_row[i];
-    const bool owned = i >= F;
+    const bool owned = !geo.cache && i >= F;  // (a local buffer drops its victims' copies)
     const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
-    if (v >= geo.S || hs >= geo.H || (owned && hd >= geo.H) || (out && row >= p.out_cap)) {
+    // the source: the miss's host slot, or (local buffer) its owner partition's GPU slot
+    const uint32_t part = hs >> kSrcShift, pslot = hs & ((1u << kSrcShift) - 1u);
+    const bool src_bad = geo.cache ? (part >= p.src.P || pslot >= p.src.S) : hs >= geo.H;
+    if (v >= geo.S || src_bad || (owned && hd >= geo.H) || (out && row >= p.out_cap)) {
       if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
       continue;
     }
     uint4 *gp = reinterpret_cast<uint4 *>(g.gpu_pool + (size_t)v * sb);
-    const uint4 *src = reinterpret_cast<const uint4 *>(g.host_pool + (size_t)hs * sb);
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        geo.cache ? p.src.pool[part] + (size_t)pslot * sb : g.host_pool + (size_t)hs * sb);
     uint4 *dst = reinterpret_cast<uint4 *>(g.host_pool + (size_t)hd * sb);
     for (uint32_t c0 = 0; c0 < nvec; c0 += 32 * kMoveUnroll) {
       uint4 fill[kMoveUnroll], back[kMoveUnroll];
@@ -866,15 +880,18 @@ __global__ void k_commit(MoveParams p) {
     const uint32_t v = g.victims[i];
     const uint32_t a = p.miss_list[i];
     const uint32_t hs = p.miss_hs[i];
-    const bool owned = i >= F;
+    const bool owned = !geo.cache && i >= F;
     const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
     const uint32_t o = v < geo.S ? g.owner[v] : kNone;
-    if (v >= geo.S || a >= geo.max_logical || hs >= geo.H ||
-        (owned ? (hd >= geo.H || o >= geo.max_logical) : o != kNone)) {
+    const bool bad = geo.cache ? (o != kNone && o >= geo.max_logical)
+                               : (hs >= geo.H || (owned ? (hd >= geo.H || o >= geo.max_logical)
+                                                        : o != kNone));
+    if (v >= geo.S || a >= geo.max_logical || bad) {
       latch(p.status, ULA_ERR_INTERNAL);
       continue;
     }
     if (owned) g.map[o] = kHostBit | hd;
+    else if (geo.cache && o != kNone) g.map[o] = kUnalloc;  // the buffer's old copy is dropped
     g.map[a] = v;
     g.owner[v] = a;
     const uint32_t c = slot_class(geo, g.stamp[v], p.round);
@@ -884,7 +901,7 @@ __global__ void k_commit(MoveParams p) {
       bm_set(class_bitmap(g, geo, to), v);
     }
     g.stamp[v] = p.round;
-    bm_set(host_free_bitmap(g), hs);
+    if (!geo.cache) bm_set(host_free_bitmap(g), hs);
   }
 }
 
@@ -1634,7 +1651,8 @@ __global__ void __launch_bounds__(256) k_alloc_place(AllocParams p) {
       if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
       continue;
     }
-    const uint4 *src = reinterpret_cast<const uint4 *>(p.rows + p.group_off[gi] + (size_t)i * sb);
+    const uint4 *src =
+        reinterpret_cast<const uint4 *>(p.rows + p.group_off[gi] + (size_t)i * p.row_stride * sb);
     uint4 *dst = reinterpret_cast<uint4 *>((on_gpu ? g.gpu_pool : g.host_pool) + (size_t)slot * sb);
     for (uint32_t c = lane; c < nvec; c += 32) dst[c] = src[c];
     __syncwarp();
@@ -1662,8 +1680,8 @@ __global__ void k_free(FreeParams p) {
   if (i >= p.n) return;
   const uint32_t a = p.base + i;
   const uint32_t m = g.map[a];
-  if (m == kUnalloc) {
-    latch(p.status, ULA_ERR_INTERNAL);
+  if (m == kUnalloc) {  // (a local buffer need not hold every address it drops)
+    if (!geo.cache) latch(p.status, ULA_ERR_INTERNAL);
     return;
   }
   if (m & kHostBit) {
@@ -1691,6 +1709,19 @@ __global__ void k_free(FreeParams p) {
     atomicAdd(&g.cnt->free_gpu, 1u);
   }
   g.map[a] = kUnalloc;
+}
+
+// TP mode: each entry as every partition and every rank's buffer sees it.
+__global__ void k_tp_split(const uint32_t *sel, uint32_t E, uint32_t P, uint32_t *part_sel,
+                           uint32_t *buf_sel, uint32_t stride) {
+  const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= E) return;
+  const uint32_t a = sel[e];
+  const uint32_t own = a == kPad ? kNone : a % P;
+  for (uint32_t p = 0; p < P; ++p) {
+    part_sel[(size_t)p * stride + e] = own == p ? a / P : kPad;
+    buf_sel[(size_t)p * stride + e] = (own == kNone || own == p) ? kPad : a;
+  }
 }
 
 // A model consumer of one layer: one block polls the layer's flag (acquire) until
@@ -1809,6 +1840,12 @@ cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
                                    s, p);
   if (e != cudaSuccess) return e;
   return launch_dependent(k_commit, dim3(blocks), dim3(256), s, p);  // grid-stride over the victims
+}
+
+cudaError_t launch_tp_split(const uint32_t *sel, uint32_t E, uint32_t P, uint32_t *part_sel,
+                            uint32_t *buf_sel, uint32_t stride, cudaStream_t s) {
+  if (E) k_tp_split<<<div_up(E, 256), 256, 0, s>>>(sel, E, P, part_sel, buf_sel, stride);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_consume(const uint32_t *flag, uint32_t round, const uint8_t *out,

@@ -114,6 +114,20 @@ def _load():
     lib.ula_debug_layer_times.restype = i32
     lib.ula_debug_consume.argtypes = [p, u32, u32, u32, p, u32, u32, p, p]
     lib.ula_debug_consume.restype = i32
+    lib.ula_tp_create.argtypes = [C.POINTER(ula_config), u32, u32, p, p, p, p, C.POINTER(p)]
+    lib.ula_tp_create.restype = i32
+    lib.ula_tp_alloc.argtypes = [p, u32, p, C.POINTER(u32)]
+    lib.ula_tp_alloc.restype = i32
+    lib.ula_tp_free.argtypes = [p, u32, u32]
+    lib.ula_tp_free.restype = i32
+    lib.ula_tp_step_group.argtypes = [p, u32, p, u32, u32, u32, p, p, u32, p, p, p, p, p]
+    lib.ula_tp_step_group.restype = i32
+    lib.ula_tp_sync.argtypes = [p, p]
+    lib.ula_tp_sync.restype = i32
+    lib.ula_tp_context.argtypes = [p, i32, u32]
+    lib.ula_tp_context.restype = p
+    lib.ula_tp_destroy.argtypes = [p]
+    lib.ula_tp_destroy.restype = i32
     return lib
 
 
@@ -222,6 +236,49 @@ def ula_debug_consume(ctx: int, group: int, layer: int, round_: int, d_out: int,
                       out_cap_rows: int, n_rows: int, d_result: int, stream) -> None:
     _check(lib.ula_debug_consume(ctx, group, layer, round_, d_out, out_cap_rows, n_rows,
                                  d_result, stream), "ula_debug_consume")
+
+
+def ula_tp_create(cfg: ula_config, parts: int, buffer_slots: int, gpu_pools, host_pools,
+                  buffer_pools, stream) -> int:
+    out = C.c_void_p()
+    hp = _ptr_array(host_pools) if host_pools else None
+    _check(lib.ula_tp_create(C.byref(cfg), parts, buffer_slots, _ptr_array(gpu_pools), hp,
+                             _ptr_array(buffer_pools), stream, C.byref(out)), "ula_tp_create")
+    return out.value
+
+
+def ula_tp_alloc(tp: int, n: int, rows: int) -> int:
+    base = C.c_uint32()
+    _check(lib.ula_tp_alloc(tp, n, rows, C.byref(base)), "ula_tp_alloc")
+    return base.value
+
+
+def ula_tp_free(tp: int, base: int, n: int) -> None:
+    _check(lib.ula_tp_free(tp, base, n), "ula_tp_free")
+
+
+def ula_tp_step_group(tp: int, group: int, d_sel: int, n_req: int, q: int, k: int, local_out,
+                      remote_out, out_cap_rows: int, local_entry_row, local_req_off,
+                      remote_entry_row, remote_req_off, stream) -> None:
+    _check(lib.ula_tp_step_group(tp, group, d_sel, n_req, q, k, _ptr_array(local_out),
+                                 _ptr_array(remote_out), out_cap_rows,
+                                 _ptr_array(local_entry_row), _ptr_array(local_req_off),
+                                 _ptr_array(remote_entry_row), _ptr_array(remote_req_off),
+                                 stream), "ula_tp_step_group")
+
+
+def ula_tp_sync(tp: int, parts: int) -> list:
+    st = (ula_stats * (2 * parts))()
+    _check(lib.ula_tp_sync(tp, C.cast(st, C.c_void_p)), "ula_tp_sync")
+    return [s.as_dict() for s in st]
+
+
+def ula_tp_context(tp: int, kind: int, index: int) -> int:
+    return lib.ula_tp_context(tp, kind, index) or 0
+
+
+def ula_tp_destroy(tp: int) -> None:
+    lib.ula_tp_destroy(tp)
 
 
 def ula_debug_inject(ctx: int, code: int) -> None:
