@@ -55,6 +55,11 @@ def parse_args(argv=None):
                          "each layer is ready)")
     ap.add_argument("--latency-steps", type=int, default=20,
                     help="steps of the per-layer ready-time pass (synchronised per step)")
+    ap.add_argument("--tp", type=int, default=1,
+                    help="TP mode emulated with this many partitions (reports the local "
+                         "buffers' hit rate and the fetched bytes)")
+    ap.add_argument("--buffer-frac", type=float, default=2.0,
+                    help="TP local buffer slots per rank and group, in steps' entries")
     ap.add_argument("--pool-frac", type=float, default=None,
                     help="GPU pool as a fraction of the history (policy comparisons)")
     ap.add_argument("--requests", type=int, default=None,
@@ -226,6 +231,91 @@ def gen_steps(trace, w, n, synth, np):
                                     out=rows[g])
         steps.append((sel, ev, rows))
     return steps
+
+
+def run_tp(args, local):
+    """TP mode emulated on one GPU: P partitions and per-rank local buffers, K timed steps."""
+    import numpy as np
+    import torch
+
+    import synth
+    from serving_step_sparse_gb300.cache import UlaTP
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workload_for(args)
+    P = args.tp
+    G, L, W, R = w.n_groups, w.layers_per_group, w.row_bytes, w.n_live
+    E = w.entries_per_step
+    S = -(-w.gpu_slots // P)
+    H = -(-w.max_live_history // P) - S + E
+    slots = int(args.buffer_frac * E)
+    stream = torch.cuda.current_stream(dev)
+    tp = UlaTP(row_bytes=W, layers_per_group=[L] * G, parts=P, gpu_slots=S, host_slots=H,
+               ring_buckets=w.ring_buckets, max_logical=w.max_logical, max_entries=E,
+               buffer_slots=slots, device=dev, stream=stream)
+    trace = synth.Trace(w)
+    ctx, base, total = trace.initial()
+    chunk = 32768
+    stage = torch.empty(chunk * G * L * W, dtype=torch.uint8, pin_memory=True)
+    for b0, n0 in zip(base.tolist(), ctx.tolist()):
+        off = 0
+        while off < n0:
+            m = min(chunk, n0 - off)
+            view = stage[: m * G * L * W].numpy().reshape(G, m, L, W)
+            for g in range(G):
+                synth.content_range(w.seed, g, L, b0 + off, m, W, out=view[g])
+            assert tp.alloc(m, stage[: m * G * L * W]) == b0 + off
+            tp.sync()
+            off += m
+    n = args.warmup + args.steps
+    steps = gen_steps(trace, w, n, synth, np)
+    sel_dev = torch.from_numpy(np.stack([x[0] for x in steps]).view(np.int32)).to(dev)
+    rows_dev = [torch.from_numpy(x[2].reshape(-1)).to(dev) if x[2] is not None else None
+                for x in steps]
+    lo = [[tp.out_buffer(g, E) for _ in range(P)] for g in range(G)]
+    ro = [[tp.out_buffer(g, E) for _ in range(P)] for g in range(G)]
+    mk = lambda k: [torch.empty(k, dtype=torch.int32, device=dev) for _ in range(P)]
+    ler, lrq, rer, rrq = mk(E), mk(R + 1), mk(E), mk(R + 1)
+
+    def do_step(t):
+        for g in range(G):
+            tp.step_group(g, sel_dev[t][g], lo[g], ro[g], ler, lrq, rer, rrq)
+        ev = steps[t][1]
+        if ev["append_n"]:
+            assert tp.alloc(ev["append_n"], rows_dev[t]) == ev["append_base"]
+
+    for t in range(args.warmup):
+        do_step(t)
+    st0 = tp.sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for t in range(args.warmup, n):
+        do_step(t)
+    e1.record(stream)
+    st1 = tp.sync()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    d = [{k: st1[i][k] - st0[i][k] for k in st1[i]} for i in range(2 * P)]
+    rows = sum(x["rows_gathered"] for x in d)
+    rem_uniq = sum(x["uniq"] for x in d[P:])
+    rem_hits = sum(x["hits"] for x in d[P:])
+    fetched = sum(x["bytes_h2d"] for x in d[P:])
+    host = sum(x["bytes_h2d"] for x in d[:P])
+    tp.close()
+    return {"metric": METRIC, "value": rows / (ms / 1e3), "unit": "rows/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+            "data": "synthetic (seeded trace; rows are seeded random bytes)",
+            "config": dict(w.summary(), parallelism=f"TP emulated: {P} partitions on one GPU",
+                           partition_gpu_slots=S, partition_host_slots=H, buffer_slots=slots),
+            "tp": {"parts": P, "buffer_hit_rate": rem_hits / max(1, rem_uniq),
+                   "remote_rows_per_step": rem_uniq / args.steps,
+                   "fetched_bytes_per_step": fetched / args.steps,
+                   "host_fill_bytes_per_step": host / args.steps,
+                   "note": "all P ranks' work runs on this one GPU; a fetch is a copy inside "
+                           "HBM, standing in for the cross-GPU copy of TP mode"}}
 
 
 def run_gpu(args, rank, world, local):
@@ -605,6 +695,10 @@ def main(argv=None):
         print(json.dumps(line), flush=True)
         return 0
 
+    if args.tp > 1:
+        if rank == 0:
+            print(json.dumps(run_tp(args, local)), flush=True)
+        return 0
     if world > 1:
         import torch
         import torch.distributed as dist
