@@ -8,7 +8,7 @@
  *   §2 "Unified logical addresses" -- the engine allocates and selects KV by
  *      logical address only; a mapping table names the GPU slot or CPU slot
  *      holding each entry; in DP mode a GPU owns its GPU pool and CPU pool and
- *      an entry lives in one of them, never both; a layer group sharing one
+ *      an entry lives in exactly one of them; a layer group sharing one
  *      sparse selection does address lookup and dedup once and prefetches
  *      later layers on a separate CUDA stream.
  *   §3 "PB-LRU" -- bucketed replacement for the shared GPU pool: one bucket
@@ -92,8 +92,8 @@ typedef struct ula_config {
  * wait that expires latches ULA_ERR_TIMEOUT. */
 #define ULA_FLAG_EXACT_LRU 2u
 
-/* Per-layer signal (§2 "two more details": the current layer computes while later
- * layers' data arrives; §3: data first, then the signal).  The fill runs layer by
+/* Per-layer signal (§2, the paragraph on layer groups sharing a selection: a layer
+ * computes while later layers' data arrives; §3: data first, then the signal).  The fill runs layer by
  * layer (layer 0 of every miss, then layer 1, ...), and as soon as out[j] holds every
  * unique row of the step (hit rows gathered, missed rows filled) the library stores
  * the step's round number into the group's device flag j (a release store).  A
@@ -353,8 +353,8 @@ int ula_dedup_noalloc(const uint32_t *d_sel, uint32_t n, uint32_t *d_uniq,
 /*
  * TP mode, emulated on one GPU (§2 "Unified logical addresses", TP paragraph): the
  * pools of P GPUs form one distributed address space in which logical address t
- * lives on "GPU" t mod P; each computing GPU keeps a local buffer of recently
- * selected KV from the others.  Here P partitions of this GPU stand in for the P
+ * lives on "GPU" t mod P, and a GPU that computes caches copies of the entries it
+ * fetched from the others.  Here P partitions of this GPU stand in for the P
  * GPUs: partition p is a DP residency context (everything above) over local ids
  * t / P with its own GPU and host pools, and rank r's local buffer (per group) holds
  * copies of remote rows (t mod P != r) in buffer_slots slots under PB-LRU, evicted

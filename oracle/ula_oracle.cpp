@@ -610,8 +610,8 @@ int orc_lru_step(void *h, uint32_t gi, const uint32_t *sel, size_t n_entries, ui
 // TP mode, emulated (§2 "Unified logical addresses", TP paragraph): address t
 // belongs to partition t mod P (P partitions stand in for P GPUs).  Each
 // partition is a DP residency (the code above) over its own addresses, with
-// local ids t / P.  Each rank r keeps, per group, a local buffer of recently
-// selected remote rows (t mod P != r): PB-LRU over the buffer's own slots and
+// local ids t / P.  Each rank r also caches, per group, copies of the remote
+// rows (t mod P != r) its steps selected: PB-LRU over the buffer's own slots and
 // ring, a victim's copy is dropped (the owner keeps the entry), and a missing
 // row is fetched from its owner's GPU slot, where the owner's step has just made
 // it resident.

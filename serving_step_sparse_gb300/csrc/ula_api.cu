@@ -1,7 +1,7 @@
 // Host orchestrator behind the C ABI (include/ula.h): context set-up, argument
 // checks, stream/event ordering, and the per-call kernel sequences.
 //
-// Ordering rules (UlaCache summary page, §2 "two more details" and §3 last
+// Ordering rules (UlaCache summary page, §2 (the paragraph on layer groups sharing a selection) and §3 last
 // paragraph): a step's kernels run in stream order -- dedup/translate ->
 // capacity check -> rotate/mark -> victim selection -> move+commit -> signal
 // -> gather; layer 0 is gathered on the caller's stream, later layers on the

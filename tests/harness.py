@@ -131,7 +131,7 @@ def check_step_outputs(sel_g, res, g, w, mode):
 
 
 def check_invariants(st, S, H, live):
-    """Never both, slot ownership, class partition (oracle export format)."""
+    """One tier per entry, slot ownership, class partition (oracle export format)."""
     tier, slot, cls, owner = st["tier"], st["slot"], st["cls"], st["owner"]
     host_free, host_owner = st["host_free"], st["host_owner"]
     live_arr = np.array(sorted(live), dtype=np.int64)

@@ -11,7 +11,7 @@ reasoning fix -- independent of the oracle's own code:
   evicted first) against the same brute force's round-granular LRU order, for any
   number of ring buckets, and the per-slot timestamps against the brute force's;
 * the gathered rows against the generator's closed form (byte for byte);
-* invariants: never both tiers (§2), slot ownership, class partition, the
+* invariants: one tier per entry (§2), slot ownership, class partition, the
   current round's slots never evicted (§3), rotation changes labels only (§3),
   errors leave the state untouched.
 """
