@@ -662,7 +662,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   mp.cur = cur;
   mp.src = c->tp_src[group];
   mp.status = c->status;
-  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, 2, [&] { return launch_move(mp, c->move_blocks, s); }));
+  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, c->geo.signal ? 2 : 1, [&] { return launch_move(mp, c->move_blocks, s); }));
   // signal: the commit event; layer j is ready once its hit rows are gathered too
   ULA_CUDA(cudaEventRecord(c->commit_evt, s));
   if (gather) ULA_CUDA(cudaStreamWaitEvent(s, c->hit0_evt, 0));

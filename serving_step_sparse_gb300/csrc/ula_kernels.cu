@@ -662,7 +662,51 @@ __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
 // reached directly over the host link.  The per-victim plan (victim slot, host
 // slots, row) is read up front from arrays filled by the compaction and the
 // selection, so a warp starts its copies after one round of independent loads.
-// Then, in the next kernel, the map and the labels (k_commit).
+// Once a warp's copies of victim i are done, its lane 0 commits victim i's map
+// and labels (the readers of the map are later kernels).
+// (5) The map after the data: victim i's old owner now maps to its host slot (a
+// local buffer drops it), miss i to the victim slot; the slot joins the current
+// bucket (clears on its old class, sets on cur); the miss's host slot is released
+// (sets only on the host-free bitmap).  Called once victim i's copies are done.
+__device__ __forceinline__ void commit_victim(const MoveParams &p, uint32_t i, uint32_t F) {
+  const GroupDev &g = p.grp;
+  const Geometry &geo = p.geo;
+  const uint32_t v = g.victims[i];
+  const uint32_t a = p.miss_list[i];
+  const uint32_t hs = p.miss_hs[i];
+  const bool owned = !geo.cache && i >= F;
+  const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
+  const uint32_t o = v < geo.S ? g.owner[v] : kNone;
+  const bool bad = geo.cache ? (o != kNone && o >= geo.max_logical)
+                             : (hs >= geo.H || (owned ? (hd >= geo.H || o >= geo.max_logical)
+                                                      : o != kNone));
+  if (v >= geo.S || a >= geo.max_logical || bad) {
+    latch(p.status, ULA_ERR_INTERNAL);
+    return;
+  }
+  if (owned) g.map[o] = kHostBit | hd;
+  else if (geo.cache && o != kNone) g.map[o] = kUnalloc;  // the buffer's old copy is dropped
+  g.map[a] = v;
+  g.owner[v] = a;
+  const uint32_t c = slot_class(geo, g.stamp[v], p.round);
+  const uint32_t to = access_class(geo, p.cur);
+  if (c != to) {
+    bm_clear(class_bitmap(g, geo, c), v);
+    bm_set(class_bitmap(g, geo, to), v);
+  }
+  g.stamp[v] = p.round;
+  if (!geo.cache) bm_set(host_free_bitmap(g), hs);
+}
+
+// (1) every entry's unique row (grid-stride over the selection)
+__device__ __forceinline__ void write_entry_rows(const MoveParams &p) {
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < p.E; e += stride) {
+    const uint32_t a = p.sel[e];
+    p.entry_row[e] = a == kPad ? -1 : (int32_t)p.addr_row[a];
+  }
+}
+
 constexpr int kMoveUnroll = ULA_MOVE_UNROLL;
 
 __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) {
@@ -678,6 +722,7 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) 
   const uint32_t nvec = (uint32_t)(sb / 16);
   const uint32_t CW = geo.W / 16;
   uint4 *out = reinterpret_cast<uint4 *>(p.out);
+  write_entry_rows(p);
   // overflow bypass: misses [M, M + Mx) are copied from their host slots to the
   // output only (they stay on the host)
   for (uint32_t i = M + warp; i < M + Mx; i += nwarps) {
@@ -757,6 +802,8 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) 
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) commit_victim(p, i, F);  // (5) this victim's map, after its copies
   }
 }
 
@@ -868,41 +915,11 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move_layers(MovePar
 __global__ void k_commit(MoveParams p) {
   pdl_wait();
   if (*(volatile int *)p.status) return;
-  const GroupDev &g = p.grp;
-  const Geometry &geo = p.geo;
-  const uint32_t M = g.cnt->M, F = g.cnt->F;
+  const uint32_t M = p.grp.cnt->M, F = p.grp.cnt->F;
   const uint32_t stride = gridDim.x * blockDim.x;
-  for (uint32_t e = blockIdx.x * blockDim.x + threadIdx.x; e < p.E; e += stride) {
-    const uint32_t a = p.sel[e];
-    p.entry_row[e] = a == kPad ? -1 : (int32_t)p.addr_row[a];
-  }
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < M; i += stride) {
-    const uint32_t v = g.victims[i];
-    const uint32_t a = p.miss_list[i];
-    const uint32_t hs = p.miss_hs[i];
-    const bool owned = !geo.cache && i >= F;
-    const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
-    const uint32_t o = v < geo.S ? g.owner[v] : kNone;
-    const bool bad = geo.cache ? (o != kNone && o >= geo.max_logical)
-                               : (hs >= geo.H || (owned ? (hd >= geo.H || o >= geo.max_logical)
-                                                        : o != kNone));
-    if (v >= geo.S || a >= geo.max_logical || bad) {
-      latch(p.status, ULA_ERR_INTERNAL);
-      continue;
-    }
-    if (owned) g.map[o] = kHostBit | hd;
-    else if (geo.cache && o != kNone) g.map[o] = kUnalloc;  // the buffer's old copy is dropped
-    g.map[a] = v;
-    g.owner[v] = a;
-    const uint32_t c = slot_class(geo, g.stamp[v], p.round);
-    const uint32_t to = access_class(geo, p.cur);
-    if (c != to) {
-      bm_clear(class_bitmap(g, geo, c), v);
-      bm_set(class_bitmap(g, geo, to), v);
-    }
-    g.stamp[v] = p.round;
-    if (!geo.cache) bm_set(host_free_bitmap(g), hs);
-  }
+  write_entry_rows(p);
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < M; i += stride)
+    commit_victim(p, i, F);
 }
 
 // ------------------------------------------------------------------ gather
@@ -1836,10 +1853,13 @@ cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm) {
 }
 
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
-  cudaError_t e = launch_dependent(p.geo.signal ? k_move_layers : k_move, dim3(blocks), dim3(256),
-                                   s, p);
+  if (!p.geo.signal)  // copies, then each victim's map, in one kernel
+    return launch_dependent(k_move, dim3(blocks), dim3(256), s, p);
+  // layer by layer: a victim's chunks are spread over warps, so the map follows in
+  // a second kernel, once every copy is done
+  cudaError_t e = launch_dependent(k_move_layers, dim3(blocks), dim3(256), s, p);
   if (e != cudaSuccess) return e;
-  return launch_dependent(k_commit, dim3(blocks), dim3(256), s, p);  // grid-stride over the victims
+  return launch_dependent(k_commit, dim3(blocks), dim3(256), s, p);
 }
 
 cudaError_t launch_tp_split(const uint32_t *sel, uint32_t E, uint32_t P, uint32_t *part_sel,
