@@ -17,8 +17,9 @@ if torch.cuda.is_available():
     from oracle import COLD, FREE, OracleTP
     from serving_step_sparse_gb300 import ula
     from serving_step_sparse_gb300.cache import UlaTP
-    from tests.gpu_harness import (compare_states, gpu_state_in_oracle_terms, unpack_bits)
-    from tests.harness import apply_events, initial_allocs
+    from tests.gpu_harness import (compare_states, expand_id_rows, gpu_state_in_oracle_terms,
+                                   unpack_bits)
+    from tests.harness import ID_ROW_BYTES, alloc_rows, apply_events, initial_allocs
 
 
 class _Geo:
@@ -43,7 +44,9 @@ def _buffer_state(st, slots, B):
     return where, st["owner"], cls, st["cur"]
 
 
-def run_tp(w, P, steps, buffer_slots=None):
+def run_tp(w, P, steps, buffer_slots=None, mode="bytes", sample_rows=None, seed=0):
+    """mode "id": the oracle holds 8-byte id rows (exact: a row's bytes are a function of
+    its address) and the gathered bytes are compared on sample_rows rows per output."""
     G, L, W, R = w.n_groups, w.layers_per_group, w.row_bytes, w.n_live
     E = w.entries_per_step
     S = -(-w.gpu_slots // P)
@@ -52,16 +55,21 @@ def run_tp(w, P, steps, buffer_slots=None):
     tp = UlaTP(row_bytes=W, layers_per_group=[L] * G, parts=P, gpu_slots=S, host_slots=H,
                ring_buckets=w.ring_buckets, max_logical=w.max_logical, max_entries=E,
                buffer_slots=slots)
-    orc = OracleTP(W, [L] * G, P, S, H, w.ring_buckets, w.max_logical, slots)
+    orc = OracleTP(W if mode == "bytes" else ID_ROW_BYTES, [L] * G, P, S, H, w.ring_buckets,
+                   w.max_logical, slots)
+    rng = np.random.default_rng(seed)
     trace = synth.Trace(w)
     dev = tp.device
 
     def alloc(base, n):
-        rows = _rows(w, base, n)
-        t = torch.from_numpy(rows.reshape(-1)).pin_memory()
-        assert tp.alloc(n, t) == base
-        tp.sync()
-        assert orc.alloc(n, rows.reshape(-1)) == base
+        for off in range(0, n, 16384):  # staged in pieces
+            m = min(16384, n - off)
+            rows = _rows(w, base + off, m)
+            t = torch.from_numpy(rows.reshape(-1)).pin_memory()
+            assert tp.alloc(m, t) == base + off
+            tp.sync()
+            orows = rows.reshape(-1) if mode == "bytes" else alloc_rows(w, base + off, m, "id")
+            assert orc.alloc(m, orows) == base + off
         return base
 
     def free(base, n):
@@ -91,8 +99,16 @@ def run_tp(w, P, steps, buffer_slots=None):
                         U = int(o["req_off"][-1])
                         assert np.array_equal(rq[r].cpu().numpy(), o["req_off"]), f"{where} {side} {r}"
                         assert np.array_equal(er[r].cpu().numpy(), o["entry_row"]), f"{where} {side} {r}"
-                        assert np.array_equal(out[r][:, :U].cpu().numpy(), o["out"][:, :U]), \
-                            f"{where} {side} rows {r}"
+                        if mode == "bytes":
+                            assert np.array_equal(out[r][:, :U].cpu().numpy(), o["out"][:, :U]), \
+                                f"{where} {side} rows {r}"
+                        else:
+                            rows = rng.choice(U, min(U, sample_rows), replace=False) if U else np.zeros(0, int)
+                            rt = torch.from_numpy(rows).to(dev)
+                            for j in range(L):
+                                got = out[r][j].index_select(0, rt).cpu().numpy()
+                                exp = expand_id_rows(o["out"][j, rows], w.seed, g, j, W)
+                                assert np.array_equal(got, exp), f"{where} {side} rows {r} layer {j}"
                     # partition r's state
                     go = gpu_state_in_oracle_terms(tp.parts[r].export(g), _Geo(S, H, w.ring_buckets))
                     compare_states(go, orc.partition(r).export(g), f"{where} partition {r}")
@@ -124,6 +140,15 @@ def test_tp_parity(name, P):
     assert remote > 0 and hits > 0 and fetched > 0
     # fetched bytes are the buffers' fills
     assert sum(s["bytes_h2d"] for s in stats[P:]) == fetched * w.layers_per_group * w.row_bytes
+
+
+def test_tp_full_size_sampled():
+    """The long-document workload at full size with 4 partitions (oracle in id mode):
+    states and entry rows exact, gathered bytes on sampled rows."""
+    from synth.configs import WORKLOADS
+    w = WORKLOADS["longdoc"]
+    fetched, hits, remote, stats = run_tp(w, 4, 3, mode="id", sample_rows=2048)
+    assert hits > 0 and fetched > 0
 
 
 def test_tp_small_buffer_recycles_slots():
