@@ -7,19 +7,23 @@
 // (bucket ring + cold bucket, rotation by relabelling, victim order, bitmaps
 // with summary levels, parallel hit detection/dedup, move -> map -> signal).
 //
-// One step of one group is seven launches on the critical path:
+// One step of one group is six launches on the critical path, chained by
+// programmatic dependent launch:
 //   k_dedup_stamp       (1) every entry bids to be its address's first occurrence
 //   k_dedup_count_scan  (1)(2) per-block counts of first occurrences / misses; the
 //                       last block scans them and runs the capacity check
 //   k_rotate_emit       (3a) ring rotation + cold fold (labels only), and the
-//                       compaction of unique rows / misses / CSR offsets
-//   k_mark_select       (3b) hits move to the current bucket, entry rows; the last
+//                       compaction of unique rows / misses / CSR offsets; each hit's
+//                       slot, stamp and bit in the step's hit map
+//   k_mark_select       (3b) the hit map applied to the labels, word by word; the last
 //                       block walks the segment counts (4) in class order
 //   k_select_emit       (4) the victims' and write-back slots' indices
-//   k_move              (5) write-back and fill; (6) the missed rows' outputs
-//   k_commit            (5) map, labels and host slots, after the copies
-// and k_gather (6) for the rows that hit, on the prefetch stream, concurrent with
-// the selection and the move (hit slots never move in their round).
+//   k_move              (5) write-back and fill, then each victim's map, labels and
+//                       host slot; (6) the missed rows' outputs; entry rows
+// and k_gather (6) for the rows that hit, on the prefetch streams, concurrent with
+// the selection and the move (hit slots never move in their round).  Options:
+// k_lru_select (exact LRU's scan, after the marking), k_move_layers + k_commit
+// (per-layer signal), cache mode (a TP rank's local buffer).
 //
 // Concurrency discipline for the bitmaps: inside one kernel a given bitmap is
 // either only set or only cleared.  That keeps the summary levels and the
