@@ -281,7 +281,7 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(cudaEventCreateWithFlags(&c->commit_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->marked_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->hit0_evt, cudaEventDisableTiming));
-  ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks));
+  ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks, cfg.row_bytes));
   c->gather_fit_per_sm = c->gather_blocks;
   // The move is bound by the host link and needs few SMs to saturate it; the hit
   // gathers run beside it.  ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune

@@ -279,7 +279,9 @@ cudaError_t launch_consume(const uint32_t *flag, uint32_t round, const uint8_t *
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s);
 cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);
-// resident 256-thread blocks per SM of the persistent kernels
-cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm);
+// resident blocks per SM of the persistent kernels (the gather's shape depends on the rows)
+cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t row_bytes);
+bool gather_uses_tma(uint32_t row_bytes);
+size_t gather_tma_smem(uint32_t row_bytes);
 
 }  // namespace ula

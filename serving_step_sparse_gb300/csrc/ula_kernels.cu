@@ -60,6 +60,9 @@ constexpr int kMarkClasses = 8;     // class words a marking warp loads at once
 #define ULA_MOVE_UNROLL 6
 #endif
 constexpr int kGatherThreads = ULA_GATHER_THREADS;
+#ifndef ULA_GATHER_TMA
+#define ULA_GATHER_TMA 0  // the hit gather with bulk copies (k_gather_tma)
+#endif
 
 __device__ __forceinline__ void latch(int *status, int code) { atomicCAS(status, 0, code); }
 
@@ -1008,6 +1011,116 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
   }
 }
 
+// (6) The same gather with bulk copies (TMA, cp.async.bulk): a block is one warp
+// and every lane runs its own pipeline of kTmaStages row buffers in shared memory
+// -- a bulk load of the pool row into a buffer, completed on the buffer's
+// mbarrier, then a bulk store of the buffer to the output row -- so a warp keeps
+// 32 * kTmaStages rows in flight without holding their bytes in registers and
+// without the load/store units.  Lanes take rows tid, tid + threads, ...; rows
+// that missed are skipped.  Waits are bounded (1 s, then ULA_ERR_TIMEOUT).
+constexpr int kTmaStages = 3;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
+  return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long t0) {
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+    if (done) return true;
+    if (global_ns() - t0 > 1000000000ull) return false;
+  }
+}
+
+__global__ void __launch_bounds__(32) k_gather_tma(GatherParams p) {
+  extern __shared__ __align__(128) uint8_t tma_smem[];
+  if (*(volatile int *)p.status) return;
+  const GroupDev &g = p.grp;
+  const Geometry &geo = p.geo;
+  const uint32_t U = g.cnt->U;
+  if (U > p.out_cap) {  // only a re-gather into a short buffer can get here
+    if (blockIdx.x == 0 && threadIdx.x == 0) latch(p.status, ULA_ERR_CAPACITY);
+    return;
+  }
+  const uint32_t W = geo.W, lane = threadIdx.x;
+  const uint32_t bars = smem_u32(tma_smem) + lane * kTmaStages * 8;   // [32][stages] mbarriers
+  uint8_t *buf = tma_smem + 32 * kTmaStages * 8 + (size_t)lane * kTmaStages * W;
+  for (int st = 0; st < kTmaStages; ++st)
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8 * st) : "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  const size_t sb = (size_t)g.layers * W;
+  const uint8_t *pool = g.gpu_pool + (size_t)p.layer * W;
+  uint8_t *out = p.out + (size_t)p.layer * p.out_cap * W;
+  const uint32_t nthr = gridDim.x * 32;
+  uint32_t next = blockIdx.x * 32 + lane;  // the next row this lane looks at
+  uint32_t rows[kTmaStages];
+  // the next hit row at or after `next` (and its slot); false when none is left
+  auto next_hit = [&](uint32_t &row, uint32_t &slot) -> bool {
+    while (next < U) {
+      const uint32_t r = next, m = g.row_slot[r];
+      next += nthr;
+      if (m == kNone) continue;  // a miss: written by the move
+      if (m >= geo.S) {
+        latch(p.status, ULA_ERR_INTERNAL);
+        continue;
+      }
+      row = r;
+      slot = m;
+      return true;
+    }
+    return false;
+  };
+  auto load = [&](int st, uint32_t slot) {
+    const uint32_t bar = bars + 8 * st;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(W)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(buf + (size_t)st * W)), "l"(pool + (size_t)slot * sb), "r"(W), "r"(bar)
+        : "memory");
+  };
+  uint32_t issued = 0;
+  for (int st = 0; st < kTmaStages; ++st) {  // prime every stage
+    uint32_t row, slot;
+    if (!next_hit(row, slot)) break;
+    rows[st] = row;
+    load(st, slot);
+    ++issued;
+  }
+  const unsigned long long t0 = global_ns();
+  for (uint32_t k = 0; k < issued; ++k) {
+    const int st = (int)(k % kTmaStages);
+    if (!mbar_wait(bars + 8 * st, (k / kTmaStages) & 1u, t0)) {
+      latch(p.status, ULA_ERR_TIMEOUT);
+      break;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(out + (size_t)rows[st] * W), "r"(smem_u32(buf + (size_t)st * W)), "r"(W)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    uint32_t row, slot;
+    if (next_hit(row, slot)) {
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the buffer is read
+      rows[st] = row;
+      load(st, slot);
+      ++issued;
+    }
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // every store has landed
+  if (p.signal) {  // per-layer signal: the hit rows of this layer are one contribution
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    if (last_block(&g.gather_done[p.layer]) && threadIdx.x == 0)
+      layer_contrib(g, p.layer, 2u, p.round);
+  }
+}
+
 // ------------------------------------------------------------- exact LRU
 //
 // Exact LRU's victims beyond the free slots (§3 "PB-LRU", first paragraph: a
@@ -1850,9 +1963,19 @@ cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStre
   return cudaGetLastError();
 }
 
-cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm) {
+size_t gather_tma_smem(uint32_t row_bytes) {
+  return 32 * kTmaStages * 8 + (size_t)32 * kTmaStages * row_bytes;
+}
+
+cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t row_bytes) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move, 256, 0);
   if (e != cudaSuccess) return e;
+  if (gather_uses_tma(row_bytes)) {
+    const size_t smem = gather_tma_smem(row_bytes);
+    e = cudaFuncSetAttribute(k_gather_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather_tma, 32, smem);
+  }
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather, kGatherThreads, 0);
 }
 
@@ -1890,8 +2013,15 @@ cudaError_t launch_lru_select(const LruParams &p, int blocks, cudaStream_t s) {
                                      dim3(kLruThreads), args, 0, s);
 }
 
+bool gather_uses_tma(uint32_t row_bytes) {
+  return ULA_GATHER_TMA && gather_tma_smem(row_bytes) <= 160 * 1024;
+}
+
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s) {
-  k_gather<<<blocks, kGatherThreads, 0, s>>>(p);
+  if (gather_uses_tma(p.geo.W))
+    k_gather_tma<<<blocks, 32, gather_tma_smem(p.geo.W), s>>>(p);
+  else
+    k_gather<<<blocks, kGatherThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
