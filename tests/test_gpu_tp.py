@@ -155,3 +155,27 @@ def test_tp_small_buffer_recycles_slots():
     w = small("batch8_32k").replace(steps=12)
     E = w.entries_per_step
     run_tp(w, 2, w.steps, buffer_slots=E)  # exactly one step's worth: evictions every step
+
+
+def test_tp_validation():
+    """Out-of-range partition counts, a zero-slot buffer and the unsupported option
+    combinations are refused before anything is created."""
+    L, W, S, H = 1, 16, 4, 4
+    gp = [torch.empty(S * L * W, dtype=torch.uint8, device="cuda") for _ in range(9)]
+    hp = [torch.empty(H * L * W, dtype=torch.uint8, pin_memory=True) for _ in range(9)]
+    bp = [torch.empty(4 * L * W, dtype=torch.uint8, device="cuda") for _ in range(9)]
+    ptrs = lambda xs, n: [x.data_ptr() for x in xs[:n]]
+    for parts, slots, flags in ((0, 4, 0), (9, 4, 0), (2, 0, 0), (2, 4, ula.FLAG_EXACT_LRU),
+                                (2, 4, ula.FLAG_LAYER_SIGNAL)):
+        cfg = ula.make_config(W, [L], S, H, 2, 64, 8, flags)
+        n = max(parts, 1)
+        with pytest.raises(ula.UlaError) as ei:
+            ula.ula_tp_create(cfg, parts, slots, ptrs(gp, n), ptrs(hp, n), ptrs(bp, n), None)
+        assert ei.value.code == ula.ERR_INVALID_ARG
+    cfg = ula.make_config(W, [L], S, H, 2, 64, 8, 0)
+    tp = ula.ula_tp_create(cfg, 2, 4, ptrs(gp, 2), ptrs(hp, 2), ptrs(bp, 2), None)
+    assert ula.ula_tp_context(tp, 0, 1) and ula.ula_tp_context(tp, 1, 1)
+    assert ula.ula_tp_context(tp, 0, 2) == 0 and ula.ula_tp_context(tp, 2, 0) == 0
+    with pytest.raises(ula.UlaError):  # beyond what was allocated
+        ula.ula_tp_free(tp, 0, 1)
+    ula.ula_tp_destroy(tp)
