@@ -568,8 +568,8 @@ def isolated_gather(cache, ula, torch, dev, stream, W, reps=20):
 # kernel, per gathered row, together with the hash of the gather kernel's source (its
 # launch-shape defaults and its body) it was taken on.  Reported only while that source
 # is unchanged.
-GATHER_TRAFFIC = {"source_sha256": "f7ca8314203cf8056dd3311bc34d430ca642ed520687407e2368932d1dec4186",
-                  "bytes_per_row": 18767616 / 24255}  # 24,255 hit rows, 12-request case
+GATHER_TRAFFIC = {"source_sha256": "c07c3f8b76e6d22b1c75373cc5990047b1b3fe06ea9371b26ede09c97f25d7f0",
+                  "bytes_per_row": 18775040 / 24255}  # 24,255 hit rows, 12-request case
 
 
 def gather_source_sha256() -> str:

@@ -48,10 +48,10 @@ constexpr int kMarkClasses = 8;     // class words a marking warp loads at once
 #define ULA_GATHER_THREADS 256
 #endif
 #ifndef ULA_GATHER_MINBLOCKS
-#define ULA_GATHER_MINBLOCKS 4
+#define ULA_GATHER_MINBLOCKS 2
 #endif
 #ifndef ULA_GATHER_UNROLL
-#define ULA_GATHER_UNROLL 8
+#define ULA_GATHER_UNROLL 16
 #endif
 #ifndef ULA_MOVE_MINBLOCKS
 #define ULA_MOVE_MINBLOCKS 3
