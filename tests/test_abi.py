@@ -70,3 +70,26 @@ def test_calls_reject_null_context_without_gpu(libpath):
     assert ula.lib.ula_sync(None, None) == ula.ERR_INVALID_ARG
     assert ula.lib.ula_create(None, None, None, None, None) == ula.ERR_INVALID_ARG
     ula.lib.ula_destroy(None)
+
+
+def test_binding_flags_match_header(libpath):
+    from serving_step_sparse_gb300 import ula
+    src = open(HEADER).read()
+    for name, val in (("ULA_FLAG_BYPASS_OVERFLOW", 1), ("ULA_FLAG_EXACT_LRU", 2),
+                      ("ULA_FLAG_LAYER_SIGNAL", 4), ("ULA_DEBUG_STALL_SCAN_BARRIER", 0x100),
+                      ("ULA_NOALLOC_MAX_ENTRIES", 65536)):
+        m = re.search(rf"#define {name} (0x[0-9a-fA-F]+|\d+)u?\b", src)
+        assert m and int(m.group(1), 0) == val, name
+        assert getattr(ula, name[4:]) == val, name
+
+
+def test_tp_calls_reject_null_without_gpu(libpath):
+    from serving_step_sparse_gb300 import ula
+    base = C.c_uint32()
+    assert ula.lib.ula_tp_alloc(None, 1, None, C.byref(base)) == ula.ERR_INVALID_ARG
+    assert ula.lib.ula_tp_free(None, 0, 1) == ula.ERR_INVALID_ARG
+    assert ula.lib.ula_tp_sync(None, None) == ula.ERR_INVALID_ARG
+    assert ula.lib.ula_tp_destroy(None) == ula.ERR_INVALID_ARG
+    assert not ula.lib.ula_tp_context(None, 0, 0)
+    assert ula.lib.ula_tp_create(None, 2, 4, None, None, None, None, None) == ula.ERR_INVALID_ARG
+    assert ula.lib.ula_layer_signal(None, 0, None, None) == ula.ERR_INVALID_ARG
