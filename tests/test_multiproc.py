@@ -59,3 +59,21 @@ def test_replica_aggregation_gloo(world):
 def test_single_rank_aggregation_is_identity():
     import bench
     assert bench.aggregate({"rows": 5.0, "value_ms": 2.0}, 1) == {"rows": 5.0, "value_ms": 2.0}
+
+
+def test_reference_arm_line(capsys):
+    """`bench.py --impl reference` prints one JSON line with the contract's keys: the oracle
+    timed single-threaded on a bounded sample, its e2e equal to its value, no host copies."""
+    import json
+
+    import bench
+    assert bench.main(["--impl", "reference", "--workload", "tiny_1x4k", "--steps", "4",
+                       "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "rows/s" and line["value"] > 0
+    assert line["steps"] == 4 and line["warmup"] == 3 and line["higher_is_better"] is True
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"].startswith("1 request")
