@@ -14,7 +14,7 @@ from tests.harness import ID_ROW_BYTES, apply_events, initial_allocs
 STAGE_ADDRS = 16384  # addresses per staged alloc chunk
 
 
-class GpuRun:
+class GpuReplay:
     def __init__(self, w, out_cap: int | None = None, stage_addrs: int = STAGE_ADDRS):
         self.w = w
         G, L = w.n_groups, w.layers_per_group

@@ -19,12 +19,12 @@ from tests.harness import OracleRun, check_invariants, check_step_outputs
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from tests.gpu_harness import (GpuRun, check_gpu_internal, check_layer_signal, compare_states,
+    from tests.gpu_harness import (GpuReplay, check_gpu_internal, check_layer_signal, compare_states,
                                    expand_id_rows, gpu_state_in_oracle_terms)
 
 
 def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2048, seed=0):
-    gpu = GpuRun(w)
+    gpu = GpuReplay(w)
     orc = OracleRun(w, mode)
     rng = np.random.default_rng(seed)
     try:
@@ -220,7 +220,7 @@ def test_layer_signal_consumers_on_another_stream():
     from serving_step_sparse_gb300 import ula
     from tests.harness import apply_events
     w = WORKLOADS["batch8_32k"].replace(layer_signal=True, steps=10)
-    gpu = GpuRun(w)
+    gpu = GpuReplay(w)
     orc = OracleRun(w, "bytes")
     L = w.layers_per_group
     side = torch.cuda.Stream()
@@ -539,7 +539,7 @@ def test_layer_ready_events_and_side_stream_order():
     """Layer j's event completes after its rows are written; a consumer waiting on
     each event (on another stream) reads the right bytes."""
     w = small("batch8_32k").replace(steps=6)
-    gpu = GpuRun(w)
+    gpu = GpuReplay(w)
     orc = OracleRun(w, "bytes")
     consumer = torch.cuda.Stream()
     try:
@@ -574,7 +574,7 @@ def test_regather_reproduces_hit_rows():
     """ula_debug_regather (used to time the gather alone) writes the same hit rows."""
     from serving_step_sparse_gb300 import ula
     w = small("batch8_32k").replace(steps=5)
-    gpu = GpuRun(w)
+    gpu = GpuReplay(w)
     try:
         for _ in range(w.steps):
             gpu.step()

@@ -36,12 +36,12 @@ def _noalloc(ula, d_sel, stream):
 @pytest.mark.parametrize("pads", [0.0, 0.05])
 def test_noalloc_dedup_matches_step_group(pads):
     from serving_step_sparse_gb300 import ula
-    from tests.gpu_harness import GpuRun
+    from tests.gpu_harness import GpuReplay
     from tests.harness import apply_events
 
     w = small("longdoc").replace(pad_prob=pads, steps=3)  # 3 query tokens: duplicates across them
     assert w.entries_per_step <= ula.NOALLOC_MAX_ENTRIES
-    gpu = GpuRun(w)
+    gpu = GpuReplay(w)
     stream = torch.cuda.Stream()
     calls = 0
     try:
