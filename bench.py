@@ -370,10 +370,14 @@ def run_gpu(args, rank, world, local):
     if args.traffic_case:
         st = cache.export(0)
         out = cache.out_buffer(0, max(1, st["U"]))
+        # the step's two launch kinds: layer 0 alone, then the later layers together
         ula.ula_debug_regather(cache.ctx, 0, 0, out.data_ptr(), out.shape[1], stream.cuda_stream)
+        if L > 1:
+            ula.ula_debug_regather(cache.ctx, 0, 1, out.data_ptr(), out.shape[1],
+                                   stream.cuda_stream, n_layers=L - 1)
         torch.cuda.synchronize()
         print(json.dumps({"traffic_case": {"hit_rows": st["hits"], "unique_rows": st["U"],
-                                           "gather_launches_before": args.warmup * G * L}}))
+                                           "gather_launches_before": args.warmup * G * min(L, 2)}}))
         cache.close()
         sys.exit(0)
     ula.ula_profile_read(cache.ctx, reset=True)
@@ -482,10 +486,12 @@ def run_gpu(args, rank, world, local):
                "d2h": d2h_bytes / n_e2e}
     clk = clocks.stop()
 
-    # ---- roofline of the gather: one launch per layer gathers the step's hit rows
-    # (algorithmic bytes: read the row from the pool, write it to out); missed rows'
-    # outputs are written by the move from the bytes it moves
-    hit_rows_prof = (st2["hits"] - st2a["hits"]) * L
+    # ---- roofline of the gather: two launches per group-step gather the step's hit
+    # rows (layer 0, then the later layers together; algorithmic bytes: read each
+    # layer's row from the pool, write it to out); missed rows' outputs are written by
+    # the move from the bytes it moves
+    hits_prof = st2["hits"] - st2a["hits"]
+    hit_rows_prof = hits_prof * L
     g_launch = prof["gather"]["timed"]
     g_ms = prof["gather"]["ms"]
     hbm_peak, hbm_src = measured_peaks()
@@ -493,10 +499,10 @@ def run_gpu(args, rank, world, local):
     per_launch_bytes = rows_per_launch * 2 * W
     avg_launch_s = g_ms / max(1, g_launch) / 1e3
     achieved = per_launch_bytes / avg_launch_s / 1e9 if avg_launch_s > 0 else 0.0
-    iso = isolated_gather(cache, ula, torch, dev, stream, W)
+    iso = isolated_gather(cache, ula, torch, dev, stream, W, L)
     roof = {"bound": "hbm", "kernel": "k_gather", "achieved": round(achieved, 1),
             "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-            "traffic": traffic_per_launch(rows_per_launch),
+            "traffic": traffic_per_launch(hits_prof, L, g_launch),
             "peak_source": f"{hbm_src} (hbm_gbs, STREAM-style copy)",
             "avg_launch_us": round(avg_launch_s * 1e6, 2),
             "rows_per_launch": round(rows_per_launch, 1), "bytes_per_row": 2 * W,
@@ -533,43 +539,54 @@ def run_gpu(args, rank, world, local):
     return res
 
 
-def isolated_gather(cache, ula, torch, dev, stream, W, reps=20):
-    """The gather kernel alone: re-gather group 0's last hit rows (layer 0), L2 flushed
-    between launches, CUDA events on the launching stream; with the step's grid and
-    with every block that fits on the SMs."""
+def isolated_gather(cache, ula, torch, dev, stream, W, L, reps=20):
+    """The gather kernel alone, in the step's two launches: re-gather group 0's last hit
+    rows (layer 0 alone, then layers 1..L-1 together), L2 flushed before each launch,
+    CUDA events on the launching stream; with the step's grid and with every block
+    that fits on the SMs."""
     st = cache.export(0)
     hits = st["hits"]
     out = cache.out_buffer(0, max(1, st["U"]))
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     peak, _ = measured_peaks()
+    kinds = [(0, 1)] + ([(1, L - 1)] if L > 1 else [])
     res = {}
     for name, bps in (("step_grid", 0), ("full_grid", 64)):
-        ms = []
+        ms = {k: [] for k in kinds}
         for i in range(reps + 2):
-            flush.zero_()
-            e0.record(stream)
-            ula.ula_debug_regather(cache.ctx, 0, 0, out.data_ptr(), out.shape[1], stream.cuda_stream,
-                                   blocks_per_sm=bps)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= 2:
-                ms.append(e0.elapsed_time(e1))
-        avg = sum(ms) / len(ms)
-        ach = hits * 2 * W / (avg / 1e3) / 1e9
+            for k in kinds:
+                flush.zero_()
+                e0.record(stream)
+                ula.ula_debug_regather(cache.ctx, 0, k[0], out.data_ptr(), out.shape[1],
+                                       stream.cuda_stream, blocks_per_sm=bps, n_layers=k[1])
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 2:
+                    ms[k].append(e0.elapsed_time(e1))
+        avg = {k: sum(v) / len(v) for k, v in ms.items()}
+        ach = hits * L * 2 * W / (sum(avg.values()) / 1e3) / 1e9
         res[name] = {"achieved": round(ach, 1), "frac": round(ach / peak, 4),
-                     "avg_launch_us": round(avg * 1e3, 2)}
-    res.update({"rows_per_launch": hits, "launches": reps,
+                     "avg_launch_us": round(sum(avg.values()) / len(avg) * 1e3, 2),
+                     "launch_us": {f"layers {k[0]}..{k[0] + k[1] - 1}": round(v * 1e3, 2)
+                                   for k, v in avg.items()}}
+        if L > 1:
+            k = kinds[1]
+            a1 = hits * k[1] * 2 * W / (avg[k] / 1e3) / 1e9
+            res[name]["later_layers"] = {"achieved": round(a1, 1), "frac": round(a1 / peak, 4)}
+    res.update({"hit_rows": hits, "launches": reps * len(kinds),
                 "l2": "flushed (512 MB write) before each launch"})
     return res
 
 
 # Traffic measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for the gather
-# kernel, per gathered row, together with the hash of the gather kernel's source (its
-# launch-shape defaults and its body) it was taken on.  Reported only while that source
-# is unchanged.
-GATHER_TRAFFIC = {"source_sha256": "c07c3f8b76e6d22b1c75373cc5990047b1b3fe06ea9371b26ede09c97f25d7f0",
-                  "bytes_per_row": 18775040 / 24255}  # 24,255 hit rows, 12-request case
+# kernel per gathered row, for each of the step's two launch kinds (layer 0 alone; the
+# later layers together, per slot), together with the hash of the gather kernel's
+# source (its launch-shape defaults and its body) it was taken on.  Reported only
+# while that source is unchanged.
+GATHER_TRAFFIC = {"source_sha256": "e62f8e069d3c64c3cdbd2040b9cf5c5d7ab81e1ae9b55abde3d1ba6724d044c9",
+                  "layer0_bytes_per_row": 18786048 / 24255,  # 24,255 hit rows, 12-request case
+                  "later_bytes_per_slot": 51863040 / 24255}  # layers 1-3 of the same rows
 
 
 def gather_source_sha256() -> str:
@@ -582,10 +599,14 @@ def gather_source_sha256() -> str:
     return hashlib.sha256("\n".join(keep).encode()).hexdigest()
 
 
-def traffic_per_launch(rows_per_launch):
-    if GATHER_TRAFFIC["source_sha256"] != gather_source_sha256():
+def traffic_per_launch(hits, L, launches):
+    """DRAM bytes per gather launch in the step: `hits` hit rows gathered by layer-0
+    launches and by later-layer launches (L - 1 layers each), `launches` of both kinds."""
+    t = GATHER_TRAFFIC
+    if t["source_sha256"] != gather_source_sha256() or not launches:
         return None
-    return round(GATHER_TRAFFIC["bytes_per_row"] * rows_per_launch)
+    later = t["later_bytes_per_slot"] if L > 1 else 0.0
+    return round(hits * (t["layer0_bytes_per_row"] + later) / launches)
 
 
 # ------------------------------------------------------------- CPU oracle arm

@@ -286,20 +286,24 @@ int ula_debug_layer_times(ula_ctx *ctx, uint32_t group, unsigned long long *ns);
 int ula_debug_consume(ula_ctx *ctx, uint32_t group, uint32_t layer, uint32_t round,
                       const void *d_out, uint32_t out_cap_rows, uint32_t n_rows,
                       unsigned long long *d_result, void *stream);
-/* Re-run the gather of the hit rows of `group`'s last step for one layer into d_out
- * ([L_g][out_cap_rows][row_bytes], device) on `stream`, changing no state (for timing
- * the gather kernel on its own).  Launches at once: the caller orders it after the
- * step (e.g. ula_sync) and before the group's slots change again (its next step, or
- * any alloc/free).  More rows than out_cap_rows latch ULA_ERR_CAPACITY. */
-int ula_debug_regather(ula_ctx *ctx, uint32_t group, uint32_t layer, void *d_out,
-                       uint32_t out_cap_rows, uint32_t blocks_per_sm, void *stream);
+/* Re-run the gather of the hit rows of `group`'s last step for layers
+ * [layer, layer + n_layers) in one launch, as the step does (layer 0 alone, the later
+ * layers together), into d_out ([L_g][out_cap_rows][row_bytes], device) on `stream`,
+ * changing no state (for timing the gather kernel on its own).  Launches at once: the
+ * caller orders it after the step (e.g. ula_sync) and before the group's slots change
+ * again (its next step, or any alloc/free).  n_layers 0 or past L_g is
+ * ULA_ERR_INVALID_ARG; more rows than out_cap_rows latch ULA_ERR_CAPACITY. */
+int ula_debug_regather(ula_ctx *ctx, uint32_t group, uint32_t layer, uint32_t n_layers,
+                       void *d_out, uint32_t out_cap_rows, uint32_t blocks_per_sm,
+                       void *stream);
 /* blocks_per_sm: 0 = the grid the step uses; otherwise that many blocks per SM (at most
  * what fits). */
 
 /* ------------------------------------------------------------ profiling
  * Kernel launches are counted per phase always.  When enabled, every phase
  * instance is bracketed by two CUDA events recorded on the stream it is launched
- * on (the gather: once per layer, on the caller's or the side stream), and
+ * on (the gather: once for layer 0 and once for the later layers together, on
+ * their two streams), and
  * ula_profile_read sums their durations.  Reading synchronises the context.
  */
 enum {
@@ -308,7 +312,7 @@ enum {
   ULA_PHASE_MARK,       /* hit marking, entry rows, victim walk over segment counts */
   ULA_PHASE_SELECT,     /* victim (or free-slot) index emission */
   ULA_PHASE_MOVE,       /* write-back, fill (and the missed rows' outputs), map commit */
-  ULA_PHASE_GATHER,     /* one layer's gather of the hit rows */
+  ULA_PHASE_GATHER,     /* a gather of the hit rows: layer 0, or the later layers */
   ULA_PHASE_ALLOC,      /* alloc placement and copy-in */
   ULA_PHASE_FREE,       /* free */
   ULA_PHASE_COUNT

@@ -2,10 +2,13 @@
 // checks, stream/event ordering, and the per-call kernel sequences.
 //
 // Ordering rules (UlaCache summary page, §2 (the paragraph on layer groups sharing a selection) and §3 last
-// paragraph): a step's kernels run in stream order -- dedup/translate ->
-// capacity check -> rotate/mark -> victim selection -> move+commit -> signal
-// -> gather; layer 0 is gathered on the caller's stream, later layers on the
-// context's side stream after the commit event (prefetch).  Every call is
+// paragraph): a step's critical-path kernels run in stream order on an internal
+// high-priority stream -- dedup/translate + capacity check -> rotate/compact ->
+// mark/victim walk -> victim emit -> move+commit -> signal.  The hit rows are
+// gathered once the marking is done, beside the move: layer 0 on a second
+// high-priority stream (the caller's stream waits for it and the commit), the
+// later layers in one launch on the low-priority side stream (prefetch; their
+// ready events follow it and the commit).  Every call is
 // ordered after the previous call on the context (event wait when the stream
 // changes), and anything touching group g first waits for group g's pending
 // side-stream gathers, so a slot is never refilled while an earlier gather of
@@ -20,6 +23,12 @@
 using namespace ula;
 
 namespace {
+
+// The later layers' hit rows in one launch per step (a slot's rows of those layers
+// are contiguous); 0 launches one gather per layer instead.
+#ifndef ULA_GATHER_MERGE_LAYERS
+#define ULA_GATHER_MERGE_LAYERS 1
+#endif
 
 constexpr uint32_t kAllocChunk = 65536;
 // Internal: a TP rank's local buffer (misses fetched from the owner partitions,
@@ -621,17 +630,20 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   if (gather) {
     // (6) the hit rows, while the misses are being moved (a hit's slot does not
     // change in its round): layer 0 on a high-priority stream, the later layers
-    // on the low-priority prefetch stream
+    // together (one contiguous read per slot) on the low-priority prefetch stream
     ULA_CUDA(cudaEventRecord(c->marked_evt, s));
     ULA_CUDA(cudaStreamWaitEvent(c->first, c->marked_evt, 0));
     gp.layer = 0;
+    gp.nlayers = 1;
     ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->first, 1,
                       [&] { return launch_gather(gp, c->gather_blocks, c->first); }));
     ULA_CUDA(cudaEventRecord(c->hit0_evt, c->first));
     ULA_CUDA(cudaStreamWaitEvent(c->side, c->marked_evt, 0));
-    for (uint32_t j = 1; j < gd.layers; ++j) {
+    const uint32_t per = ULA_GATHER_MERGE_LAYERS ? gd.layers - 1 : 1;
+    for (uint32_t j = 1; j < gd.layers; j += per) {
       gp.layer = j;
-      ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, 1,
+      gp.nlayers = per;
+      ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, gather_launches(c->geo.W, per),
                         [&] { return launch_gather(gp, c->gather_blocks, c->side); }));
     }
   }
@@ -829,12 +841,13 @@ int ula_profile_read(ula_ctx *c, ula_profile *out, int reset) {
   return ULA_OK;
 }
 
-int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, void *d_out,
-                       uint32_t out_cap_rows, uint32_t blocks_per_sm, void *stream) {
+int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, uint32_t n_layers,
+                       void *d_out, uint32_t out_cap_rows, uint32_t blocks_per_sm, void *stream) {
   if (!c || group >= c->cfg.n_groups || !d_out || !aligned16(d_out)) return ULA_ERR_INVALID_ARG;
   if (c->poisoned) return ULA_ERR_POISONED;
   const GroupDev &gd = c->groups_h[group];
-  if (layer >= gd.layers || out_cap_rows < 1) return ULA_ERR_INVALID_ARG;
+  if (layer >= gd.layers || n_layers < 1 || n_layers > gd.layers - layer || out_cap_rows < 1)
+    return ULA_ERR_INVALID_ARG;
   ULA_CUDA(c->ensure_device());
   cudaStream_t caller = static_cast<cudaStream_t>(stream);
   GatherParams gp{};
@@ -843,6 +856,7 @@ int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, void *d_out,
   gp.out = static_cast<uint8_t *>(d_out);
   gp.out_cap = out_cap_rows;
   gp.layer = layer;
+  gp.nlayers = n_layers;
   gp.status = c->status;
   int blocks = c->gather_blocks;
   if (blocks_per_sm) {

@@ -227,8 +227,9 @@ struct GatherParams {
   GroupDev grp;
   uint8_t *out;             // [L][out_cap][W]
   uint32_t out_cap;
-  uint32_t layer;
-  uint32_t signal;          // contributes to the layer's signal (a step's gather)
+  uint32_t layer;           // the launch gathers layers [layer, layer + nlayers)
+  uint32_t nlayers;
+  uint32_t signal;          // contributes to the layers' signals (a step's gather)
   uint32_t round;
   int *status;
 };
@@ -264,6 +265,7 @@ cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int block
 cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s);
 cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s);  // copies, then commit
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
+int gather_launches(uint32_t row_bytes, uint32_t nlayers);  // kernels one launch_gather makes
 // exact LRU: victims [F, M) by a scan of the slot timestamps (cooperative launch of
 // `blocks` co-resident blocks)
 cudaError_t launch_lru_select(const LruParams &p, int blocks, cudaStream_t s);

@@ -931,14 +931,15 @@ __global__ void k_commit(MoveParams p) {
 
 // ------------------------------------------------------------------ gather
 //
-// (6) out[layer][u] = layer `layer` of unique row u's slot, for the rows that hit
-// (recorded by the marking; a hit's slot does not change in its round, so this
-// runs while the misses are being moved; missed rows are written by the move).
-// The U rows are spread over all warps (rows_per_warp = ceil(U / warps), at most
-// 32): lanes read the warp's slots, then the warp streams the rows' 16-byte
-// chunks, consecutive lanes on consecutive chunks (coalesced within a row; the
-// warp's output rows are contiguous).  Loads are issued kGatherUnroll deep before
-// the stores.
+// (6) out[j][u] = layer j of unique row u's slot for the layers j of this launch,
+// [layer, layer + nlayers), for the rows that hit (recorded by the marking; a hit's
+// slot does not change in its round, so this runs while the misses are being moved;
+// missed rows are written by the move).  A slot holds its layers' rows back to back,
+// so the launch reads nlayers * W contiguous bytes per slot.  The U rows are spread
+// over all warps (rows_per_warp = ceil(U / warps), at most 32): lanes read the warp's
+// slots, then the warp streams the rows' 16-byte chunks, consecutive lanes on
+// consecutive chunks (coalesced within a slot; per layer, the warp's output rows are
+// contiguous).  Loads are issued kGatherUnroll deep before the stores.
 constexpr int kGatherUnroll = ULA_GATHER_UNROLL;
 
 __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather(GatherParams p) {
@@ -954,12 +955,16 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
   const uint32_t CW = geo.W / 16;
+  const uint32_t NL = p.nlayers;
+  const uint32_t RW = NL * CW;                 // chunks per slot in this launch
   const size_t sbv = (size_t)g.layers * CW;  // slot stride in uint4
+  const size_t lsv = (size_t)p.out_cap * CW;  // output layer stride in uint4
   const uint4 *pool = reinterpret_cast<const uint4 *>(g.gpu_pool) + (size_t)p.layer * CW;
-  uint4 *out = reinterpret_cast<uint4 *>(p.out) + (size_t)p.layer * p.out_cap * CW;
+  uint4 *out = reinterpret_cast<uint4 *>(p.out) + (size_t)p.layer * lsv;
   uint32_t rpw = (U + nwarps - 1) / nwarps;
   rpw = rpw < 1 ? 1 : (rpw > 32 ? 32 : rpw);
-  const uint32_t r0 = lane / CW, c0 = lane % CW;  // chunk (row, col) of f = lane
+  // chunk f = lane of a warp's rows: row r0, layer j0, column c0
+  const uint32_t r0 = lane / RW, j0 = (lane % RW) / CW, c0 = lane % CW;
   for (uint32_t row0 = warp * rpw; row0 < U; row0 += nwarps * rpw) {
     const uint32_t nrows = min(rpw, U - row0);
     uint32_t slot = kNone;
@@ -973,41 +978,49 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
       if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
       continue;
     }
-    const uint32_t total = nrows * CW;
+    const uint32_t total = nrows * RW;
     uint4 *orow = out + (size_t)row0 * CW;
-    uint32_t r = r0, c = c0;
+    uint32_t r = r0, j = j0, c = c0;
     for (uint32_t f0 = 0; f0 < total; f0 += 32 * kGatherUnroll) {
       uint4 v[kGatherUnroll];
-      const uint32_t rs = r, cs = c;
+      const uint32_t rs = r, js = j, cs = c;
 #pragma unroll
       for (int u = 0; u < kGatherUnroll; ++u) {
         const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
-        if (f0 + u * 32 + lane < total && s != kNone) v[u] = __ldcs(pool + (size_t)s * sbv + c);
+        if (f0 + u * 32 + lane < total && s != kNone)
+          v[u] = __ldcs(pool + (size_t)s * sbv + j * CW + c);
         c += 32;
         while (c >= CW) {
           c -= CW;
-          ++r;
+          if (++j == NL) {
+            j = 0;
+            ++r;
+          }
         }
       }
       r = rs;
+      j = js;
       c = cs;
 #pragma unroll
       for (int u = 0; u < kGatherUnroll; ++u) {
         const uint32_t s = __shfl_sync(0xffffffffu, slot, r & 31);
-        if (f0 + u * 32 + lane < total && s != kNone) orow[(size_t)r * CW + c] = v[u];
+        if (f0 + u * 32 + lane < total && s != kNone) orow[j * lsv + (size_t)r * CW + c] = v[u];
         c += 32;
         while (c >= CW) {
           c -= CW;
-          ++r;
+          if (++j == NL) {
+            j = 0;
+            ++r;
+          }
         }
       }
     }
   }
-  // per-layer signal: the hit rows of this layer are one of its two contributions
+  // per-layer signal: the hit rows of a layer are one of its two contributions
   if (p.signal) {
     __threadfence();  // every thread's output writes before the block's ticket
     if (last_block(&g.gather_done[p.layer]) && threadIdx.x == 0)
-      layer_contrib(g, p.layer, 2u, p.round);
+      for (uint32_t j = p.layer; j < p.layer + NL; ++j) layer_contrib(g, j, 2u, p.round);
   }
 }
 
@@ -2018,11 +2031,21 @@ bool gather_uses_tma(uint32_t row_bytes) {
 }
 
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s) {
-  if (gather_uses_tma(p.geo.W))
-    k_gather_tma<<<blocks, 32, gather_tma_smem(p.geo.W), s>>>(p);
-  else
+  if (gather_uses_tma(p.geo.W)) {  // one launch per layer
+    for (uint32_t j = 0; j < p.nlayers; ++j) {
+      GatherParams q = p;
+      q.layer = p.layer + j;
+      q.nlayers = 1;
+      k_gather_tma<<<blocks, 32, gather_tma_smem(p.geo.W), s>>>(q);
+    }
+  } else {
     k_gather<<<blocks, kGatherThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
+}
+
+int gather_launches(uint32_t row_bytes, uint32_t nlayers) {
+  return gather_uses_tma(row_bytes) ? (int)nlayers : 1;
 }
 
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,

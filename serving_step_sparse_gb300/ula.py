@@ -104,7 +104,7 @@ def _load():
     lib.ula_profile_enable.restype = i32
     lib.ula_profile_read.argtypes = [p, C.POINTER(ula_profile), i32]
     lib.ula_profile_read.restype = i32
-    lib.ula_debug_regather.argtypes = [p, u32, u32, p, u32, u32, p]
+    lib.ula_debug_regather.argtypes = [p, u32, u32, u32, p, u32, u32, p]
     lib.ula_debug_regather.restype = i32
     lib.ula_dedup_noalloc.argtypes = [p, u32, p, p, p, p]
     lib.ula_dedup_noalloc.restype = i32
@@ -286,9 +286,9 @@ def ula_debug_inject(ctx: int, code: int) -> None:
 
 
 def ula_debug_regather(ctx: int, group: int, layer: int, d_out: int, out_cap_rows: int,
-                       stream, blocks_per_sm: int = 0) -> None:
-    _check(lib.ula_debug_regather(ctx, group, layer, d_out, out_cap_rows, blocks_per_sm, stream),
-           "ula_debug_regather")
+                       stream, blocks_per_sm: int = 0, n_layers: int = 1) -> None:
+    _check(lib.ula_debug_regather(ctx, group, layer, n_layers, d_out, out_cap_rows,
+                                  blocks_per_sm, stream), "ula_debug_regather")
 
 
 def ula_profile_enable(ctx: int, on: bool) -> None:

@@ -592,5 +592,23 @@ def test_regather_reproduces_hit_rows():
                 got = buf[j, :U].cpu().numpy()[hit]
                 exp = gpu.outs[g][j, :U].cpu().numpy()[hit]
                 assert np.array_equal(got, exp)
+            # layer ranges in one launch (the step gathers layers 1..L-1 together)
+            L = w.layers_per_group
+            for j0, n in ((1, L - 1), (0, L), (0, L - 1)):
+                buf = torch.zeros_like(gpu.outs[g])
+                ula.ula_debug_regather(gpu.cache.ctx, g, j0, buf.data_ptr(), buf.shape[1],
+                                       torch.cuda.current_stream().cuda_stream,
+                                       blocks_per_sm=2 if j0 else 0, n_layers=n)
+                torch.cuda.synchronize()
+                got = buf[:, :U].cpu().numpy()
+                exp = gpu.outs[g][:, :U].cpu().numpy()
+                for j in range(L):
+                    if j0 <= j < j0 + n:
+                        assert np.array_equal(got[j][hit], exp[j][hit]), (j0, n, j)
+                    else:
+                        assert not got[j].any(), (j0, n, j)  # other layers untouched
+            with pytest.raises(ula.UlaError):
+                ula.ula_debug_regather(gpu.cache.ctx, g, 1, buf.data_ptr(), buf.shape[1],
+                                       torch.cuda.current_stream().cuda_stream, n_layers=L)
     finally:
         gpu.close()
