@@ -43,15 +43,17 @@ constexpr int kStampThreads = 256;
 constexpr int kWalkSegs = 4;        // segments per thread per step of the victim walk
 constexpr int kMarkClasses = 8;     // class words a marking warp loads at once
 
-// Launch shapes of the two persistent copy kernels (build-time tunables).
+// Launch shapes of the two persistent copy kernels (build-time tunables).  A gather
+// block (<= 80 registers a thread at 3 blocks per SM) fits in the register file
+// beside two move blocks (80 registers), so the hit gathers and the move share the SMs.
 #ifndef ULA_GATHER_THREADS
 #define ULA_GATHER_THREADS 256
 #endif
 #ifndef ULA_GATHER_MINBLOCKS
-#define ULA_GATHER_MINBLOCKS 2
+#define ULA_GATHER_MINBLOCKS 3
 #endif
 #ifndef ULA_GATHER_UNROLL
-#define ULA_GATHER_UNROLL 16
+#define ULA_GATHER_UNROLL 12
 #endif
 #ifndef ULA_MOVE_MINBLOCKS
 #define ULA_MOVE_MINBLOCKS 3
