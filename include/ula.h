@@ -181,9 +181,10 @@ int ula_free(ula_ctx *ctx, uint32_t logical_base, uint32_t n);
  *       to the j-th lowest free host slot), fill each miss from its host slot, then
  *       update the map (moves complete before the map changes) and signal,
  *   (6) gather out[j][u] = layer j of unique address u, for every layer of the group.
- *       Rows that hit are gathered on the context's low-priority side stream as soon
- *       as the hits are known (their slots never move in this round); rows that
- *       missed are written by the fill itself, from the bytes it moves.
+ *       Rows that hit are gathered as soon as the hits are known (their slots never
+ *       move in this round), beside the move: layer 0 on an internal high-priority
+ *       stream, the later layers together on the context's low-priority side stream;
+ *       rows that missed are written by the fill itself, from the bytes it moves.
  * The work runs on the context's internal highest-priority stream, ordered after
  * everything already enqueued on `stream`; `stream` is made to wait for the commit
  * and for layer 0, so work the caller enqueues next on `stream` sees layer 0 and the
