@@ -513,7 +513,8 @@ def run_gpu(args, rank, world, local):
     mv_s = prof["move"]["ms"] / 1e3
     h2d_b = st2["bytes_h2d"] - st2a["bytes_h2d"]
     d2h_b = st2["bytes_d2h"] - st2a["bytes_d2h"]
-    host = {"kernel": "k_move_commit", "fill_gbs": round(h2d_b / mv_s / 1e9, 1) if mv_s else 0,
+    host = {"kernel": "k_move_layers + k_commit" if args.layer_signal else "k_move",
+            "fill_gbs": round(h2d_b / mv_s / 1e9, 1) if mv_s else 0,
             "writeback_gbs": round(d2h_b / mv_s / 1e9, 1) if mv_s else 0,
             "peak_h2d_gbs": round(link["h2d_gbs"], 1), "peak_d2h_gbs": round(link["d2h_gbs"], 1),
             "peak_bidir_gbs": round(link["bidir_gbs"], 1),
