@@ -77,3 +77,23 @@ def test_reference_arm_line(capsys):
     assert line["e2e"] == {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"].startswith("1 request")
+
+
+def test_roofline_helpers(monkeypatch):
+    """The gather's DRAM traffic per launch: the two launch kinds' per-row figures times
+    the hits, averaged over launches; withheld once the kernel's source hash moves."""
+    import bench
+    t = dict(bench.GATHER_TRAFFIC)
+    # DRAM reads cover at least the algorithmic reads: one 656-byte row, three of a slot
+    assert 656 <= t["layer0_bytes_per_row"] < 2 * 656
+    assert 3 * 656 <= t["later_bytes_per_slot"] < 2 * 3 * 656
+    monkeypatch.setattr(bench, "gather_source_sha256", lambda: t["source_sha256"])
+    hits, L, launches = 1000, 4, 2
+    exp = hits * (t["layer0_bytes_per_row"] + t["later_bytes_per_slot"]) / launches
+    assert bench.traffic_per_launch(hits, L, launches) == round(exp)
+    assert bench.traffic_per_launch(hits, 1, 1) == round(hits * t["layer0_bytes_per_row"])
+    assert bench.traffic_per_launch(hits, L, 0) is None
+    monkeypatch.setattr(bench, "gather_source_sha256", lambda: "0" * 64)
+    assert bench.traffic_per_launch(hits, L, launches) is None
+    peak, src = bench.measured_peaks()
+    assert peak > 1000 and src in ("measured", "fallback")
