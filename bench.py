@@ -46,6 +46,10 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="longdoc")
     ap.add_argument("--policy", choices=["pblru", "exact"], default="pblru",
                     help="replacement policy: PB-LRU, or exact LRU (timestamp scan)")
+    ap.add_argument("--repeats", type=int, default=3,
+                    help="timed regions of --steps steps each; value = their median")
+    ap.add_argument("--gather-beside", action="store_true",
+                    help="run the hit gather beside the move (ULA_FLAG_GATHER_BESIDE_MOVE)")
     ap.add_argument("--profile-steps", type=int, default=60)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -191,6 +195,35 @@ def host_link_peaks(torch, nbytes=1 << 30):
            "bidir_gbs": 2 * nbytes / best(both) / 1e9}
     del h, h2, d, d2
     return out
+
+
+class LinkProbe:
+    """The copy engines' bidirectional pinned-copy rate right now (both directions at
+    once, `nbytes` each way, best of `reps`): taken beside each timed region, so that a
+    region's move rate can be set against the link as it was at that moment (the host
+    link is shared with other work on the machine)."""
+
+    def __init__(self, torch, nbytes=256 << 20):
+        self.torch, self.n = torch, nbytes
+        self.h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        self.h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+        self.d = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.d2 = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.s1, self.s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def bidir_gbs(self, reps=3):
+        torch = self.torch
+        best = 1e9
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            with torch.cuda.stream(self.s1):
+                self.d.copy_(self.h, non_blocking=True)
+            with torch.cuda.stream(self.s2):
+                self.h2.copy_(self.d2, non_blocking=True)
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return 2 * self.n / best / 1e9
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -340,11 +373,12 @@ def run_gpu(args, rank, world, local):
                      host_slots=w.host_slots, ring_buckets=w.ring_buckets,
                      max_logical=w.max_logical, max_entries=E, device=dev, stream=stream,
                      bypass_overflow=w.bypass, exact_lru=w.exact_lru,
-                     layer_signal=args.layer_signal)
+                     layer_signal=args.layer_signal, gather_beside_move=args.gather_beside)
     trace = stage_initial(cache, w, synth, torch)
-    n_value, n_prof = args.steps, min(args.profile_steps, args.steps)
-    n_lat = min(args.latency_steps, args.steps)
-    n_e2e = 0 if args.no_e2e else args.steps
+    K, reps = args.steps, max(1, args.repeats)
+    n_value, n_prof = K * reps, min(args.profile_steps, K)
+    n_lat = min(args.latency_steps, K)
+    n_e2e = 0 if args.no_e2e else K
     steps = gen_steps(trace, w, args.warmup + n_value + n_prof + n_lat + n_e2e, synth, np)
     outs = [cache.out_buffer(g, E) for g in range(G)]
     entry_row = [torch.empty(E, dtype=torch.int32, device=dev) for _ in range(G)]
@@ -370,14 +404,12 @@ def run_gpu(args, rank, world, local):
     if args.traffic_case:
         st = cache.export(0)
         out = cache.out_buffer(0, max(1, st["U"]))
-        # the step's two launch kinds: layer 0 alone, then the later layers together
-        ula.ula_debug_regather(cache.ctx, 0, 0, out.data_ptr(), out.shape[1], stream.cuda_stream)
-        if L > 1:
-            ula.ula_debug_regather(cache.ctx, 0, 1, out.data_ptr(), out.shape[1],
-                                   stream.cuda_stream, n_layers=L - 1)
+        # the step's gather launch: every layer of group 0's hit rows in one launch
+        ula.ula_debug_regather(cache.ctx, 0, 0, out.data_ptr(), out.shape[1], stream.cuda_stream,
+                               n_layers=L)
         torch.cuda.synchronize()
         print(json.dumps({"traffic_case": {"hit_rows": st["hits"], "unique_rows": st["U"],
-                                           "gather_launches_before": args.warmup * G * min(L, 2)}}))
+                                           "gather_launches_before": args.warmup * G}}))
         cache.close()
         sys.exit(0)
     ula.ula_profile_read(cache.ctx, reset=True)
@@ -388,27 +420,43 @@ def run_gpu(args, rank, world, local):
 
     clocks = ClockSampler(local)
     clocks.start()
-    # ---- value: inputs resident in HBM
+    # ---- value: inputs resident in HBM; `reps` timed regions of K steps each, with the
+    # copy kernels' device spans recorded in the same pass
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_push("timed")
-    e0.record(stream)
-    for t in range(args.warmup, args.warmup + n_value):
-        do_step(sel_dev[t], steps[t][1], rows_dev[t])
-    e1.record(stream)
-    torch.cuda.nvtx.range_pop()
+    probe = LinkProbe(torch)
+    repeats = []
+    launches = 0
+    t = args.warmup
+    for rep in range(reps):
+        sa = cache.sync()
+        ula.ula_profile_spans(cache.ctx, True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(K):
+            do_step(sel_dev[t], steps[t][1], rows_dev[t])
+            t += 1
+        e1.record(stream)
+        sb = cache.sync()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ms = e0.elapsed_time(e1)
+        spans = ula.ula_profile_spans_read(cache.ctx)
+        ula.ula_profile_spans(cache.ctx, False)
+        launches += sum(p["kernels"] for p in ula.ula_profile_read(cache.ctx, reset=True).values())
+        d = {k: sb[k] - sa[k] for k in sb}
+        repeats.append({"ms": ms, "stats": d, "spans": span_summary(spans, d, L, W, G * K),
+                        "ce_bidir_gbs": probe.bidir_gbs()})
+    launches //= reps
+    order = sorted(range(reps), key=lambda i: repeats[i]["ms"])
+    med = repeats[order[reps // 2]]
+    value_ms = med["ms"]
+    rows_value = med["stats"]["rows_gathered"]
     st1 = cache.sync()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    value_ms = e0.elapsed_time(e1)
-    prof_value = ula.ula_profile_read(cache.ctx, reset=True)
-    launches = sum(p["kernels"] for p in prof_value.values())
-    rows_value = st1["rows_gathered"] - st0["rows_gathered"]
 
-    # ---- profiled pass: per-launch gather / move durations on their own streams
+    # ---- profiled pass: per-phase CUDA-event durations (metadata phases included)
     ula.ula_profile_enable(cache.ctx, True)
     st2a = cache.sync()
     for t in range(args.warmup + n_value, args.warmup + n_value + n_prof):
@@ -486,50 +534,70 @@ def run_gpu(args, rank, world, local):
                "d2h": d2h_bytes / n_e2e}
     clk = clocks.stop()
 
-    # ---- roofline of the gather: two launches per group-step gather the step's hit
-    # rows (layer 0, then the later layers together; algorithmic bytes: read each
-    # layer's row from the pool, write it to out); missed rows' outputs are written by
-    # the move from the bytes it moves
-    hits_prof = st2["hits"] - st2a["hits"]
-    hit_rows_prof = hits_prof * L
-    g_launch = prof["gather"]["timed"]
-    g_ms = prof["gather"]["ms"]
+    # ---- roofline of the gather (the dominant HBM bytes): one launch per group-step gathers
+    # every layer of the step's hit rows (algorithmic bytes: each layer's row read from the
+    # pool and written to out; missed rows' outputs are written by the move from the bytes
+    # it moves).  Durations are the launches' device spans in the median timed region.
     hbm_peak, hbm_src = measured_peaks()
-    rows_per_launch = hit_rows_prof / max(1, g_launch)
-    per_launch_bytes = rows_per_launch * 2 * W
-    avg_launch_s = g_ms / max(1, g_launch) / 1e3
-    achieved = per_launch_bytes / avg_launch_s / 1e9 if avg_launch_s > 0 else 0.0
+    sp = med["spans"]
+    ga = sp.get("gather", {"launches": 0, "sum_us": 0.0, "union_us": 0.0})
+    hit_rows = med["stats"]["hits"] * L
+    g_bytes = hit_rows * 2 * W
+    avg_launch_us = ga["sum_us"] / max(1, ga["launches"])
+    achieved = g_bytes / (ga["sum_us"] * 1e3) if ga["sum_us"] else 0.0  # bytes/ns = GB/s
     iso = isolated_gather(cache, ula, torch, dev, stream, W, L)
     roof = {"bound": "hbm", "kernel": "k_gather", "achieved": round(achieved, 1),
             "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-            "traffic": traffic_per_launch(hits_prof, L, g_launch),
+            "traffic": traffic_per_launch(med["stats"]["hits"], ga["launches"], w.name),
             "peak_source": f"{hbm_src} (hbm_gbs, STREAM-style copy)",
-            "avg_launch_us": round(avg_launch_s * 1e6, 2),
-            "rows_per_launch": round(rows_per_launch, 1), "bytes_per_row": 2 * W,
-            "timing": "in the step: per-launch CUDA events on the launching stream, "
-                      "running beside the move and the next group's metadata",
+            "avg_launch_us": round(avg_launch_us, 2),
+            "bytes_per_launch": round(g_bytes / max(1, ga["launches"])),
+            "rows_per_launch": round(hit_rows / max(1, ga["launches"]), 1), "bytes_per_row": 2 * W,
+            "union_us_per_step": round(ga["union_us"] / K, 2),
+            "timing": ("in the timed region (median repeat): device globaltimer span of each "
+                       "gather launch, first warp start to last warp end; achieved = hit-gather "
+                       "bytes / summed spans (the launches do not overlap: union "
+                       f"{ga['union_us']:.1f} us, sum {ga['sum_us']:.1f} us)"),
             "isolated": iso}
-    # ---- host link: the move kernel moves fills (H2D) and write-backs (D2H) at once
-    mv_s = prof["move"]["ms"] / 1e3
-    h2d_b = st2["bytes_h2d"] - st2a["bytes_h2d"]
-    d2h_b = st2["bytes_d2h"] - st2a["bytes_d2h"]
+    # ---- host link: the move kernel moves fills (H2D) and write-backs (D2H) at once;
+    # its device spans in the same timed region
+    mv = sp.get("move", {"launches": 0, "sum_us": 0.0, "union_us": 0.0})
+    mv_s = mv["sum_us"] / 1e6
+    h2d_b, d2h_b = med["stats"]["bytes_h2d"], med["stats"]["bytes_d2h"]
     host = {"kernel": "k_move_layers + k_commit" if args.layer_signal else "k_move",
             "fill_gbs": round(h2d_b / mv_s / 1e9, 1) if mv_s else 0,
             "writeback_gbs": round(d2h_b / mv_s / 1e9, 1) if mv_s else 0,
+            "total_gbs": round((h2d_b + d2h_b) / mv_s / 1e9, 1) if mv_s else 0,
             "peak_h2d_gbs": round(link["h2d_gbs"], 1), "peak_d2h_gbs": round(link["d2h_gbs"], 1),
             "peak_bidir_gbs": round(link["bidir_gbs"], 1),
-            "peak_source": "measured in this run: pinned cudaMemcpyAsync, 1 GiB"}
+            "peak_source": "measured in this run: pinned cudaMemcpyAsync, 1 GiB",
+            "timing": "device spans of the move launches in the median timed region",
+            "move_us_per_step": round(mv["sum_us"] / K, 2)}
     if mv_s:
         host["frac_fill"] = round(h2d_b / mv_s / 1e9 / link["h2d_gbs"], 4)
         host["frac_total"] = round((h2d_b + d2h_b) / mv_s / 1e9 / link["bidir_gbs"], 4)
+    rep_lines = []
+    for r in repeats:
+        m = r["spans"].get("move", {"sum_us": 0.0})
+        gsp = r["spans"].get("gather", {"sum_us": 0.0})
+        mb = r["stats"]["bytes_h2d"] + r["stats"]["bytes_d2h"]
+        gb = r["stats"]["hits"] * L * 2 * W
+        mg = mb / (m["sum_us"] * 1e3) if m["sum_us"] else None
+        rep_lines.append({"value": r["stats"]["rows_gathered"] / (r["ms"] / 1e3),
+                          "ms_per_step": round(r["ms"] / K, 4),
+                          "move_gbs": round(mg, 1) if mg else None,
+                          "ce_bidir_gbs_after": round(r["ce_bidir_gbs"], 1),
+                          "move_frac_of_ce_after": round(mg / r["ce_bidir_gbs"], 4) if mg else None,
+                          "gather_gbs": round(gb / (gsp["sum_us"] * 1e3), 1) if gsp["sum_us"] else None})
     phases = {k: round(v["ms"] / max(1, n_prof), 4) for k, v in prof.items() if v["timed"]}
 
     agg = aggregate({"rows": rows_value, "value_ms": value_ms}, world, dev)
     res = {
         "rows": agg["rows"], "value_ms": agg["value_ms"], "launches": launches,
         "roofline": roof, "host_link": host, "clocks": clk, "phases": phases, "e2e": e2e,
-        "layer_ready": layer_ready,
-        "setup_s": setup_s, "stats": {k: st1[k] - st0[k] for k in st1},
+        "layer_ready": layer_ready, "repeats": rep_lines,
+        "spans_us_per_step": {k: round(v["sum_us"] / K, 2) for k, v in sp.items()},
+        "setup_s": setup_s, "stats": med["stats"],
     }
     if e2e is not None:
         a = aggregate({"rows": e2e["rows"], "e2e_ms": e2e["e2e_ms"]}, world, dev)
@@ -551,7 +619,7 @@ def isolated_gather(cache, ula, torch, dev, stream, W, L, reps=20):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     peak, _ = measured_peaks()
-    kinds = [(0, 1)] + ([(1, L - 1)] if L > 1 else [])
+    kinds = [(0, L)]
     res = {}
     for name, bps in (("step_grid", 0), ("full_grid", 64)):
         ms = {k: [] for k in kinds}
@@ -571,23 +639,42 @@ def isolated_gather(cache, ula, torch, dev, stream, W, L, reps=20):
                      "avg_launch_us": round(sum(avg.values()) / len(avg) * 1e3, 2),
                      "launch_us": {f"layers {k[0]}..{k[0] + k[1] - 1}": round(v * 1e3, 2)
                                    for k, v in avg.items()}}
-        if L > 1:
-            k = kinds[1]
-            a1 = hits * k[1] * 2 * W / (avg[k] / 1e3) / 1e9
-            res[name]["later_layers"] = {"achieved": round(a1, 1), "frac": round(a1 / peak, 4)}
     res.update({"hit_rows": hits, "launches": reps * len(kinds),
                 "l2": "flushed (512 MB write) before each launch"})
     return res
 
 
-# Traffic measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for the gather
-# kernel per gathered row, for each of the step's two launch kinds (layer 0 alone; the
-# later layers together, per slot), together with the hash of the gather kernel's
-# source (its launch-shape defaults and its body) it was taken on.  Reported only
-# while that source is unchanged.
-GATHER_TRAFFIC = {"source_sha256": "4109236a604978b3b74a56cf2a1fe0e5e271988c145f7f332a432159e571ce07",
-                  "layer0_bytes_per_row": 18778880 / 24255,  # 24,255 hit rows, 12-request case
-                  "later_bytes_per_slot": 51984384 / 24255}  # layers 1-3 of the same rows
+def union_ns(iv) -> int:
+    """Length of the union of [a, b) intervals."""
+    tot, c0, c1 = 0, None, None
+    for a, b in sorted(iv):
+        if c1 is None or a > c1:
+            if c1 is not None:
+                tot += c1 - c0
+            c0, c1 = a, b
+        else:
+            c1 = max(c1, b)
+    if c1 is not None:
+        tot += c1 - c0
+    return tot
+
+
+def span_summary(spans, d, L, W, group_steps):
+    """Per copy kernel of one timed region: launches, summed and united device spans (us)."""
+    by = {}
+    for ph, _g, t0, t1 in spans:
+        if t1 >= t0 > 0:
+            by.setdefault(ph, []).append((t0, t1))
+    return {ph: {"launches": len(iv), "sum_us": sum(b - a for a, b in iv) / 1e3,
+                 "union_us": union_ns(iv) / 1e3} for ph, iv in by.items()}
+
+
+# DRAM traffic of the gather kernel measured by ncu (dram__bytes_read.sum and
+# dram__bytes_write.sum of one launch), per hit row, with the case it was taken on and
+# the hash of the gather kernel's source (its launch-shape defaults and its body).
+# Reported only while that source is unchanged and for the workload it was taken on.
+GATHER_TRAFFIC = {"source_sha256": None, "workload": None, "hit_rows": None,
+                  "read_bytes_per_hit": None, "write_bytes_per_hit": None}
 
 
 def gather_source_sha256() -> str:
@@ -600,14 +687,14 @@ def gather_source_sha256() -> str:
     return hashlib.sha256("\n".join(keep).encode()).hexdigest()
 
 
-def traffic_per_launch(hits, L, launches):
-    """DRAM bytes per gather launch in the step: `hits` hit rows gathered by layer-0
-    launches and by later-layer launches (L - 1 layers each), `launches` of both kinds."""
+def traffic_per_launch(hits, launches, workload):
+    """DRAM bytes (read + write) per gather launch in the step, from the ncu figures per
+    hit row; None when they were taken on another gather source or workload."""
     t = GATHER_TRAFFIC
-    if t["source_sha256"] != gather_source_sha256() or not launches:
+    if (not launches or t["source_sha256"] is None or t["source_sha256"] != gather_source_sha256()
+            or t["workload"] != workload):
         return None
-    later = t["later_bytes_per_slot"] if L > 1 else 0.0
-    return round(hits * (t["layer0_bytes_per_row"] + later) / launches)
+    return round(hits * (t["read_bytes_per_hit"] + t["write_bytes_per_hit"]) / launches)
 
 
 # ------------------------------------------------------------- CPU oracle arm
@@ -631,7 +718,7 @@ def run_oracle(name, warmup, steps=None, seconds=None, exact=False):
 
     import synth
     from oracle import ExactLru
-    from tests.harness import OracleRun, alloc_rows, apply_events
+    from oracle.replay import OracleRun, alloc_rows, apply_events
 
     w = cpu_sample_workload(name, exact)
     run = OracleRun(w, "bytes")
@@ -745,7 +832,13 @@ def main(argv=None):
                                                     for k in ("rotate", "mark", "select")), 4),
                 "metadata_ms_per_step": round(sum(r["phases"].get(k, 0.0)
                                                   for k in ("dedup", "rotate", "mark", "select")), 4),
-                "hit_rate": r["stats"]["hits"] / max(1, r["stats"]["uniq"])}
+                "hit_rate": r["stats"]["hits"] / max(1, r["stats"]["uniq"]),
+                "repeats": r["repeats"], "value_median": value,
+                "value_spread": [min(x["value"] for x in r["repeats"]),
+                                 max(x["value"] for x in r["repeats"])],
+                "spans_us_per_step": r["spans_us_per_step"]}
+        if args.gather_beside:
+            line["config"]["gather"] = "beside the move"
         if r["e2e"] is not None:
             line["e2e"] = r["e2e"]
         if world == 1 and not args.no_cpu_baseline:

@@ -103,6 +103,17 @@ typedef struct ula_config {
  * recorded.  The map commit follows the last layer, as without the flag. */
 #define ULA_FLAG_LAYER_SIGNAL 4u
 
+/* The hit gather beside the move.  By default a step gathers its hit rows right after
+ * the hits are known and starts the move (write-back and fill) when the gather is
+ * done: the move's host-link traffic and the gather's HBM traffic slow each other
+ * down on the SMs they share (the gather ran at about a third of its rate beside the
+ * move, on a GB300), so the step keeps them apart.  With this flag the gather runs
+ * on a low-priority stream beside the move instead: the step's outputs are complete
+ * sooner when the host link is the bottleneck, at the price of every HBM-bound kernel
+ * that runs beside the move (this gather, or the caller's attention) going slower.
+ * ULA_FLAG_LAYER_SIGNAL implies it. */
+#define ULA_FLAG_GATHER_BESIDE_MOVE 8u
+
 /* ULA_FLAG_LAYER_SIGNAL: *d_flags receives the device address of group `group`'s
  * flags (uint32 [L_g], owned by the context, valid until ula_destroy); *round receives
  * the round number of the group's most recently issued ula_step_group (rounds count
@@ -137,8 +148,10 @@ typedef struct ula_stats {
  *   stream     : the context's home stream: alloc/free are ordered after the work already
  *                on it, and it waits for them; NULL = legacy stream.
  *   out        : receives the context.
- * The library allocates its metadata (map, slot stamps, bitmaps, scratch) with
- * cudaMalloc here and frees it in ula_destroy; it creates one side stream.
+ * The library allocates its metadata (map, slot stamps, bitmaps, scratch, and a
+ * staging area of min(max_entries, S) slots of the largest group for the write-backs)
+ * with cudaMalloc here and frees it in ula_destroy; it creates three internal streams
+ * (the step's critical path and the hit gather's two placements).
  * All slots start free; the current ring bucket starts at 0.
  */
 int ula_create(const ula_config *cfg, void *const *gpu_pools, void *const *host_pools,
@@ -181,14 +194,21 @@ int ula_free(ula_ctx *ctx, uint32_t logical_base, uint32_t n);
  *       to the j-th lowest free host slot), fill each miss from its host slot, then
  *       update the map (moves complete before the map changes) and signal,
  *   (6) gather out[j][u] = layer j of unique address u, for every layer of the group.
- *       Rows that hit are gathered as soon as the hits are known (their slots never
- *       move in this round), beside the move: layer 0 on an internal high-priority
- *       stream, the later layers together on the context's low-priority side stream;
- *       rows that missed are written by the fill itself, from the bytes it moves.
+ *       Rows that hit are gathered, every layer in one launch, as soon as the
+ *       compaction has recorded their slots (their slots never move in this round),
+ *       on an internal stream of their own while the hits are marked and the victims
+ *       chosen: finished before the move starts by default, beside the move with
+ *       ULA_FLAG_GATHER_BESIDE_MOVE; rows that missed are written by the fill itself,
+ *       from the bytes it moves.
+ * The move writes every victim that holds data back from a staging copy in HBM (made
+ * right after the victims are known), so its write-backs (in victim order, which is
+ * ascending host-slot order) and its fills (sorted by the miss's host slot) each
+ * sweep the host pool in address order; the pairing of miss i with victim i is
+ * unchanged.
  * The work runs on the context's internal highest-priority stream, ordered after
  * everything already enqueued on `stream`; `stream` is made to wait for the commit
- * and for layer 0, so work the caller enqueues next on `stream` sees layer 0 and the
- * other outputs; later layers are signalled through layer_ready.
+ * and for the hit gather, so work the caller enqueues next on `stream` sees every
+ * output; layer_ready events are recorded at that point too.
  *   d_sel       : device [n_req][q][k] uint32 logical addresses; ULA_ADDR_PAD = none.
  *   d_out       : device [L_g][out_cap_rows][row_bytes]; rows [0, U) are written.
  *   d_entry_row : device [n_req*q*k] int32: row u of each entry, -1 for pads.
@@ -209,7 +229,7 @@ int ula_step_group(ula_ctx *ctx, uint32_t group, const uint32_t *d_sel, uint32_t
                    void *stream);
 
 /*
- * ula_sync -- wait for all work of the context (both streams), then return the first
+ * ula_sync -- wait for all work of the context (all its streams), then return the first
  * latched device error (or ULA_OK).  stats: host, optional; receives the counters.
  */
 int ula_sync(ula_ctx *ctx, ula_stats *stats);
@@ -288,8 +308,7 @@ int ula_debug_consume(ula_ctx *ctx, uint32_t group, uint32_t layer, uint32_t rou
                       const void *d_out, uint32_t out_cap_rows, uint32_t n_rows,
                       unsigned long long *d_result, void *stream);
 /* Re-run the gather of the hit rows of `group`'s last step for layers
- * [layer, layer + n_layers) in one launch, as the step does (layer 0 alone, the later
- * layers together), into d_out ([L_g][out_cap_rows][row_bytes], device) on `stream`,
+ * [layer, layer + n_layers) in one launch (the step gathers all layers in one), into d_out ([L_g][out_cap_rows][row_bytes], device) on `stream`,
  * changing no state (for timing the gather kernel on its own).  Launches at once: the
  * caller orders it after the step (e.g. ula_sync) and before the group's slots change
  * again (its next step, or any alloc/free).  n_layers 0 or past L_g is
@@ -303,19 +322,18 @@ int ula_debug_regather(ula_ctx *ctx, uint32_t group, uint32_t layer, uint32_t n_
 /* ------------------------------------------------------------ profiling
  * Kernel launches are counted per phase always.  When enabled, every phase
  * instance is bracketed by two CUDA events recorded on the stream it is launched
- * on (the gather: once for layer 0 and once for the later layers together, on
- * their two streams), and
- * ula_profile_read sums their durations.  Reading synchronises the context.
+ * on, and ula_profile_read sums their durations.  Reading synchronises the context.
  */
 enum {
   ULA_PHASE_DEDUP = 0,  /* dedup, translate, capacity check */
   ULA_PHASE_ROTATE,     /* ring rotation + compaction of unique rows and misses */
   ULA_PHASE_MARK,       /* hit marking, entry rows, victim walk over segment counts */
-  ULA_PHASE_SELECT,     /* victim (or free-slot) index emission */
+  ULA_PHASE_SELECT,     /* victim (or free-slot) index emission, the fill order */
   ULA_PHASE_MOVE,       /* write-back, fill (and the missed rows' outputs), map commit */
-  ULA_PHASE_GATHER,     /* a gather of the hit rows: layer 0, or the later layers */
+  ULA_PHASE_GATHER,     /* the gather of the hit rows (every layer in one launch) */
   ULA_PHASE_ALLOC,      /* alloc placement and copy-in */
   ULA_PHASE_FREE,       /* free */
+  ULA_PHASE_STAGE,      /* victims' rows copied to the staging area before the move */
   ULA_PHASE_COUNT
 };
 
@@ -328,6 +346,28 @@ typedef struct ula_profile {
 int ula_profile_enable(ula_ctx *ctx, int on);
 /* Copies the accumulated profile into *out (may be NULL) and, if reset != 0, zeroes it. */
 int ula_profile_read(ula_ctx *ctx, ula_profile *out, int reset);
+
+/* Launch spans of a step's kernels, measured on the device itself: while recording is
+ * on, every launch of the hit gather, the staging copy and the move, and every step's
+ * metadata kernels taken together, keep the device globaltimer of the first warp's
+ * start and of the last warp's end (two atomics per warp, so recording costs next to
+ * nothing and can stay on in a timed run).  Spans of kernels that overlap are kept
+ * apart, unlike summed event durations. */
+typedef struct ula_span {
+  uint32_t phase;     /* ULA_PHASE_GATHER, ULA_PHASE_STAGE, ULA_PHASE_MOVE, or
+                         ULA_PHASE_SELECT for the step's metadata: from its first dedup
+                         thread to the end of its last victim-emission warp */
+  uint32_t group;
+  uint64_t start_ns;  /* globaltimer (ns); 0 and 0 when the launch returned early */
+  uint64_t end_ns;
+} ula_span;
+/* Waits for the context's work, clears the recorded spans and turns recording on or
+ * off.  At most 65,536 launches are recorded between reads; later ones are not. */
+int ula_profile_spans(ula_ctx *ctx, int on);
+/* Waits for the context's work, copies the first min(cap, n) of the n spans recorded
+ * since the last read or enable (in launch order) into out (host), sets *count = n,
+ * and clears them (recording stays as it was). */
+int ula_profile_spans_read(ula_ctx *ctx, ula_span *out, uint32_t cap, uint32_t *count);
 
 /* ------------------------------------------------------------ no-allocation dedup
  * The pages have no counterpart for this entry point; it serves callers that must

@@ -20,7 +20,7 @@
 //       oldest to newest; the current bucket is never chosen; data moves
 //       first, then the mapping is updated, then completion is signalled.
 //
-// Readings where the pages are silent (each also listed in the design notes):
+// Readings where the pages are silent:
 //   * one GPU slot holds the rows of all L_g layers of one address for one
 //     group; each group has its own map, pools, ring and cold bucket;
 //   * one scheduling round = one step call for that group; rotation happens

@@ -74,7 +74,7 @@ class UlaCache:
                  ring_buckets: int, max_logical: int, max_entries: int, device="cuda",
                  stream: torch.cuda.Stream | None = None, huge_host_pages: bool = True,
                  bypass_overflow: bool = False, exact_lru: bool = False,
-                 layer_signal: bool = False):
+                 layer_signal: bool = False, gather_beside_move: bool = False):
         self.device = torch.device(device)
         self.W = int(row_bytes)
         self.layers = [int(x) for x in layers_per_group]
@@ -91,7 +91,8 @@ class UlaCache:
                               self.max_entries,
                               (ula.FLAG_BYPASS_OVERFLOW if bypass_overflow else 0)
                               | (ula.FLAG_EXACT_LRU if exact_lru else 0)
-                              | (ula.FLAG_LAYER_SIGNAL if layer_signal else 0))
+                              | (ula.FLAG_LAYER_SIGNAL if layer_signal else 0)
+                              | (ula.FLAG_GATHER_BESIDE_MOVE if gather_beside_move else 0))
         with torch.cuda.device(self.device):
             self.ctx = ula.ula_create(cfg, [p.data_ptr() for p in self.gpu_pools],
                                       [p.data_ptr() for p in self.host_pools] if self.H else None,

@@ -24,13 +24,14 @@ using namespace ula;
 
 namespace {
 
-// The later layers' hit rows in one launch per step (a slot's rows of those layers
-// are contiguous); 0 launches one gather per layer instead.
-#ifndef ULA_GATHER_MERGE_LAYERS
-#define ULA_GATHER_MERGE_LAYERS 1
-#endif
-
 constexpr uint32_t kAllocChunk = 65536;
+constexpr size_t kSpanCap = 1u << 16;  // span records kept between reads
+// Where the step releases its hit gather: 0 = once the compaction has recorded the
+// hits' slots (beside the marking and the victim selection), 1 = after the victims are
+// emitted (beside the staging copy only).
+#ifndef ULA_GATHER_AFTER_EMIT
+#define ULA_GATHER_AFTER_EMIT 0
+#endif
 // Internal: a TP rank's local buffer (misses fetched from the owner partitions,
 // evicted copies dropped).  Not accepted by the public ula_create.
 constexpr uint32_t kFlagCacheInternal = 1u << 31;
@@ -49,15 +50,13 @@ struct ula_ctx {
   int sm_count = 0;
   cudaStream_t home = nullptr;  // the caller's stream given at create (alloc/free order)
   cudaStream_t crit = nullptr;  // internal, highest priority: the step's critical path
-  cudaStream_t side = nullptr;  // internal, lowest priority: later layers' hit gathers
-  cudaStream_t first = nullptr; // internal, highest priority: layer 0's hit gather
+  cudaStream_t side = nullptr;  // internal, lowest priority: the hit gather
   cudaEvent_t in_evt = nullptr, out_evt = nullptr, commit_evt = nullptr;
-  cudaEvent_t marked_evt = nullptr, hit0_evt = nullptr;
+  cudaEvent_t marked_evt = nullptr, hit_evt = nullptr;
   int move_blocks = 0, gather_blocks = 0;  // persistent grids (resident blocks)
   int gather_fit_per_sm = 0;
-  int emit_blocks = 0;
-  cudaEvent_t side_evt[ULA_MAX_GROUPS] = {};
-  bool side_pending[ULA_MAX_GROUPS] = {};
+  int emit_blocks = 0, stage_blocks = 0;
+  bool beside = false;  // the hit gather runs beside the move (else before it)
   Geometry geo{};
   std::vector<GroupDev> groups_h;
   GroupDev *groups_d = nullptr;
@@ -66,6 +65,13 @@ struct ula_ctx {
   uint32_t *addr_row = nullptr;
   uint2 *blk = nullptr;
   uint32_t *miss_list = nullptr, *miss_hs = nullptr, *miss_row = nullptr;
+  uint32_t *fill_order = nullptr;  // [decision_cap] the move's fill order
+  uint32_t *vdone = nullptr;       // [decision_cap] copies done per victim
+  uint8_t *stage = nullptr;        // [max_entries][max L_g][W] staged victim rows
+  // launch spans of the copy kernels (diagnostics): a ring of records on the device
+  SpanRec *spans_d = nullptr;
+  bool span_on = false;
+  std::vector<uint32_t> span_meta;  // phase << 16 | group of each record taken
   TpSource tp_src[ULA_MAX_GROUPS] = {};  // TP local buffer: the owner partitions per group
   LruScratch lru{};     // exact LRU's scan scratch (ULA_FLAG_EXACT_LRU only)
   int lru_blocks = 0;   // its cooperative grid
@@ -118,10 +124,12 @@ struct ula_ctx {
     return e != cudaSuccess ? e : cudaStreamWaitEvent(caller, out_evt, 0);
   }
 
-  cudaError_t wait_side(cudaStream_t s, uint32_t g) {
-    if (!side_pending[g]) return cudaSuccess;
-    side_pending[g] = false;
-    return cudaStreamWaitEvent(s, side_evt[g], 0);
+  // the next span record for a launch of `phase` in `group`, or NULL (not recording,
+  // or the ring is full)
+  SpanRec *take_span(int phase, uint32_t group) {
+    if (!span_on || span_meta.size() >= kSpanCap) return nullptr;
+    span_meta.push_back(((uint32_t)phase << 16) | group);
+    return spans_d + (span_meta.size() - 1);
   }
 
 
@@ -168,11 +176,18 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Persistent grids, sized so the critical path's kernels keep SMs while the hit
-// gathers run beside the move (measured on the long-document workload: 2 move
-// blocks and 1 gather block of 256 threads per SM gave the shortest step).
-constexpr int kMoveBlocksPerSm = 2;
-constexpr int kGatherBlocksPerSm = 1;
+// Persistent grid of the move: one block of 128 threads per SM (the host link is
+// saturated by 4 warps on every SM; more warps or fewer SMs move less, measured).
+constexpr int kMoveBlocksPerSm = 1;
+// The step's hit gather is not persistent: short blocks of kGatherRowsPerBlock rows
+// on the lowest-priority stream, so the step's metadata kernels (highest priority) get
+// SM room as gather blocks retire.  Its grid is sized from the entry count (U <= E);
+// blocks past the last row exit at once.
+constexpr uint32_t kGatherRowsPerBlock = 64;
+int gather_step_blocks(uint64_t entries) {
+  const uint64_t b = (entries + kGatherRowsPerBlock - 1) / kGatherRowsPerBlock;
+  return (int)(b < 1 ? 1 : (b > 65535 ? 65535 : b));
+}
 
 // blocks per SM from the environment (or `dflt`), clamped to [1, fit]
 int env_blocks(const char *name, int dflt, int fit) {
@@ -220,7 +235,8 @@ int validate_config(const ula_config *c) {
   if (c->ring_buckets == 0 || c->ring_buckets > ULA_MAX_BUCKETS) return ULA_ERR_INVALID_ARG;
   if (c->max_logical == 0 || c->max_logical > kSlotMask) return ULA_ERR_INVALID_ARG;
   if (c->max_entries == 0) return ULA_ERR_INVALID_ARG;
-  if ((c->flags & ~(ULA_FLAG_BYPASS_OVERFLOW | ULA_FLAG_EXACT_LRU | ULA_FLAG_LAYER_SIGNAL)) != 0)
+  if ((c->flags & ~(ULA_FLAG_BYPASS_OVERFLOW | ULA_FLAG_EXACT_LRU | ULA_FLAG_LAYER_SIGNAL |
+                    ULA_FLAG_GATHER_BESIDE_MOVE)) != 0)
     return ULA_ERR_INVALID_ARG;
   return ULA_OK;
 }
@@ -230,14 +246,11 @@ void destroy_resources(ula_ctx *c) {
   c->allocations.clear();
   if (c->side) cudaStreamDestroy(c->side);
   if (c->crit) cudaStreamDestroy(c->crit);
-  if (c->first) cudaStreamDestroy(c->first);
   if (c->in_evt) cudaEventDestroy(c->in_evt);
   if (c->out_evt) cudaEventDestroy(c->out_evt);
   if (c->commit_evt) cudaEventDestroy(c->commit_evt);
   if (c->marked_evt) cudaEventDestroy(c->marked_evt);
-  if (c->hit0_evt) cudaEventDestroy(c->hit0_evt);
-  for (uint32_t g = 0; g < ULA_MAX_GROUPS; ++g)
-    if (c->side_evt[g]) cudaEventDestroy(c->side_evt[g]);
+  if (c->hit_evt) cudaEventDestroy(c->hit_evt);
   for (auto &t : c->prof_pending) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
@@ -265,6 +278,14 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   geo.hd = dims_for(H);
   geo.nseg = geo.gd.n1;
   geo.hseg = geo.hd.n1;
+  {  // fill-order buckets: host slot >> fill_shift < kFillBuckets (a local buffer's miss
+     // source is partition << 29 | slot: the top 11 bits)
+    uint32_t bits = 0;
+    while (bits < 32 && (1ull << bits) < (uint64_t)(geo.cache ? 0xFFFFFFFFu : H)) ++bits;
+    const uint32_t bucket_bits = 11;  // 2^11 = kFillBuckets
+    geo.fill_shift = bits > bucket_bits ? bits - bucket_bits : 0u;
+  }
+  c->beside = geo.signal || (cfg.flags & ULA_FLAG_GATHER_BESIDE_MOVE);
   c->decision_cap = cfg.max_entries > kAllocChunk ? cfg.max_entries : kAllocChunk;
 
   // pools: caller-owned, borrowed
@@ -284,24 +305,21 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest));
   ULA_CUDA(cudaStreamCreateWithPriority(&c->crit, cudaStreamNonBlocking, prio_greatest));
   ULA_CUDA(cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, prio_least));
-  ULA_CUDA(cudaStreamCreateWithPriority(&c->first, cudaStreamNonBlocking, prio_greatest));
   ULA_CUDA(cudaEventCreateWithFlags(&c->in_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->out_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->commit_evt, cudaEventDisableTiming));
   ULA_CUDA(cudaEventCreateWithFlags(&c->marked_evt, cudaEventDisableTiming));
-  ULA_CUDA(cudaEventCreateWithFlags(&c->hit0_evt, cudaEventDisableTiming));
+  ULA_CUDA(cudaEventCreateWithFlags(&c->hit_evt, cudaEventDisableTiming));
   ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks, cfg.row_bytes));
   c->gather_fit_per_sm = c->gather_blocks;
-  // The move is bound by the host link and needs few SMs to saturate it; the hit
-  // gathers run beside it.  ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune
-  // the persistent grids (clamped to what fits on an SM).
+  // ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune the persistent grids
+  // (clamped to what fits on an SM).
   c->move_blocks = env_blocks("ULA_MOVE_BLOCKS_PER_SM", kMoveBlocksPerSm, c->move_blocks);
-  c->gather_blocks = env_blocks("ULA_GATHER_BLOCKS_PER_SM", kGatherBlocksPerSm, c->gather_blocks);
+  c->gather_blocks = env_blocks("ULA_GATHER_BLOCKS_PER_SM", c->gather_blocks, c->gather_blocks);
   c->move_blocks *= c->sm_count;
   c->gather_blocks *= c->sm_count;
   c->emit_blocks = c->sm_count;
-  for (uint32_t g = 0; g < G; ++g)
-    ULA_CUDA(cudaEventCreateWithFlags(&c->side_evt[g], cudaEventDisableTiming));
+  c->stage_blocks = 2 * c->sm_count;
 
   // shared scratch (main-stream kernels only)
   const uint32_t max_blk = (cfg.max_entries + 255) / 256 + 1;
@@ -311,6 +329,16 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(c->alloc(&c->miss_list, cfg.max_entries));
   ULA_CUDA(c->alloc(&c->miss_hs, cfg.max_entries));
   ULA_CUDA(c->alloc(&c->miss_row, cfg.max_entries));
+  ULA_CUDA(c->alloc(&c->fill_order, c->decision_cap));
+  ULA_CUDA(c->alloc(&c->vdone, c->decision_cap));
+  ULA_CUDA(cudaMemsetAsync(c->vdone, 0, sizeof(uint32_t) * c->decision_cap, c->home));
+  if (H && !geo.cache && !geo.signal) {  // staged victim rows (the slot-major move only)
+    uint32_t lmax = 0;
+    for (uint32_t g = 0; g < G; ++g) lmax = cfg.layers_per_group[g] > lmax ? cfg.layers_per_group[g] : lmax;
+    const size_t rows = cfg.max_entries < S ? cfg.max_entries : S;  // victims per step <= both
+    ULA_CUDA(c->alloc(&c->stage, rows * lmax * cfg.row_bytes));
+  }
+  ULA_CUDA(c->alloc(&c->spans_d, kSpanCap));
   ULA_CUDA(c->alloc(&c->status, 1));
   ULA_CUDA(c->alloc(&c->cnt_d, G));
   ULA_CUDA(c->alloc(&c->groups_d, G));
@@ -464,7 +492,6 @@ static int alloc_impl(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logica
   if (!rows_d || !aligned16(rows_d)) return ULA_ERR_INVALID_ARG;
   cudaStream_t s = c->crit;
   ULA_CUDA(c->enter(c->home));
-  for (uint32_t g = 0; g < cfg.n_groups; ++g) ULA_CUDA(c->wait_side(s, g));
 
   const uint32_t base = c->next_logical;
   for (uint32_t off = 0; off < n; off += kAllocChunk) {
@@ -525,7 +552,6 @@ static int free_impl(ula_ctx *c, uint32_t base, uint32_t n, bool drop) {
   ULA_CUDA(c->ensure_device());
   cudaStream_t s = c->crit;
   ULA_CUDA(c->enter(c->home));
-  for (uint32_t g = 0; g < c->cfg.n_groups; ++g) ULA_CUDA(c->wait_side(s, g));
   FreeParams fp{};
   fp.geo = c->geo;
   fp.groups = c->groups_d;
@@ -560,7 +586,6 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   cudaStream_t caller = static_cast<cudaStream_t>(stream);
   cudaStream_t s = c->crit;
   ULA_CUDA(c->enter(caller));
-  ULA_CUDA(c->wait_side(s, group));
 
   if (++c->epoch == 0) {  // dedup stamps wrap: clear them
     ULA_CUDA(cudaMemsetAsync(c->tbl, 0, sizeof(unsigned long long) * cfg.max_logical, s));
@@ -599,15 +624,46 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.order.cls[1] = B;
   for (uint32_t d = 1; d < B; ++d) p.order.cls[1 + d] = (cur + d) % B;
   if (c->geo.exact) p.order.n_cls = 1;  // exact LRU walks the free slots; the scan does the rest
+  SpanRec *meta_span = c->take_span(ULA_PHASE_SELECT, group);  // dedup .. victim emission
+  p.span = meta_span;
+  const bool gather = out_cap_rows != 0;
+  GatherParams gp{};
+  gp.geo = c->geo;
+  gp.grp = gd;
+  gp.out = static_cast<uint8_t *>(d_out);
+  gp.out_cap = out_cap_rows;
+  gp.layer = 0;
+  gp.nlayers = gd.layers;
+  gp.signal = c->geo.signal;
+  gp.round = r;
+  gp.status = c->status;
+  cudaStream_t gs = c->side;
+  // (6) the hit rows of every layer, one launch (a slot's layers are one contiguous
+  // read), released once the compaction has recorded each hit's slot (a hit's slot
+  // does not change in its round).  It runs on its own stream while the hits are
+  // marked and the victims chosen, emitted and staged, and the move starts once it is
+  // done: beside the move, each slows the other (the move's host-link traffic holds up
+  // the gather's HBM traffic on every SM it shares).  Beside the move instead with
+  // ULA_FLAG_GATHER_BESIDE_MOVE or the per-layer signal.
+  auto release_gather = [&]() -> cudaError_t {
+    cudaError_t e = cudaEventRecord(c->marked_evt, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(gs, c->marked_evt, 0);
+    if (e != cudaSuccess) return e;
+    gp.span = c->take_span(ULA_PHASE_GATHER, group);
+    e = c->phase(ULA_PHASE_GATHER, gs, gather_launches(c->geo.W, gd.layers),
+                 [&] { return launch_gather(gp, gather_step_blocks(E), gs); });
+    return e != cudaSuccess ? e : cudaEventRecord(c->hit_evt, gs);
+  };
   // (1)(2) dedup + translate + capacity check
   ULA_CUDA(c->phase(ULA_PHASE_DEDUP, s, E ? 2 : 1, [&] { return launch_dedup(p, s); }));
   // (3a) rotation + compaction of unique rows and misses
   ULA_CUDA(c->phase(ULA_PHASE_ROTATE, s, 1, [&] { return launch_rotate_emit(p, s); }));
+  if (gather && !c->geo.exact && !ULA_GATHER_AFTER_EMIT) ULA_CUDA(release_gather());
   // (3b) hits into the current bucket, entry rows; the victim walk
   ULA_CUDA(c->phase(ULA_PHASE_MARK, s, 1, [&] { return launch_mark_select(p, s); }));
   if (c->geo.exact) {
-    // (4) exact LRU: the timestamp scan, before the hit gathers are released (its
-    // grid-wide phases run several times slower beside them)
+    // (4) exact LRU: the timestamp scan, before the hit gather is released (its
+    // grid-wide phases run several times slower beside it)
     LruParams lp{};
     lp.geo = c->geo;
     lp.grp = gd;
@@ -617,46 +673,23 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
     lp.status = c->status;
     ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
                       [&] { return launch_lru_select(lp, c->lru_blocks, s); }));
+    if (gather && !ULA_GATHER_AFTER_EMIT) ULA_CUDA(release_gather());
   }
-  const bool gather = out_cap_rows != 0;
-  GatherParams gp{};
-  gp.geo = c->geo;
-  gp.grp = gd;
-  gp.out = static_cast<uint8_t *>(d_out);
-  gp.out_cap = out_cap_rows;
-  gp.signal = c->geo.signal;
-  gp.round = r;
-  gp.status = c->status;
-  if (gather) {
-    // (6) the hit rows, while the misses are being moved (a hit's slot does not
-    // change in its round): layer 0 on a high-priority stream, the later layers
-    // together (one contiguous read per slot) on the low-priority prefetch stream
-    ULA_CUDA(cudaEventRecord(c->marked_evt, s));
-    ULA_CUDA(cudaStreamWaitEvent(c->first, c->marked_evt, 0));
-    gp.layer = 0;
-    gp.nlayers = 1;
-    ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->first, 1,
-                      [&] { return launch_gather(gp, c->gather_blocks, c->first); }));
-    ULA_CUDA(cudaEventRecord(c->hit0_evt, c->first));
-    ULA_CUDA(cudaStreamWaitEvent(c->side, c->marked_evt, 0));
-    const uint32_t per = ULA_GATHER_MERGE_LAYERS ? gd.layers - 1 : 1;
-    for (uint32_t j = 1; j < gd.layers; j += per) {
-      gp.layer = j;
-      gp.nlayers = per;
-      ULA_CUDA(c->phase(ULA_PHASE_GATHER, c->side, gather_launches(c->geo.W, per),
-                        [&] { return launch_gather(gp, c->gather_blocks, c->side); }));
-    }
-  }
-  // (4) victims' and write-back slots' indices
+  // (4) victims' and write-back slots' indices; (5) the fill order
+  const bool staged = !c->geo.signal;  // the slot-major move (not the layer-major one)
   EmitParams ep{};
   ep.geo = c->geo;
   ep.groups = c->groups_d;
   ep.group0 = group;
   ep.order = p.order;
   ep.quota = 0xffffffffu;
+  ep.miss_hs = c->miss_hs;
+  ep.fill_order = c->geo.signal ? nullptr : c->fill_order;
+  ep.span = meta_span;
   ep.status = c->status;
   ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
                     [&] { return launch_select_emit(ep, 1, c->emit_blocks, s); }));
+  if (gather && ULA_GATHER_AFTER_EMIT) ULA_CUDA(release_gather());
   // (5) write-back, fill (writing the missed rows' outputs), then map commit
   MoveParams mp{};
   mp.geo = c->geo;
@@ -673,38 +706,33 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   mp.round = r;
   mp.cur = cur;
   mp.src = c->tp_src[group];
+  mp.fill_order = c->fill_order;
+  mp.stage = c->stage;
+  mp.vdone = c->vdone;
   mp.status = c->status;
-  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, c->geo.signal ? 2 : 1, [&] { return launch_move(mp, c->move_blocks, s); }));
-  // signal: the commit event; layer j is ready once its hit rows are gathered too
-  ULA_CUDA(cudaEventRecord(c->commit_evt, s));
-  if (gather) ULA_CUDA(cudaStreamWaitEvent(s, c->hit0_evt, 0));
-  if (layer_ready && layer_ready[0])
-    ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[0]), s));
-  if (gather) {
-    ULA_CUDA(cudaStreamWaitEvent(c->side, c->commit_evt, 0));
-    for (uint32_t j = 1; j < gd.layers; ++j)
-      if (layer_ready && layer_ready[j])
-        ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), c->side));
-    ULA_CUDA(cudaEventRecord(c->side_evt[group], c->side));
-    c->side_pending[group] = true;
-  } else {
-    for (uint32_t j = 1; j < gd.layers; ++j)
-      if (layer_ready && layer_ready[j])
-        ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), s));
+  if (staged) {  // entry rows; the rows of the victims that hold data, to the staging area
+    mp.span = c->take_span(ULA_PHASE_STAGE, group);
+    ULA_CUDA(c->phase(ULA_PHASE_STAGE, s, 1, [&] { return launch_stage(mp, c->stage_blocks, s); }));
   }
+  const bool after_gather = gather && !c->beside;
+  if (after_gather) ULA_CUDA(cudaStreamWaitEvent(s, c->hit_evt, 0));
+  mp.span = c->take_span(ULA_PHASE_MOVE, group);
+  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, c->geo.signal ? 2 : 1,
+                    [&] { return launch_move(mp, c->move_blocks, !after_gather, s); }));
+  // signal: the commit event; every layer is ready once its hit rows are gathered too
+  ULA_CUDA(cudaEventRecord(c->commit_evt, s));
+  if (gather && c->beside) ULA_CUDA(cudaStreamWaitEvent(s, c->hit_evt, 0));
+  for (uint32_t j = 0; j < gd.layers; ++j)
+    if (layer_ready && layer_ready[j])
+      ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), s));
   ULA_CUDA(c->leave(caller));
   return ULA_OK;
 }
 
 static int sync_impl(ula_ctx *c) {
   ULA_CUDA(c->ensure_device());
-  for (uint32_t g = 0; g < c->cfg.n_groups; ++g)
-    if (c->side_pending[g]) {
-      ULA_CUDA(cudaEventSynchronize(c->side_evt[g]));
-      c->side_pending[g] = false;
-    }
   ULA_CUDA(cudaStreamSynchronize(c->crit));
-  ULA_CUDA(cudaStreamSynchronize(c->first));
+  ULA_CUDA(cudaStreamSynchronize(c->side));
   ULA_CUDA(cudaStreamSynchronize(c->home));
   return ULA_OK;
 }
@@ -841,6 +869,42 @@ int ula_profile_read(ula_ctx *c, ula_profile *out, int reset) {
   return ULA_OK;
 }
 
+static cudaError_t reset_spans(ula_ctx *c) {
+  c->span_meta.clear();
+  return cudaMemset(c->spans_d, 0xff, sizeof(SpanRec) * kSpanCap);
+}
+
+int ula_profile_spans(ula_ctx *c, int on) {
+  if (!c) return ULA_ERR_INVALID_ARG;
+  int rc = sync_impl(c);
+  if (rc) return rc;
+  ULA_CUDA(reset_spans(c));
+  c->span_on = on != 0;
+  return ULA_OK;
+}
+
+int ula_profile_spans_read(ula_ctx *c, ula_span *out, uint32_t cap, uint32_t *count) {
+  if (!c || !count || (cap && !out)) return ULA_ERR_INVALID_ARG;
+  int rc = sync_impl(c);
+  if (rc) return rc;
+  const size_t n = c->span_meta.size();
+  *count = (uint32_t)n;
+  const size_t k = n < cap ? n : cap;
+  if (k) {
+    std::vector<SpanRec> h(k);
+    ULA_CUDA(cudaMemcpy(h.data(), c->spans_d, sizeof(SpanRec) * k, cudaMemcpyDeviceToHost));
+    for (size_t i = 0; i < k; ++i) {
+      out[i].phase = c->span_meta[i] >> 16;
+      out[i].group = c->span_meta[i] & 0xffffu;
+      const bool ran = h[i].t0 != ~0ull && h[i].t1n != ~0ull;
+      out[i].start_ns = ran ? h[i].t0 : 0;
+      out[i].end_ns = ran ? ~h[i].t1n : 0;
+    }
+  }
+  ULA_CUDA(reset_spans(c));
+  return ULA_OK;
+}
+
 int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, uint32_t n_layers,
                        void *d_out, uint32_t out_cap_rows, uint32_t blocks_per_sm, void *stream) {
   if (!c || group >= c->cfg.n_groups || !d_out || !aligned16(d_out)) return ULA_ERR_INVALID_ARG;
@@ -858,7 +922,7 @@ int ula_debug_regather(ula_ctx *c, uint32_t group, uint32_t layer, uint32_t n_la
   gp.layer = layer;
   gp.nlayers = n_layers;
   gp.status = c->status;
-  int blocks = c->gather_blocks;
+  int blocks = gather_step_blocks(c->cfg.max_entries);
   if (blocks_per_sm) {
     const int fit = c->gather_fit_per_sm;
     blocks = c->sm_count * ((int)blocks_per_sm < fit ? (int)blocks_per_sm : fit);
@@ -1061,7 +1125,6 @@ int ula_tp_step_group(ula_tp *t, uint32_t group, const uint32_t *d_sel, uint32_t
                                   d_local_out[p], out_cap_rows, d_local_entry_row[p],
                                   d_local_req_off[p], nullptr, t->ps[p]);
     if (rc) return rc;
-    ULA_CUDA(c->wait_side(t->ps[p], group));  // the later layers' gathers too
     ULA_CUDA(cudaEventRecord(t->pdone[p], t->ps[p]));
   }
   for (uint32_t r = 0; r < P; ++r) {  // then every rank's buffer fetches from them
@@ -1071,7 +1134,6 @@ int ula_tp_step_group(ula_tp *t, uint32_t group, const uint32_t *d_sel, uint32_t
                                   d_remote_out[r], out_cap_rows, d_remote_entry_row[r],
                                   d_remote_req_off[r], nullptr, t->bs[r]);
     if (rc) return rc;
-    ULA_CUDA(c->wait_side(t->bs[r], group));
     ULA_CUDA(cudaEventRecord(t->bdone[r], t->bs[r]));
   }
   c = c0;

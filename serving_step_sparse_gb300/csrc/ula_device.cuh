@@ -103,7 +103,17 @@ struct Geometry {
                          // evicted copies are dropped (no host pool, no write-back)
   Dims gd, hd;           // bitmap dims for GPU-slot and host-slot bitmaps
   uint32_t nseg, hseg;   // segments (= level-1 words) per bitmap
+  uint32_t fill_shift;   // a miss's host slot >> fill_shift = its bucket in the fill order
 };
+
+// Device time span of one launch of a copy kernel (diagnostics): the earliest warp
+// start and the latest warp end, both kept as minima (the end complemented), so an
+// all-ones record is empty and a ring of records is reset with one memset.
+struct SpanRec {
+  unsigned long long t0;   // min over warps of the start (globaltimer, ns)
+  unsigned long long t1n;  // min over warps of ~end
+};
+constexpr uint32_t kFillBuckets = 2048;  // buckets of the fill order (host-address order)
 
 __host__ __device__ inline Bitmap class_bitmap(const GroupDev &g, const Geometry &geo, uint32_t c) {
   Bitmap b;
@@ -162,6 +172,7 @@ struct StepParams {
   uint32_t *miss_hs;        // [max_entries]: host slot of miss i
   uint32_t *miss_row;       // [max_entries]: unique row of miss i
   TpSource src;             // cache mode: the owner partitions
+  SpanRec *span;            // the step's metadata span (its start), or NULL
   int *status;              // latched device error (0 = none)
 };
 
@@ -172,6 +183,9 @@ struct EmitParams {
   uint32_t group0;          // first group (blockIdx.y adds to it)
   Order order;
   uint32_t quota;           // GPU quota (alloc), or 0xFFFFFFFF = the group's M (step)
+  const uint32_t *miss_hs;  // step: [M] host slot of miss i (the fill order's keys)
+  uint32_t *fill_order;     // step: [M] out: miss indices in host-slot bucket order (or NULL)
+  SpanRec *span;            // step: the metadata span (its end), or NULL
   int *status;
 };
 
@@ -189,6 +203,10 @@ struct MoveParams {
   uint32_t out_cap;
   uint32_t round, cur;
   TpSource src;               // cache mode: the owner partitions' GPU pools
+  const uint32_t *fill_order; // [M]: the order in which the fills run (miss indices)
+  uint8_t *stage;             // [M - F][L][W]: the rows of victims F.. staged before the move
+  uint32_t *vdone;            // [M]: copies done per victim (reset by its commit)
+  SpanRec *span;              // this launch's time span, or NULL
   int *status;
 };
 
@@ -231,6 +249,7 @@ struct GatherParams {
   uint32_t nlayers;
   uint32_t signal;          // contributes to the layers' signals (a step's gather)
   uint32_t round;
+  SpanRec *span;            // this launch's time span, or NULL
   int *status;
 };
 
@@ -263,7 +282,12 @@ cudaError_t launch_mark_select(const StepParams &p, cudaStream_t s);
 cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int blocks, cudaStream_t s);
 // alloc: walk of the free class and the host-free bitmap for a quota of n, per group
 cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s);
-cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s);  // copies, then commit
+// the rows of the step's victims that hold data, copied to the staging area (HBM)
+cudaError_t launch_stage(const MoveParams &p, int blocks, cudaStream_t s);
+// copies, then commit; dependent = chained by programmatic dependent launch to the
+// previous kernel on s (false when s waits on an event in between)
+cudaError_t launch_move(const MoveParams &p, int blocks, bool dependent, cudaStream_t s);
+int move_threads();
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
 int gather_launches(uint32_t row_bytes, uint32_t nlayers);  // kernels one launch_gather makes
 // exact LRU: victims [F, M) by a scan of the slot timestamps (cooperative launch of

@@ -55,8 +55,11 @@ constexpr int kMarkClasses = 8;     // class words a marking warp loads at once
 #ifndef ULA_GATHER_UNROLL
 #define ULA_GATHER_UNROLL 12
 #endif
+#ifndef ULA_MOVE_THREADS
+#define ULA_MOVE_THREADS 128
+#endif
 #ifndef ULA_MOVE_MINBLOCKS
-#define ULA_MOVE_MINBLOCKS 3
+#define ULA_MOVE_MINBLOCKS 4
 #endif
 #ifndef ULA_MOVE_UNROLL
 #define ULA_MOVE_UNROLL 6
@@ -221,6 +224,14 @@ __device__ __forceinline__ uint32_t access_class(const Geometry &geo, uint32_t c
   return geo.exact ? geo.B : cur;
 }
 
+// Span of a launch (diagnostics): each warp folds its start and end into the record.
+__device__ __forceinline__ void span_open(SpanRec *r) {
+  if (r && lane_id() == 0) atomicMin(&r->t0, global_ns());
+}
+__device__ __forceinline__ void span_close(SpanRec *r) {
+  if (r && lane_id() == 0) atomicMin(&r->t1n, ~global_ns());
+}
+
 // ------------------------------------------------------------------ init
 
 // all of [0, nbits) set, with exact summaries and segment counts
@@ -255,6 +266,7 @@ __global__ void k_dedup_stamp(StepParams p) {
   pdl_launch();
   if (*(volatile int *)p.status) return;
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e == 0 && p.span) atomicMin(&p.span->t0, global_ns());  // the step's metadata starts
   if (p.inject && e == 0) latch(p.status, p.inject);
   if (p.geo.signal && e == 0) p.grp.layer_ns[p.grp.layers] = global_ns();  // step start
   if (e >= p.E) return;
@@ -292,8 +304,10 @@ __global__ void __launch_bounds__(kEntryThreads) k_dedup_count_scan(StepParams p
   pdl_wait();
   pdl_launch();
   if (block_skips(p.status)) return;
-  if (p.geo.signal && p.E == 0 && blockIdx.x == 0 && threadIdx.x == 0)
-    p.grp.layer_ns[p.grp.layers] = global_ns();  // step start (no entries: no stamp kernel)
+  if (p.E == 0 && blockIdx.x == 0 && threadIdx.x == 0) {  // (no entries: no stamp kernel)
+    if (p.geo.signal) p.grp.layer_ns[p.grp.layers] = global_ns();  // step start
+    if (p.span) atomicMin(&p.span->t0, global_ns());
+  }
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   const Flags f = entry_flags(p, e);
   __shared__ uint32_t sf[kEntryThreads / 32], sm[kEntryThreads / 32];
@@ -617,14 +631,74 @@ __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
   select_walk<kEntryThreads>(g, geo, p.order, quota, M, true, p.status);
 }
 
+// (5) The order in which the move runs the fills: miss indices [0, M) sorted by
+// bucket of their host slot (host slot >> fill_shift, kFillBuckets buckets; any order
+// inside a bucket), one block.  The pairing of miss i with victim i is unchanged;
+// only the order of the copies changes, so that at any moment the move's warps read
+// a narrow, advancing window of the host pool instead of all of it at random (the
+// GPU keeps too few address translations for random 2.6 KB reads over tens of GB of
+// host memory).  The write-backs need no sort: the j-th victim that holds data goes to
+// the j-th lowest free host slot, so victim order is host-address order already.
+constexpr int kOrderThreads = 256;
+
+__device__ void fill_order_block(const EmitParams &p, const GroupDev &g) {
+  __shared__ uint32_t hist[kFillBuckets];
+  const uint32_t M = __ldcg(&g.cnt->M);
+  const uint32_t shift = p.geo.fill_shift;
+  const uint32_t lane = lane_id();
+  for (uint32_t b = threadIdx.x; b < kFillBuckets; b += kOrderThreads) hist[b] = 0;
+  __syncthreads();
+  // lanes of a warp with the same bucket (neighbouring misses often share one) take
+  // their positions with one atomic
+  auto claim = [&](uint32_t i0) -> uint32_t {  // position of miss i0 + threadIdx.x, or kNone
+    const uint32_t i = i0 + threadIdx.x;
+    const bool act = i < M;
+    const uint32_t b = act ? min(__ldcg(&p.miss_hs[i]) >> shift, kFillBuckets - 1) : kNone;
+    const uint32_t peers = __match_any_sync(0xffffffffu, b);
+    const uint32_t leader = __ffs(peers) - 1;
+    uint32_t base = 0;
+    if (act && lane == leader) base = atomicAdd(&hist[b], (uint32_t)__popc(peers));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    return act ? base + __popc(peers & ((1u << lane) - 1u)) : kNone;
+  };
+  for (uint32_t i0 = 0; i0 < M; i0 += kOrderThreads) claim(i0);  // bucket sizes
+  __syncthreads();
+  constexpr uint32_t kPer = kFillBuckets / kOrderThreads;
+  uint32_t v[kPer], mine = 0;
+#pragma unroll
+  for (uint32_t j = 0; j < kPer; ++j) {
+    v[j] = hist[threadIdx.x * kPer + j];
+    mine += v[j];
+  }
+  uint32_t total;
+  uint32_t run = block_incl_scan<kOrderThreads>(mine, &total) - mine;
+#pragma unroll
+  for (uint32_t j = 0; j < kPer; ++j) {
+    hist[threadIdx.x * kPer + j] = run;  // exclusive start of each bucket
+    run += v[j];
+  }
+  __syncthreads();
+  for (uint32_t i0 = 0; i0 < M; i0 += kOrderThreads) {
+    const uint32_t pos = claim(i0);
+    if (pos != kNone) p.fill_order[pos] = i0 + threadIdx.x;
+  }
+}
+
 // (4) Each work entry's segment: its set bits in ascending order get the ranks
 // [base, base + count); ranks below the quota are written out.  Host entries
 // claim their slots (clears only on the host-free bitmap; GPU classes read only).
-__global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
+// With a fill order to compute (a step), the grid has one more block, which does that.
+__global__ void __launch_bounds__(kOrderThreads) k_select_emit(EmitParams p) {
   pdl_wait();
   pdl_launch();
   if (*(volatile int *)p.status) return;
   const GroupDev g = p.groups[p.group0 + blockIdx.y];
+  const uint32_t nblk = p.fill_order ? gridDim.x - 1 : gridDim.x;  // blocks that emit
+  if (blockIdx.x >= nblk) {
+    fill_order_block(p, g);
+    span_close(p.span);
+    return;
+  }
   const Geometry &geo = p.geo;
   const GroupCounters *c = g.cnt;
   const uint32_t n_work = c->n_work;
@@ -632,7 +706,7 @@ __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
   const uint32_t q_host = c->K;
   const uint32_t lane = lane_id();
   const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const uint32_t nwarps = (nblk * blockDim.x) >> 5;
   for (uint32_t i = warp; i < n_work; i += nwarps) {
     const uint4 e = g.work[i];
     const bool host = e.x == kHostPos;
@@ -659,6 +733,7 @@ __global__ void __launch_bounds__(256) k_select_emit(EmitParams p) {
     }
     if (host && taken) bm_clear_mask(bm, wi, taken);  // claim the write-back targets
   }
+  span_close(p.span);
 }
 
 // -------------------------------------------------------- move and commit
@@ -717,10 +792,81 @@ __device__ __forceinline__ void write_entry_rows(const MoveParams &p) {
 }
 
 constexpr int kMoveUnroll = ULA_MOVE_UNROLL;
+constexpr int kMoveThreads = ULA_MOVE_THREADS;
 
-__global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) {
+// (5) Before the move: the rows of every victim that holds data (victims F..M-1) are
+// copied to the staging area, one warp per victim (HBM to HBM).  The move then writes
+// victims back from the staging area and fills them, each in its own order, with no
+// ordering between a victim's write-back and its fill.
+__global__ void __launch_bounds__(256) k_stage(MoveParams p) {
+  pdl_wait();
+  pdl_launch();
+  if (*(volatile int *)p.status) return;
+  const GroupDev &g = p.grp;
+  const Geometry &geo = p.geo;
+  span_open(p.span);
+  write_entry_rows(p);  // (1) every entry's unique row
+  if (geo.cache || !p.stage) {  // a local buffer writes nothing back
+    span_close(p.span);
+    return;
+  }
+  const uint32_t M = g.cnt->M, F = g.cnt->F;
+  const uint32_t lane = lane_id();
+  const uint32_t warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * blockDim.x) >> 5;
+  const size_t sb = (size_t)g.layers * geo.W;
+  const uint32_t nvec = (uint32_t)(sb / 16);
+  for (uint32_t i = F + warp; i < M; i += nwarps) {
+    const uint32_t v = g.victims[i];
+    if (v >= geo.S) {
+      if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
+      continue;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(g.gpu_pool + (size_t)v * sb);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.stage + (size_t)(i - F) * sb);
+    for (uint32_t c0 = 0; c0 < nvec; c0 += 32 * kMoveUnroll) {
+      uint4 x[kMoveUnroll];
+#pragma unroll
+      for (int u = 0; u < kMoveUnroll; ++u) {
+        const uint32_t c = c0 + u * 32 + lane;
+        if (c < nvec) x[u] = __ldcs(src + c);
+      }
+#pragma unroll
+      for (int u = 0; u < kMoveUnroll; ++u) {
+        const uint32_t c = c0 + u * 32 + lane;
+        if (c < nvec) dst[c] = x[u];
+      }
+    }
+  }
+  span_close(p.span);
+}
+
+// One of victim x's copies is done (its write-back, or the fill of its miss); the
+// last one commits x (a victim that holds data has two, a free slot or a local
+// buffer's victim one).  Called by one lane per completed copy, after a fence that
+// orders the warp's copy writes before it.
+__device__ __forceinline__ void copy_done(const MoveParams &p, uint32_t x, uint32_t F) {
+  const bool two = !p.geo.cache && x >= F;
+  if (two) {
+    if (atomicAdd(&p.vdone[x], 1u) != 1u) return;  // the other copy is still running
+    p.vdone[x] = 0;                                   // ready for the next step
+  }
+  commit_victim(p, x, F);
+}
+
+// (5) Data first: task t (one warp) writes victim t's staged rows back to its host
+// slot if it holds data (victim order = ascending host slots), and fills miss
+// i = fill_order[t] (host-slot bucket order) from its host slot into victim i's GPU
+// slot, writing the missed row's outputs (6) from the moved bytes.  Both directions of
+// the host link are busy in every warp.  Host memory is reached directly over the host
+// link.  Completed copies are counted per victim; the lanes of a warp commit up to 32
+// victims at a time, each once both of its copies are done (the map after the data).
+constexpr uint32_t kCommitBatch = 16;  // tasks per warp between commit rounds (2 copies each)
+
+__global__ void __launch_bounds__(kMoveThreads, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) {
   pdl_wait();  // (no early trigger: the commit's blocks would hold SM room for the whole move)
   if (*(volatile int *)p.status) return;
+  span_open(p.span);
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
   const uint32_t M = g.cnt->M, F = g.cnt->F, Mx = g.cnt->Mx;
@@ -731,7 +877,6 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) 
   const uint32_t nvec = (uint32_t)(sb / 16);
   const uint32_t CW = geo.W / 16;
   uint4 *out = reinterpret_cast<uint4 *>(p.out);
-  write_entry_rows(p);
   // overflow bypass: misses [M, M + Mx) are copied from their host slots to the
   // output only (they stay on the host)
   for (uint32_t i = M + warp; i < M + Mx; i += nwarps) {
@@ -759,40 +904,55 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) 
       }
     }
   }
-  for (uint32_t i = warp; i < M; i += nwarps) {
-    const uint32_t v = g.victims[i];
-    const uint32_t hs = p.miss_hs[i];
-    const uint32_t row = p.miss_row[i];
-    const bool owned = !geo.cache && i >= F;  // (a local buffer drops its victims' copies)
-    const uint32_t hd = owned ? g.wb_host[i - F] : 0u;
-    // the source: the miss's host slot, or (local buffer) its owner partition's GPU slot
+  uint32_t mine = kNone;  // the victim whose copy this lane reports at the next commit round
+  uint32_t batch = 0;
+  auto commit_round = [&]() {
+    __threadfence();  // this lane's copy writes before any commit that counts them
+    __syncwarp();
+    if (mine != kNone) copy_done(p, mine, F);
+    mine = kNone;
+    batch = 0;
+    __syncwarp();
+  };
+  for (uint32_t t = warp; t < M; t += nwarps) {
+    const bool back = !geo.cache && t >= F;  // (a local buffer drops its victims' copies)
+    const uint32_t hd = back ? g.wb_host[t - F] : 0u;
+    const uint32_t i = p.fill_order[t];
+    const bool bad_i = i >= M;
+    const uint32_t v = bad_i ? kNone : g.victims[i];
+    const uint32_t hs = bad_i ? kNone : p.miss_hs[i];
+    const uint32_t row = bad_i ? kNone : p.miss_row[i];
+    // the fill's source: the miss's host slot, or (local buffer) its owner partition's GPU slot
     const uint32_t part = hs >> kSrcShift, pslot = hs & ((1u << kSrcShift) - 1u);
     const bool src_bad = geo.cache ? (part >= p.src.P || pslot >= p.src.S) : hs >= geo.H;
-    if (v >= geo.S || src_bad || (owned && hd >= geo.H) || (out && row >= p.out_cap)) {
+    if (bad_i || v >= geo.S || src_bad || (back && (hd >= geo.H || !p.stage)) ||
+        (out && row >= p.out_cap)) {
       if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
       continue;
     }
     uint4 *gp = reinterpret_cast<uint4 *>(g.gpu_pool + (size_t)v * sb);
     const uint4 *src = reinterpret_cast<const uint4 *>(
         geo.cache ? p.src.pool[part] + (size_t)pslot * sb : g.host_pool + (size_t)hs * sb);
-    uint4 *dst = reinterpret_cast<uint4 *>(g.host_pool + (size_t)hd * sb);
+    const uint4 *bsrc =
+        back ? reinterpret_cast<const uint4 *>(p.stage + (size_t)(t - F) * sb) : nullptr;
+    uint4 *bdst = back ? reinterpret_cast<uint4 *>(g.host_pool + (size_t)hd * sb) : nullptr;
     for (uint32_t c0 = 0; c0 < nvec; c0 += 32 * kMoveUnroll) {
-      uint4 fill[kMoveUnroll], back[kMoveUnroll];
+      uint4 fill[kMoveUnroll], wb[kMoveUnroll];
 #pragma unroll
       for (int u = 0; u < kMoveUnroll; ++u) {
         const uint32_t c = c0 + u * 32 + lane;
         if (c < nvec) fill[u] = src[c];
       }
-      if (owned) {
+      if (back) {
 #pragma unroll
         for (int u = 0; u < kMoveUnroll; ++u) {
           const uint32_t c = c0 + u * 32 + lane;
-          if (c < nvec) back[u] = gp[c];
+          if (c < nvec) wb[u] = __ldcs(bsrc + c);
         }
 #pragma unroll
         for (int u = 0; u < kMoveUnroll; ++u) {
           const uint32_t c = c0 + u * 32 + lane;
-          if (c < nvec) dst[c] = back[u];
+          if (c < nvec) bdst[c] = wb[u];
         }
       }
 #pragma unroll
@@ -811,9 +971,13 @@ __global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move(MoveParams p) 
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) commit_victim(p, i, F);  // (5) this victim's map, after its copies
+    // report both copies of this task at the next commit round (lanes 2b, 2b + 1)
+    if (lane == 2 * batch) mine = back ? t : kNone;
+    if (lane == 2 * batch + 1) mine = i;
+    if (++batch == kCommitBatch) commit_round();
   }
+  commit_round();
+  span_close(p.span);
 }
 
 // (5) With the per-layer signal: the same moves, layer by layer.  The chunks of
@@ -831,7 +995,7 @@ constexpr int kMoveLayerUnroll = 4;
 #endif
 constexpr uint32_t kMoveBatch = ULA_MOVE_BATCH;  // chunks handed out at a time (a multiple of 32)
 
-__global__ void __launch_bounds__(256, ULA_MOVE_MINBLOCKS) k_move_layers(MoveParams p) {
+__global__ void __launch_bounds__(256, 3) k_move_layers(MoveParams p) {
   pdl_wait();
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
@@ -946,6 +1110,7 @@ constexpr int kGatherUnroll = ULA_GATHER_UNROLL;
 
 __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather(GatherParams p) {
   if (*(volatile int *)p.status) return;
+  span_open(p.span);
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
   const uint32_t U = g.cnt->U;
@@ -1018,6 +1183,7 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
       }
     }
   }
+  span_close(p.span);
   // per-layer signal: the hit rows of a layer are one of its two contributions
   if (p.signal) {
     __threadfence();  // every thread's output writes before the block's ticket
@@ -1970,7 +2136,8 @@ cudaError_t launch_mark_select(const StepParams &p, cudaStream_t s) {
 }
 
 cudaError_t launch_select_emit(const EmitParams &p, uint32_t n_groups, int blocks, cudaStream_t s) {
-  return launch_dependent(k_select_emit, dim3(blocks > 0 ? blocks : 1, n_groups), dim3(256), s, p);
+  const uint32_t grid = (uint32_t)(blocks > 0 ? blocks : 1) + (p.fill_order ? 1u : 0u);
+  return launch_dependent(k_select_emit, dim3(grid, n_groups), dim3(kOrderThreads), s, p);
 }
 
 cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStream_t s) {
@@ -1983,7 +2150,7 @@ size_t gather_tma_smem(uint32_t row_bytes) {
 }
 
 cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t row_bytes) {
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move, 256, 0);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move, kMoveThreads, 0);
   if (e != cudaSuccess) return e;
   if (gather_uses_tma(row_bytes)) {
     const size_t smem = gather_tma_smem(row_bytes);
@@ -1994,9 +2161,18 @@ cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t row_b
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather, kGatherThreads, 0);
 }
 
-cudaError_t launch_move(const MoveParams &p, int blocks, cudaStream_t s) {
-  if (!p.geo.signal)  // copies, then each victim's map, in one kernel
-    return launch_dependent(k_move, dim3(blocks), dim3(256), s, p);
+int move_threads() { return kMoveThreads; }
+
+cudaError_t launch_stage(const MoveParams &p, int blocks, cudaStream_t s) {
+  return launch_dependent(k_stage, dim3(blocks > 0 ? blocks : 1), dim3(256), s, p);
+}
+
+cudaError_t launch_move(const MoveParams &p, int blocks, bool dependent, cudaStream_t s) {
+  if (!p.geo.signal) {  // copies, then each victim's map, in one kernel
+    if (dependent) return launch_dependent(k_move, dim3(blocks), dim3(kMoveThreads), s, p);
+    k_move<<<blocks, kMoveThreads, 0, s>>>(p);
+    return cudaGetLastError();
+  }
   // layer by layer: a victim's chunks are spread over warps, so the map follows in
   // a second kernel, once every copy is done
   cudaError_t e = launch_dependent(k_move_layers, dim3(blocks), dim3(256), s, p);

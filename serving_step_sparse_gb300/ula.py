@@ -18,6 +18,7 @@ ADDR_PAD = 0xFFFFFFFF
 FLAG_BYPASS_OVERFLOW = 1
 FLAG_EXACT_LRU = 2
 FLAG_LAYER_SIGNAL = 4
+FLAG_GATHER_BESIDE_MOVE = 8
 MAP_UNALLOCATED = 0xFFFFFFFF
 MAP_HOST = 0x80000000
 STAMP_FREE = 0xFFFFFFFF
@@ -32,7 +33,7 @@ DEBUG_STALL_SCAN_BARRIER = 0x100  # ula_debug_inject: the next exact-LRU scan wa
 ERR_POISONED = 6
 ERR_INTERNAL = 7
 
-PHASES = ["dedup", "rotate", "mark", "select", "move", "gather", "alloc", "free"]
+PHASES = ["dedup", "rotate", "mark", "select", "move", "gather", "alloc", "free", "stage"]
 NOALLOC_MAX_ENTRIES = 65536
 
 
@@ -75,6 +76,11 @@ class ula_profile(C.Structure):
                     "ms": float(self.ms[i])} for i, p in enumerate(PHASES)}
 
 
+class ula_span(C.Structure):
+    _fields_ = [("phase", C.c_uint32), ("group", C.c_uint32), ("start_ns", C.c_uint64),
+                ("end_ns", C.c_uint64)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"CUDA library not built: {LIB_PATH} (run __graft_entry__.build())")
@@ -104,6 +110,10 @@ def _load():
     lib.ula_profile_enable.restype = i32
     lib.ula_profile_read.argtypes = [p, C.POINTER(ula_profile), i32]
     lib.ula_profile_read.restype = i32
+    lib.ula_profile_spans.argtypes = [p, i32]
+    lib.ula_profile_spans.restype = i32
+    lib.ula_profile_spans_read.argtypes = [p, p, u32, C.POINTER(u32)]
+    lib.ula_profile_spans_read.restype = i32
     lib.ula_debug_regather.argtypes = [p, u32, u32, u32, p, u32, u32, p]
     lib.ula_debug_regather.restype = i32
     lib.ula_dedup_noalloc.argtypes = [p, u32, p, p, p, p]
@@ -299,6 +309,19 @@ def ula_profile_read(ctx: int, reset: bool = False) -> dict:
     pr = ula_profile()
     _check(lib.ula_profile_read(ctx, C.byref(pr), 1 if reset else 0), "ula_profile_read")
     return pr.as_dict()
+
+
+def ula_profile_spans(ctx: int, on: bool) -> None:
+    _check(lib.ula_profile_spans(ctx, 1 if on else 0), "ula_profile_spans")
+
+
+def ula_profile_spans_read(ctx: int, cap: int = 1 << 16) -> list:
+    """The recorded copy-kernel launch spans: [(phase name, group, start_ns, end_ns)]."""
+    buf = (ula_span * cap)()
+    n = C.c_uint32()
+    _check(lib.ula_profile_spans_read(ctx, buf, cap, C.byref(n)), "ula_profile_spans_read")
+    return [(PHASES[buf[i].phase], int(buf[i].group), int(buf[i].start_ns), int(buf[i].end_ns))
+            for i in range(min(n.value, cap))]
 
 
 def ula_dedup_noalloc(d_sel: int, n: int, d_uniq: int, d_entry_row: int, d_n_uniq: int,

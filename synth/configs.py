@@ -52,6 +52,7 @@ class Workload:
     bypass: bool = False        # overflow bypass: misses beyond the pool are read in place
     exact_lru: bool = False     # exact LRU (timestamp per slot) in place of PB-LRU
     layer_signal: bool = False  # layer-major fill with a device flag per layer
+    gather_beside: bool = False  # the hit gather runs beside the move (not before it)
     _cache: dict = field(default_factory=dict, compare=False, hash=False, repr=False)
 
     @property

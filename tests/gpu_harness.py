@@ -22,7 +22,8 @@ class GpuReplay:
                               gpu_slots=w.gpu_slots, host_slots=w.host_slots,
                               ring_buckets=w.ring_buckets, max_logical=w.max_logical,
                               max_entries=w.entries_per_step, bypass_overflow=w.bypass,
-                              exact_lru=w.exact_lru, layer_signal=w.layer_signal)
+                              exact_lru=w.exact_lru, layer_signal=w.layer_signal,
+                              gather_beside_move=w.gather_beside)
         self.cap = out_cap if out_cap is not None else w.entries_per_step
         self.outs = [self.cache.out_buffer(g, self.cap) for g in range(G)]
         E = w.entries_per_step

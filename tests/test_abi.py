@@ -53,7 +53,12 @@ def test_binding_struct_sizes_match_header(libpath):
     assert C.sizeof(ula.ula_stats) == 8 * 13
     assert C.sizeof(ula.ula_debug_layout) == 4 * 8
     assert C.sizeof(ula.ula_debug_state) == 8 * 15 + 4 * 9 + 4  # padded to 8
+    assert C.sizeof(ula.ula_span) == 4 * 2 + 8 * 2
+    assert C.sizeof(ula.ula_profile) == (8 + 8 + 8) * len(ula.PHASES)
     src = open(HEADER).read()
+    phases = re.search(r"ULA_PHASE_DEDUP = 0,(.*?)ULA_PHASE_COUNT", src, flags=re.S).group(1)
+    names = re.findall(r"ULA_PHASE_(\w+)", re.sub(r"/\*.*?\*/", "", phases))
+    assert ["dedup"] + [n.lower() for n in names] == ula.PHASES
     assert "#define ULA_MAX_GROUPS 64" in src and "#define ULA_MAX_BUCKETS 64" in src
     for name, val in (("ULA_ERR_INVALID_ARG", 1), ("ULA_ERR_CAPACITY", 2), ("ULA_ERR_UNMAPPED", 3),
                       ("ULA_ERR_CUDA", 4), ("ULA_ERR_TIMEOUT", 5), ("ULA_ERR_POISONED", 6),
@@ -76,7 +81,8 @@ def test_binding_flags_match_header(libpath):
     from serving_step_sparse_gb300 import ula
     src = open(HEADER).read()
     for name, val in (("ULA_FLAG_BYPASS_OVERFLOW", 1), ("ULA_FLAG_EXACT_LRU", 2),
-                      ("ULA_FLAG_LAYER_SIGNAL", 4), ("ULA_DEBUG_STALL_SCAN_BARRIER", 0x100),
+                      ("ULA_FLAG_LAYER_SIGNAL", 4), ("ULA_FLAG_GATHER_BESIDE_MOVE", 8),
+                      ("ULA_DEBUG_STALL_SCAN_BARRIER", 0x100),
                       ("ULA_NOALLOC_MAX_ENTRIES", 65536)):
         m = re.search(rf"#define {name} (0x[0-9a-fA-F]+|\d+)u?\b", src)
         assert m and int(m.group(1), 0) == val, name

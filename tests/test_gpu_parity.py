@@ -104,6 +104,57 @@ def test_parity_full_size_sampled(name, steps):
     assert stats["steps"] == steps * w.n_groups
 
 
+@pytest.mark.parametrize("name", ["longdoc", "low_overlap_256"])
+def test_parity_small_gather_beside_move(name):
+    """The hit gather beside the move (ULA_FLAG_GATHER_BESIDE_MOVE): same results."""
+    w = small(name).replace(gather_beside=True)
+    stats = run_parity(w, w.steps)
+    assert stats["misses"] > 0
+
+
+def test_parity_full_size_sampled_gather_beside_move():
+    w = WORKLOADS["longdoc"].replace(gather_beside=True)
+    stats = run_parity(w, 6, mode="id", state_every=1, out_every=10**9, sample_rows=4096)
+    assert stats["steps"] == 6 * w.n_groups
+
+
+@pytest.mark.parametrize("beside", [False, True])
+def test_copy_kernel_spans(beside):
+    """Every step records one span per copy kernel (gather, staging, move) and one for its
+    metadata (dedup through victim emission), each with a start no later than its end,
+    in launch order; by default the move starts after the gather ended."""
+    from serving_step_sparse_gb300 import ula
+    w = small("longdoc").replace(steps=6, gather_beside=beside)
+    gpu = GpuReplay(w)
+    try:
+        gpu.step()
+        ula.ula_profile_spans(gpu.cache.ctx, True)
+        n = 3
+        for _ in range(n):
+            gpu.step()
+        spans = ula.ula_profile_spans_read(gpu.cache.ctx)
+        ula.ula_profile_spans(gpu.cache.ctx, False)
+        assert ula.ula_profile_spans_read(gpu.cache.ctx) == []  # read clears
+        kinds = [(ph, g) for ph, g, _, _ in spans]
+        for g in range(w.n_groups):
+            for ph in ("select", "gather", "stage", "move"):  # select: dedup .. victim emission
+                assert kinds.count((ph, g)) == n, (ph, g)
+        for ph, g, t0, t1 in spans:
+            assert 0 < t0 <= t1, (ph, g, t0, t1)
+        per = {}
+        for ph, g, t0, t1 in spans:
+            per.setdefault(g, []).append((ph, t0, t1))
+        for g, lst in per.items():  # per group step, in launch order
+            for i in range(0, len(lst), 4):
+                (pq, q0, q1), (pg, g0, g1), (ps, s0, _), (pm, m0, _) = lst[i:i + 4]
+                assert (pq, pg, ps, pm) == ("select", "gather", "stage", "move")
+                assert g0 >= q0 and s0 >= q1 and m0 >= q1
+                if not beside:
+                    assert m0 >= g1, "the move starts after the hit gather"
+    finally:
+        gpu.close()
+
+
 # ----------------------------------------------------------------- edge cases
 
 def test_pads_and_ragged_sizes():
@@ -592,7 +643,7 @@ def test_regather_reproduces_hit_rows():
                 got = buf[j, :U].cpu().numpy()[hit]
                 exp = gpu.outs[g][j, :U].cpu().numpy()[hit]
                 assert np.array_equal(got, exp)
-            # layer ranges in one launch (the step gathers layers 1..L-1 together)
+            # layer ranges in one launch (the step gathers every layer in one)
             L = w.layers_per_group
             for j0, n in ((1, L - 1), (0, L), (0, L - 1)):
                 buf = torch.zeros_like(gpu.outs[g])

@@ -80,20 +80,30 @@ def test_reference_arm_line(capsys):
 
 
 def test_roofline_helpers(monkeypatch):
-    """The gather's DRAM traffic per launch: the two launch kinds' per-row figures times
-    the hits, averaged over launches; withheld once the kernel's source hash moves."""
+    """Span bookkeeping (union of overlapping launch spans, per-kernel sums) and the
+    gather's DRAM traffic per launch from the ncu figures per hit row, withheld once the
+    kernel's source hash moves or on another workload."""
     import bench
+    assert bench.union_ns([]) == 0
+    assert bench.union_ns([(0, 10), (5, 20), (30, 40)]) == 30
+    assert bench.union_ns([(30, 40), (0, 10), (10, 12)]) == 22
+    spans = [("gather", 0, 100, 300), ("move", 0, 300, 1300), ("gather", 1, 1300, 1500),
+             ("move", 1, 1500, 2500), ("stage", 1, 0, 0)]  # an empty record is skipped
+    sm = bench.span_summary(spans, {}, 4, 656, 2)
+    assert sm["gather"] == {"launches": 2, "sum_us": 0.4, "union_us": 0.4}
+    assert sm["move"]["launches"] == 2 and sm["move"]["sum_us"] == 2.0 and "stage" not in sm
     t = dict(bench.GATHER_TRAFFIC)
-    # DRAM reads cover at least the algorithmic reads: one 656-byte row, three of a slot
-    assert 656 <= t["layer0_bytes_per_row"] < 2 * 656
-    assert 3 * 656 <= t["later_bytes_per_slot"] < 2 * 3 * 656
-    monkeypatch.setattr(bench, "gather_source_sha256", lambda: t["source_sha256"])
-    hits, L, launches = 1000, 4, 2
-    exp = hits * (t["layer0_bytes_per_row"] + t["later_bytes_per_slot"]) / launches
-    assert bench.traffic_per_launch(hits, L, launches) == round(exp)
-    assert bench.traffic_per_launch(hits, 1, 1) == round(hits * t["layer0_bytes_per_row"])
-    assert bench.traffic_per_launch(hits, L, 0) is None
+    if t["source_sha256"] is not None:  # DRAM reads cover at least the algorithmic reads
+        assert 4 * 656 <= t["read_bytes_per_hit"] < 2 * 4 * 656
+        assert t["hit_rows"] > 0 and t["workload"]
+    fake = {"source_sha256": "f" * 64, "workload": "longdoc", "hit_rows": 100,
+            "read_bytes_per_hit": 2700.0, "write_bytes_per_hit": 2624.0}
+    monkeypatch.setattr(bench, "GATHER_TRAFFIC", fake)
+    monkeypatch.setattr(bench, "gather_source_sha256", lambda: "f" * 64)
+    assert bench.traffic_per_launch(1000, 2, "longdoc") == round(1000 * (2700 + 2624) / 2)
+    assert bench.traffic_per_launch(1000, 0, "longdoc") is None
+    assert bench.traffic_per_launch(1000, 2, "low_evict") is None
     monkeypatch.setattr(bench, "gather_source_sha256", lambda: "0" * 64)
-    assert bench.traffic_per_launch(hits, L, launches) is None
+    assert bench.traffic_per_launch(1000, 2, "longdoc") is None
     peak, src = bench.measured_peaks()
     assert peak > 1000 and src in ("measured", "fallback")
