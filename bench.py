@@ -48,6 +48,10 @@ def parse_args(argv=None):
                     help="replacement policy: PB-LRU, or exact LRU (timestamp scan)")
     ap.add_argument("--repeats", type=int, default=3,
                     help="timed regions of --steps steps each; value = their median")
+    ap.add_argument("--one-stream", action="store_true",
+                    help="issue every group's call on the one caller stream (each group's "
+                         "step then waits for the previous group's); by default each group "
+                         "has its own caller stream, so later groups' steps are issued ahead")
     ap.add_argument("--gather-beside", action="store_true",
                     help="run the hit gather beside the move (ULA_FLAG_GATHER_BESIDE_MOVE)")
     ap.add_argument("--profile-steps", type=int, default=60)
@@ -391,9 +395,37 @@ def run_gpu(args, rank, world, local):
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
 
-    def do_step(sel_t, ev, rows_t):
+    # Each group's calls go on a caller stream of their own, so later groups' (and the
+    # next step's) calls are issued ahead: the library orders each group's step after that
+    # group's previous step and alloc only, and runs a group's metadata while earlier
+    # calls' copies run.  The step's appended tokens are allocated on the main stream (the
+    # library places them in each group after that group's step).  `wait` makes the
+    # group streams wait for the main stream first (inputs copied there).
+    gstreams = [stream] * G if args.one_stream else [torch.cuda.Stream(dev) for _ in range(G)]
+    step_evt = [torch.cuda.Event() for _ in range(4)]
+    nstep = [0]
+
+    def issue_groups(sel_t, wait=False):
+        if args.one_stream:
+            for g in range(G):
+                cache.step_group(g, sel_t[g], outs[g], entry_row[g], req_off[g])
+            return
+        if wait:
+            e = step_evt[nstep[0] % len(step_evt)]
+            nstep[0] += 1
+            e.record(stream)
+            for g in range(G):
+                gstreams[g].wait_event(e)
         for g in range(G):
-            cache.step_group(g, sel_t[g], outs[g], entry_row[g], req_off[g])
+            cache.step_group(g, sel_t[g], outs[g], entry_row[g], req_off[g], stream=gstreams[g])
+
+    def join_groups():
+        if not args.one_stream:
+            for g in range(G):
+                stream.wait_stream(gstreams[g])
+
+    def do_step(sel_t, ev, rows_t):
+        issue_groups(sel_t)
         if ev["append_n"]:
             got = cache.alloc(ev["append_n"], rows_t)
             assert got == ev["append_base"]
@@ -437,6 +469,7 @@ def run_gpu(args, rank, world, local):
         for _ in range(K):
             do_step(sel_dev[t], steps[t][1], rows_dev[t])
             t += 1
+        join_groups()
         e1.record(stream)
         sb = cache.sync()
         torch.cuda.synchronize()
@@ -516,11 +549,11 @@ def run_gpu(args, rank, world, local):
             buf.copy_(sel_host[i], non_blocking=True)
             h2d_bytes += buf.numel() * 4
             ev = steps[n_dev + i][1]
-            for g in range(G):
-                cache.step_group(g, buf[g], outs[g], entry_row[g], req_off[g])
+            issue_groups(buf, wait=True)
             if ev["append_n"]:
                 cache.alloc(ev["append_n"], rows_host[i])  # read from pinned host memory
                 h2d_bytes += rows_host[i].numel()
+            join_groups()
             for g in range(G):
                 res_host[i, g].copy_(req_off[g], non_blocking=True)
                 d2h_bytes += (R + 1) * 4
@@ -839,6 +872,8 @@ def main(argv=None):
                 "spans_us_per_step": r["spans_us_per_step"]}
         if args.gather_beside:
             line["config"]["gather"] = "beside the move"
+        line["config"]["group_calls"] = ("one caller stream" if args.one_stream else
+                                         "one caller stream per group (later groups issued ahead)")
         if r["e2e"] is not None:
             line["e2e"] = r["e2e"]
         if world == 1 and not args.no_cpu_baseline:

@@ -49,10 +49,16 @@ struct ula_ctx {
   int device = 0;
   int sm_count = 0;
   cudaStream_t home = nullptr;  // the caller's stream given at create (alloc/free order)
-  cudaStream_t crit = nullptr;  // internal, highest priority: the step's critical path
-  cudaStream_t side = nullptr;  // internal, lowest priority: the hit gather
-  cudaEvent_t in_evt = nullptr, out_evt = nullptr, commit_evt = nullptr;
-  cudaEvent_t marked_evt = nullptr, hit_evt = nullptr;
+  // Internal streams.  crit: the steps' metadata kernels, alloc and free, in call order.
+  // copy: every step's copy kernels (the hit gather before the move, the staging copy,
+  // the move), in call order.  side: the hit gather beside the move.  A step's metadata
+  // thus runs while the previous call's copies occupy the SMs and the host link (the
+  // calls of different groups are independent: each group has its own state and step
+  // scratch).
+  cudaStream_t crit = nullptr;  // highest priority
+  cudaStream_t copy = nullptr;  // highest priority
+  cudaStream_t side = nullptr;  // lowest priority
+  cudaEvent_t in_evt = nullptr;
   int move_blocks = 0, gather_blocks = 0;  // persistent grids (resident blocks)
   int gather_fit_per_sm = 0;
   int emit_blocks = 0, stage_blocks = 0;
@@ -61,13 +67,29 @@ struct ula_ctx {
   std::vector<GroupDev> groups_h;
   GroupDev *groups_d = nullptr;
   GroupCounters *cnt_d = nullptr;
-  unsigned long long *tbl = nullptr;
-  uint32_t *addr_row = nullptr;
-  uint2 *blk = nullptr;
-  uint32_t *miss_list = nullptr, *miss_hs = nullptr, *miss_row = nullptr;
-  uint32_t *fill_order = nullptr;  // [decision_cap] the move's fill order
-  uint32_t *vdone = nullptr;       // [decision_cap] copies done per victim
-  uint8_t *stage = nullptr;        // [max_entries][max L_g][W] staged victim rows
+  // A group's step scratch (its own, so that a group's metadata can run while another
+  // group's copies still read theirs) and the events that order its steps.
+  struct GroupStep {
+    unsigned long long *tbl = nullptr;  // [max_logical] dedup stamps
+    uint32_t *addr_row = nullptr;       // [max_logical]
+    uint2 *blk = nullptr;
+    uint32_t *miss_list = nullptr, *miss_hs = nullptr, *miss_row = nullptr;
+    uint32_t *fill_order = nullptr;     // [decision_cap] the move's fill order
+    uint32_t *vdone = nullptr;          // [decision_cap] copies done per victim
+    uint32_t epoch = 0;
+    cudaEvent_t rot_evt = nullptr;      // compaction done (the gather may start)
+    cudaEvent_t meta_evt = nullptr;     // victims emitted (the copies may start)
+    cudaEvent_t commit_evt = nullptr;   // the step's move committed
+    cudaEvent_t hit_evt = nullptr;      // the step's hit gather done
+    bool in_flight = false;             // commit_evt/hit_evt mark this group's last step
+    // alloc/free of this group run on its own stream, after its last step's copies, so
+    // that a later step of one group need not wait for every group's copies
+    cudaStream_t upd = nullptr;
+    cudaEvent_t upd_evt = nullptr;      // the group's last alloc/free done
+    bool upd_pending = false;
+  };
+  std::vector<GroupStep> steps;
+  uint8_t *stage = nullptr;        // [min(max_entries, S)][max L_g][W] staged victim rows
   // launch spans of the copy kernels (diagnostics): a ring of records on the device
   SpanRec *spans_d = nullptr;
   bool span_on = false;
@@ -77,7 +99,6 @@ struct ula_ctx {
   int lru_blocks = 0;   // its cooperative grid
   int *status = nullptr;
   uint32_t decision_cap = 0;
-  uint32_t epoch = 0;
   uint32_t round[ULA_MAX_GROUPS] = {};
   uint32_t next_logical = 0;
   uint64_t live_count = 0;
@@ -118,10 +139,25 @@ struct ula_ctx {
     return e != cudaSuccess ? e : cudaStreamWaitEvent(crit, in_evt, 0);
   }
 
-  // the caller's stream continues after the call's work on `crit`
-  cudaError_t leave(cudaStream_t caller) {
-    cudaError_t e = cudaEventRecord(out_evt, crit);
-    return e != cudaSuccess ? e : cudaStreamWaitEvent(caller, out_evt, 0);
+  // alloc/free of group g: on the group's own stream, after everything on the home
+  // stream (in_evt, recorded by the caller of this helper) and after the group's last
+  // step (its copies and gather) and last alloc/free
+  cudaError_t begin_update(uint32_t g) {
+    GroupStep &st = steps[g];
+    cudaError_t e = cudaStreamWaitEvent(st.upd, in_evt, 0);
+    if (e == cudaSuccess && st.in_flight) e = cudaStreamWaitEvent(st.upd, st.commit_evt, 0);
+    if (e == cudaSuccess && st.in_flight) e = cudaStreamWaitEvent(st.upd, st.hit_evt, 0);
+    return e;
+  }
+  // ... and the home stream continues after every group's update
+  cudaError_t end_updates(cudaStream_t home_s) {
+    for (GroupStep &st : steps) {
+      cudaError_t e = cudaEventRecord(st.upd_evt, st.upd);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(home_s, st.upd_evt, 0);
+      if (e != cudaSuccess) return e;
+      st.upd_pending = true;
+    }
+    return cudaSuccess;
   }
 
   // the next span record for a launch of `phase` in `group`, or NULL (not recording,
@@ -246,11 +282,13 @@ void destroy_resources(ula_ctx *c) {
   c->allocations.clear();
   if (c->side) cudaStreamDestroy(c->side);
   if (c->crit) cudaStreamDestroy(c->crit);
+  if (c->copy) cudaStreamDestroy(c->copy);
   if (c->in_evt) cudaEventDestroy(c->in_evt);
-  if (c->out_evt) cudaEventDestroy(c->out_evt);
-  if (c->commit_evt) cudaEventDestroy(c->commit_evt);
-  if (c->marked_evt) cudaEventDestroy(c->marked_evt);
-  if (c->hit_evt) cudaEventDestroy(c->hit_evt);
+  for (auto &st : c->steps) {
+    for (cudaEvent_t e : {st.rot_evt, st.meta_evt, st.commit_evt, st.hit_evt, st.upd_evt})
+      if (e) cudaEventDestroy(e);
+    if (st.upd) cudaStreamDestroy(st.upd);
+  }
   for (auto &t : c->prof_pending) {
     cudaEventDestroy(t.a);
     cudaEventDestroy(t.b);
@@ -304,12 +342,9 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   int prio_least = 0, prio_greatest = 0;
   ULA_CUDA(cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest));
   ULA_CUDA(cudaStreamCreateWithPriority(&c->crit, cudaStreamNonBlocking, prio_greatest));
+  ULA_CUDA(cudaStreamCreateWithPriority(&c->copy, cudaStreamNonBlocking, prio_greatest));
   ULA_CUDA(cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, prio_least));
   ULA_CUDA(cudaEventCreateWithFlags(&c->in_evt, cudaEventDisableTiming));
-  ULA_CUDA(cudaEventCreateWithFlags(&c->out_evt, cudaEventDisableTiming));
-  ULA_CUDA(cudaEventCreateWithFlags(&c->commit_evt, cudaEventDisableTiming));
-  ULA_CUDA(cudaEventCreateWithFlags(&c->marked_evt, cudaEventDisableTiming));
-  ULA_CUDA(cudaEventCreateWithFlags(&c->hit_evt, cudaEventDisableTiming));
   ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks, cfg.row_bytes));
   c->gather_fit_per_sm = c->gather_blocks;
   // ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune the persistent grids
@@ -321,17 +356,28 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   c->emit_blocks = c->sm_count;
   c->stage_blocks = 2 * c->sm_count;
 
-  // shared scratch (main-stream kernels only)
+  // per-group step scratch and events
   const uint32_t max_blk = (cfg.max_entries + 255) / 256 + 1;
-  ULA_CUDA(c->alloc(&c->tbl, cfg.max_logical));
-  ULA_CUDA(c->alloc(&c->addr_row, cfg.max_logical));
-  ULA_CUDA(c->alloc(&c->blk, max_blk));
-  ULA_CUDA(c->alloc(&c->miss_list, cfg.max_entries));
-  ULA_CUDA(c->alloc(&c->miss_hs, cfg.max_entries));
-  ULA_CUDA(c->alloc(&c->miss_row, cfg.max_entries));
-  ULA_CUDA(c->alloc(&c->fill_order, c->decision_cap));
-  ULA_CUDA(c->alloc(&c->vdone, c->decision_cap));
-  ULA_CUDA(cudaMemsetAsync(c->vdone, 0, sizeof(uint32_t) * c->decision_cap, c->home));
+  c->steps.resize(G);
+  for (uint32_t g = 0; g < G; ++g) {
+    ula_ctx::GroupStep &st = c->steps[g];
+    ULA_CUDA(c->alloc(&st.tbl, cfg.max_logical));
+    ULA_CUDA(c->alloc(&st.addr_row, cfg.max_logical));
+    ULA_CUDA(c->alloc(&st.blk, max_blk));
+    ULA_CUDA(c->alloc(&st.miss_list, cfg.max_entries));
+    ULA_CUDA(c->alloc(&st.miss_hs, cfg.max_entries));
+    ULA_CUDA(c->alloc(&st.miss_row, cfg.max_entries));
+    ULA_CUDA(c->alloc(&st.fill_order, c->decision_cap));
+    ULA_CUDA(c->alloc(&st.vdone, c->decision_cap));
+    ULA_CUDA(cudaMemsetAsync(st.vdone, 0, sizeof(uint32_t) * c->decision_cap, c->home));
+    ULA_CUDA(cudaMemsetAsync(st.tbl, 0, sizeof(unsigned long long) * cfg.max_logical, c->home));
+    for (cudaEvent_t *e : {&st.rot_evt, &st.meta_evt, &st.commit_evt, &st.hit_evt, &st.upd_evt})
+      ULA_CUDA(cudaEventCreateWithFlags(e, cudaEventDisableTiming));
+    ULA_CUDA(cudaStreamCreateWithPriority(&st.upd, cudaStreamNonBlocking, prio_greatest));
+  }
+  ULA_CUDA(c->alloc(&c->status, 1));
+  ULA_CUDA(c->alloc(&c->cnt_d, G));
+  ULA_CUDA(c->alloc(&c->groups_d, G));
   if (H && !geo.cache && !geo.signal) {  // staged victim rows (the slot-major move only)
     uint32_t lmax = 0;
     for (uint32_t g = 0; g < G; ++g) lmax = cfg.layers_per_group[g] > lmax ? cfg.layers_per_group[g] : lmax;
@@ -339,9 +385,6 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
     ULA_CUDA(c->alloc(&c->stage, rows * lmax * cfg.row_bytes));
   }
   ULA_CUDA(c->alloc(&c->spans_d, kSpanCap));
-  ULA_CUDA(c->alloc(&c->status, 1));
-  ULA_CUDA(c->alloc(&c->cnt_d, G));
-  ULA_CUDA(c->alloc(&c->groups_d, G));
   cudaStream_t s = c->home;
   if (geo.exact) {  // one cooperative block per SM (it must fit beside the gathers)
     int per_sm = 0;
@@ -362,7 +405,6 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
     ULA_CUDA(c->alloc(&c->lru.blist, (size_t)c->lru.per * nb));
     ULA_CUDA(cudaMemsetAsync(c->lru.bar, 0, 3 * sizeof(uint32_t), s));
   }
-  ULA_CUDA(cudaMemsetAsync(c->tbl, 0, sizeof(unsigned long long) * cfg.max_logical, s));
   ULA_CUDA(cudaMemsetAsync(c->status, 0, sizeof(int), s));
 
   const uint32_t ncls = B + 2;
@@ -490,43 +532,46 @@ static int alloc_impl(ula_ctx *c, uint32_t n, const void *rows, uint32_t *logica
   const uint8_t *rows_d =
       static_cast<const uint8_t *>(device_address(rows, c->device, true, true));
   if (!rows_d || !aligned16(rows_d)) return ULA_ERR_INVALID_ARG;
-  cudaStream_t s = c->crit;
-  ULA_CUDA(c->enter(c->home));
-
+  // per group, on the group's update stream: after the group's last step only
+  ULA_CUDA(cudaEventRecord(c->in_evt, c->home));
   const uint32_t base = c->next_logical;
-  for (uint32_t off = 0; off < n; off += kAllocChunk) {
-    const uint32_t m = n - off < kAllocChunk ? n - off : kAllocChunk;
-    EmitParams sp{};
-    sp.geo = c->geo;
-    sp.groups = c->groups_d;
-    sp.group0 = 0;
-    sp.order.n_cls = 1;
-    sp.order.cls[0] = c->geo.B + 1;  // free slots only: alloc never evicts
-    sp.quota = m;
-    sp.status = c->status;
-    ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 2, [&] {
-      cudaError_t e = launch_alloc_select(sp, cfg.n_groups, s);
-      return e != cudaSuccess ? e : launch_select_emit(sp, cfg.n_groups, c->emit_blocks, s);
-    }));
-    AllocParams ap{};
-    ap.geo = c->geo;
-    ap.groups = c->groups_d;
-    ap.rows = rows_d;
-    unsigned long long acc = 0;
-    for (uint32_t g = 0; g < cfg.n_groups; ++g) {
-      const unsigned long long sb = (unsigned long long)cfg.layers_per_group[g] * cfg.row_bytes;
+  for (uint32_t g = 0; g < cfg.n_groups; ++g) {
+    ULA_CUDA(c->begin_update(g));
+    cudaStream_t s = c->steps[g].upd;
+    unsigned long long acc = 0;  // byte offset of group g's rows
+    for (uint32_t h = 0; h < g; ++h)
+      acc += (unsigned long long)total * cfg.layers_per_group[h] * cfg.row_bytes;
+    const unsigned long long sb = (unsigned long long)cfg.layers_per_group[g] * cfg.row_bytes;
+    for (uint32_t off = 0; off < n; off += kAllocChunk) {
+      const uint32_t m = n - off < kAllocChunk ? n - off : kAllocChunk;
+      EmitParams sp{};
+      sp.geo = c->geo;
+      sp.groups = c->groups_d;
+      sp.group0 = g;
+      sp.order.n_cls = 1;
+      sp.order.cls[0] = c->geo.B + 1;  // free slots only: alloc never evicts
+      sp.quota = m;
+      sp.status = c->status;
+      ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 2, [&] {
+        cudaError_t e = launch_alloc_select(sp, 1, s);
+        return e != cudaSuccess ? e : launch_select_emit(sp, 1, c->emit_blocks, s);
+      }));
+      AllocParams ap{};
+      ap.geo = c->geo;
+      ap.groups = c->groups_d;
+      ap.rows = rows_d;
       ap.group_off[g] = acc + ((unsigned long long)phase + (unsigned long long)off * stride) * sb;
       ap.round[g] = c->round[g];
-      acc += (unsigned long long)total * sb;
+      ap.group0 = g;
+      ap.row_stride = stride;
+      ap.base = base + off;
+      ap.n = m;
+      ap.status = c->status;
+      ULA_CUDA(c->phase(ULA_PHASE_ALLOC, s, 1,
+                        [&] { return launch_alloc_place(ap, 1, c->move_blocks, s); }));
     }
-    ap.row_stride = stride;
-    ap.base = base + off;
-    ap.n = m;
-    ap.status = c->status;
-    ULA_CUDA(c->phase(ULA_PHASE_ALLOC, s, 1,
-                      [&] { return launch_alloc_place(ap, cfg.n_groups, c->move_blocks, s); }));
   }
-  ULA_CUDA(c->leave(c->home));
+  ULA_CUDA(c->end_updates(c->home));
   for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 1;
   c->live_count += n;
   c->next_logical = base + n;
@@ -550,17 +595,21 @@ static int free_impl(ula_ctx *c, uint32_t base, uint32_t n, bool drop) {
   }
   if (n == 0) return ULA_OK;
   ULA_CUDA(c->ensure_device());
-  cudaStream_t s = c->crit;
-  ULA_CUDA(c->enter(c->home));
-  FreeParams fp{};
-  fp.geo = c->geo;
-  fp.groups = c->groups_d;
-  for (uint32_t g = 0; g < c->cfg.n_groups; ++g) fp.round[g] = c->round[g];
-  fp.base = base;
-  fp.n = n;
-  fp.status = c->status;
-  ULA_CUDA(c->phase(ULA_PHASE_FREE, s, 1, [&] { return launch_free(fp, c->cfg.n_groups, s); }));
-  ULA_CUDA(c->leave(c->home));
+  ULA_CUDA(cudaEventRecord(c->in_evt, c->home));
+  for (uint32_t g = 0; g < c->cfg.n_groups; ++g) {  // per group, after its last step only
+    ULA_CUDA(c->begin_update(g));
+    cudaStream_t s = c->steps[g].upd;
+    FreeParams fp{};
+    fp.geo = c->geo;
+    fp.groups = c->groups_d;
+    fp.round[g] = c->round[g];
+    fp.group0 = g;
+    fp.base = base;
+    fp.n = n;
+    fp.status = c->status;
+    ULA_CUDA(c->phase(ULA_PHASE_FREE, s, 1, [&] { return launch_free(fp, 1, s); }));
+  }
+  ULA_CUDA(c->end_updates(c->home));
   if (!drop) {
     for (uint32_t i = 0; i < n; ++i) c->live[base + i] = 0;
     c->live_count -= n;
@@ -585,11 +634,20 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   ULA_CUDA(c->ensure_device());
   cudaStream_t caller = static_cast<cudaStream_t>(stream);
   cudaStream_t s = c->crit;
+  ula_ctx::GroupStep &st = c->steps[group];
   ULA_CUDA(c->enter(caller));
+  if (st.in_flight) {  // this group's previous step: its move committed, its gather done
+    ULA_CUDA(cudaStreamWaitEvent(s, st.commit_evt, 0));
+    ULA_CUDA(cudaStreamWaitEvent(s, st.hit_evt, 0));
+  }
+  if (st.upd_pending) {  // and its last alloc/free
+    ULA_CUDA(cudaStreamWaitEvent(s, st.upd_evt, 0));
+    st.upd_pending = false;
+  }
 
-  if (++c->epoch == 0) {  // dedup stamps wrap: clear them
-    ULA_CUDA(cudaMemsetAsync(c->tbl, 0, sizeof(unsigned long long) * cfg.max_logical, s));
-    c->epoch = 1;
+  if (++st.epoch == 0) {  // dedup stamps wrap: clear them
+    ULA_CUDA(cudaMemsetAsync(st.tbl, 0, sizeof(unsigned long long) * cfg.max_logical, s));
+    st.epoch = 1;
   }
   const uint32_t r = ++c->round[group];
   const uint32_t B = c->geo.B, cur = r % B;
@@ -602,7 +660,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.E = (uint32_t)E;
   p.QK = q * k;
   p.n_req = n_req;
-  p.epoch = c->epoch;
+  p.epoch = st.epoch;
   p.round = r;
   p.cur = cur;
   p.out_cap = out_cap_rows;
@@ -610,12 +668,12 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   p.inject = stall ? 0 : c->inject;
   p.entry_row = d_entry_row;
   p.req_off = d_req_off;
-  p.tbl = c->tbl;
-  p.addr_row = c->addr_row;
-  p.blk = c->blk;
-  p.miss_list = c->miss_list;
-  p.miss_hs = c->miss_hs;
-  p.miss_row = c->miss_row;
+  p.tbl = st.tbl;
+  p.addr_row = st.addr_row;
+  p.blk = st.blk;
+  p.miss_list = st.miss_list;
+  p.miss_hs = st.miss_hs;
+  p.miss_row = st.miss_row;
   p.src = c->tp_src[group];
   p.status = c->status;
   c->inject = 0;
@@ -637,33 +695,33 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   gp.signal = c->geo.signal;
   gp.round = r;
   gp.status = c->status;
-  cudaStream_t gs = c->side;
   // (6) the hit rows of every layer, one launch (a slot's layers are one contiguous
-  // read), released once the compaction has recorded each hit's slot (a hit's slot
-  // does not change in its round).  It runs on its own stream while the hits are
-  // marked and the victims chosen, emitted and staged, and the move starts once it is
-  // done: beside the move, each slows the other (the move's host-link traffic holds up
-  // the gather's HBM traffic on every SM it shares).  Beside the move instead with
-  // ULA_FLAG_GATHER_BESIDE_MOVE or the per-layer signal.
-  auto release_gather = [&]() -> cudaError_t {
-    cudaError_t e = cudaEventRecord(c->marked_evt, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(gs, c->marked_evt, 0);
-    if (e != cudaSuccess) return e;
+  // read); a hit's slot does not change in its round.  By default it is the first of
+  // the step's copy kernels, so it never runs beside a move: the move's host-link
+  // traffic holds up HBM traffic on every SM it shares (each slows the other).  With
+  // ULA_FLAG_GATHER_BESIDE_MOVE (or the per-layer signal) it runs on the low-priority
+  // side stream as soon as the compaction has recorded the hits' slots, beside the
+  // marking, the victim selection and the move.
+  auto launch_hit_gather = [&](cudaStream_t gs) -> cudaError_t {
     gp.span = c->take_span(ULA_PHASE_GATHER, group);
-    e = c->phase(ULA_PHASE_GATHER, gs, gather_launches(c->geo.W, gd.layers),
-                 [&] { return launch_gather(gp, gather_step_blocks(E), gs); });
-    return e != cudaSuccess ? e : cudaEventRecord(c->hit_evt, gs);
+    return c->phase(ULA_PHASE_GATHER, gs, gather_launches(c->geo.W, gd.layers),
+                    [&] { return launch_gather(gp, gather_step_blocks(E), gs); });
   };
   // (1)(2) dedup + translate + capacity check
   ULA_CUDA(c->phase(ULA_PHASE_DEDUP, s, E ? 2 : 1, [&] { return launch_dedup(p, s); }));
   // (3a) rotation + compaction of unique rows and misses
   ULA_CUDA(c->phase(ULA_PHASE_ROTATE, s, 1, [&] { return launch_rotate_emit(p, s); }));
-  if (gather && !c->geo.exact && !ULA_GATHER_AFTER_EMIT) ULA_CUDA(release_gather());
+  if (gather && c->beside) {
+    ULA_CUDA(cudaEventRecord(st.rot_evt, s));
+    ULA_CUDA(cudaStreamWaitEvent(c->side, st.rot_evt, 0));
+    ULA_CUDA(launch_hit_gather(c->side));
+    ULA_CUDA(cudaEventRecord(st.hit_evt, c->side));
+  }
   // (3b) hits into the current bucket, entry rows; the victim walk
   ULA_CUDA(c->phase(ULA_PHASE_MARK, s, 1, [&] { return launch_mark_select(p, s); }));
   if (c->geo.exact) {
-    // (4) exact LRU: the timestamp scan, before the hit gather is released (its
-    // grid-wide phases run several times slower beside it)
+    // (4) exact LRU: the timestamp scan (a cooperative launch; its blocks fit on the
+    // SMs beside the move's)
     LruParams lp{};
     lp.geo = c->geo;
     lp.grp = gd;
@@ -673,7 +731,6 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
     lp.status = c->status;
     ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
                       [&] { return launch_lru_select(lp, c->lru_blocks, s); }));
-    if (gather && !ULA_GATHER_AFTER_EMIT) ULA_CUDA(release_gather());
   }
   // (4) victims' and write-back slots' indices; (5) the fill order
   const bool staged = !c->geo.signal;  // the slot-major move (not the layer-major one)
@@ -683,56 +740,66 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   ep.group0 = group;
   ep.order = p.order;
   ep.quota = 0xffffffffu;
-  ep.miss_hs = c->miss_hs;
-  ep.fill_order = c->geo.signal ? nullptr : c->fill_order;
+  ep.miss_hs = st.miss_hs;
+  ep.fill_order = c->geo.signal ? nullptr : st.fill_order;
   ep.span = meta_span;
   ep.status = c->status;
   ULA_CUDA(c->phase(ULA_PHASE_SELECT, s, 1,
                     [&] { return launch_select_emit(ep, 1, c->emit_blocks, s); }));
-  if (gather && ULA_GATHER_AFTER_EMIT) ULA_CUDA(release_gather());
+  // the copies, on the copy stream after this step's metadata and after every earlier
+  // call's copies
+  cudaStream_t cs = c->copy;
+  ULA_CUDA(cudaEventRecord(st.meta_evt, s));
+  ULA_CUDA(cudaStreamWaitEvent(cs, st.meta_evt, 0));
+  if (gather && !c->beside) {
+    ULA_CUDA(launch_hit_gather(cs));
+    ULA_CUDA(cudaEventRecord(st.hit_evt, cs));
+  }
   // (5) write-back, fill (writing the missed rows' outputs), then map commit
   MoveParams mp{};
   mp.geo = c->geo;
   mp.grp = gd;
   mp.sel = d_sel;
   mp.entry_row = d_entry_row;
-  mp.addr_row = c->addr_row;
+  mp.addr_row = st.addr_row;
   mp.E = (uint32_t)E;
-  mp.miss_list = c->miss_list;
-  mp.miss_hs = c->miss_hs;
-  mp.miss_row = c->miss_row;
+  mp.miss_list = st.miss_list;
+  mp.miss_hs = st.miss_hs;
+  mp.miss_row = st.miss_row;
   mp.out = gather ? static_cast<uint8_t *>(d_out) : nullptr;
   mp.out_cap = out_cap_rows;
   mp.round = r;
   mp.cur = cur;
   mp.src = c->tp_src[group];
-  mp.fill_order = c->fill_order;
+  mp.fill_order = st.fill_order;
   mp.stage = c->stage;
-  mp.vdone = c->vdone;
+  mp.vdone = st.vdone;
   mp.status = c->status;
   if (staged) {  // entry rows; the rows of the victims that hold data, to the staging area
     mp.span = c->take_span(ULA_PHASE_STAGE, group);
-    ULA_CUDA(c->phase(ULA_PHASE_STAGE, s, 1, [&] { return launch_stage(mp, c->stage_blocks, s); }));
+    ULA_CUDA(c->phase(ULA_PHASE_STAGE, cs, 1, [&] { return launch_stage(mp, c->stage_blocks, cs); }));
   }
-  const bool after_gather = gather && !c->beside;
-  if (after_gather) ULA_CUDA(cudaStreamWaitEvent(s, c->hit_evt, 0));
   mp.span = c->take_span(ULA_PHASE_MOVE, group);
-  ULA_CUDA(c->phase(ULA_PHASE_MOVE, s, c->geo.signal ? 2 : 1,
-                    [&] { return launch_move(mp, c->move_blocks, !after_gather, s); }));
-  // signal: the commit event; every layer is ready once its hit rows are gathered too
-  ULA_CUDA(cudaEventRecord(c->commit_evt, s));
-  if (gather && c->beside) ULA_CUDA(cudaStreamWaitEvent(s, c->hit_evt, 0));
+  ULA_CUDA(c->phase(ULA_PHASE_MOVE, cs, c->geo.signal ? 2 : 1,
+                    [&] { return launch_move(mp, c->move_blocks, staged, cs); }));
+  // signal: the commit (and the hit gather) complete every layer of the output
+  ULA_CUDA(cudaEventRecord(st.commit_evt, cs));
+  if (!gather) ULA_CUDA(cudaEventRecord(st.hit_evt, cs));  // nothing to gather
+  st.in_flight = true;
+  ULA_CUDA(cudaStreamWaitEvent(caller, st.commit_evt, 0));
+  ULA_CUDA(cudaStreamWaitEvent(caller, st.hit_evt, 0));
   for (uint32_t j = 0; j < gd.layers; ++j)
     if (layer_ready && layer_ready[j])
-      ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), s));
-  ULA_CUDA(c->leave(caller));
+      ULA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(layer_ready[j]), caller));
   return ULA_OK;
 }
 
 static int sync_impl(ula_ctx *c) {
   ULA_CUDA(c->ensure_device());
   ULA_CUDA(cudaStreamSynchronize(c->crit));
+  ULA_CUDA(cudaStreamSynchronize(c->copy));
   ULA_CUDA(cudaStreamSynchronize(c->side));
+  for (auto &st : c->steps) ULA_CUDA(cudaStreamSynchronize(st.upd));
   ULA_CUDA(cudaStreamSynchronize(c->home));
   return ULA_OK;
 }

@@ -260,6 +260,7 @@ struct AllocParams {
   unsigned long long group_off[ULA_MAX_GROUPS];  // byte offset of group g's rows
   uint32_t row_stride;      // address i of the range is row i * row_stride (TP partitions)
   uint32_t round[ULA_MAX_GROUPS];
+  uint32_t group0;          // first group (blockIdx.y adds to it)
   uint32_t base, n;
   int *status;
 };
@@ -268,6 +269,7 @@ struct FreeParams {
   Geometry geo;
   const GroupDev *groups;
   uint32_t round[ULA_MAX_GROUPS];
+  uint32_t group0;          // first group (blockIdx.y adds to it)
   uint32_t base, n;
   int *status;
 };

@@ -1948,7 +1948,7 @@ __global__ void __launch_bounds__(kScanThreads) k_alloc_select(EmitParams p) {
 // lowest ones, joining the current bucket), the rest to the selected host slots.
 __global__ void __launch_bounds__(256) k_alloc_place(AllocParams p) {
   if (*(volatile int *)p.status) return;
-  const uint32_t gi = blockIdx.y;
+  const uint32_t gi = p.group0 + blockIdx.y;
   const GroupDev g = p.groups[gi];
   const Geometry &geo = p.geo;
   const uint32_t F = g.cnt->F;
@@ -1988,7 +1988,7 @@ __global__ void __launch_bounds__(256) k_alloc_place(AllocParams p) {
 // Free: every address's slot is released (GPU: leaves its class, joins free).
 __global__ void k_free(FreeParams p) {
   if (*(volatile int *)p.status) return;
-  const uint32_t gi = blockIdx.y;
+  const uint32_t gi = p.group0 + blockIdx.y;
   const GroupDev g = p.groups[gi];
   const Geometry &geo = p.geo;
   const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -2164,7 +2164,9 @@ cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t row_b
 int move_threads() { return kMoveThreads; }
 
 cudaError_t launch_stage(const MoveParams &p, int blocks, cudaStream_t s) {
-  return launch_dependent(k_stage, dim3(blocks > 0 ? blocks : 1), dim3(256), s, p);
+  // (an ordinary launch: the stream waits on the step's metadata event before it)
+  k_stage<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_move(const MoveParams &p, int blocks, bool dependent, cudaStream_t s) {

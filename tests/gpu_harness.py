@@ -15,7 +15,11 @@ STAGE_ADDRS = 16384  # addresses per staged alloc chunk
 
 
 class GpuReplay:
-    def __init__(self, w, out_cap: int | None = None, stage_addrs: int = STAGE_ADDRS):
+    """group_streams: each group's call on a caller stream of its own (as the benchmark
+    issues them: later groups' steps run ahead of earlier groups' copies)."""
+
+    def __init__(self, w, out_cap: int | None = None, stage_addrs: int = STAGE_ADDRS,
+                 group_streams: bool = False):
         self.w = w
         G, L = w.n_groups, w.layers_per_group
         self.cache = UlaCache(row_bytes=w.row_bytes, layers_per_group=[L] * G,
@@ -36,6 +40,7 @@ class GpuReplay:
                                  pin_memory=True)
         self.trace = synth.Trace(w)
         self.live = set()
+        self.gstreams = [torch.cuda.Stream(dev) for _ in range(G)] if group_streams else None
         for base, n in initial_allocs(w, self.trace):
             self.alloc(base, n)
 
@@ -65,9 +70,17 @@ class GpuReplay:
 
     def run_groups(self, sel: np.ndarray):
         self.sel_d.copy_(torch.from_numpy(np.ascontiguousarray(sel).view(np.int32)))
+        main = self.cache.stream
         for g in range(self.w.n_groups):
+            s = None
+            if self.gstreams:
+                s = self.gstreams[g]
+                s.wait_stream(main)
             self.cache.step_group(g, self.sel_d[g], self.outs[g], self.entry_row[g],
-                                  self.req_off[g])
+                                  self.req_off[g], stream=s)
+        if self.gstreams:
+            for s in self.gstreams:
+                main.wait_stream(s)
         return self.cache.sync()
 
     def step(self):

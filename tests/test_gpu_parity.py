@@ -14,7 +14,7 @@ import torch
 
 import synth
 from synth.configs import WORKLOADS, small
-from tests.harness import OracleRun, check_invariants, check_step_outputs
+from tests.harness import OracleRun, apply_events, check_invariants, check_step_outputs
 
 pytestmark = pytest.mark.gpu
 
@@ -23,8 +23,9 @@ if torch.cuda.is_available():
                                    expand_id_rows, gpu_state_in_oracle_terms)
 
 
-def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2048, seed=0):
-    gpu = GpuReplay(w)
+def run_parity(w, steps, mode="bytes", state_every=1, out_every=1, sample_rows=2048, seed=0,
+               group_streams=False):
+    gpu = GpuReplay(w, group_streams=group_streams)
     orc = OracleRun(w, mode)
     rng = np.random.default_rng(seed)
     try:
@@ -98,10 +99,80 @@ def test_parity_batch8_32k_full():
 @pytest.mark.parametrize("name,steps", [("longdoc", 12), ("low_evict", 12), ("low_overlap", 13),
                                         ("low_overlap_256", 6)])
 def test_parity_full_size_sampled(name, steps):
-    """Full-size workloads: state compared every step, gathered bytes sampled."""
+    """Full-size workloads in the benchmark's launch configuration (each group's call on
+    its own caller stream): state compared every step, gathered bytes sampled."""
     w = WORKLOADS[name]
-    stats = run_parity(w, steps, mode="id", state_every=1, out_every=10**9, sample_rows=4096)
+    stats = run_parity(w, steps, mode="id", state_every=1, out_every=10**9, sample_rows=4096,
+                       group_streams=True)
     assert stats["steps"] == steps * w.n_groups
+
+
+@pytest.mark.parametrize("name,beside,exact", [("longdoc", False, False), ("low_overlap", False, False),
+                                               ("low_overlap_256", True, False),
+                                               ("low_evict", False, True), ("longdoc", True, True)])
+def test_parity_small_group_streams(name, beside, exact):
+    """Each group's call on its own caller stream: a group's metadata runs while earlier
+    groups' copies (and, beside the move, gathers) are still running; same results."""
+    w = small(name).replace(gather_beside=beside, exact_lru=exact)
+    stats = run_parity(w, w.steps, group_streams=True)
+    assert stats["misses"] > 0
+
+
+@pytest.mark.parametrize("name,beside,exact", [("longdoc", False, False), ("low_overlap", False, False),
+                                               ("longdoc", True, False), ("low_evict", False, True)])
+def test_pipelined_steps_match_oracle(name, beside, exact):
+    """Steps issued ahead with no synchronisation between them, as the benchmark issues
+    them: each group's calls on its own caller stream, each step's alloc/free on the main
+    stream (rows in buffers of their own), per-step outputs.  After one final sync, every
+    step's outputs and the final state equal the oracle's."""
+    from oracle.replay import alloc_rows
+    w = small(name).replace(gather_beside=beside, exact_lru=exact)
+    n = 12
+    gpu = GpuReplay(w, group_streams=True)
+    orc = OracleRun(w, "bytes")
+    G, E, R = w.n_groups, w.entries_per_step, w.n_live
+    dev = gpu.cache.device
+    try:
+        sels, evs = [], []
+        for _ in range(n):
+            sel, ev = gpu.trace.step()
+            sels.append(sel)
+            evs.append(ev)
+        sel_d = torch.from_numpy(np.stack(sels).view(np.int32)).to(dev)
+        torch.cuda.synchronize()
+        outs = [[gpu.cache.out_buffer(g, E) for g in range(G)] for _ in range(n)]
+        ers = [[torch.empty(E, dtype=torch.int32, device=dev) for _ in range(G)] for _ in range(n)]
+        ros = [[torch.empty(R + 1, dtype=torch.int32, device=dev) for _ in range(G)] for _ in range(n)]
+        keep = []
+
+        def dev_alloc(base, m):
+            rows = torch.from_numpy(alloc_rows(w, base, m, "bytes")).pin_memory()
+            keep.append(rows)
+            return gpu.cache.alloc(m, rows)
+
+        for t in range(n):
+            for g in range(G):
+                gpu.cache.step_group(g, sel_d[t, g], outs[t][g], ers[t][g], ros[t][g],
+                                     stream=gpu.gstreams[g])
+            apply_events(dev_alloc, gpu.cache.free, evs[t])
+        gpu.cache.sync()
+        torch.cuda.synchronize()
+        for t in range(n):
+            for g in range(G):
+                ro = orc.o.step_group(g, sels[t][g])
+                where = f"step {t} group {g}"
+                assert np.array_equal(ros[t][g].cpu().numpy(), ro["req_off"]), where
+                assert np.array_equal(ers[t][g].cpu().numpy(), ro["entry_row"]), where
+                U = int(ro["req_off"][-1])
+                assert np.array_equal(outs[t][g][:, :U].cpu().numpy(), ro["out"][:, :U]), where
+            apply_events(orc.alloc, orc.free, evs[t])
+        for g in range(G):
+            st = gpu.cache.export(g)
+            check_gpu_internal(st, w)
+            compare_states(gpu_state_in_oracle_terms(st, w), orc.o.export(g), f"final g{g}",
+                           orc.o.stamps(g))
+    finally:
+        gpu.close()
 
 
 @pytest.mark.parametrize("name", ["longdoc", "low_overlap_256"])
@@ -114,7 +185,8 @@ def test_parity_small_gather_beside_move(name):
 
 def test_parity_full_size_sampled_gather_beside_move():
     w = WORKLOADS["longdoc"].replace(gather_beside=True)
-    stats = run_parity(w, 6, mode="id", state_every=1, out_every=10**9, sample_rows=4096)
+    stats = run_parity(w, 6, mode="id", state_every=1, out_every=10**9, sample_rows=4096,
+                       group_streams=True)
     assert stats["steps"] == 6 * w.n_groups
 
 
