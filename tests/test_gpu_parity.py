@@ -96,17 +96,6 @@ def test_parity_batch8_32k_full():
     assert stats["steps"] == w.steps * w.n_groups and stats["writebacks"] > 0
 
 
-@pytest.mark.parametrize("name,steps", [("longdoc", 12), ("low_evict", 12), ("low_overlap", 13),
-                                        ("low_overlap_256", 6)])
-def test_parity_full_size_sampled(name, steps):
-    """Full-size workloads in the benchmark's launch configuration (each group's call on
-    its own caller stream): state compared every step, gathered bytes sampled."""
-    w = WORKLOADS[name]
-    stats = run_parity(w, steps, mode="id", state_every=1, out_every=10**9, sample_rows=4096,
-                       group_streams=True)
-    assert stats["steps"] == steps * w.n_groups
-
-
 @pytest.mark.parametrize("name,beside,exact", [("longdoc", False, False), ("low_overlap", False, False),
                                                ("low_overlap_256", True, False),
                                                ("low_evict", False, True), ("longdoc", True, True)])
