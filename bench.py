@@ -48,6 +48,9 @@ def parse_args(argv=None):
                     help="replacement policy: PB-LRU, or exact LRU (timestamp scan)")
     ap.add_argument("--repeats", type=int, default=3,
                     help="timed regions of --steps steps each; value = their median")
+    ap.add_argument("--hit-rates", action="store_true",
+                    help="CPU only: the oracle over the workload's whole trace, PB-LRU against "
+                         "exact LRU hit rates (one JSON line)")
     ap.add_argument("--one-stream", action="store_true",
                     help="issue every group's call on the one caller stream (each group's "
                          "step then waits for the previous group's); by default each group "
@@ -55,7 +58,7 @@ def parse_args(argv=None):
     ap.add_argument("--gather-beside", action="store_true",
                     help="run the hit gather beside the move (ULA_FLAG_GATHER_BESIDE_MOVE)")
     ap.add_argument("--profile-steps", type=int, default=60)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layer-signal", action="store_true",
@@ -189,14 +192,26 @@ def host_link_peaks(torch, nbytes=1 << 30):
         with torch.cuda.stream(s1):
             h.copy_(d, non_blocking=True)
 
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
     def both():
+        ev[0].record(torch.cuda.current_stream())
+        s1.wait_event(ev[0])
+        s2.wait_event(ev[0])
         with torch.cuda.stream(s1):
             d.copy_(h, non_blocking=True)
+            ev[1].record(s1)
         with torch.cuda.stream(s2):
             h2.copy_(d2, non_blocking=True)
+            ev[2].record(s2)
 
+    h2d_beside = 0.0
+    for _ in range(4):  # the H2D stream's own time while a D2H copy runs beside it
+        both()
+        torch.cuda.synchronize()
+        h2d_beside = max(h2d_beside, nbytes / (ev[0].elapsed_time(ev[1]) / 1e3) / 1e9)
     out = {"h2d_gbs": nbytes / best(h2d) / 1e9, "d2h_gbs": nbytes / best(d2h) / 1e9,
-           "bidir_gbs": 2 * nbytes / best(both) / 1e9}
+           "bidir_gbs": 2 * nbytes / best(both) / 1e9, "h2d_beside_d2h_gbs": h2d_beside}
     del h, h2, d, d2
     return out
 
@@ -255,19 +270,39 @@ def stage_initial(cache, w, synth, torch):
 
 
 def gen_steps(trace, w, n, synth, np):
+    """n steps of the trace: (selection, events, (rows of a joining request or None, rows of
+    the appended tokens or None)), rows per group [G][n][L][W]."""
+    G, L, W = w.n_groups, w.layers_per_group, w.row_bytes
+
+    def rows_for(base, m):
+        rows = np.empty((G, m, L, W), dtype=np.uint8)
+        for g in range(G):
+            synth.content_range(w.seed, g, L, base, m, W, out=rows[g])
+        return rows
+
     steps = []
     for _ in range(n):
         sel, ev = trace.step()
-        assert not ev["free_n"] and not ev["join_n"], "benchmark workload has no turnover"
-        rows = None
-        if ev["append_n"]:
-            G, L, W = w.n_groups, w.layers_per_group, w.row_bytes
-            rows = np.empty((G, ev["append_n"], L, W), dtype=np.uint8)
-            for g in range(G):
-                synth.content_range(w.seed, g, L, ev["append_base"], ev["append_n"], W,
-                                    out=rows[g])
-        steps.append((sel, ev, rows))
+        join = rows_for(ev["join_base"], ev["join_n"]) if ev["join_n"] else None
+        app = rows_for(ev["append_base"], ev["append_n"]) if ev["append_n"] else None
+        steps.append((sel, ev, (join, app)))
     return steps
+
+
+def rows_to(rows, to):
+    """A step's (join, append) rows as flat tensors made by `to` (device or pinned)."""
+    return tuple(to(r) if r is not None else None for r in rows)
+
+
+def apply_step_events(lib_cache, ev, rows_t):
+    """The step's finishing request, joining request and appended tokens, in the order
+    the trace assigned logical ranges."""
+    if ev["free_n"]:
+        lib_cache.free(ev["free_base"], ev["free_n"])
+    if ev["join_n"]:
+        assert lib_cache.alloc(ev["join_n"], rows_t[0]) == ev["join_base"]
+    if ev["append_n"]:
+        assert lib_cache.alloc(ev["append_n"], rows_t[1]) == ev["append_base"]
 
 
 def run_tp(args, local):
@@ -308,8 +343,7 @@ def run_tp(args, local):
     n = args.warmup + args.steps
     steps = gen_steps(trace, w, n, synth, np)
     sel_dev = torch.from_numpy(np.stack([x[0] for x in steps]).view(np.int32)).to(dev)
-    rows_dev = [torch.from_numpy(x[2].reshape(-1)).to(dev) if x[2] is not None else None
-                for x in steps]
+    rows_dev = [rows_to(x[2], lambda r: torch.from_numpy(r.reshape(-1)).to(dev)) for x in steps]
     lo = [[tp.out_buffer(g, E) for _ in range(P)] for g in range(G)]
     ro = [[tp.out_buffer(g, E) for _ in range(P)] for g in range(G)]
     mk = lambda k: [torch.empty(k, dtype=torch.int32, device=dev) for _ in range(P)]
@@ -318,9 +352,7 @@ def run_tp(args, local):
     def do_step(t):
         for g in range(G):
             tp.step_group(g, sel_dev[t][g], lo[g], ro[g], ler, lrq, rer, rrq)
-        ev = steps[t][1]
-        if ev["append_n"]:
-            assert tp.alloc(ev["append_n"], rows_dev[t]) == ev["append_base"]
+        apply_step_events(tp, steps[t][1], rows_dev[t])
 
     for t in range(args.warmup):
         do_step(t)
@@ -379,10 +411,10 @@ def run_gpu(args, rank, world, local):
                      bypass_overflow=w.bypass, exact_lru=w.exact_lru,
                      layer_signal=args.layer_signal, gather_beside_move=args.gather_beside)
     trace = stage_initial(cache, w, synth, torch)
-    K, reps = args.steps, max(1, args.repeats)
-    n_value, n_prof = K * reps, min(args.profile_steps, K)
-    n_lat = min(args.latency_steps, K)
-    n_e2e = 0 if args.no_e2e else K
+    NS, reps = args.steps, max(1, args.repeats)
+    n_value, n_prof = NS * reps, min(args.profile_steps, NS)
+    n_lat = min(args.latency_steps, NS)
+    n_e2e = 0 if args.no_e2e else NS
     steps = gen_steps(trace, w, args.warmup + n_value + n_prof + n_lat + n_e2e, synth, np)
     outs = [cache.out_buffer(g, E) for g in range(G)]
     entry_row = [torch.empty(E, dtype=torch.int32, device=dev) for _ in range(G)]
@@ -390,7 +422,7 @@ def run_gpu(args, rank, world, local):
     # device-resident inputs for the value, profiled and latency passes
     n_dev = args.warmup + n_value + n_prof + n_lat
     sel_dev = torch.from_numpy(np.stack([s[0] for s in steps[:n_dev]]).view(np.int32)).to(dev)
-    rows_dev = [torch.from_numpy(s[2].reshape(-1)).to(dev) if s[2] is not None else None
+    rows_dev = [rows_to(s[2], lambda r: torch.from_numpy(r.reshape(-1)).to(dev))
                 for s in steps[:n_dev]]
     torch.cuda.synchronize()
     setup_s = time.perf_counter() - t_setup
@@ -426,9 +458,7 @@ def run_gpu(args, rank, world, local):
 
     def do_step(sel_t, ev, rows_t):
         issue_groups(sel_t)
-        if ev["append_n"]:
-            got = cache.alloc(ev["append_n"], rows_t)
-            assert got == ev["append_base"]
+        apply_step_events(cache, ev, rows_t)
 
     for t in range(args.warmup):
         do_step(sel_dev[t], steps[t][1], rows_dev[t])
@@ -436,6 +466,8 @@ def run_gpu(args, rank, world, local):
     if args.traffic_case:
         st = cache.export(0)
         out = cache.out_buffer(0, max(1, st["U"]))
+        torch.empty(512 << 20, dtype=torch.uint8, device=dev).zero_()  # flush L2 (129 MB)
+        torch.cuda.synchronize()
         # the step's gather launch: every layer of group 0's hit rows in one launch
         ula.ula_debug_regather(cache.ctx, 0, 0, out.data_ptr(), out.shape[1], stream.cuda_stream,
                                n_layers=L)
@@ -452,7 +484,7 @@ def run_gpu(args, rank, world, local):
 
     clocks = ClockSampler(local)
     clocks.start()
-    # ---- value: inputs resident in HBM; `reps` timed regions of K steps each, with the
+    # ---- value: inputs resident in HBM; `reps` timed regions of NS steps each, with the
     # copy kernels' device spans recorded in the same pass
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     probe = LinkProbe(torch)
@@ -465,12 +497,14 @@ def run_gpu(args, rank, world, local):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed")
         e0.record(stream)
-        for _ in range(K):
+        for _ in range(NS):
             do_step(sel_dev[t], steps[t][1], rows_dev[t])
             t += 1
         join_groups()
         e1.record(stream)
+        torch.cuda.nvtx.range_pop()
         sb = cache.sync()
         torch.cuda.synchronize()
         if world > 1:
@@ -480,7 +514,7 @@ def run_gpu(args, rank, world, local):
         ula.ula_profile_spans(cache.ctx, False)
         launches += sum(p["kernels"] for p in ula.ula_profile_read(cache.ctx, reset=True).values())
         d = {k: sb[k] - sa[k] for k in sb}
-        repeats.append({"ms": ms, "stats": d, "spans": span_summary(spans, d, L, W, G * K),
+        repeats.append({"ms": ms, "stats": d, "spans": span_summary(spans, d, L, W, G * NS),
                         "ce_bidir_gbs": probe.bidir_gbs()})
     launches //= reps
     order = sorted(range(reps), key=lambda i: repeats[i]["ms"])
@@ -519,9 +553,7 @@ def run_gpu(args, rank, world, local):
                 ns = ula.ula_debug_layer_times(cache.ctx, g, L)
                 for j in range(L):
                     flag_ms[j].append((int(ns[j]) - int(ns[L])) / 1e6)
-        if ev["append_n"]:
-            got = cache.alloc(ev["append_n"], rows_t)
-            assert got == ev["append_base"]
+        apply_step_events(cache, ev, rows_t)
     cache.sync()
     layer_ready = {"layer_ready_event_ms": [round(float(np.median(x)), 4) for x in ev_ms],
                    "how": "median over groups and steps; one group call at a time, from an "
@@ -536,7 +568,7 @@ def run_gpu(args, rank, world, local):
     if n_e2e:
         sel_host = torch.from_numpy(np.stack([s[0] for s in steps[n_dev:]]).view(np.int32))
         sel_host = sel_host.pin_memory()
-        rows_host = [torch.from_numpy(s[2].reshape(-1)).pin_memory() if s[2] is not None else None
+        rows_host = [rows_to(s[2], lambda r: torch.from_numpy(r.reshape(-1)).pin_memory())
                      for s in steps[n_dev:]]
         sel_buf = [torch.empty((G, R, Q, K), dtype=torch.int32, device=dev) for _ in range(2)]
         res_host = torch.empty((n_e2e, G, R + 1), dtype=torch.int32, pin_memory=True)
@@ -550,9 +582,8 @@ def run_gpu(args, rank, world, local):
             h2d_bytes += buf.numel() * 4
             ev = steps[n_dev + i][1]
             issue_groups(buf, wait=True)
-            if ev["append_n"]:
-                cache.alloc(ev["append_n"], rows_host[i])  # read from pinned host memory
-                h2d_bytes += rows_host[i].numel()
+            apply_step_events(cache, ev, rows_host[i])  # rows read from pinned host memory
+            h2d_bytes += sum(r.numel() for r in rows_host[i] if r is not None)
             join_groups()
             for g in range(G):
                 res_host[i, g].copy_(req_off[g], non_blocking=True)
@@ -581,12 +612,15 @@ def run_gpu(args, rank, world, local):
     iso = isolated_gather(cache, ula, torch, dev, stream, W, L)
     roof = {"bound": "hbm", "kernel": "k_gather", "achieved": round(achieved, 1),
             "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
-            "traffic": traffic_per_launch(med["stats"]["hits"], ga["launches"], w.name),
+            "traffic": traffic_per_launch(med["stats"]["hits"], ga["launches"], args.workload),
+            "traffic_read_per_hit_row": (round(GATHER_TRAFFIC["read_bytes_per_hit"], 1)
+                                         if traffic_per_launch(1, 1, args.workload) else None),
+            "algorithmic_read_per_hit_row": L * W,
             "peak_source": f"{hbm_src} (hbm_gbs, STREAM-style copy)",
             "avg_launch_us": round(avg_launch_us, 2),
             "bytes_per_launch": round(g_bytes / max(1, ga["launches"])),
             "rows_per_launch": round(hit_rows / max(1, ga["launches"]), 1), "bytes_per_row": 2 * W,
-            "union_us_per_step": round(ga["union_us"] / K, 2),
+            "union_us_per_step": round(ga["union_us"] / NS, 2),
             "timing": ("in the timed region (median repeat): device globaltimer span of each "
                        "gather launch, first warp start to last warp end; achieved = hit-gather "
                        "bytes / summed spans (the launches do not overlap: union "
@@ -603,11 +637,16 @@ def run_gpu(args, rank, world, local):
             "total_gbs": round((h2d_b + d2h_b) / mv_s / 1e9, 1) if mv_s else 0,
             "peak_h2d_gbs": round(link["h2d_gbs"], 1), "peak_d2h_gbs": round(link["d2h_gbs"], 1),
             "peak_bidir_gbs": round(link["bidir_gbs"], 1),
+            "peak_h2d_beside_d2h_gbs": round(link["h2d_beside_d2h_gbs"], 1),
             "peak_source": "measured in this run: pinned cudaMemcpyAsync, 1 GiB",
             "timing": "device spans of the move launches in the median timed region",
-            "move_us_per_step": round(mv["sum_us"] / K, 2)}
+            "move_us_per_step": round(mv["sum_us"] / NS, 2)}
     if mv_s:
+        # fills against the H2D copy alone, and against H2D while a D2H copy runs beside
+        # it (the move's write-backs share the link with its fills); fills and write-backs
+        # together against both directions at once
         host["frac_fill"] = round(h2d_b / mv_s / 1e9 / link["h2d_gbs"], 4)
+        host["frac_fill_beside_d2h"] = round(h2d_b / mv_s / 1e9 / link["h2d_beside_d2h_gbs"], 4)
         host["frac_total"] = round((h2d_b + d2h_b) / mv_s / 1e9 / link["bidir_gbs"], 4)
     rep_lines = []
     for r in repeats:
@@ -617,7 +656,7 @@ def run_gpu(args, rank, world, local):
         gb = r["stats"]["hits"] * L * 2 * W
         mg = mb / (m["sum_us"] * 1e3) if m["sum_us"] else None
         rep_lines.append({"value": r["stats"]["rows_gathered"] / (r["ms"] / 1e3),
-                          "ms_per_step": round(r["ms"] / K, 4),
+                          "ms_per_step": round(r["ms"] / NS, 4),
                           "move_gbs": round(mg, 1) if mg else None,
                           "ce_bidir_gbs_after": round(r["ce_bidir_gbs"], 1),
                           "move_frac_of_ce_after": round(mg / r["ce_bidir_gbs"], 4) if mg else None,
@@ -629,7 +668,7 @@ def run_gpu(args, rank, world, local):
         "rows": agg["rows"], "value_ms": agg["value_ms"], "launches": launches,
         "roofline": roof, "host_link": host, "clocks": clk, "phases": phases, "e2e": e2e,
         "layer_ready": layer_ready, "repeats": rep_lines,
-        "spans_us_per_step": {k: round(v["sum_us"] / K, 2) for k, v in sp.items()},
+        "spans_us_per_step": {k: round(v["sum_us"] / NS, 2) for k, v in sp.items()},
         "setup_s": setup_s, "stats": med["stats"],
     }
     if e2e is not None:
@@ -706,8 +745,13 @@ def span_summary(spans, d, L, W, group_steps):
 # dram__bytes_write.sum of one launch), per hit row, with the case it was taken on and
 # the hash of the gather kernel's source (its launch-shape defaults and its body).
 # Reported only while that source is unchanged and for the workload it was taken on.
-GATHER_TRAFFIC = {"source_sha256": None, "workload": None, "hit_rows": None,
-                  "read_bytes_per_hit": None, "write_bytes_per_hit": None}
+GATHER_TRAFFIC = {"source_sha256": "302cd1d24fec69c10d815bf9eb73cd393ac5fec1cb26eacce79a8156caa384ed",
+                  "workload": "longdoc",  # the recipe; the case had 12 of its 32 requests
+                  "case": "long-document recipe with 12 requests: group 0's hit rows after 3 "
+                          "steps, re-gathered in the step's one all-layer launch, L2 flushed",
+                  "hit_rows": 24255,
+                  "read_bytes_per_hit": 64372224 / 24255,   # 2,654 B per 2,624-B slot read
+                  "write_bytes_per_hit": 9538560 / 24255}   # written rows mostly stay in L2
 
 
 def gather_source_sha256() -> str:
@@ -722,7 +766,8 @@ def gather_source_sha256() -> str:
 
 def traffic_per_launch(hits, launches, workload):
     """DRAM bytes (read + write) per gather launch in the step, from the ncu figures per
-    hit row; None when they were taken on another gather source or workload."""
+    hit row scaled by the hits (reads grow in proportion to the rows gathered); None when
+    they were taken on another gather source or another workload's recipe."""
     t = GATHER_TRAFFIC
     if (not launches or t["source_sha256"] is None or t["source_sha256"] != gather_source_sha256()
             or t["workload"] != workload):
@@ -732,68 +777,84 @@ def traffic_per_launch(hits, launches, workload):
 
 # ------------------------------------------------------------- CPU oracle arm
 
-def cpu_sample_workload(name, exact=False):
-    from synth.configs import WORKLOADS
-    w = WORKLOADS[name]
-    n = min(4, w.n_live)
-    kw = dict(n_live=n, name=w.name + "_cpu_sample", exact_lru=exact,
-              description=w.description + f" (first {n} requests)")
-    if w.n_total is not None:
-        kw["n_total"] = n
-        kw["turnover_period"] = 0
-    return w.replace(**kw)
-
-
-def run_oracle(name, warmup, steps=None, seconds=None, exact=False):
-    """The oracle as it stands, single-threaded, on a bounded sample of the workload
-    (exact: its exact-LRU mode)."""
-    import numpy as np
-
-    import synth
+def run_oracle(w, warmup, steps=None, seconds=None):
+    """The oracle as it stands, single-threaded and pinned to one host core, on the same
+    workload `w` (its exact-LRU mode for an exact-LRU workload), for `steps` steps or until `seconds`
+    of oracle time.  It runs in content-id mode (8-byte rows naming their address, group
+    and layer: exact, since a row's bytes are a function of those): the byte mode needs
+    about 40 GB and a quarter of an hour to set up the long-document pools, and moving
+    8 instead of 656 bytes per row only makes the oracle faster.  The clock covers the
+    oracle's group steps and its alloc/free of the step's events; the selections and the
+    rows of joining requests and appended tokens are generated before it starts."""
     from oracle import ExactLru
     from oracle.replay import OracleRun, alloc_rows, apply_events
 
-    w = cpu_sample_workload(name, exact)
-    run = OracleRun(w, "bytes")
-    lru = ExactLru(w.n_groups, w.gpu_slots, w.max_logical)
-    for b, n in [(int(b), int(c)) for b, c in zip(*run.trace.initial()[1::-1])]:
-        lru.alloc(n)
+    run = OracleRun(w, "id")
+    # the exact-LRU hit rate on the same trace: the companion (hit counts only), or, where
+    # the overflow bypass is on (the companion has none), the oracle's exact-LRU mode
+    lru = ExactLru(w.n_groups, w.gpu_slots, w.max_logical) if not w.bypass else None
+    exact_run = OracleRun(w.replace(exact_lru=True), "id") if w.bypass else None
+    exact_acc = [0, 0]  # unique, hits (timed steps)
+    if lru is not None:
+        for b, n in [(int(b), int(c)) for b, c in zip(*run.trace.initial()[1::-1])]:
+            lru.alloc(n)
     t_oracle = 0.0
     rows = hits = uniq = 0
     n_done = 0
     limit = steps if steps is not None else 10 ** 9
-    while n_done < warmup + limit:
-        if n_done == warmup:
-            lru.acc[:] = 0  # hit rates over the timed steps only
-        sel, ev = run.trace.step()
-        # the rows of joining requests and appended tokens are inputs: made before the clock
-        rows_of = {ev[f"{k}_base"]: alloc_rows(w, ev[f"{k}_base"], ev[f"{k}_n"], "bytes")
-                   for k in ("join", "append") if ev[f"{k}_n"]}
-        t0 = time.perf_counter()
-        res = [run.o.step_group(g, sel[g]) for g in range(w.n_groups)]
-        apply_events(lambda base, n: run.o.alloc(n, rows_of[base]), run.o.free, ev)
-        dt = time.perf_counter() - t0
-        for g in range(w.n_groups):
-            lru.step_group(g, sel[g])
-        if ev["append_n"]:
-            lru.alloc(ev["append_n"])
-        if n_done >= warmup:
-            t_oracle += dt
-            for r in res:
-                rows += r["counters"]["rows_gathered"]
-                hits += r["counters"]["hits"]
-                uniq += r["counters"]["uniq"]
-        n_done += 1
-        if seconds is not None and t_oracle >= seconds and n_done >= warmup + 4:
-            break
+    allowed = os.sched_getaffinity(0)
+    core = max(allowed)
+    os.sched_setaffinity(0, {core})  # this thread only, for the timed loop
+    try:
+        while n_done < warmup + limit:
+            if n_done == warmup and lru is not None:
+                lru.acc[:] = 0  # hit rates over the timed steps only
+            sel, ev = run.trace.step()
+            rows_of = {ev[f"{k}_base"]: alloc_rows(w, ev[f"{k}_base"], ev[f"{k}_n"], "id")
+                       for k in ("join", "append") if ev[f"{k}_n"]}
+            t0 = time.perf_counter()
+            res = [run.o.step_group(g, sel[g]) for g in range(w.n_groups)]
+            apply_events(lambda base, n: run.o.alloc(n, rows_of[base]), run.o.free, ev)
+            dt = time.perf_counter() - t0
+            if lru is not None:
+                for g in range(w.n_groups):
+                    lru.step_group(g, sel[g])
+                if ev["free_n"]:
+                    lru.free(ev["free_base"], ev["free_n"])
+                for k in ("join", "append"):
+                    if ev[f"{k}_n"]:
+                        lru.alloc(ev[f"{k}_n"])
+            else:
+                xr = [exact_run.o.step_group(g, sel[g]) for g in range(w.n_groups)]
+                apply_events(lambda base, n: exact_run.o.alloc(n, rows_of[base]),
+                             exact_run.o.free, ev)
+                if n_done >= warmup:
+                    exact_acc[0] += sum(r["counters"]["uniq"] for r in xr)
+                    exact_acc[1] += sum(r["counters"]["hits"] for r in xr)
+            if n_done >= warmup:
+                t_oracle += dt
+                for r in res:
+                    rows += r["counters"]["rows_gathered"]
+                    hits += r["counters"]["hits"]
+                    uniq += r["counters"]["uniq"]
+            n_done += 1
+            if seconds is not None and t_oracle >= seconds and n_done >= warmup + 4:
+                break
+    finally:
+        os.sched_setaffinity(0, allowed)
     timed_steps = n_done - warmup
     return {"value": rows / t_oracle if t_oracle else 0.0, "unit": "rows/s", "cores": 1,
-            "kind": "oracle", "steps": timed_steps, "seconds": round(t_oracle, 3),
-            "sample": (f"{w.description}: {w.n_live} requests, S={w.gpu_slots}, "
-                       f"H={w.host_slots}, {timed_steps} decode steps after {warmup} warm-up, "
-                       f"656-byte rows moved, single-threaded"),
-            "policy": "exact LRU" if exact else "PB-LRU",
-            "hit_rate": hits / max(1, uniq), "exact_lru_hit_rate": lru.hit_rate}
+            "pinned_core": core, "host_cores": os.cpu_count(), "kind": "oracle",
+            "steps": timed_steps, "seconds": round(t_oracle, 3),
+            "sample": (f"{w.description}: the whole workload ({w.n_live} requests, "
+                       f"S={w.gpu_slots}, H={w.host_slots}), {timed_steps} decode steps after "
+                       f"{warmup} warm-up, rows as 8-byte content ids, single-threaded, pinned "
+                       f"to host core {core} of {os.cpu_count()}"),
+            "rows": "content ids (8 B per row)",
+            "policy": "exact LRU" if w.exact_lru else "PB-LRU",
+            "hit_rate": hits / max(1, uniq),
+            "exact_lru_hit_rate": (lru.hit_rate if lru is not None
+                                   else exact_acc[1] / max(1, exact_acc[0]))}
 
 
 # -------------------------------------------------------------------- main
@@ -826,10 +887,17 @@ def main(argv=None):
                     f"{w.gpu_slots * w.n_groups * w.layers_per_group * w.row_bytes / 1e9:.1f} GB, "
                     "rows gathered at random slots")
 
+    if args.hit_rates:  # the policy comparison over the whole trace, on the host
+        cb = run_oracle(w, 0, steps=w.steps)
+        print(json.dumps({"workload": w.name, "steps": cb["steps"], "pblru_hit_rate": cb["hit_rate"],
+                          "exact_lru_hit_rate": cb["exact_lru_hit_rate"],
+                          "difference_pp": round(100 * (cb["exact_lru_hit_rate"] - cb["hit_rate"]), 4),
+                          "oracle_rows_per_s": cb["value"], "config": config}), flush=True)
+        return 0
     if args.impl == "reference":
         if rank != 0:
             return 0
-        cb = run_oracle(args.workload, args.warmup, steps=args.steps, exact=w.exact_lru)
+        cb = run_oracle(w, args.warmup, steps=args.steps)
         line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "rows/s",
                 "n_gpus": args.gpus, "steps": cb["steps"], "warmup": args.warmup,
                 "ms_per_step": round(cb["seconds"] / max(1, cb["steps"]) * 1e3, 3),
@@ -877,8 +945,7 @@ def main(argv=None):
         if r["e2e"] is not None:
             line["e2e"] = r["e2e"]
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = run_oracle(args.workload, 2, seconds=args.cpu_seconds,
-                                              exact=w.exact_lru)
+            line["cpu_baseline"] = run_oracle(w, 2, seconds=args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -386,7 +386,9 @@ int ula_profile_spans_read(ula_ctx *ctx, ula_span *out, uint32_t cap, uint32_t *
  * n above ULA_NOALLOC_MAX_ENTRIES returns ULA_ERR_CAPACITY; NULL buffers return
  * ULA_ERR_INVALID_ARG (nothing is launched in either case).  The first call on a
  * device looks up the scratch array's device address (with that device current);
- * make that first call before any stream capture.  Every call on a device uses the
+ * make that first call before any stream capture.  The address is kept for the life
+ * of the process: after a cudaDeviceReset the library's device code may be loaded
+ * elsewhere, so the entry point must not be called again in that process.  Every call on a device uses the
  * same scratch and clears what it needs first, so calls that overlap on the GPU
  * (on different streams, or from different host threads) race and must not be
  * issued; calls on one stream are ordered and safe.

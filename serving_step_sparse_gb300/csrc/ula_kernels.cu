@@ -641,9 +641,8 @@ __global__ void __launch_bounds__(kEntryThreads) k_mark_select(StepParams p) {
 // the j-th lowest free host slot, so victim order is host-address order already.
 constexpr int kOrderThreads = 256;
 
-__device__ void fill_order_block(const EmitParams &p, const GroupDev &g) {
-  __shared__ uint32_t hist[kFillBuckets];
-  const uint32_t M = __ldcg(&g.cnt->M);
+// One range [lo, hi) of miss indices, sorted into fill_order[lo, hi).
+__device__ void fill_order_range(const EmitParams &p, uint32_t lo, uint32_t hi, uint32_t *hist) {
   const uint32_t shift = p.geo.fill_shift;
   const uint32_t lane = lane_id();
   for (uint32_t b = threadIdx.x; b < kFillBuckets; b += kOrderThreads) hist[b] = 0;
@@ -652,7 +651,7 @@ __device__ void fill_order_block(const EmitParams &p, const GroupDev &g) {
   // their positions with one atomic
   auto claim = [&](uint32_t i0) -> uint32_t {  // position of miss i0 + threadIdx.x, or kNone
     const uint32_t i = i0 + threadIdx.x;
-    const bool act = i < M;
+    const bool act = i < hi;
     const uint32_t b = act ? min(__ldcg(&p.miss_hs[i]) >> shift, kFillBuckets - 1) : kNone;
     const uint32_t peers = __match_any_sync(0xffffffffu, b);
     const uint32_t leader = __ffs(peers) - 1;
@@ -661,7 +660,7 @@ __device__ void fill_order_block(const EmitParams &p, const GroupDev &g) {
     base = __shfl_sync(0xffffffffu, base, leader);
     return act ? base + __popc(peers & ((1u << lane) - 1u)) : kNone;
   };
-  for (uint32_t i0 = 0; i0 < M; i0 += kOrderThreads) claim(i0);  // bucket sizes
+  for (uint32_t i0 = lo; i0 < hi; i0 += kOrderThreads) claim(i0);  // bucket sizes
   __syncthreads();
   constexpr uint32_t kPer = kFillBuckets / kOrderThreads;
   uint32_t v[kPer], mine = 0;
@@ -671,17 +670,27 @@ __device__ void fill_order_block(const EmitParams &p, const GroupDev &g) {
     mine += v[j];
   }
   uint32_t total;
-  uint32_t run = block_incl_scan<kOrderThreads>(mine, &total) - mine;
+  uint32_t run = lo + block_incl_scan<kOrderThreads>(mine, &total) - mine;
 #pragma unroll
   for (uint32_t j = 0; j < kPer; ++j) {
     hist[threadIdx.x * kPer + j] = run;  // exclusive start of each bucket
     run += v[j];
   }
   __syncthreads();
-  for (uint32_t i0 = 0; i0 < M; i0 += kOrderThreads) {
+  for (uint32_t i0 = lo; i0 < hi; i0 += kOrderThreads) {
     const uint32_t pos = claim(i0);
     if (pos != kNone) p.fill_order[pos] = i0 + threadIdx.x;
   }
+  __syncthreads();
+}
+
+// The misses made resident [0, M), then those the overflow bypass reads in place
+// [M, M + Mx), each range in host-slot bucket order.
+__device__ void fill_order_block(const EmitParams &p, const GroupDev &g) {
+  __shared__ uint32_t hist[kFillBuckets];
+  const uint32_t M = __ldcg(&g.cnt->M), Mx = __ldcg(&g.cnt->Mx);
+  fill_order_range(p, 0, M, hist);
+  if (Mx) fill_order_range(p, M, M + Mx, hist);
 }
 
 // (4) Each work entry's segment: its set bits in ascending order get the ranks
@@ -878,11 +887,13 @@ __global__ void __launch_bounds__(kMoveThreads, ULA_MOVE_MINBLOCKS) k_move(MoveP
   const uint32_t CW = geo.W / 16;
   uint4 *out = reinterpret_cast<uint4 *>(p.out);
   // overflow bypass: misses [M, M + Mx) are copied from their host slots to the
-  // output only (they stay on the host)
-  for (uint32_t i = M + warp; i < M + Mx; i += nwarps) {
-    const uint32_t hs = p.miss_hs[i];
-    const uint32_t row = p.miss_row[i];
-    if (!out || hs >= geo.H || row >= p.out_cap) {
+  // output only (they stay on the host), in host-slot bucket order as well
+  for (uint32_t t = M + warp; t < M + Mx; t += nwarps) {
+    const uint32_t i = p.fill_order[t];
+    const bool bad_i = i < M || i >= M + Mx;
+    const uint32_t hs = bad_i ? kNone : p.miss_hs[i];
+    const uint32_t row = bad_i ? kNone : p.miss_row[i];
+    if (bad_i || !out || hs >= geo.H || row >= p.out_cap) {
       if (lane == 0) latch(p.status, ULA_ERR_INTERNAL);
       continue;
     }

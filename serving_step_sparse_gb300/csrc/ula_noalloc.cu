@@ -40,49 +40,63 @@ struct Scratch {
 
 __device__ __align__(256) Scratch g_dedup_scratch;
 
-__device__ __forceinline__ uint32_t hash_slot(uint32_t a) {
-  // multiplicative hashing (Knuth), top bits select the slot
-  return (a * 2654435761u) >> (32 - 17);
-}
-static_assert(kTable == (1u << 17), "hash_slot uses 17 bits");
+// A call uses the first 2^bits slots of the table, the smallest power of two at or
+// above 2n (load factor <= 1/2 whatever n is), so that it clears and probes no more
+// than its size needs.
+constexpr uint32_t kTableBits = 17;
+static_assert(kTable == (1u << kTableBits), "table of 2^17 slots");
 
-__device__ __forceinline__ uint32_t find_slot(const Scratch *s, uint32_t a) {
-  uint32_t h = hash_slot(a);
-  for (uint32_t i = 0; i < kTable; ++i) {
+uint32_t table_bits(uint32_t n) {
+  uint32_t bits = 1;
+  while (bits < kTableBits && (1u << bits) < 2 * n) ++bits;
+  return bits;
+}
+
+__device__ __forceinline__ uint32_t hash_slot(uint32_t a, uint32_t bits) {
+  // multiplicative hashing (Knuth), top bits select the slot
+  return (a * 2654435761u) >> (32 - bits);
+}
+
+__device__ __forceinline__ uint32_t find_slot(const Scratch *s, uint32_t a, uint32_t bits) {
+  const uint32_t mask = (1u << bits) - 1;
+  uint32_t h = hash_slot(a, bits);
+  for (uint32_t i = 0; i <= mask; ++i) {
     if (s->keys[h] == a) return h;
-    h = (h + 1) & (kTable - 1);
+    h = (h + 1) & mask;
   }
   return kEmpty;
 }
 
-__global__ void k_clear(Scratch *s) {
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < kTable; i += gridDim.x * blockDim.x) {
+__global__ void k_clear(Scratch *s, uint32_t bits) {
+  const uint32_t size = 1u << bits;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < size; i += gridDim.x * blockDim.x) {
     s->keys[i] = kEmpty;
     s->first[i] = kEmpty;
   }
 }
 
-__global__ void k_insert(Scratch *s, const uint32_t *sel, uint32_t n) {
+__global__ void k_insert(Scratch *s, const uint32_t *sel, uint32_t n, uint32_t bits) {
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n) return;
   const uint32_t a = sel[e];
   if (a == ULA_ADDR_PAD) return;
-  uint32_t h = hash_slot(a);
-  for (uint32_t i = 0; i < kTable; ++i) {
+  const uint32_t mask = (1u << bits) - 1;
+  uint32_t h = hash_slot(a, bits);
+  for (uint32_t i = 0; i <= mask; ++i) {
     const uint32_t k = atomicCAS(&s->keys[h], kEmpty, a);
     if (k == kEmpty || k == a) {
       atomicMin(&s->first[h], e);
       return;
     }
-    h = (h + 1) & (kTable - 1);
+    h = (h + 1) & mask;
   }
 }
 
 __device__ __forceinline__ uint32_t is_first(const Scratch *s, const uint32_t *sel, uint32_t n,
-                                             uint32_t e, uint32_t *slot) {
+                                             uint32_t bits, uint32_t e, uint32_t *slot) {
   *slot = kEmpty;
   if (e >= n || sel[e] == ULA_ADDR_PAD) return 0;
-  *slot = find_slot(s, sel[e]);
+  *slot = find_slot(s, sel[e], bits);
   return *slot != kEmpty && s->first[*slot] == e ? 1u : 0u;
 }
 
@@ -96,9 +110,10 @@ __device__ __forceinline__ uint32_t warp_incl(uint32_t v) {
 }
 
 // per-block counts of first occurrences
-__global__ void __launch_bounds__(kThreads) k_count(Scratch *s, const uint32_t *sel, uint32_t n) {
+__global__ void __launch_bounds__(kThreads) k_count(Scratch *s, const uint32_t *sel, uint32_t n,
+                                                    uint32_t bits) {
   uint32_t slot;
-  const uint32_t f = is_first(s, sel, n, blockIdx.x * blockDim.x + threadIdx.x, &slot);
+  const uint32_t f = is_first(s, sel, n, bits, blockIdx.x * blockDim.x + threadIdx.x, &slot);
   const uint32_t c = __syncthreads_count(f);
   if (threadIdx.x == 0) s->blk[blockIdx.x] = c;
 }
@@ -126,11 +141,11 @@ __global__ void __launch_bounds__(kThreads) k_offsets(Scratch *s, uint32_t nblk,
 }
 
 __global__ void __launch_bounds__(kThreads) k_emit(Scratch *s, const uint32_t *sel, uint32_t n,
-                                                   uint32_t *uniq) {
+                                                   uint32_t bits, uint32_t *uniq) {
   __shared__ uint32_t wsum[kThreads / 32];
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   uint32_t slot;
-  const uint32_t f = is_first(s, sel, n, e, &slot);
+  const uint32_t f = is_first(s, sel, n, bits, e, &slot);
   const uint32_t inc = warp_incl(f);
   if ((threadIdx.x & 31) == 31) wsum[threadIdx.x >> 5] = inc;
   __syncthreads();
@@ -142,7 +157,8 @@ __global__ void __launch_bounds__(kThreads) k_emit(Scratch *s, const uint32_t *s
   }
 }
 
-__global__ void k_rows(const Scratch *s, const uint32_t *sel, uint32_t n, int32_t *entry_row) {
+__global__ void k_rows(const Scratch *s, const uint32_t *sel, uint32_t n, uint32_t bits,
+                       int32_t *entry_row) {
   const uint32_t e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n) return;
   const uint32_t a = sel[e];
@@ -150,11 +166,14 @@ __global__ void k_rows(const Scratch *s, const uint32_t *sel, uint32_t n, int32_
     entry_row[e] = -1;
     return;
   }
-  const uint32_t h = find_slot(s, a);
+  const uint32_t h = find_slot(s, a, bits);
   entry_row[e] = h == kEmpty ? -1 : (int32_t)s->row[h];
 }
 
 // Device address of the scratch, looked up once per device (with that device current).
+// A device reset (cudaDeviceReset) reloads the library's device code, possibly at
+// another address: the cached address is then stale, and the entry point must not be
+// used again in this process.
 constexpr int kMaxDevices = 64;
 std::mutex g_lock;
 Scratch *g_addr[kMaxDevices] = {};
@@ -166,13 +185,24 @@ int scratch_for_current_device(Scratch **out) {
   if (!g_addr[dev]) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_dedup_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
+      cudaGetLastError();  // (this call's own error)
       return ULA_ERR_CUDA;
     }
     g_addr[dev] = static_cast<Scratch *>(p);
   }
   *out = g_addr[dev];
   return ULA_OK;
+}
+
+// One launch; its own status (not an earlier error left on this thread).
+template <typename... Args>
+cudaError_t launch(void (*kernel)(Args...), uint32_t grid, uint32_t block, cudaStream_t st,
+                   Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace
@@ -186,15 +216,13 @@ extern "C" int ula_dedup_noalloc(const uint32_t *d_sel, uint32_t n, uint32_t *d_
   if (rc != ULA_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const uint32_t nblk = (n + kThreads - 1) / kThreads;
-  k_clear<<<128, 256, 0, st>>>(s);
-  if (nblk) {
-    k_insert<<<nblk, kThreads, 0, st>>>(s, d_sel, n);
-    k_count<<<nblk, kThreads, 0, st>>>(s, d_sel, n);
-  }
-  k_offsets<<<1, kThreads, 0, st>>>(s, nblk, d_n_uniq);
-  if (nblk) {
-    k_emit<<<nblk, kThreads, 0, st>>>(s, d_sel, n, d_uniq);
-    k_rows<<<nblk, kThreads, 0, st>>>(s, d_sel, n, d_entry_row);
-  }
-  return cudaGetLastError() == cudaSuccess ? ULA_OK : ULA_ERR_CUDA;
+  const uint32_t bits = table_bits(n);
+  const uint32_t clear_blocks = ((1u << bits) + 255) / 256;
+  cudaError_t e = launch(k_clear, clear_blocks < 128 ? clear_blocks : 128, 256, st, s, bits);
+  if (e == cudaSuccess && nblk) e = launch(k_insert, nblk, kThreads, st, s, d_sel, n, bits);
+  if (e == cudaSuccess && nblk) e = launch(k_count, nblk, kThreads, st, s, d_sel, n, bits);
+  if (e == cudaSuccess) e = launch(k_offsets, 1, kThreads, st, s, nblk, d_n_uniq);
+  if (e == cudaSuccess && nblk) e = launch(k_emit, nblk, kThreads, st, s, d_sel, n, bits, d_uniq);
+  if (e == cudaSuccess && nblk) e = launch(k_rows, nblk, kThreads, st, static_cast<const Scratch *>(s), d_sel, n, bits, d_entry_row);
+  return e == cudaSuccess ? ULA_OK : ULA_ERR_CUDA;
 }

@@ -74,6 +74,8 @@ def test_reference_arm_line(capsys):
     assert line["steps"] == 4 and line["warmup"] == 3 and line["higher_is_better"] is True
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"]
+    assert cb["host_cores"] == os.cpu_count() and cb["pinned_core"] in os.sched_getaffinity(0)
+    assert os.sched_getaffinity(0) != {cb["pinned_core"]} or os.cpu_count() == 1  # restored
     assert line["e2e"] == {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"].startswith("1 request")

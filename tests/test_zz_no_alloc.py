@@ -27,6 +27,7 @@ def _noalloc(ula, d_sel, stream):
     uniq = torch.full((max(n, 1),), -7, dtype=torch.int32, device=d_sel.device)
     rows = torch.full((max(n, 1),), -7, dtype=torch.int32, device=d_sel.device)
     count = torch.full((1,), -7, dtype=torch.int32, device=d_sel.device)
+    stream.wait_stream(torch.cuda.current_stream(d_sel.device))  # the fills and the input
     ula.ula_dedup_noalloc(d_sel.data_ptr(), n, uniq.data_ptr(), rows.data_ptr(),
                           count.data_ptr(), stream.cuda_stream)
     stream.synchronize()
