@@ -231,18 +231,27 @@ class LinkProbe:
         self.s1, self.s2 = torch.cuda.Stream(), torch.cuda.Stream()
 
     def bidir_gbs(self, reps=3):
+        """(both directions together, H2D's own rate while D2H runs beside it), GB/s."""
         torch = self.torch
-        best = 1e9
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        best, best_h2d = 0.0, 0.0
         for _ in range(reps):
             torch.cuda.synchronize()
-            t0 = time.perf_counter()
+            ev[0].record(torch.cuda.current_stream())
+            self.s1.wait_event(ev[0])
+            self.s2.wait_event(ev[0])
             with torch.cuda.stream(self.s1):
                 self.d.copy_(self.h, non_blocking=True)
+                ev[1].record(self.s1)
             with torch.cuda.stream(self.s2):
                 self.h2.copy_(self.d2, non_blocking=True)
+                ev[2].record(self.s2)
             torch.cuda.synchronize()
-            best = min(best, time.perf_counter() - t0)
-        return 2 * self.n / best / 1e9
+            t_h2d = ev[0].elapsed_time(ev[1]) / 1e3
+            t_all = max(t_h2d, ev[0].elapsed_time(ev[2]) / 1e3)
+            best = max(best, 2 * self.n / t_all / 1e9)
+            best_h2d = max(best_h2d, self.n / t_h2d / 1e9)
+        return best, best_h2d
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -514,8 +523,9 @@ def run_gpu(args, rank, world, local):
         ula.ula_profile_spans(cache.ctx, False)
         launches += sum(p["kernels"] for p in ula.ula_profile_read(cache.ctx, reset=True).values())
         d = {k: sb[k] - sa[k] for k in sb}
+        ce, ce_h2d = probe.bidir_gbs()
         repeats.append({"ms": ms, "stats": d, "spans": span_summary(spans, d, L, W, G * NS),
-                        "ce_bidir_gbs": probe.bidir_gbs()})
+                        "ce_bidir_gbs": ce, "ce_h2d_beside_d2h_gbs": ce_h2d})
     launches //= reps
     order = sorted(range(reps), key=lambda i: repeats[i]["ms"])
     med = repeats[order[reps // 2]]
@@ -629,6 +639,11 @@ def run_gpu(args, rank, world, local):
     # ---- host link: the move kernel moves fills (H2D) and write-backs (D2H) at once;
     # its device spans in the same timed region
     mv = sp.get("move", {"launches": 0, "sum_us": 0.0, "union_us": 0.0})
+    # the link is shared with the machine's other work: its capacity is the best the copy
+    # engines showed in this run (at set-up, and after every timed region)
+    link = dict(link, bidir_gbs=max([link["bidir_gbs"]] + [r["ce_bidir_gbs"] for r in repeats]),
+                h2d_beside_d2h_gbs=max([link["h2d_beside_d2h_gbs"]] +
+                                       [r["ce_h2d_beside_d2h_gbs"] for r in repeats]))
     mv_s = mv["sum_us"] / 1e6
     h2d_b, d2h_b = med["stats"]["bytes_h2d"], med["stats"]["bytes_d2h"]
     host = {"kernel": "k_move_layers + k_commit" if args.layer_signal else "k_move",
@@ -638,7 +653,9 @@ def run_gpu(args, rank, world, local):
             "peak_h2d_gbs": round(link["h2d_gbs"], 1), "peak_d2h_gbs": round(link["d2h_gbs"], 1),
             "peak_bidir_gbs": round(link["bidir_gbs"], 1),
             "peak_h2d_beside_d2h_gbs": round(link["h2d_beside_d2h_gbs"], 1),
-            "peak_source": "measured in this run: pinned cudaMemcpyAsync, 1 GiB",
+            "peak_source": ("measured in this run: pinned cudaMemcpyAsync, 1 GiB each way at "
+                            "set-up, 256 MiB each way after every timed region (both directions: "
+                            "the best of these)"),
             "timing": "device spans of the move launches in the median timed region",
             "move_us_per_step": round(mv["sum_us"] / NS, 2)}
     if mv_s:
@@ -669,6 +686,9 @@ def run_gpu(args, rank, world, local):
         "roofline": roof, "host_link": host, "clocks": clk, "phases": phases, "e2e": e2e,
         "layer_ready": layer_ready, "repeats": rep_lines,
         "spans_us_per_step": {k: round(v["sum_us"] / NS, 2) for k, v in sp.items()},
+        "metadata_beside_copies": (round(sp["select"]["beside_copies_us"] /
+                                         max(1e-9, sp["select"]["union_us"]), 4)
+                                   if "select" in sp else None),
         "setup_s": setup_s, "stats": med["stats"],
     }
     if e2e is not None:
@@ -731,14 +751,46 @@ def union_ns(iv) -> int:
     return tot
 
 
+def merged(iv):
+    """The union of [a, b) intervals as sorted disjoint intervals."""
+    out = []
+    for a, b in sorted(iv):
+        if out and a <= out[-1][1]:
+            out[-1][1] = max(out[-1][1], b)
+        else:
+            out.append([a, b])
+    return out
+
+
+def overlap_ns(x, y) -> int:
+    """Length of the intersection of two unions of intervals."""
+    xs, ys = merged(x), merged(y)
+    i = j = tot = 0
+    while i < len(xs) and j < len(ys):
+        lo, hi = max(xs[i][0], ys[j][0]), min(xs[i][1], ys[j][1])
+        if hi > lo:
+            tot += hi - lo
+        if xs[i][1] < ys[j][1]:
+            i += 1
+        else:
+            j += 1
+    return tot
+
+
 def span_summary(spans, d, L, W, group_steps):
-    """Per copy kernel of one timed region: launches, summed and united device spans (us)."""
+    """Per kernel kind of one timed region: launches, summed and united device spans (us);
+    for the metadata ("select": dedup through victim emission), how much of it ran while
+    the copy kernels (gather, staging, move) were running."""
     by = {}
     for ph, _g, t0, t1 in spans:
         if t1 >= t0 > 0:
             by.setdefault(ph, []).append((t0, t1))
-    return {ph: {"launches": len(iv), "sum_us": sum(b - a for a, b in iv) / 1e3,
-                 "union_us": union_ns(iv) / 1e3} for ph, iv in by.items()}
+    out = {ph: {"launches": len(iv), "sum_us": sum(b - a for a, b in iv) / 1e3,
+                "union_us": union_ns(iv) / 1e3} for ph, iv in by.items()}
+    if "select" in by:
+        copies = [x for ph in ("gather", "stage", "move") for x in by.get(ph, [])]
+        out["select"]["beside_copies_us"] = overlap_ns(by["select"], copies) / 1e3
+    return out
 
 
 # DRAM traffic of the gather kernel measured by ncu (dram__bytes_read.sum and
@@ -937,7 +989,8 @@ def main(argv=None):
                 "repeats": r["repeats"], "value_median": value,
                 "value_spread": [min(x["value"] for x in r["repeats"]),
                                  max(x["value"] for x in r["repeats"])],
-                "spans_us_per_step": r["spans_us_per_step"]}
+                "spans_us_per_step": r["spans_us_per_step"],
+                "metadata_beside_copies": r["metadata_beside_copies"]}
         if args.gather_beside:
             line["config"]["gather"] = "beside the move"
         line["config"]["group_calls"] = ("one caller stream" if args.one_stream else

@@ -93,6 +93,10 @@ def test_roofline_helpers(monkeypatch):
              ("move", 1, 1500, 2500), ("stage", 1, 0, 0)]  # an empty record is skipped
     sm = bench.span_summary(spans, {}, 4, 656, 2)
     assert sm["gather"] == {"launches": 2, "sum_us": 0.4, "union_us": 0.4}
+    assert bench.overlap_ns([(0, 10), (20, 30)], [(5, 25)]) == 10
+    assert bench.overlap_ns([(0, 10)], [(10, 20)]) == 0
+    spans2 = spans + [("select", 1, 200, 1400)]  # metadata beside the move and the gather
+    assert bench.span_summary(spans2, {}, 4, 656, 2)["select"]["beside_copies_us"] == 1.2
     assert sm["move"]["launches"] == 2 and sm["move"]["sum_us"] == 2.0 and "stage" not in sm
     t = dict(bench.GATHER_TRAFFIC)
     if t["source_sha256"] is not None:  # DRAM reads cover at least the algorithmic reads
