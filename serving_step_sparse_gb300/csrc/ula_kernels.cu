@@ -7,8 +7,8 @@
 // (bucket ring + cold bucket, rotation by relabelling, victim order, bitmaps
 // with summary levels, parallel hit detection/dedup, move -> map -> signal).
 //
-// One step of one group is six launches on the critical path, chained by
-// programmatic dependent launch:
+// One step of one group is five metadata launches, chained by programmatic
+// dependent launch:
 //   k_dedup_stamp       (1) every entry bids to be its address's first occurrence
 //   k_dedup_count_scan  (1)(2) per-block counts of first occurrences / misses; the
 //                       last block scans them and runs the capacity check
@@ -17,13 +17,19 @@
 //                       slot, stamp and bit in the step's hit map
 //   k_mark_select       (3b) the hit map applied to the labels, word by word; the last
 //                       block walks the segment counts (4) in class order
-//   k_select_emit       (4) the victims' and write-back slots' indices
-//   k_move              (5) write-back and fill, then each victim's map, labels and
-//                       host slot; (6) the missed rows' outputs; entry rows
-// and k_gather (6) for the rows that hit, on the prefetch streams, concurrent with
-// the selection and the move (hit slots never move in their round).  Options:
-// k_lru_select (exact LRU's scan, after the marking), k_move_layers + k_commit
-// (per-layer signal), cache mode (a TP rank's local buffer).
+//   k_select_emit       (4) the victims' and write-back slots' indices; (5) the order
+//                       of the fills (one more block)
+// then three copy launches, one after the other:
+//   k_gather            (6) every layer of the rows that hit (hit slots never move in
+//                       their round)
+//   k_stage             (1) entry rows; (5) the rows of the victims that hold data,
+//                       copied to the staging area
+//   k_move              (5) write-backs (from the staging area) and fills over the host
+//                       link, then each victim's map, labels and host slot; (6) the
+//                       missed rows' outputs
+// Options: k_lru_select (exact LRU's scan, after the marking), the gather beside the
+// move, k_move_layers + k_commit (per-layer signal), cache mode (a TP rank's local
+// buffer).
 //
 // Concurrency discipline for the bitmaps: inside one kernel a given bitmap is
 // either only set or only cleared.  That keeps the summary levels and the
@@ -808,8 +814,7 @@ constexpr int kMoveThreads = ULA_MOVE_THREADS;
 // victims back from the staging area and fills them, each in its own order, with no
 // ordering between a victim's write-back and its fill.
 __global__ void __launch_bounds__(256) k_stage(MoveParams p) {
-  pdl_wait();
-  pdl_launch();
+  pdl_launch();  // the move may be scheduled early (it waits for this kernel to finish)
   if (*(volatile int *)p.status) return;
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
@@ -2175,7 +2180,10 @@ cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t row_b
 int move_threads() { return kMoveThreads; }
 
 cudaError_t launch_stage(const MoveParams &p, int blocks, cudaStream_t s) {
-  // (an ordinary launch: the stream waits on the step's metadata event before it)
+  // An ordinary launch, after the hit gather has ended (or after the stream's wait on the
+  // step's metadata).  Chained to the gather by programmatic dependent launch it started
+  // in the gather's tail, and the move that followed carried 246-252 GB/s instead of
+  // 295-301 (three paired runs on the long-document workload): not used.
   k_stage<<<blocks > 0 ? blocks : 1, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
