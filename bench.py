@@ -40,8 +40,8 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="longdoc")
     ap.add_argument("--policy", choices=["pblru", "exact"], default="pblru",
@@ -57,7 +57,7 @@ def parse_args(argv=None):
                          "has its own caller stream, so later groups' steps are issued ahead")
     ap.add_argument("--gather-beside", action="store_true",
                     help="run the hit gather beside the move (ULA_FLAG_GATHER_BESIDE_MOVE)")
-    ap.add_argument("--profile-steps", type=int, default=60)
+    ap.add_argument("--profile-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -424,7 +424,10 @@ def run_gpu(args, rank, world, local):
     n_value, n_prof = NS * reps, min(args.profile_steps, NS)
     n_lat = min(args.latency_steps, NS)
     n_e2e = 0 if args.no_e2e else NS
-    steps = gen_steps(trace, w, args.warmup + n_value + n_prof + n_lat + n_e2e, synth, np)
+    # warm-up, timed, profiled, latency and e2e passes run consecutive steps of the trace
+    # (past the recipe's trace length the generator continues the same recipe)
+    need = args.warmup + n_value + n_prof + n_lat + n_e2e
+    steps = gen_steps(trace, w, need, synth, np)
     outs = [cache.out_buffer(g, E) for g in range(G)]
     entry_row = [torch.empty(E, dtype=torch.int32, device=dev) for _ in range(G)]
     req_off = [torch.empty(R + 1, dtype=torch.int32, device=dev) for _ in range(G)]
