@@ -26,12 +26,6 @@ namespace {
 
 constexpr uint32_t kAllocChunk = 65536;
 constexpr size_t kSpanCap = 1u << 16;  // span records kept between reads
-// Where the step releases its hit gather: 0 = once the compaction has recorded the
-// hits' slots (beside the marking and the victim selection), 1 = after the victims are
-// emitted (beside the staging copy only).
-#ifndef ULA_GATHER_AFTER_EMIT
-#define ULA_GATHER_AFTER_EMIT 0
-#endif
 // Internal: a TP rank's local buffer (misses fetched from the owner partitions,
 // evicted copies dropped).  Not accepted by the public ula_create.
 constexpr uint32_t kFlagCacheInternal = 1u << 31;

@@ -205,11 +205,14 @@ def test_copy_kernel_spans(beside):
         per = {}
         for ph, g, t0, t1 in spans:
             per.setdefault(g, []).append((ph, t0, t1))
-        for g, lst in per.items():  # per group step, in launch order
+        for g, lst in per.items():  # per group step: its four records, the move's last
             for i in range(0, len(lst), 4):
-                (pq, q0, q1), (pg, g0, g1), (ps, s0, _), (pm, m0, _) = lst[i:i + 4]
-                assert (pq, pg, ps, pm) == ("select", "gather", "stage", "move")
-                assert g0 >= q0 and s0 >= q1 and m0 >= q1
+                rec = {ph: (t0, t1) for ph, t0, t1 in lst[i:i + 4]}
+                assert sorted(rec) == ["gather", "move", "select", "stage"], lst[i:i + 4]
+                assert lst[i][0] == "select" and lst[i + 3][0] == "move"
+                (q0, q1), (g0, g1), (s0, s1), (m0, m1) = (rec[k] for k in ("select", "gather",
+                                                                          "stage", "move"))
+                assert g0 >= q0 and s0 >= q1 and m0 >= q1 and m0 >= s1
                 if not beside:
                     assert m0 >= g1, "the move starts after the hit gather"
     finally:
