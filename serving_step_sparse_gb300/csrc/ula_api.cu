@@ -25,6 +25,9 @@ using namespace ula;
 namespace {
 
 constexpr uint32_t kAllocChunk = 65536;
+#ifndef ULA_CACHE_MOVE_BLOCKS
+#define ULA_CACHE_MOVE_BLOCKS 4  // move blocks per SM of a TP rank's local buffer (HBM copies)
+#endif
 constexpr size_t kSpanCap = 1u << 16;  // span records kept between reads
 // Internal: a TP rank's local buffer (misses fetched from the owner partitions,
 // evicted copies dropped).  Not accepted by the public ula_create.
@@ -343,7 +346,8 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   c->gather_fit_per_sm = c->gather_blocks;
   // ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune the persistent grids
   // (clamped to what fits on an SM).
-  c->move_blocks = env_blocks("ULA_MOVE_BLOCKS_PER_SM", kMoveBlocksPerSm, c->move_blocks);
+  c->move_blocks = env_blocks("ULA_MOVE_BLOCKS_PER_SM",
+                              geo.cache ? ULA_CACHE_MOVE_BLOCKS : kMoveBlocksPerSm, c->move_blocks);
   c->gather_blocks = env_blocks("ULA_GATHER_BLOCKS_PER_SM", c->gather_blocks, c->gather_blocks);
   c->move_blocks *= c->sm_count;
   c->gather_blocks *= c->sm_count;
