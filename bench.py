@@ -623,7 +623,7 @@ def run_gpu(args, rank, world, local):
     avg_launch_us = ga["sum_us"] / max(1, ga["launches"])
     achieved = g_bytes / (ga["sum_us"] * 1e3) if ga["sum_us"] else 0.0  # bytes/ns = GB/s
     iso = isolated_gather(cache, ula, torch, dev, stream, W, L)
-    roof = {"bound": "hbm", "kernel": "k_gather", "achieved": round(achieved, 1),
+    roof = {"bound": "hbm", "kernel": "k_gather_bulk", "achieved": round(achieved, 1),
             "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
             "traffic": traffic_per_launch(med["stats"]["hits"], ga["launches"], args.workload),
             "traffic_read_per_hit_row": (round(GATHER_TRAFFIC["read_bytes_per_hit"], 1)
@@ -693,6 +693,7 @@ def run_gpu(args, rank, world, local):
                                          max(1e-9, sp["select"]["union_us"]), 4)
                                    if "select" in sp else None),
         "setup_s": setup_s, "stats": med["stats"],
+        "host_huge": [None if f is None else round(f, 3) for f in cache.host_huge_fraction],
     }
     if e2e is not None:
         a = aggregate({"rows": e2e["rows"], "e2e_ms": e2e["e2e_ms"]}, world, dev)
@@ -704,10 +705,9 @@ def run_gpu(args, rank, world, local):
 
 
 def isolated_gather(cache, ula, torch, dev, stream, W, L, reps=20):
-    """The gather kernel alone, in the step's two launches: re-gather group 0's last hit
-    rows (layer 0 alone, then layers 1..L-1 together), L2 flushed before each launch,
-    CUDA events on the launching stream; with the step's grid and with every block
-    that fits on the SMs."""
+    """The gather kernel alone, in the step's launch (every layer of group 0's last hit
+    rows), L2 flushed before each launch, CUDA events on the launching stream; with the
+    step's grid and with every block that fits on the SMs."""
     st = cache.export(0)
     hits = st["hits"]
     out = cache.out_buffer(0, max(1, st["U"]))
@@ -800,22 +800,24 @@ def span_summary(spans, d, L, W, group_steps):
 # dram__bytes_write.sum of one launch), per hit row, with the case it was taken on and
 # the hash of the gather kernel's source (its launch-shape defaults and its body).
 # Reported only while that source is unchanged and for the workload it was taken on.
-GATHER_TRAFFIC = {"source_sha256": "302cd1d24fec69c10d815bf9eb73cd393ac5fec1cb26eacce79a8156caa384ed",
+GATHER_TRAFFIC = {"source_sha256": "0001e758e1cafa8159303f83b95ab22d89bcb7de0a46017016194da97a457ee6",
                   "workload": "longdoc",  # the recipe; the case had 12 of its 32 requests
                   "case": "long-document recipe with 12 requests: group 0's hit rows after 3 "
                           "steps, re-gathered in the step's one all-layer launch, L2 flushed",
                   "hit_rows": 24255,
-                  "read_bytes_per_hit": 64372224 / 24255,   # 2,654 B per 2,624-B slot read
-                  "write_bytes_per_hit": 9538560 / 24255}   # written rows mostly stay in L2
+                  "read_bytes_per_hit": 64330240 / 24255,   # 2,652 B per 2,624-B slot read
+                  "write_bytes_per_hit": 10951936 / 24255}  # written rows mostly stay in L2
 
 
 def gather_source_sha256() -> str:
-    src = os.path.join(ROOT, "serving_step_sparse_gb300", "csrc", "ula_kernels.cu")
-    lines = open(src).read().splitlines()
-    keep = [ln for ln in lines if ln.startswith("#define ULA_GATHER_")]
-    start = next(i for i, ln in enumerate(lines) if ln.startswith("constexpr int kGatherUnroll"))
-    end = next(i for i in range(start, len(lines)) if lines[i] == "}")
-    keep += lines[start:end + 1]
+    src = os.path.join(ROOT, "serving_step_sparse_gb300", "csrc")
+    lines = open(os.path.join(src, "ula_kernels.cu")).read().splitlines()
+    start = next(i for i, ln in enumerate(lines) if ln.startswith("constexpr int kBulkThreads"))
+    body = next(i for i, ln in enumerate(lines) if "k_gather_bulk(GatherParams p) {" in ln)
+    end = next(i for i in range(body, len(lines)) if lines[i] == "}")
+    keep = lines[start:end + 1]
+    keep += [ln for ln in open(os.path.join(src, "ula_api.cu")).read().splitlines()
+             if ln.startswith("constexpr uint32_t kGatherRowsPerBlock")]
     return hashlib.sha256("\n".join(keep).encode()).hexdigest()
 
 
@@ -994,6 +996,7 @@ def main(argv=None):
                                  max(x["value"] for x in r["repeats"])],
                 "spans_us_per_step": r["spans_us_per_step"],
                 "metadata_beside_copies": r["metadata_beside_copies"]}
+        line["config"]["host_pool_huge_page_fraction"] = r["host_huge"]
         if args.gather_beside:
             line["config"]["gather"] = "beside the move"
         line["config"]["group_calls"] = ("one caller stream" if args.one_stream else

@@ -21,6 +21,22 @@ def _thp_bytes() -> int:
         return 2 << 20
 
 
+def _huge_fraction(addr: int, nbytes: int) -> float | None:
+    try:
+        with open("/proc/self/smaps") as f:
+            inside = False
+            for line in f:
+                head = line.split(None, 1)[0]
+                if "-" in head and not head.endswith(":"):
+                    lo, hi = (int(x, 16) for x in head.split("-"))
+                    inside = lo <= addr < hi
+                elif inside and head == "AnonHugePages:":
+                    return min(1.0, int(line.split()[1]) * 1024 / max(1, nbytes))
+    except (OSError, ValueError):
+        pass
+    return None
+
+
 class PinnedHostBuffer:
     """Page-locked host memory for a host slot pool.
 
@@ -48,6 +64,11 @@ class PinnedHostBuffer:
         if getattr(rc, "value", rc) != 0:
             raise RuntimeError(f"cudaHostRegister failed: {rc}")
         self._registered = True
+
+    def huge_fraction(self) -> float | None:
+        """The fraction of the buffer backed by transparent huge pages (from the process's
+        memory map), or None where that is not readable."""
+        return _huge_fraction(self.tensor.data_ptr(), self.nbytes)
 
     def close(self):
         if getattr(self, "_registered", False):
@@ -87,6 +108,7 @@ class UlaCache:
         self._host_bufs = ([PinnedHostBuffer(self.H * L * self.W, huge_host_pages)
                             for L in self.layers] if self.H else [])
         self.host_pools = [b.tensor for b in self._host_bufs] if self.H else None
+        self.host_huge_fraction = [b.huge_fraction() for b in self._host_bufs] if self.H else []
         cfg = ula.make_config(self.W, self.layers, self.S, self.H, self.B, self.max_logical,
                               self.max_entries,
                               (ula.FLAG_BYPASS_OVERFLOW if bypass_overflow else 0)

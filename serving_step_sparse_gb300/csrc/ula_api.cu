@@ -212,10 +212,11 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Persistent grid of the move: one block of 128 threads per SM (the host link is
 // saturated by 4 warps on every SM; more warps or fewer SMs move less, measured).
 constexpr int kMoveBlocksPerSm = 1;
-// The step's hit gather is not persistent: short blocks of kGatherRowsPerBlock rows
-// on the lowest-priority stream, so the step's metadata kernels (highest priority) get
-// SM room as gather blocks retire.  Its grid is sized from the entry count (U <= E);
-// blocks past the last row exit at once.
+// The step's hit gather is not persistent: short blocks of kGatherRowsPerBlock entries'
+// worth of rows, so that the metadata kernels of later calls (highest priority) get SM
+// room as its blocks retire and are done before the move, instead of piling up beside
+// it.  Its grid is sized from the entry count (U <= E); blocks past the last row exit at
+// once.
 constexpr uint32_t kGatherRowsPerBlock = 64;
 int gather_step_blocks(uint64_t entries) {
   const uint64_t b = (entries + kGatherRowsPerBlock - 1) / kGatherRowsPerBlock;
@@ -342,7 +343,9 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(cudaStreamCreateWithPriority(&c->copy, cudaStreamNonBlocking, prio_greatest));
   ULA_CUDA(cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, prio_least));
   ULA_CUDA(cudaEventCreateWithFlags(&c->in_evt, cudaEventDisableTiming));
-  ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks, cfg.row_bytes));
+  uint32_t lmax = 0;
+  for (uint32_t g = 0; g < G; ++g) lmax = cfg.layers_per_group[g] > lmax ? cfg.layers_per_group[g] : lmax;
+  ULA_CUDA(resident_blocks(&c->move_blocks, &c->gather_blocks, lmax * cfg.row_bytes));
   c->gather_fit_per_sm = c->gather_blocks;
   // ULA_MOVE_BLOCKS_PER_SM / ULA_GATHER_BLOCKS_PER_SM tune the persistent grids
   // (clamped to what fits on an SM).
@@ -377,8 +380,6 @@ int create_impl(ula_ctx *c, void *const *gpu_pools, void *const *host_pools) {
   ULA_CUDA(c->alloc(&c->cnt_d, G));
   ULA_CUDA(c->alloc(&c->groups_d, G));
   if (H && !geo.cache && !geo.signal) {  // staged victim rows (the slot-major move only)
-    uint32_t lmax = 0;
-    for (uint32_t g = 0; g < G; ++g) lmax = cfg.layers_per_group[g] > lmax ? cfg.layers_per_group[g] : lmax;
     const size_t rows = cfg.max_entries < S ? cfg.max_entries : S;  // victims per step <= both
     ULA_CUDA(c->alloc(&c->stage, rows * lmax * cfg.row_bytes));
   }
@@ -702,7 +703,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   // marking, the victim selection and the move.
   auto launch_hit_gather = [&](cudaStream_t gs) -> cudaError_t {
     gp.span = c->take_span(ULA_PHASE_GATHER, group);
-    return c->phase(ULA_PHASE_GATHER, gs, gather_launches(c->geo.W, gd.layers),
+    return c->phase(ULA_PHASE_GATHER, gs, 1,
                     [&] { return launch_gather(gp, gather_step_blocks(E), gs); });
   };
   // (1)(2) dedup + translate + capacity check

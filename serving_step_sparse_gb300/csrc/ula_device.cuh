@@ -291,7 +291,6 @@ cudaError_t launch_stage(const MoveParams &p, int blocks, cudaStream_t s);
 cudaError_t launch_move(const MoveParams &p, int blocks, bool dependent, cudaStream_t s);
 int move_threads();
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s);
-int gather_launches(uint32_t row_bytes, uint32_t nlayers);  // kernels one launch_gather makes
 // exact LRU: victims [F, M) by a scan of the slot timestamps (cooperative launch of
 // `blocks` co-resident blocks)
 cudaError_t launch_lru_select(const LruParams &p, int blocks, cudaStream_t s);
@@ -307,9 +306,7 @@ cudaError_t launch_consume(const uint32_t *flag, uint32_t round, const uint8_t *
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,
                                cudaStream_t s);
 cudaError_t launch_free(const FreeParams &p, uint32_t n_groups, cudaStream_t s);
-// resident blocks per SM of the persistent kernels (the gather's shape depends on the rows)
-cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t row_bytes);
-bool gather_uses_tma(uint32_t row_bytes);
-size_t gather_tma_smem(uint32_t row_bytes);
+// blocks of the move and of the hit gather (for rows of up to slot_bytes) that fit on an SM
+cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t slot_bytes);
 
 }  // namespace ula

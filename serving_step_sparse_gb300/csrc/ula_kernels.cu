@@ -20,8 +20,9 @@
 //   k_select_emit       (4) the victims' and write-back slots' indices; (5) the order
 //                       of the fills (one more block)
 // then three copy launches, one after the other:
-//   k_gather            (6) every layer of the rows that hit (hit slots never move in
-//                       their round)
+//   k_gather_bulk       (6) every layer of the rows that hit (hit slots never move in
+//                       their round), a whole row per bulk copy through shared memory
+//                       (k_gather, with registers, for rows too long for its buffers)
 //   k_stage             (1) entry rows; (5) the rows of the victims that hold data,
 //                       copied to the staging area
 //   k_move              (5) write-backs (from the staging area) and fills over the host
@@ -49,9 +50,7 @@ constexpr int kStampThreads = 256;
 constexpr int kWalkSegs = 4;        // segments per thread per step of the victim walk
 constexpr int kMarkClasses = 8;     // class words a marking warp loads at once
 
-// Launch shapes of the two persistent copy kernels (build-time tunables).  A gather
-// block (<= 80 registers a thread at 3 blocks per SM) fits in the register file
-// beside two move blocks (80 registers), so the hit gathers and the move share the SMs.
+// Launch shapes of the register gather and of the move (build-time tunables).
 #ifndef ULA_GATHER_THREADS
 #define ULA_GATHER_THREADS 256
 #endif
@@ -71,9 +70,6 @@ constexpr int kMarkClasses = 8;     // class words a marking warp loads at once
 #define ULA_MOVE_UNROLL 6
 #endif
 constexpr int kGatherThreads = ULA_GATHER_THREADS;
-#ifndef ULA_GATHER_TMA
-#define ULA_GATHER_TMA 0  // the hit gather with bulk copies (k_gather_tma)
-#endif
 
 __device__ __forceinline__ void latch(int *status, int code) { atomicCAS(status, 0, code); }
 
@@ -1115,9 +1111,11 @@ __global__ void k_commit(MoveParams p) {
 //
 // (6) out[j][u] = layer j of unique row u's slot for the layers j of this launch,
 // [layer, layer + nlayers), for the rows that hit (recorded by the marking; a hit's
-// slot does not change in its round, so this runs while the misses are being moved;
+// slot does not change in its round, so this may run while the misses are being moved;
 // missed rows are written by the move).  A slot holds its layers' rows back to back,
-// so the launch reads nlayers * W contiguous bytes per slot.  The U rows are spread
+// so the launch reads nlayers * W contiguous bytes per slot.  Two kernels: the bulk
+// gather below (rows that fit its per-thread buffers), and this one, with registers,
+// for longer rows.  The U rows are spread
 // over all warps (rows_per_warp = ceil(U / warps), at most 32): lanes read the warp's
 // slots, then the warp streams the rows' 16-byte chunks, consecutive lanes on
 // consecutive chunks (coalesced within a slot; per layer, the warp's output rows are
@@ -1208,20 +1206,25 @@ __global__ void __launch_bounds__(kGatherThreads, ULA_GATHER_MINBLOCKS) k_gather
   }
 }
 
-// (6) The same gather with bulk copies (TMA, cp.async.bulk): a block is one warp
-// and every lane runs its own pipeline of kTmaStages row buffers in shared memory
-// -- a bulk load of the pool row into a buffer, completed on the buffer's
-// mbarrier, then a bulk store of the buffer to the output row -- so a warp keeps
-// 32 * kTmaStages rows in flight without holding their bytes in registers and
-// without the load/store units.  Lanes take rows tid, tid + threads, ...; rows
-// that missed are skipped.  Waits are bounded (1 s, then ULA_ERR_TIMEOUT).
-constexpr int kTmaStages = 3;
+// (6) The same gather with bulk copies (cp.async.bulk through shared memory), for
+// slots that fit a thread's buffer: each thread moves whole rows -- one bulk load brings
+// a hit row's layers [layer, layer + nlayers) (nlayers * W contiguous bytes of its slot)
+// into the thread's buffer, completing on the thread's mbarrier; one bulk store per
+// layer then writes the row to that layer's output plane; the thread's next load waits
+// until those stores have read the buffer.  No row's bytes pass through registers and
+// the load/store units stay free, so many rows are in flight per SM (kBulkThreads per
+// block, several blocks per SM).  Threads take rows tid, tid + threads, ... of the
+// unique rows; rows that missed are skipped (the move writes them).  Waits are bounded
+// (1 s, then ULA_ERR_TIMEOUT).
+constexpr int kBulkThreads = 16;
+constexpr uint32_t kBulkBars = 128;  // the mbarriers' bytes at the head of shared memory
 
 __device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
   return (uint32_t)__cvta_generic_to_shared(ptr);
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long t0) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
   for (;;) {
     uint32_t done;
     asm volatile(
@@ -1233,9 +1236,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
   }
 }
 
-__global__ void __launch_bounds__(32) k_gather_tma(GatherParams p) {
-  extern __shared__ __align__(128) uint8_t tma_smem[];
+__global__ void __launch_bounds__(kBulkThreads) k_gather_bulk(GatherParams p) {
+  extern __shared__ __align__(128) uint8_t bulk_smem[];
   if (*(volatile int *)p.status) return;
+  span_open(p.span);
   const GroupDev &g = p.grp;
   const Geometry &geo = p.geo;
   const uint32_t U = g.cnt->U;
@@ -1243,19 +1247,16 @@ __global__ void __launch_bounds__(32) k_gather_tma(GatherParams p) {
     if (blockIdx.x == 0 && threadIdx.x == 0) latch(p.status, ULA_ERR_CAPACITY);
     return;
   }
-  const uint32_t W = geo.W, lane = threadIdx.x;
-  const uint32_t bars = smem_u32(tma_smem) + lane * kTmaStages * 8;   // [32][stages] mbarriers
-  uint8_t *buf = tma_smem + 32 * kTmaStages * 8 + (size_t)lane * kTmaStages * W;
-  for (int st = 0; st < kTmaStages; ++st)
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8 * st) : "memory");
+  const uint32_t W = geo.W, NL = p.nlayers, rb = NL * W;  // bytes per row moved
+  const uint32_t bar = smem_u32(bulk_smem) + threadIdx.x * 8;
+  const uint32_t buf = smem_u32(bulk_smem) + kBulkBars + threadIdx.x * rb;
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncwarp();
   const size_t sb = (size_t)g.layers * W;
   const uint8_t *pool = g.gpu_pool + (size_t)p.layer * W;
   uint8_t *out = p.out + (size_t)p.layer * p.out_cap * W;
-  const uint32_t nthr = gridDim.x * 32;
-  uint32_t next = blockIdx.x * 32 + lane;  // the next row this lane looks at
-  uint32_t rows[kTmaStages];
+  const uint32_t nthr = gridDim.x * blockDim.x;
+  uint32_t next = blockIdx.x * blockDim.x + threadIdx.x;  // the next row this thread looks at
   // the next hit row at or after `next` (and its slot); false when none is left
   auto next_hit = [&](uint32_t &row, uint32_t &slot) -> bool {
     while (next < U) {
@@ -1272,49 +1273,42 @@ __global__ void __launch_bounds__(32) k_gather_tma(GatherParams p) {
     }
     return false;
   };
-  auto load = [&](int st, uint32_t slot) {
-    const uint32_t bar = bars + 8 * st;
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(W)
+  auto load = [&](uint32_t slot) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(rb)
                  : "memory");
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_u32(buf + (size_t)st * W)), "l"(pool + (size_t)slot * sb), "r"(W), "r"(bar)
+        ::"r"(buf), "l"(pool + (size_t)slot * sb), "r"(rb), "r"(bar)
         : "memory");
   };
-  uint32_t issued = 0;
-  for (int st = 0; st < kTmaStages; ++st) {  // prime every stage
-    uint32_t row, slot;
-    if (!next_hit(row, slot)) break;
-    rows[st] = row;
-    load(st, slot);
-    ++issued;
-  }
-  const unsigned long long t0 = global_ns();
-  for (uint32_t k = 0; k < issued; ++k) {
-    const int st = (int)(k % kTmaStages);
-    if (!mbar_wait(bars + 8 * st, (k / kTmaStages) & 1u, t0)) {
+  uint32_t row, slot, parity = 0;
+  bool have = next_hit(row, slot);
+  if (have) load(slot);
+  while (have) {
+    if (!mbar_wait(bar, parity)) {
       latch(p.status, ULA_ERR_TIMEOUT);
+      mbar_wait(bar, parity);  // (once more, bounded, for the load still in flight)
       break;
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 ::"l"(out + (size_t)rows[st] * W), "r"(smem_u32(buf + (size_t)st * W)), "r"(W)
-                 : "memory");
+    parity ^= 1u;
+    for (uint32_t j = 0; j < NL; ++j)
+      asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                   ::"l"(out + ((size_t)j * p.out_cap + row) * W), "r"(buf + j * W), "r"(W)
+                   : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-    uint32_t row, slot;
-    if (next_hit(row, slot)) {
+    have = next_hit(row, slot);
+    if (have) {
       asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the buffer is read
-      rows[st] = row;
-      load(st, slot);
-      ++issued;
+      load(slot);
     }
   }
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // every store has landed
-  if (p.signal) {  // per-layer signal: the hit rows of this layer are one contribution
+  span_close(p.span);
+  if (p.signal) {  // per-layer signal: the hit rows of these layers are one contribution
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __threadfence();
     if (last_block(&g.gather_done[p.layer]) && threadIdx.x == 0)
-      layer_contrib(g, p.layer, 2u, p.round);
+      for (uint32_t j = p.layer; j < p.layer + NL; ++j) layer_contrib(g, j, 2u, p.round);
   }
 }
 
@@ -2161,19 +2155,25 @@ cudaError_t launch_alloc_select(const EmitParams &p, uint32_t n_groups, cudaStre
   return cudaGetLastError();
 }
 
-size_t gather_tma_smem(uint32_t row_bytes) {
-  return 32 * kTmaStages * 8 + (size_t)32 * kTmaStages * row_bytes;
+size_t gather_bulk_smem(uint32_t slot_bytes) {
+  return kBulkBars + (size_t)kBulkThreads * slot_bytes;
 }
 
-cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t row_bytes) {
+// The bulk gather's shared memory is capped so that at least two of its blocks fit on an
+// SM beside the other kernels' blocks.
+constexpr size_t kBulkMaxSmem = 100 * 1024;
+
+bool gather_uses_bulk(uint32_t slot_bytes) { return gather_bulk_smem(slot_bytes) <= kBulkMaxSmem; }
+
+cudaError_t resident_blocks(int *move_per_sm, int *gather_per_sm, uint32_t slot_bytes) {
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(move_per_sm, k_move, kMoveThreads, 0);
   if (e != cudaSuccess) return e;
-  if (gather_uses_tma(row_bytes)) {
-    const size_t smem = gather_tma_smem(row_bytes);
-    e = cudaFuncSetAttribute(k_gather_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather_tma, 32, smem);
-  }
+  e = cudaFuncSetAttribute(k_gather_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kBulkMaxSmem);
+  if (e != cudaSuccess) return e;
+  if (gather_uses_bulk(slot_bytes))
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather_bulk, kBulkThreads,
+                                                         gather_bulk_smem(slot_bytes));
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(gather_per_sm, k_gather, kGatherThreads, 0);
 }
 
@@ -2225,26 +2225,13 @@ cudaError_t launch_lru_select(const LruParams &p, int blocks, cudaStream_t s) {
                                      dim3(kLruThreads), args, 0, s);
 }
 
-bool gather_uses_tma(uint32_t row_bytes) {
-  return ULA_GATHER_TMA && gather_tma_smem(row_bytes) <= 160 * 1024;
-}
-
 cudaError_t launch_gather(const GatherParams &p, int blocks, cudaStream_t s) {
-  if (gather_uses_tma(p.geo.W)) {  // one launch per layer
-    for (uint32_t j = 0; j < p.nlayers; ++j) {
-      GatherParams q = p;
-      q.layer = p.layer + j;
-      q.nlayers = 1;
-      k_gather_tma<<<blocks, 32, gather_tma_smem(p.geo.W), s>>>(q);
-    }
-  } else {
+  const uint32_t rb = p.nlayers * p.geo.W;
+  if (gather_uses_bulk(rb))
+    k_gather_bulk<<<blocks, kBulkThreads, gather_bulk_smem(rb), s>>>(p);
+  else
     k_gather<<<blocks, kGatherThreads, 0, s>>>(p);
-  }
   return cudaGetLastError();
-}
-
-int gather_launches(uint32_t row_bytes, uint32_t nlayers) {
-  return gather_uses_tma(row_bytes) ? (int)nlayers : 1;
 }
 
 cudaError_t launch_alloc_place(const AllocParams &p, uint32_t n_groups, int max_blocks,

@@ -310,6 +310,36 @@ def test_mixed_layers_duplicates_across_requests_and_empty_steps():
         c.close()
 
 
+def test_bulk_and_register_gathers_by_row_length():
+    """Group 0's rows (2 layers x 656 B) fit the bulk gather's per-thread buffers; group 1's
+    (10 layers x 656 B = 6,560 B) do not and take the register gather.  Both, and the moves
+    beside them, bit-exact with the oracle over steps with evictions in both groups."""
+    from tests.gpu_harness import gpu_state_in_oracle_terms
+    layers, W, S, H, B = (2, 10), 656, 48, 512, 3
+    c, o = _direct(S=S, H=H, B=B, layers=layers, W=W, max_logical=512, max_entries=256)
+    try:
+        n = 400
+        rows = _rows(layers, 0, n, W)
+        t = torch.from_numpy(rows).pin_memory()
+        assert c.alloc(n, t) == 0 and o.alloc(n, rows) == 0
+        c.sync()
+        rng = np.random.default_rng(11)
+        misses = writebacks = 0
+        for step in range(24):
+            g = step % 2
+            sel = rng.choice(n, (2, 2, 8)).astype(np.uint32)  # at most 32 unique rows (S = 48)
+            sel[1, 1, 5] = 0xFFFFFFFF
+            res = _step_both(c, o, g, sel)
+            misses += res["counters"]["misses"]
+            writebacks += res["counters"]["writebacks"]
+            for gg in range(2):
+                go = gpu_state_in_oracle_terms(c.export(gg), _W(S, H, B))
+                compare_states(go, o.export(gg), f"step {step} g{gg}")
+        assert misses > 0 and writebacks > 0
+    finally:
+        c.close()
+
+
 # --------------------------------------------------------- per-layer signal
 
 @pytest.mark.parametrize("name", ["tiny_1x4k", "batch8_32k", "longdoc", "low_overlap",
