@@ -472,6 +472,10 @@ def run_gpu(args, rank, world, local):
         issue_groups(sel_t)
         apply_step_events(cache, ev, rows_t)
 
+    # The clock sampler starts (and its start-up pause passes) before the warm-up steps,
+    # so that the first timed region follows the warm-up without an idle gap.
+    clocks = ClockSampler(local)
+    clocks.start()
     for t in range(args.warmup):
         do_step(sel_dev[t], steps[t][1], rows_dev[t])
     st0 = cache.sync()
@@ -486,6 +490,7 @@ def run_gpu(args, rank, world, local):
         torch.cuda.synchronize()
         print(json.dumps({"traffic_case": {"hit_rows": st["hits"], "unique_rows": st["U"],
                                            "gather_launches_before": args.warmup * G}}))
+        clocks.stop()
         cache.close()
         sys.exit(0)
     ula.ula_profile_read(cache.ctx, reset=True)
@@ -494,8 +499,6 @@ def run_gpu(args, rank, world, local):
         dist.barrier()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(local)
-    clocks.start()
     # ---- value: inputs resident in HBM; `reps` timed regions of NS steps each, with the
     # copy kernels' device spans recorded in the same pass
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
