@@ -812,12 +812,17 @@ GATHER_TRAFFIC = {"source_sha256": "0001e758e1cafa8159303f83b95ab22d89bcb7de0a46
                   "write_bytes_per_hit": 10951936 / 24255}  # written rows mostly stay in L2
 
 
-def gather_source_sha256() -> str:
+def gather_source_sha256() -> str | None:
+    """Hash of the hit gather's source (its shared-memory constants and helpers, the kernel,
+    and the step grid's constant), or None where the source does not have that shape."""
     src = os.path.join(ROOT, "serving_step_sparse_gb300", "csrc")
     lines = open(os.path.join(src, "ula_kernels.cu")).read().splitlines()
-    start = next(i for i, ln in enumerate(lines) if ln.startswith("constexpr int kBulkThreads"))
-    body = next(i for i, ln in enumerate(lines) if "k_gather_bulk(GatherParams p) {" in ln)
-    end = next(i for i in range(body, len(lines)) if lines[i] == "}")
+    try:
+        start = next(i for i, ln in enumerate(lines) if ln.startswith("constexpr int kBulkThreads"))
+        body = next(i for i, ln in enumerate(lines) if "k_gather_bulk(GatherParams p) {" in ln)
+        end = next(i for i in range(body, len(lines)) if lines[i] == "}")
+    except StopIteration:
+        return None
     keep = lines[start:end + 1]
     keep += [ln for ln in open(os.path.join(src, "ula_api.cu")).read().splitlines()
              if ln.startswith("constexpr uint32_t kGatherRowsPerBlock")]
