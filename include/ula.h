@@ -194,12 +194,12 @@ int ula_free(ula_ctx *ctx, uint32_t logical_base, uint32_t n);
  *       to the j-th lowest free host slot), fill each miss from its host slot, then
  *       update the map (moves complete before the map changes) and signal,
  *   (6) gather out[j][u] = layer j of unique address u, for every layer of the group.
- *       Rows that hit are gathered, every layer in one launch, as soon as the
- *       compaction has recorded their slots (their slots never move in this round),
- *       on an internal stream of their own while the hits are marked and the victims
- *       chosen: finished before the move starts by default, beside the move with
- *       ULA_FLAG_GATHER_BESIDE_MOVE; rows that missed are written by the fill itself,
- *       from the bytes it moves.
+ *       Rows that hit are gathered, every layer in one launch (their slots never move
+ *       in this round): by default after the step's metadata and before the move, on
+ *       the context's copy stream; with ULA_FLAG_GATHER_BESIDE_MOVE on an internal
+ *       low-priority stream as soon as the compaction has recorded their slots, beside
+ *       the marking, the victim choice and the move.  Rows that missed are written by
+ *       the fill itself, from the bytes it moves.
  * The move writes every victim that holds data back from a staging copy in HBM (made
  * right after the victims are known), so its write-backs (in victim order, which is
  * ascending host-slot order) and its fills (sorted by the miss's host slot) each

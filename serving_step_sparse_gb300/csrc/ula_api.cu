@@ -750,10 +750,7 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
   cudaStream_t cs = c->copy;
   ULA_CUDA(cudaEventRecord(st.meta_evt, s));
   ULA_CUDA(cudaStreamWaitEvent(cs, st.meta_evt, 0));
-  if (gather && !c->beside) {
-    ULA_CUDA(launch_hit_gather(cs));
-    ULA_CUDA(cudaEventRecord(st.hit_evt, cs));
-  }
+  if (gather && !c->beside) ULA_CUDA(launch_hit_gather(cs));  // (its event after the move)
   // (5) write-back, fill (writing the missed rows' outputs), then map commit
   MoveParams mp{};
   mp.geo = c->geo;
@@ -783,7 +780,9 @@ int ula_step_group(ula_ctx *c, uint32_t group, const uint32_t *d_sel, uint32_t n
                     [&] { return launch_move(mp, c->move_blocks, staged, cs); }));
   // signal: the commit (and the hit gather) complete every layer of the output
   ULA_CUDA(cudaEventRecord(st.commit_evt, cs));
-  if (!gather) ULA_CUDA(cudaEventRecord(st.hit_evt, cs));  // nothing to gather
+  // The gather's event: here when it ran on this stream (nothing stands between the
+  // gather and the chained staging copy), or when there was nothing to gather.
+  if (!gather || !c->beside) ULA_CUDA(cudaEventRecord(st.hit_evt, cs));
   st.in_flight = true;
   ULA_CUDA(cudaStreamWaitEvent(caller, st.commit_evt, 0));
   ULA_CUDA(cudaStreamWaitEvent(caller, st.hit_evt, 0));
