@@ -591,19 +591,41 @@ def run_gpu(args, rank, world, local):
         h2d_bytes = d2h_bytes = 0
         st3a = cache.sync()
         torch.cuda.synchronize()
+        # Each step's selections go up on a stream of their own into one of two device
+        # buffers; each group's calls wait for their upload, and each group reads its CSR
+        # offsets back on its own stream right after its call, so that steps overlap as in
+        # the timed regions.  A buffer is refilled once every group's call of two steps
+        # before has ended.
+        up = stream if args.one_stream else torch.cuda.Stream(dev)
+        up_evt = [torch.cuda.Event() for _ in range(2)]
+        used = [[torch.cuda.Event() for _ in range(G)] for _ in range(2)]
         e0.record(stream)
+        up.wait_stream(stream)
+        for g in range(G):
+            gstreams[g].wait_stream(stream)
         for i in range(n_e2e):
-            buf = sel_buf[i % 2]
-            buf.copy_(sel_host[i], non_blocking=True)
+            b = i % 2
+            buf = sel_buf[b]
+            if i >= 2 and not args.one_stream:
+                for g in range(G):
+                    up.wait_event(used[b][g])
+            with torch.cuda.stream(up):
+                buf.copy_(sel_host[i], non_blocking=True)
+            up_evt[b].record(up)
             h2d_bytes += buf.numel() * 4
+            for g in range(G):
+                gs = gstreams[g]
+                gs.wait_event(up_evt[b])
+                cache.step_group(g, buf[g], outs[g], entry_row[g], req_off[g], stream=gs)
+                with torch.cuda.stream(gs):
+                    res_host[i, g].copy_(req_off[g], non_blocking=True)
+                used[b][g].record(gs)
+                d2h_bytes += (R + 1) * 4
             ev = steps[n_dev + i][1]
-            issue_groups(buf, wait=True)
             apply_step_events(cache, ev, rows_host[i])  # rows read from pinned host memory
             h2d_bytes += sum(r.numel() for r in rows_host[i] if r is not None)
-            join_groups()
-            for g in range(G):
-                res_host[i, g].copy_(req_off[g], non_blocking=True)
-                d2h_bytes += (R + 1) * 4
+        join_groups()
+        stream.wait_stream(up)
         e1.record(stream)
         st3 = cache.sync()
         torch.cuda.synchronize()
