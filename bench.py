@@ -46,7 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="longdoc")
     ap.add_argument("--policy", choices=["pblru", "exact"], default="pblru",
                     help="replacement policy: PB-LRU, or exact LRU (timestamp scan)")
-    ap.add_argument("--repeats", type=int, default=3,
+    ap.add_argument("--repeats", type=int, default=5,
                     help="timed regions of --steps steps each; value = their median")
     ap.add_argument("--hit-rates", action="store_true",
                     help="CPU only: the oracle over the workload's whole trace, PB-LRU against "
