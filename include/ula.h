@@ -103,9 +103,8 @@ typedef struct ula_config {
  * recorded.  The map commit follows the last layer, as without the flag. */
 #define ULA_FLAG_LAYER_SIGNAL 4u
 
-/* The hit gather beside the move.  By default a step gathers its hit rows right after
- * the hits are known and starts the move (write-back and fill) when the gather is
- * done: the move's host-link traffic and the gather's HBM traffic slow each other
+/* The hit gather beside the move.  By default a step gathers its hit rows after its
+ * metadata and starts the move (write-back and fill) when the gather is done: the move's host-link traffic and the gather's HBM traffic slow each other
  * down on the SMs they share (the gather ran at about a third of its rate beside the
  * move, on a GB300), so the step keeps them apart.  With this flag the gather runs
  * on a low-priority stream beside the move instead: the step's outputs are complete

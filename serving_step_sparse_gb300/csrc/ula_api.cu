@@ -1,18 +1,19 @@
 // Host orchestrator behind the C ABI (include/ula.h): context set-up, argument
 // checks, stream/event ordering, and the per-call kernel sequences.
 //
-// Ordering rules (UlaCache summary page, §2 (the paragraph on layer groups sharing a selection) and §3 last
-// paragraph): a step's critical-path kernels run in stream order on an internal
-// high-priority stream -- dedup/translate + capacity check -> rotate/compact ->
-// mark/victim walk -> victim emit -> move+commit -> signal.  The hit rows are
-// gathered once the marking is done, beside the move: layer 0 on a second
-// high-priority stream (the caller's stream waits for it and the commit), the
-// later layers in one launch on the low-priority side stream (prefetch; their
-// ready events follow it and the commit).  Every call is
-// ordered after the previous call on the context (event wait when the stream
-// changes), and anything touching group g first waits for group g's pending
-// side-stream gathers, so a slot is never refilled while an earlier gather of
-// it is still reading.
+// Ordering rules (UlaCache summary page, §2 on layer groups sharing one selection, and §3
+// last paragraph: the data moves first, then the map, then the signal).  A step's metadata
+// kernels run on the context's metadata stream, chained by programmatic dependent launch:
+// dedup/translate + capacity check -> rotate/compact -> mark/victim walk -> victim emit.
+// Its copies run on the copy stream after an event on that metadata: the hit gather (every
+// layer, one launch), the staging copy of the victims' rows, the move (write-backs, fills,
+// each victim's commit), each chained to the one before by programmatic dependent launch.
+// A group's step waits only for that group's previous step (its commit and gather
+// events) and its last alloc/free, so one call's metadata runs while earlier calls' copies
+// run.  With ULA_FLAG_GATHER_BESIDE_MOVE the gather runs instead on the low-priority side
+// stream, released after the compaction, beside the rest.  The caller's stream waits for
+// the commit and the gather; alloc/free run per group, on the group's update stream, after
+// the group's step in flight.
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
