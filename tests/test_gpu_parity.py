@@ -755,5 +755,12 @@ def test_regather_reproduces_hit_rows():
             with pytest.raises(ula.UlaError):
                 ula.ula_debug_regather(gpu.cache.ctx, g, 1, buf.data_ptr(), buf.shape[1],
                                        torch.cuda.current_stream().cuda_stream, n_layers=L)
+        # into a buffer shorter than the step's unique rows: the gather latches the capacity
+        # error on the device (and writes nothing), the next sync reports it
+        U = gpu.cache.export(0)["U"]
+        short = gpu.cache.out_buffer(0, max(1, U - 1))
+        ula.ula_debug_regather(gpu.cache.ctx, 0, 0, short.data_ptr(), short.shape[1],
+                               torch.cuda.current_stream().cuda_stream, n_layers=w.layers_per_group)
+        assert ula.ula_sync_rc(gpu.cache.ctx) == ula.ERR_CAPACITY
     finally:
         gpu.close()
