@@ -197,8 +197,11 @@ int ula_free(ula_ctx *ctx, uint32_t logical_base, uint32_t n);
  *       in this round): by default after the step's metadata and before the move, on
  *       the context's copy stream; with ULA_FLAG_GATHER_BESIDE_MOVE on an internal
  *       low-priority stream as soon as the compaction has recorded their slots, beside
- *       the marking, the victim choice and the move.  Rows that missed are written by
- *       the fill itself, from the bytes it moves.
+ *       the marking, the victim choice and the move.  The gather moves whole rows with
+ *       bulk copies through shared memory (blocks of 16 threads, one row buffer each:
+ *       42 KB per block for 4 layers of 656 bytes; rows longer than 6,392 bytes go
+ *       through registers instead).  Rows that missed are written by the fill itself,
+ *       from the bytes it moves.
  * The move writes every victim that holds data back from a staging copy in HBM (made
  * right after the victims are known), so its write-backs (in victim order, which is
  * ascending host-slot order) and its fills (sorted by the miss's host slot) each
